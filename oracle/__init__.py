@@ -1,0 +1,268 @@
+"""CPU oracle of the Higgs-Audio-style prefill + delayed-codebook path.
+
+TEST INFRASTRUCTURE ONLY.  Imported by the tests, by the smoke check and by the benchmark's
+CPU-baseline / reference arm; never by the product path.  The arithmetic lives in the plain C file
+``hra_oracle.c`` beside this module (fp32 on bf16-rounded values, loops in textbook order); this
+wrapper only marshals numpy arrays.  bf16 tensors cross this boundary as numpy ``uint16`` arrays
+holding the bf16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hra_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no FP contraction so x86 and Arm agree)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
+                               "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class OracleDims(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("n_codebooks", ctypes.c_int32), ("codebook_size", ctypes.c_int32),
+                ("bos_id", ctypes.c_int32), ("eoc_id", ctypes.c_int32)]
+
+
+class OracleLayer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.oracle_round_bf16.argtypes = [_f32p, _u16p, ctypes.c_int64]
+        L.oracle_rmsnorm.argtypes = [_u16p, _u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, _u16p]
+        L.oracle_linear.argtypes = [_u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
+        L.oracle_rope_table.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, _f32p, _f32p]
+        L.oracle_qk_norm_rope.argtypes = [_u16p, _u16p, _i32p, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_float, ctypes.c_double, _u16p]
+        L.oracle_attend.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p, ctypes.c_void_p,
+                                    ctypes.c_int]
+        L.oracle_prefill.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
+                                     _u16p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, _u16p,
+                                     ctypes.c_int, ctypes.c_int, _u16p]
+        L.oracle_decode.argtypes = [ctypes.POINTER(OracleDims), ctypes.POINTER(OracleLayer), _u16p,
+                                    _u16p, _i32p, ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int,
+                                    _u16p]
+        L.oracle_delay_step.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
+                                        ctypes.c_void_p, ctypes.c_int, _i32p, _i32p, _i32p]
+        L.oracle_code_embed_sum.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p, _i32p,
+                                            ctypes.c_int, _u16p]
+        L.oracle_codebook_step.argtypes = [ctypes.POINTER(OracleDims), _u16p, _u16p, _u16p, _i32p,
+                                           ctypes.c_void_p, ctypes.c_int, _i32p, _u16p, _i32p,
+                                           ctypes.c_void_p]
+        for f in ("oracle_prefill", "oracle_decode", "oracle_codebook_step", "oracle_max_threads"):
+            getattr(L, f).restype = ctypes.c_int
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return lib().oracle_max_threads()
+
+
+def set_threads(n: int) -> None:
+    lib().oracle_set_threads(int(n))
+
+
+# ------------------------------------------------------------------ element-wise helpers
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_round_bf16(x.reshape(-1), out.reshape(-1), x.size)
+    return out
+
+
+def bf16_value(u: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp32 values (exact)."""
+    return (np.asarray(u, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    x, g = _c(x, np.uint16), _c(g, np.uint16)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    lib().oracle_rmsnorm(x, g, x.size // n, n, eps, out)
+    return out
+
+
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """x [T, K] bf16 bits, w [N, K] bf16 bits -> fp32 [T, N] (unrounded)."""
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    T, K = x.shape
+    N = w.shape[0]
+    assert w.shape[1] == K
+    out = np.empty((T, N), np.float32)
+    lib().oracle_linear(x, w, T, N, K, out)
+    return out
+
+
+def rope_table(n_pos: int, hd: int, theta: float):
+    c = np.empty((n_pos, hd // 2), np.float32)
+    s = np.empty((n_pos, hd // 2), np.float32)
+    lib().oracle_rope_table(n_pos, hd, theta, c, s)
+    return c, s
+
+
+def qk_norm_rope(x: np.ndarray, g: np.ndarray, pos, eps: float, theta: float) -> np.ndarray:
+    x, g = _c(x, np.uint16), _c(g, np.uint16)
+    pos = _c(pos, np.int32)
+    rows, hd = x.shape
+    out = np.empty_like(x)
+    lib().oracle_qk_norm_rope(x, g, pos, rows, hd, eps, theta, out)
+    return out
+
+
+def attend(q, kc, vc, q_pos0: int, want_probs: bool = False):
+    """q [n, nq, hd], kc/vc [nkv, n_slots, hd] bf16 bits -> out [n, nq*hd] (+ probs [n, nq, keys])."""
+    q, kc, vc = _c(q, np.uint16), _c(kc, np.uint16), _c(vc, np.uint16)
+    n, nq, hd = q.shape
+    nkv, n_slots, _ = kc.shape
+    out = np.empty((n, nq * hd), np.uint16)
+    nk = q_pos0 + n
+    probs = np.zeros((n, nq, nk), np.float32) if want_probs else None
+    lib().oracle_attend(q, kc, vc, n_slots, q_pos0, n, nq, nkv, hd, out,
+                        probs.ctypes.data if want_probs else None, nk)
+    return (out, probs) if want_probs else out
+
+
+# ------------------------------------------------------------------ model level
+
+def make_dims(d) -> OracleDims:
+    return OracleDims(d.n_layers, d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.ffn, d.vocab,
+                      d.rope_theta, d.rms_eps, d.n_codebooks, d.codebook_size, d.bos_id, d.eoc_id)
+
+
+_LAYER_KEYS = ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")
+
+
+class HostWeights:
+    """Backbone weights as contiguous numpy uint16 arrays plus the ctypes layer table."""
+
+    def __init__(self, d, embed, layers, final_norm):
+        self.d = d
+        self.embed = _c(embed, np.uint16)
+        self.layers = [{k: _c(l[k], np.uint16) for k in _LAYER_KEYS} for l in layers]
+        self.final_norm = _c(final_norm, np.uint16)
+        n = len(self.layers)
+        self.table = (OracleLayer * max(n, 1))()
+        for i, l in enumerate(self.layers):
+            for k in _LAYER_KEYS:
+                setattr(self.table[i], k, l[k].ctypes.data)
+
+
+def kv_shape(d, kv_batch: int, n_slots: int):
+    return (d.n_layers, kv_batch, 2, d.n_kv_heads, n_slots, d.head_dim)
+
+
+def prefill(d, w: HostWeights, tokens: np.ndarray, lens, n_slots: int,
+            kv: Optional[np.ndarray] = None):
+    """Returns (kv [L, B, 2, nkv, n_slots, hd] uint16, last_hidden [B, H] uint16)."""
+    tokens = _c(tokens, np.int32)
+    lens = _c(lens, np.int32)
+    B, P = tokens.shape
+    if kv is None:
+        kv = np.zeros(kv_shape(d, B, n_slots), np.uint16)
+    last = np.empty((B, d.hidden), np.uint16)
+    dims = make_dims(d)
+    rc = lib().oracle_prefill(ctypes.byref(dims), w.embed, w.table, w.final_norm, tokens, lens, B, P,
+                              kv, kv.shape[1], n_slots, last)
+    if rc != 0:
+        raise ValueError("oracle_prefill rejected its arguments")
+    return kv, last
+
+
+def decode(d, w: HostWeights, in_emb: np.ndarray, pos, kv: np.ndarray, n_slots: int) -> np.ndarray:
+    in_emb = _c(in_emb, np.uint16)
+    pos = _c(pos, np.int32)
+    B = in_emb.shape[0]
+    out = np.empty((B, d.hidden), np.uint16)
+    dims = make_dims(d)
+    rc = lib().oracle_decode(ctypes.byref(dims), w.table, w.final_norm, in_emb, pos, B, kv,
+                             kv.shape[1], n_slots, out)
+    if rc != 0:
+        raise ValueError("oracle_decode rejected its arguments")
+    return out
+
+
+def delay_step(K: int, Vc: int, bos: int, eoc: int, logits: np.ndarray, eoc_bias, state: np.ndarray):
+    """State machine only (state [B,4] int32 updated in place).  Returns (codes [B,K], done [B])."""
+    logits = _c(logits, np.float32)
+    B = logits.shape[0]
+    assert state.dtype == np.int32 and state.flags.c_contiguous
+    codes = np.empty((B, K), np.int32)
+    done = np.empty((B,), np.int32)
+    bias = None if eoc_bias is None else _c(eoc_bias, np.float32)
+    lib().oracle_delay_step(K, Vc, bos, eoc, logits, None if bias is None else bias.ctypes.data, B,
+                            state, codes, done)
+    return codes, done
+
+
+def code_embed_sum(code_emb: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    code_emb = _c(code_emb, np.uint16)
+    codes = _c(codes, np.int32)
+    K, Vc, H = code_emb.shape
+    B = codes.shape[0]
+    out = np.empty((B, H), np.uint16)
+    lib().oracle_code_embed_sum(K, Vc, H, code_emb, codes, B, out)
+    return out
+
+
+def codebook_step(d, hidden, head_w, code_emb, state: np.ndarray, eoc_bias=None):
+    """Returns (codes [B,K], next [B,H] uint16, done [B], logits [B,K,Vc] fp32); state updated."""
+    hidden, head_w, code_emb = _c(hidden, np.uint16), _c(head_w, np.uint16), _c(code_emb, np.uint16)
+    B = hidden.shape[0]
+    K, Vc = d.n_codebooks, d.codebook_size
+    codes = np.empty((B, K), np.int32)
+    nxt = np.empty((B, d.hidden), np.uint16)
+    done = np.empty((B,), np.int32)
+    logits = np.empty((B, K, Vc), np.float32)
+    bias = None if eoc_bias is None else _c(eoc_bias, np.float32)
+    dims = make_dims(d)
+    rc = lib().oracle_codebook_step(ctypes.byref(dims), hidden, head_w, code_emb, state,
+                                    None if bias is None else bias.ctypes.data, B, codes, nxt, done,
+                                    logits.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_codebook_step rejected its arguments")
+    return codes, nxt, done, logits
+
+
+def host_weights_from(d, w: dict) -> HostWeights:
+    """Host copy of a backbone weight dict produced by the workloads module (torch bf16 tensors)."""
+    from workloads import to_u16
+    return HostWeights(d, to_u16(w["embed"]), [{k: to_u16(l[k]) for k in _LAYER_KEYS} for l in
+                                               w["layers"]], to_u16(w["final_norm"]))

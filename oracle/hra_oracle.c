@@ -1,0 +1,454 @@
+/*
+ * hra_oracle.c -- plain, slow CPU oracle of the Higgs-Audio-style hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests, the smoke check and the benchmark's CPU-baseline /
+ * reference arm load this file's library.  It shares no code, header or table with the CUDA
+ * library and includes none of it.
+ *
+ * What it computes (each function cites its source):
+ *   - batched prefill of a Qwen3-style decoder backbone: embedding lookup, RMSNorm, merged QKV
+ *     projection, per-head q/k RMSNorm + rotate-half RoPE with the KV-cache write, causal GQA
+ *     attention over the used keys, o-projection + residual, RMSNorm, SwiGLU MLP + residual,
+ *     final RMSNorm at the last used position ("Stabilize Higgs Audio termination and prefill",
+ *     Summary; "flashrt_structures/impls/prefill_tower/fp8_chain.py", module docstring and run());
+ *   - the single-token decode pass through the same layers, fed an embedding;
+ *   - the per-frame delayed-codebook step: audio-head logits, per-codebook argmax under the delay
+ *     pattern with BOS/EOC handling and stop flags, and the sum of the K codebook embeddings
+ *     ("Stabilize Higgs Audio termination and prefill", Summary and Root cause).
+ *
+ * Arithmetic: fp32 on bf16-rounded weights and activations.  Values are rounded to bf16
+ * (round-to-nearest-even) at these points and nowhere else: every RMSNorm output, the QKV
+ * projection output, q and k after norm+RoPE (the norm stays fp32 into RoPE), the attention
+ * output, gate and up projection outputs, the SwiGLU product, the residual after each add
+ * (one rounding of r + acc), the final hidden, and the next-input embedding sum.  Logits stay
+ * fp32.  Attention probabilities are exact fp32 (not rounded).  Dot products are summed in
+ * ascending index order; compiled with -ffp-contract=off so x86 and Arm builds agree bit for bit.
+ *
+ * Readings where the pages are silent (stated once here, used throughout):
+ *   - RMSNorm: y = bf16((x * (1/sqrt(mean(x^2) + eps))) * g), one rounding;
+ *   - q/k norm gains are shared across heads ([head_dim]); GQA maps q head h to kv head
+ *     h / (n_q / n_kv); attention scale 1/sqrt(head_dim); no biases;
+ *   - RoPE pairs (i, i + hd/2), inv_freq_i = theta^(-2i/hd), positions restart at 0 in each
+ *     sequence; cos/sin are evaluated in double and rounded to fp32;
+ *   - delay pattern: codebook k lags k frames; see oracle_delay_step.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <limits.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rope_theta, rms_eps;
+    int32_t n_codebooks, codebook_size, bos_id, eoc_id;
+} oracle_dims;
+
+typedef struct {
+    const uint16_t *attn_norm, *w_qkv, *q_norm, *k_norm, *w_o, *mlp_norm, *w_gate_up, *w_down;
+} oracle_layer;
+
+/* ---------------------------------------------------------------- bf16 storage */
+
+static float bf(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even; NaN stays NaN. */
+static uint16_t to_bf(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+void oracle_round_bf16(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = to_bf(in[i]);
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ---------------------------------------------------------------- RMSNorm */
+
+/* y[r] = bf16((x[r] * (1/sqrt(mean(x[r]^2) + eps))) * g), per row of n.
+ * Source: RMSNorm before each projection and the final norm ("fp8_chain.py", run(): the final
+ * hidden is fin * rsqrt(mean(fin^2) + eps) * final_w). */
+void oracle_rmsnorm(const uint16_t* x, const uint16_t* g, int64_t rows, int n, float eps,
+                    uint16_t* y) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* xr = x + r * (int64_t)n;
+        float ss = 0.0f;
+        for (int i = 0; i < n; ++i) ss += bf(xr[i]) * bf(xr[i]);
+        float inv = 1.0f / sqrtf(ss / (float)n + eps);
+        for (int i = 0; i < n; ++i) y[r * (int64_t)n + i] = to_bf((bf(xr[i]) * inv) * bf(g[i]));
+    }
+}
+
+/* ---------------------------------------------------------------- linear */
+
+/* y[t][j] = sum_k x[t][k] * w[j][k] in fp32, k ascending; w row-major [N][K] (out, in).
+ * The weight is transposed to fp32 once so the inner loop runs over j; each y[t][j] still sums
+ * its K products in ascending k order. */
+void oracle_linear(const uint16_t* x, const uint16_t* w, int T, int N, int K, float* y) {
+    float* wt = (float*)malloc(sizeof(float) * (size_t)K * (size_t)N);
+    #pragma omp parallel for schedule(static)
+    for (int j = 0; j < N; ++j)
+        for (int k = 0; k < K; ++k) wt[(size_t)k * N + j] = bf(w[(size_t)j * K + k]);
+    const int JB = 256;
+    int nblk = (N + JB - 1) / JB;
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        for (int jb = 0; jb < nblk; ++jb) {
+            int j0 = jb * JB, j1 = j0 + JB < N ? j0 + JB : N;
+            float acc[256];
+            for (int j = j0; j < j1; ++j) acc[j - j0] = 0.0f;
+            const uint16_t* xt = x + (size_t)t * K;
+            for (int k = 0; k < K; ++k) {
+                float xv = bf(xt[k]);
+                const float* wk = wt + (size_t)k * N;
+                for (int j = j0; j < j1; ++j) acc[j - j0] += xv * wk[j];
+            }
+            for (int j = j0; j < j1; ++j) y[(size_t)t * N + j] = acc[j - j0];
+        }
+    }
+    free(wt);
+}
+
+/* ---------------------------------------------------------------- RoPE */
+
+/* cos/sin table [n_pos][hd/2]: angle = pos * theta^(-2i/hd), evaluated in double, rounded to fp32. */
+void oracle_rope_table(int n_pos, int hd, double theta, float* cos_t, float* sin_t) {
+    int half = hd / 2;
+    for (int p = 0; p < n_pos; ++p)
+        for (int i = 0; i < half; ++i) {
+            double inv_freq = pow(theta, -(2.0 * (double)i) / (double)hd);
+            double ang = (double)p * inv_freq;
+            cos_t[p * half + i] = (float)cos(ang);
+            sin_t[p * half + i] = (float)sin(ang);
+        }
+}
+
+/* One head: RMSNorm over hd with gain g (kept fp32), then rotate-half RoPE at position pos,
+ * rounded once to bf16.  Source: per-head q/k norm + RoPE before the cache write ("Stabilize Higgs
+ * Audio termination and prefill", Summary: "q/k norm + RoPE, and KV writes"; "fp8_chain.py":
+ * keys kept in host rotate-half layout in the cache). */
+static void head_norm_rope(const uint16_t* x, const uint16_t* g, int hd, float eps,
+                           const float* cos_p, const float* sin_p, uint16_t* out) {
+    float xn[256];
+    float ss = 0.0f;
+    for (int i = 0; i < hd; ++i) ss += bf(x[i]) * bf(x[i]);
+    float inv = 1.0f / sqrtf(ss / (float)hd + eps);
+    for (int i = 0; i < hd; ++i) xn[i] = (bf(x[i]) * inv) * bf(g[i]);
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        float a = xn[i], b = xn[i + half], c = cos_p[i], s = sin_p[i];
+        out[i] = to_bf(a * c - b * s);
+        out[i + half] = to_bf(b * c + a * s);
+    }
+}
+
+/* Batch form for tests: rows of x [rows][hd], positions pos[rows]. */
+void oracle_qk_norm_rope(const uint16_t* x, const uint16_t* g, const int32_t* pos, int rows, int hd,
+                         float eps, double theta, uint16_t* out) {
+    int maxp = 0;
+    for (int r = 0; r < rows; ++r) if (pos[r] > maxp) maxp = pos[r];
+    float* ct = (float*)malloc(sizeof(float) * (size_t)(maxp + 1) * (hd / 2));
+    float* st = (float*)malloc(sizeof(float) * (size_t)(maxp + 1) * (hd / 2));
+    oracle_rope_table(maxp + 1, hd, theta, ct, st);
+    for (int r = 0; r < rows; ++r)
+        head_norm_rope(x + (size_t)r * hd, g, hd, eps, ct + (size_t)pos[r] * (hd / 2),
+                       st + (size_t)pos[r] * (hd / 2), out + (size_t)r * hd);
+    free(ct);
+    free(st);
+}
+
+/* ---------------------------------------------------------------- attention */
+
+/* Causal GQA attention of n rows at positions q_pos0 .. q_pos0+n-1 over the cache keys 0..pos.
+ *   q   [n][nq][hd]   (post-RoPE, bf16)
+ *   kc  [nkv][n_slots][hd], vc [nkv][n_slots][hd]   one sequence's cache for one layer
+ *   out [n][nq*hd]    bf16(sum_j p_j v_j / sum_j p_j), p_j = exp(s_j - max s), s_j = q.k_j / sqrt(hd)
+ *   probs (optional) [n][nq][n_keys_max]: the normalised probabilities (fp32), zeros past pos.
+ * Source: dense attention "over exactly the used keys" with trailing pads ("fp8_chain.py", module
+ * docstring and _prefill_mask_facts); causal because the backbone is a decoder. */
+void oracle_attend(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, int n_slots,
+                   int q_pos0, int n, int nq, int nkv, int hd, uint16_t* out,
+                   float* probs, int n_keys_max) {
+    const float scale = 1.0f / sqrtf((float)hd);
+    const int group = nq / nkv;
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int i = 0; i < n; ++i) {
+        for (int h = 0; h < nq; ++h) {
+            int pos = q_pos0 + i;
+            int kvh = h / group;
+            const uint16_t* qi = q + ((size_t)i * nq + h) * hd;
+            const uint16_t* kh = kc + (size_t)kvh * n_slots * hd;
+            const uint16_t* vh = vc + (size_t)kvh * n_slots * hd;
+            float* s = (float*)malloc(sizeof(float) * (size_t)(pos + 1));
+            float m = -INFINITY;
+            for (int j = 0; j <= pos; ++j) {
+                float dot = 0.0f;
+                for (int e = 0; e < hd; ++e) dot += bf(qi[e]) * bf(kh[(size_t)j * hd + e]);
+                s[j] = dot * scale;
+                if (s[j] > m) m = s[j];
+            }
+            float l = 0.0f;
+            for (int j = 0; j <= pos; ++j) {
+                s[j] = expf(s[j] - m);
+                l += s[j];
+            }
+            for (int e = 0; e < hd; ++e) {
+                float acc = 0.0f;
+                for (int j = 0; j <= pos; ++j) acc += s[j] * bf(vh[(size_t)j * hd + e]);
+                out[(size_t)i * nq * hd + (size_t)h * hd + e] = to_bf(acc / l);
+            }
+            if (probs) {
+                float* pr = probs + ((size_t)i * nq + h) * n_keys_max;
+                for (int j = 0; j < n_keys_max; ++j) pr[j] = j <= pos ? s[j] / l : 0.0f;
+            }
+            free(s);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- decoder layers */
+
+static float silu(float x) { return x / (1.0f + expf(-x)); }
+
+/* Run n new rows of ONE sequence through every layer.
+ *   x_in   [n][H] bf16 input embeddings of the new rows (positions start .. start+n-1)
+ *   kv     this sequence's layer-0 cache block; layer l starts at kv + l * layer_stride;
+ *          within a layer: K [nkv][n_slots][hd] then V [nkv][n_slots][hd]
+ *   hidden [n][H] final-RMSNorm output of every new row (may be NULL)
+ * Per layer ("fp8_chain.py", run(): norm -> QKV -> split/RoPE/cache -> attend -> o-proj, residual
+ * add -> norm -> gate/up -> gated activation -> down, residual add; SwiGLU replaces that page's
+ * GeGLU for the Qwen3-style backbone):
+ *   y = RMSNorm(r; attn_norm); qkv = bf16(y W_qkv^T)
+ *   q_h, k_j = bf16(RoPE(RMSNorm_hd(.; q_norm / k_norm), pos)); cache K[j][pos] = k_j, V[j][pos] = v_j
+ *   a = attention(q, cache keys 0..pos);  r = bf16(r + a W_o^T)
+ *   y = RMSNorm(r; mlp_norm); g = bf16(y W_gate^T), u = bf16(y W_up^T); h = bf16(silu(g) * u)
+ *   r = bf16(r + h W_down^T) */
+static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const uint16_t* final_norm,
+                         const uint16_t* x_in, int start, int n, uint16_t* kv, size_t layer_stride,
+                         int n_slots, uint16_t* hidden) {
+    const int H = d->hidden, nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim, F = d->ffn;
+    const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
+    const float eps = d->rms_eps;
+    uint16_t* r = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
+    uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
+    uint16_t* qkv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * Dqkv);
+    uint16_t* qr = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * Dq);
+    uint16_t* att = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * Dq);
+    uint16_t* hmid = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * F);
+    size_t fmax = (size_t)n * (size_t)(Dqkv > 2 * F ? Dqkv : 2 * F);
+    if (fmax < (size_t)n * H) fmax = (size_t)n * H;
+    float* acc = (float*)malloc(sizeof(float) * fmax);
+    float* ct = (float*)malloc(sizeof(float) * (size_t)(start + n) * (hd / 2));
+    float* st = (float*)malloc(sizeof(float) * (size_t)(start + n) * (hd / 2));
+    oracle_rope_table(start + n, hd, (double)d->rope_theta, ct, st);
+    memcpy(r, x_in, sizeof(uint16_t) * (size_t)n * H);
+
+    for (int l = 0; l < d->n_layers; ++l) {
+        const oracle_layer* L = &layers[l];
+        uint16_t* kc = kv + (size_t)l * layer_stride;
+        uint16_t* vc = kc + (size_t)nkv * n_slots * hd;
+        /* attention block */
+        oracle_rmsnorm(r, L->attn_norm, n, H, eps, y);
+        oracle_linear(y, L->w_qkv, n, Dqkv, H, acc);
+        for (size_t i = 0; i < (size_t)n * Dqkv; ++i) qkv[i] = to_bf(acc[i]);
+        for (int i = 0; i < n; ++i) {
+            int pos = start + i;
+            const uint16_t* row = qkv + (size_t)i * Dqkv;
+            const float* cp = ct + (size_t)pos * (hd / 2);
+            const float* sp = st + (size_t)pos * (hd / 2);
+            for (int h = 0; h < nq; ++h)
+                head_norm_rope(row + (size_t)h * hd, L->q_norm, hd, eps, cp, sp,
+                               qr + (size_t)i * Dq + (size_t)h * hd);
+            for (int j = 0; j < nkv; ++j) {
+                head_norm_rope(row + (size_t)(nq + j) * hd, L->k_norm, hd, eps, cp, sp,
+                               kc + ((size_t)j * n_slots + pos) * hd);
+                memcpy(vc + ((size_t)j * n_slots + pos) * hd, row + (size_t)(nq + nkv + j) * hd,
+                       sizeof(uint16_t) * hd);
+            }
+        }
+        oracle_attend(qr, kc, vc, n_slots, start, n, nq, nkv, hd, att, NULL, 0);
+        oracle_linear(att, L->w_o, n, H, Dq, acc);
+        for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
+        /* MLP block */
+        oracle_rmsnorm(r, L->mlp_norm, n, H, eps, y);
+        oracle_linear(y, L->w_gate_up, n, 2 * F, H, acc);
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < F; ++j) {
+                float g = bf(to_bf(acc[(size_t)i * 2 * F + j]));
+                float u = bf(to_bf(acc[(size_t)i * 2 * F + F + j]));
+                hmid[(size_t)i * F + j] = to_bf(silu(g) * u);
+            }
+        oracle_linear(hmid, L->w_down, n, H, F, acc);
+        for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
+    }
+    if (hidden) oracle_rmsnorm(r, final_norm, n, H, eps, hidden);
+    free(r); free(y); free(qkv); free(qr); free(att); free(hmid); free(acc); free(ct); free(st);
+}
+
+/* Batched prefill.  tokens [B][P_max] with trailing pads (never read); seq_lens[B] in [1, n_slots].
+ * kv [L][kv_batch][2][nkv][n_slots][hd]: slots 0..len-1 of sequence b are written, others untouched.
+ * last_hidden [B][H] = final RMSNorm of position len_b - 1.  Returns 0, or -1 on a bad argument.
+ * Source: batched prefill with KV writes ("Stabilize Higgs Audio termination and prefill",
+ * Summary); pads trail and only the used keys are attended ("fp8_chain.py", module docstring). */
+int oracle_prefill(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                   const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
+                   int B, int P_max, uint16_t* kv, int kv_batch, int n_slots, uint16_t* last_hidden) {
+    const int H = d->hidden;
+    const size_t blk = (size_t)2 * d->n_kv_heads * n_slots * d->head_dim;
+    if (B < 1 || B > kv_batch) return -1;
+    for (int b = 0; b < B; ++b) {
+        int n = seq_lens[b];
+        if (n < 1 || n > P_max || n > n_slots) return -1;
+        for (int i = 0; i < n; ++i)
+            if (tokens[(size_t)b * P_max + i] < 0 || tokens[(size_t)b * P_max + i] >= d->vocab) return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        int n = seq_lens[b];
+        uint16_t* x = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
+        uint16_t* hid = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
+        for (int i = 0; i < n; ++i)
+            memcpy(x + (size_t)i * H, embed + (size_t)tokens[(size_t)b * P_max + i] * H,
+                   sizeof(uint16_t) * H);
+        forward_rows(d, layers, final_norm, x, 0, n, kv + (size_t)b * blk, (size_t)kv_batch * blk,
+                     n_slots, hid);
+        memcpy(last_hidden + (size_t)b * H, hid + (size_t)(n - 1) * H, sizeof(uint16_t) * H);
+        free(x);
+        free(hid);
+    }
+    return 0;
+}
+
+/* Single-token decode pass: row b is the embedding in_emb[b] at position pos[b]; it writes cache
+ * slot pos[b] of every layer and attends slots 0..pos[b].  hidden [B][H] = final RMSNorm output.
+ * Source: the AR audio decode pass per frame ("Stabilize Higgs Audio termination and prefill",
+ * Performance: AR decode ms/frame); its input is the summed codebook embedding. */
+int oracle_decode(const oracle_dims* d, const oracle_layer* layers, const uint16_t* final_norm,
+                  const uint16_t* in_emb, const int32_t* pos, int B, uint16_t* kv, int kv_batch,
+                  int n_slots, uint16_t* hidden) {
+    const int H = d->hidden;
+    const size_t blk = (size_t)2 * d->n_kv_heads * n_slots * d->head_dim;
+    if (B < 1 || B > kv_batch) return -1;
+    for (int b = 0; b < B; ++b)
+        if (pos[b] < 0 || pos[b] >= n_slots) return -1;
+    for (int b = 0; b < B; ++b)
+        forward_rows(d, layers, final_norm, in_emb + (size_t)b * H, pos[b], 1, kv + (size_t)b * blk,
+                     (size_t)kv_batch * blk, n_slots, hidden + (size_t)b * H);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- delayed-codebook step */
+
+/* Delay-pattern state machine for B rows, from given fp32 logits [B][K][Vc].
+ * state [B][4] = (frame t, eoc_frame e (-1 none), done, 0), updated in place; codes [B][K]; done [B].
+ * Source: per-frame argmax with delay handling, and the delayed-EOC fix that makes EOC on any
+ * codebook terminate ("Stabilize Higgs Audio termination and prefill", Summary and Root cause).
+ * Rule, per row (codebook k lags k frames; bias adds eoc_bias[b][k] to the EOC logit):
+ *   t < k               -> BOS (codebook not started)
+ *   e >= 0, t - k >= e  -> EOC (codebook past the end)
+ *   otherwise           -> argmax over all Vc logits, lowest index on ties
+ *   if e < 0 and some argmaxed codebook chose EOC: e = min over those k of (t - k), and every
+ *   codebook with t >= k and t - k >= e is EOC in this frame too
+ *   done |= e >= 0 and t >= e + K - 1; t += 1 (a done row keeps advancing and emits all EOC). */
+void oracle_delay_step(int K, int Vc, int bos, int eoc, const float* logits, const float* eoc_bias,
+                       int B, int32_t* state, int32_t* codes, int32_t* done) {
+    for (int b = 0; b < B; ++b) {
+        int32_t* st = state + (size_t)b * 4;
+        int t = st[0], e = st[1], dn = st[2];
+        int32_t* c = codes + (size_t)b * K;
+        int forced[64];
+        for (int k = 0; k < K; ++k) {
+            if (t < k) {
+                c[k] = bos;
+                forced[k] = 1;
+            } else if (e >= 0 && t - k >= e) {
+                c[k] = eoc;
+                forced[k] = 1;
+            } else {
+                const float* lg = logits + ((size_t)b * K + k) * Vc;
+                int best = 0;
+                float bv = 0.0f;
+                for (int v = 0; v < Vc; ++v) {
+                    float x = lg[v];
+                    if (v == eoc && eoc_bias) x = x + eoc_bias[(size_t)b * K + k];
+                    if (v == 0 || x > bv) {
+                        bv = x;
+                        best = v;
+                    }
+                }
+                c[k] = best;
+                forced[k] = 0;
+            }
+        }
+        if (e < 0) {
+            int cand = INT_MAX;
+            for (int k = 0; k < K; ++k)
+                if (!forced[k] && c[k] == eoc && t - k < cand) cand = t - k;
+            if (cand != INT_MAX) {
+                e = cand;
+                for (int k = 0; k < K; ++k)
+                    if (t >= k && t - k >= e) c[k] = eoc;
+            }
+        }
+        if (e >= 0 && t >= e + K - 1) dn = 1;
+        st[0] = t + 1;
+        st[1] = e;
+        st[2] = dn;
+        st[3] = 0;
+        done[b] = dn;
+    }
+}
+
+/* next[b] = bf16(sum over k ascending of fp32 code_emb[k][codes[b][k]]).  code_emb [K][Vc][H].
+ * Source: codebook embedding accumulation into the next input ("Stabilize Higgs Audio termination
+ * and prefill", Summary). */
+void oracle_code_embed_sum(int K, int Vc, int H, const uint16_t* code_emb, const int32_t* codes,
+                           int B, uint16_t* next) {
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < H; ++i) {
+            float s = 0.0f;
+            for (int k = 0; k < K; ++k)
+                s += bf(code_emb[((size_t)k * Vc + codes[(size_t)b * K + k]) * H + i]);
+            next[(size_t)b * H + i] = to_bf(s);
+        }
+}
+
+/* Full step: logits[b][k][v] = hidden[b] . head_w[k*Vc + v] (fp32), then the delay state machine,
+ * then the embedding sum.  logits_out (optional) receives the raw logits (bias not included). */
+int oracle_codebook_step(const oracle_dims* d, const uint16_t* hidden, const uint16_t* head_w,
+                         const uint16_t* code_emb, int32_t* state, const float* eoc_bias, int B,
+                         int32_t* codes, uint16_t* next, int32_t* done, float* logits_out) {
+    const int K = d->n_codebooks, Vc = d->codebook_size, H = d->hidden;
+    if (B < 1 || K < 1 || K > 64) return -1;
+    float* lg = logits_out ? logits_out : (float*)malloc(sizeof(float) * (size_t)B * K * Vc);
+    oracle_linear(hidden, head_w, B, K * Vc, H, lg);
+    oracle_delay_step(K, Vc, d->bos_id, d->eoc_id, lg, eoc_bias, B, state, codes, done);
+    oracle_code_embed_sum(K, Vc, H, code_emb, codes, B, next);
+    if (!logits_out) free(lg);
+    return 0;
+}
