@@ -1,0 +1,188 @@
+/*
+ * hra.h -- C ABI of the GB300 (sm_103a) Higgs-Audio-style hot path.
+ *
+ * Two operations make up the path:
+ *   1. hra_prefill: batched BF16 prefill of a Qwen3-style decoder backbone -- embedding lookup,
+ *      RMSNorm, merged QKV projection, per-head q/k RMSNorm + RoPE with the KV-cache write, causal
+ *      attention over the used keys of ragged prompts, o-projection, residual + RMSNorm, SwiGLU
+ *      gate/up/down MLP -- returning the last position's final hidden and the filled cache.
+ *      Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141), Summary
+ *      ("kernelize the Higgs BF16 batched prefill path for embedding lookup, projection GEMMs,
+ *      q/k norm + RoPE, and KV writes"); the per-layer chain and the used-key rule follow
+ *      "flashrt-structures 0.2.0, prefill_tower/fp8_chain.py", module docstring and run().
+ *   2. hra_codebook_step: per-frame delayed-codebook step -- audio-head projection to K codebook
+ *      logit rows, per-codebook argmax under the delay pattern, BOS/EOC handling with stop flags,
+ *      and the sum of the K codebook embeddings into the next input.
+ *      Source: FlashRT PR #141, Summary ("shared delayed-codebook helper for per-frame argmax,
+ *      delay handling, and codebook embedding accumulation") and Root cause (delayed EOC).
+ * hra_decode is the single-token backbone pass of the autoregressive audio loop (FlashRT PR #141,
+ * Performance: "AR decode ms/frame"); its input is the summed codebook embedding.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev / device buffers are CUDA device pointers owned by the caller; the
+ *     library never allocates, frees or synchronises inside hra_prefill / hra_decode /
+ *     hra_codebook_step / hra_linear.  All work is enqueued on `stream` (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream) in stream order.
+ *   - Device pointers must be 16-byte aligned; bf16 tensors are row-major and contiguous; weight
+ *     matrices are [out_features, in_features] (each output row is one weight row).
+ *   - Host arrays (seq_lens, pos) are read before the call returns and may be reused afterwards.
+ *   - Every argument is validated before the first launch; on a non-zero return nothing was
+ *     enqueued.  Device-side faults of the input data (a token id outside [0, vocab)) never trap:
+ *     the id is clamped and a sticky bit is set in the workspace's error word, read with
+ *     hra_device_error().
+ *   - Numerics: bf16 storage, fp32 accumulation, bf16 rounding at each norm output, projection
+ *     output, q/k after norm + RoPE, attention output, gate/up/SwiGLU outputs, and the residual
+ *     after each add.  Logits are fp32.
+ */
+#ifndef HRA_H
+#define HRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------------------------- */
+#define HRA_OK 0
+#define HRA_ERR_INVALID_ARG (-1)   /* null or misaligned pointer, non-positive size              */
+#define HRA_ERR_UNSUPPORTED (-2)   /* dims outside what the kernels implement                     */
+#define HRA_ERR_WORKSPACE (-3)     /* workspace smaller than the matching *_workspace_size()      */
+#define HRA_ERR_RANGE (-4)         /* a sequence length or position outside the cache            */
+#define HRA_ERR_CUDA (-5)          /* a CUDA launch or driver call failed                        */
+
+/* Sticky device error bits (hra_device_error). */
+#define HRA_DEVERR_TOKEN_RANGE 1u  /* a token id was outside [0, vocab); it was clamped          */
+#define HRA_DEVERR_WAIT_TIMEOUT 2u /* a pipeline wait inside a kernel gave up (kernel bug guard) */
+#define HRA_DEVERR_CODE_RANGE 4u   /* a code index outside [0, codebook_size) was clamped        */
+
+/* ---- model description ---------------------------------------------------------------------- */
+/* Backbone and audio-head shape.  Supported: head_dim in {64, 128}; n_q_heads % n_kv_heads == 0;
+ * hidden, n_q_heads * head_dim and ffn multiples of 64; 1 <= n_codebooks <= 16;
+ * codebook_size >= 2 with bos_id, eoc_id < codebook_size. */
+typedef struct hra_dims {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rope_theta, rms_eps;
+    int32_t n_codebooks, codebook_size, bos_id, eoc_id;
+} hra_dims;
+
+/* One decoder layer, all bf16 device pointers, [out, in] row-major:
+ *   attn_norm [hidden]; w_qkv [(n_q + 2 n_kv) * head_dim, hidden] (q rows, then k rows, then v rows);
+ *   q_norm, k_norm [head_dim] (shared by all heads); w_o [hidden, n_q * head_dim]; mlp_norm [hidden];
+ *   w_gate_up [2 * ffn, hidden] (gate rows, then up rows); w_down [hidden, ffn]. */
+typedef struct hra_layer_weights {
+    const void *attn_norm, *w_qkv, *q_norm, *k_norm, *w_o, *mlp_norm, *w_gate_up, *w_down;
+} hra_layer_weights;
+
+/* embed [vocab, hidden] bf16 (device); layers: HOST array of n_layers entries; final_norm [hidden]. */
+typedef struct hra_weights {
+    const void* embed;
+    const hra_layer_weights* layers;
+    const void* final_norm;
+} hra_weights;
+
+/* KV cache, bf16 device memory laid out [n_layers][batch][2][n_kv_heads][n_slots][head_dim]
+ * (index 0 = K after norm + RoPE, in rotate-half order; 1 = V).  Slot p of sequence b holds
+ * position p of that sequence.  Only slots that a call writes are touched. */
+typedef struct hra_kv_cache {
+    void* base;
+    int32_t batch;
+    int32_t n_slots;
+} hra_kv_cache;
+
+/* Per-row delay state (device, 16 bytes per row): frame = frames emitted so far; eoc_frame = the
+ * stream's end frame in codebook-0 time, -1 while no EOC has been seen; done = 1 once the last
+ * codebook has emitted EOC (sticky). */
+typedef struct hra_delay_state {
+    int32_t frame, eoc_frame, done, reserved;
+} hra_delay_state;
+
+/* ---- prefill -------------------------------------------------------------------------------- */
+/* Compute the last layer for every row (default: only the rows needed for the last hidden). */
+#define HRA_PREFILL_FULL_LAST_LAYER 1u
+
+/* Bytes of workspace hra_prefill needs for this batch shape (total_tokens = sum of seq_lens). */
+size_t hra_prefill_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens,
+                                  int32_t max_len);
+
+/* Batched prefill of `batch` ragged prompts.
+ *   tokens_dev   int32 [batch, max_len] device; prompt b is tokens[b, 0 : seq_lens[b]]; the rest
+ *                are pads and are never read.
+ *   seq_lens     int32 [batch] HOST; each in [1, min(max_len, kv->n_slots)].  batch <= 1024 and
+ *                batch <= kv->batch.
+ *   kv           cache; slots [0, seq_lens[b]) of sequence b are written in every layer.
+ *   last_hidden_dev bf16 [batch, hidden]: final RMSNorm output at position seq_lens[b] - 1.
+ *   workspace    device scratch of at least hra_prefill_workspace_size() bytes (16-byte aligned).
+ * Returns HRA_OK or a negative status (nothing enqueued). */
+int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags,
+                void* stream);
+
+/* ---- decode pass ---------------------------------------------------------------------------- */
+size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots);
+
+/* One single-token pass through every layer for `batch` rows.
+ *   in_emb_dev  bf16 [batch, hidden]: the input embedding of each row (e.g. the summed codebook
+ *               embedding from hra_codebook_step).
+ *   pos         int32 [batch] HOST: the position of each row's token, in [0, kv->n_slots); the pass
+ *               writes cache slot pos[b] of row b in every layer and attends slots [0, pos[b]].
+ *   hidden_dev  bf16 [batch, hidden]: final RMSNorm output of each row. */
+int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev,
+               const int32_t* pos, int32_t batch, const hra_kv_cache* kv, void* hidden_dev,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- delayed-codebook step ------------------------------------------------------------------ */
+size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch);
+
+/* One frame for `batch` rows (batch <= 1024).
+ *   hidden_dev   bf16 [batch, hidden]
+ *   head_w_dev   bf16 [n_codebooks * codebook_size, hidden]: row k*codebook_size + v gives the logit
+ *                of code v in codebook k.
+ *   code_emb_dev bf16 [n_codebooks, codebook_size, hidden]: codebook embedding tables.
+ *   state_dev    hra_delay_state [batch], read and advanced in place.
+ *   eoc_bias_dev fp32 [batch, n_codebooks] added to each codebook's EOC logit before the argmax, or
+ *                NULL.
+ *   codes_dev    int32 [batch, n_codebooks] out; next_emb_dev bf16 [batch, hidden] out =
+ *                bf16(sum over k ascending of fp32 code_emb[k][code_k]); done_dev int32 [batch] out.
+ *   logits_dev   fp32 [batch, n_codebooks, codebook_size] out (raw logits, bias not added), or NULL.
+ * Delay rule per row (t = frame, e = eoc_frame): codebook k is BOS while t < k; EOC when e >= 0 and
+ * t - k >= e; otherwise the argmax over all codebook_size logits (lowest index on ties).  If e < 0
+ * and an argmaxed codebook k chose EOC, e becomes the smallest such t - k and every codebook with
+ * t - k >= e emits EOC in this frame.  done |= (e >= 0 and t >= e + n_codebooks - 1); t += 1. */
+int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev,
+                      const void* code_emb_dev, hra_delay_state* state_dev,
+                      const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
+                      void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* ---- projection (diagnostic access to the tensor-core GEMM used by the path) ----------------- */
+#define HRA_EPI_STORE 0     /* out bf16 [M, N] = bf16(acc)                                        */
+#define HRA_EPI_RESIDUAL 1  /* out bf16 [M, N] = bf16(out + acc)   (in place)                      */
+#define HRA_EPI_SWIGLU 2    /* w has 2N rows (gate N, then up N): out bf16 [M, N] =
+                               bf16(silu(bf16(gate)) * bf16(up))                                    */
+#define HRA_EPI_F32 3       /* out fp32 [M, N] = acc                                                */
+
+size_t hra_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue, int32_t split_k);
+
+/* out = epilogue(a_dev [M, K] x w_dev^T), w_dev [N (or 2N), K], bf16, fp32 accumulation.
+ * K must be a multiple of 64 and N of 16; split_k = 0 picks the split automatically; > 1 forces a
+ * K split whose fp32 partials go through the workspace. */
+int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
+               int32_t epilogue, int32_t split_k, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/* ---- errors --------------------------------------------------------------------------------- */
+/* Synchronise `stream` and return the sticky HRA_DEVERR_* bits of the last call that used this
+ * workspace (each call clears them first), or a negative status. */
+int32_t hra_device_error(const void* workspace, void* stream);
+
+/* Human-readable text of a status code. */
+const char* hra_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HRA_H */

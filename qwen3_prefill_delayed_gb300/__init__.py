@@ -1,0 +1,291 @@
+"""GB300-native Higgs-Audio-style hot path: batched BF16 prefill of a Qwen3-style backbone and the
+per-frame delayed-codebook step.
+
+This module is a thin ctypes binding of the in-tree CUDA library ``libhra.so`` (C ABI in
+``include/hra.h``).  It only marshals torch tensors into pointers and sizes: every step of the
+path runs in the library's kernels.  There is no CPU fallback -- calling anything here without the
+built library, or with tensors not on a CUDA device, raises.
+
+Entry points (same names as the C ABI): ``hra_prefill``, ``hra_decode``, ``hra_codebook_step``,
+``hra_linear``, ``hra_device_error``; convenience wrappers ``Backbone`` and ``AudioHead`` keep the
+weight tables and workspaces.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libhra.so")
+
+HRA_OK = 0
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported dims", -3: "workspace too small",
+          -4: "length or position outside the cache", -5: "CUDA error"}
+DEVERR_TOKEN_RANGE, DEVERR_WAIT_TIMEOUT, DEVERR_CODE_RANGE = 1, 2, 4
+EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_F32 = 0, 1, 2, 3
+PREFILL_FULL_LAST_LAYER = 1
+
+EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_decode_workspace_size", "hra_decode",
+            "hra_codebook_workspace_size", "hra_codebook_step", "hra_linear_workspace_size",
+            "hra_linear", "hra_device_error", "hra_status_string"]
+
+
+class HraError(RuntimeError):
+    pass
+
+
+class HraDims(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("n_codebooks", ctypes.c_int32), ("codebook_size", ctypes.c_int32),
+                ("bos_id", ctypes.c_int32), ("eoc_id", ctypes.c_int32)]
+
+
+class HraLayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")]
+
+
+class HraWeights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("layers", ctypes.POINTER(HraLayerWeights)),
+                ("final_norm", ctypes.c_void_p)]
+
+
+class HraKvCache(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("batch", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise HraError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        sz, i32, vp, u32 = ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p, ctypes.c_uint32
+        dp = ctypes.POINTER(HraDims)
+        L.hra_prefill_workspace_size.argtypes = [dp, i32, i32, i32]
+        L.hra_prefill_workspace_size.restype = sz
+        L.hra_prefill.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32, i32,
+                                  ctypes.POINTER(HraKvCache), vp, vp, sz, u32, vp]
+        L.hra_prefill.restype = ctypes.c_int
+        L.hra_decode_workspace_size.argtypes = [dp, i32, i32]
+        L.hra_decode_workspace_size.restype = sz
+        L.hra_decode.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32,
+                                 ctypes.POINTER(HraKvCache), vp, vp, sz, vp]
+        L.hra_decode.restype = ctypes.c_int
+        L.hra_codebook_workspace_size.argtypes = [dp, i32]
+        L.hra_codebook_workspace_size.restype = sz
+        L.hra_codebook_step.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
+        L.hra_codebook_step.restype = ctypes.c_int
+        L.hra_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.hra_linear_workspace_size.restype = sz
+        L.hra_linear.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
+        L.hra_linear.restype = ctypes.c_int
+        L.hra_device_error.argtypes = [vp, vp]
+        L.hra_device_error.restype = i32
+        L.hra_status_string.argtypes = [ctypes.c_int]
+        L.hra_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != HRA_OK:
+        msg = lib().hra_status_string(rc).decode()
+        raise HraError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise HraError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise HraError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise HraError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_dims(d) -> HraDims:
+    """HraDims from any object with the Dims field names (e.g. workloads.Dims)."""
+    return HraDims(d.n_layers, d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.ffn, d.vocab,
+                   d.rope_theta, d.rms_eps, d.n_codebooks, d.codebook_size, d.bos_id, d.eoc_id)
+
+
+def new_kv_cache(d, batch: int, n_slots: int, device="cuda", fill=None) -> torch.Tensor:
+    """Cache tensor [n_layers, batch, 2, n_kv_heads, n_slots, head_dim] bf16."""
+    shape = (d.n_layers, batch, 2, d.n_kv_heads, n_slots, d.head_dim)
+    if fill is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    return torch.full(shape, fill, dtype=torch.bfloat16, device=device)
+
+
+class _Workspace:
+    def __init__(self):
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_LAYER_KEYS = ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")
+
+
+class Backbone:
+    """A Qwen3-style backbone on the GPU: weights dict as produced by ``workloads.make_backbone``
+    (embed [V,H], layers[...] with the ``hra_layer_weights`` names, final_norm [H], bf16 CUDA)."""
+
+    def __init__(self, d, weights: dict):
+        self.d = d
+        self.dims = make_dims(d)
+        self.w = weights
+        n = d.n_layers
+        self._layers = (HraLayerWeights * n)()
+        for i in range(n):
+            for k in _LAYER_KEYS:
+                setattr(self._layers[i], k, _ptr(weights["layers"][i][k], torch.bfloat16, k).value)
+        self.table = HraWeights(_ptr(weights["embed"], torch.bfloat16, "embed").value, self._layers,
+                                _ptr(weights["final_norm"], torch.bfloat16, "final_norm").value)
+        self.ws = _Workspace()
+        self.device = weights["embed"].device
+
+    def kv(self, cache: torch.Tensor) -> HraKvCache:
+        d = self.d
+        if cache.dtype != torch.bfloat16 or cache.dim() != 6 or cache.shape[0] != d.n_layers \
+                or cache.shape[2] != 2 or cache.shape[3] != d.n_kv_heads or cache.shape[5] != d.head_dim:
+            raise HraError("KV cache must be bf16 [n_layers, batch, 2, n_kv_heads, n_slots, head_dim]")
+        return HraKvCache(_ptr(cache, torch.bfloat16, "kv cache").value, cache.shape[1], cache.shape[4])
+
+    def prefill_workspace_size(self, batch, total, max_len) -> int:
+        return lib().hra_prefill_workspace_size(ctypes.byref(self.dims), batch, total, max_len)
+
+    def prefill(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor,
+                out: Optional[torch.Tensor] = None, full_last_layer: bool = False,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """hra_prefill: tokens int32 [B, P_max] (CUDA), seq_lens host ints -> last hidden [B, H]."""
+        B, P = tokens.shape
+        lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens])
+        if out is None:
+            out = torch.empty(B, self.d.hidden, dtype=torch.bfloat16, device=tokens.device)
+        need = self.prefill_workspace_size(B, int(sum(seq_lens)), P)
+        ws = workspace if workspace is not None else self.ws.get(need, tokens.device)
+        kv = self.kv(cache)
+        rc = lib().hra_prefill(ctypes.byref(self.dims), ctypes.byref(self.table),
+                               _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
+                               _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
+                               ws.numel(), PREFILL_FULL_LAST_LAYER if full_last_layer else 0,
+                               _stream(stream))
+        _check(rc, "hra_prefill")
+        self.last_ws = ws
+        return out
+
+    def decode_workspace_size(self, batch, n_slots) -> int:
+        return lib().hra_decode_workspace_size(ctypes.byref(self.dims), batch, n_slots)
+
+    def decode(self, in_emb: torch.Tensor, pos: Sequence[int], cache: torch.Tensor,
+               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+        """hra_decode: in_emb bf16 [B, H] (CUDA), pos host ints -> hidden [B, H]."""
+        B = in_emb.shape[0]
+        p = (ctypes.c_int32 * B)(*[int(x) for x in pos])
+        if out is None:
+            out = torch.empty(B, self.d.hidden, dtype=torch.bfloat16, device=in_emb.device)
+        need = self.decode_workspace_size(B, cache.shape[4])
+        ws = workspace if workspace is not None else self.ws.get(need, in_emb.device)
+        kv = self.kv(cache)
+        rc = lib().hra_decode(ctypes.byref(self.dims), ctypes.byref(self.table),
+                              _ptr(in_emb, torch.bfloat16, "in_emb"), p, B, ctypes.byref(kv),
+                              _ptr(out, torch.bfloat16, "hidden"), _ptr(ws, None, "workspace"),
+                              ws.numel(), _stream(stream))
+        _check(rc, "hra_decode")
+        self.last_ws = ws
+        return out
+
+
+class AudioHead:
+    """Audio head [K*Vc, H] and codebook tables [K, Vc, H] (bf16, CUDA) for hra_codebook_step."""
+
+    def __init__(self, d, head_w: torch.Tensor, code_emb: torch.Tensor):
+        self.d = d
+        self.dims = make_dims(d)
+        self.head_w = head_w
+        self.code_emb = code_emb
+        self.ws = _Workspace()
+
+    def workspace_size(self, batch: int) -> int:
+        return lib().hra_codebook_workspace_size(ctypes.byref(self.dims), batch)
+
+    def step(self, hidden: torch.Tensor, state: torch.Tensor, eoc_bias: Optional[torch.Tensor] = None,
+             codes: Optional[torch.Tensor] = None, next_emb: Optional[torch.Tensor] = None,
+             done: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None):
+        """hra_codebook_step: state int32 [B, 4] (frame, eoc_frame, done, 0), advanced in place.
+        Returns (codes int32 [B, K], next_emb bf16 [B, H], done int32 [B])."""
+        B = hidden.shape[0]
+        K, Vc, H = self.d.n_codebooks, self.d.codebook_size, self.d.hidden
+        dev = hidden.device
+        if codes is None:
+            codes = torch.empty(B, K, dtype=torch.int32, device=dev)
+        if next_emb is None:
+            next_emb = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+        if done is None:
+            done = torch.empty(B, dtype=torch.int32, device=dev)
+        if state.dtype != torch.int32 or tuple(state.shape) != (B, 4):
+            raise HraError("state must be int32 [B, 4]")
+        ws = workspace if workspace is not None else self.ws.get(self.workspace_size(B), dev)
+        rc = lib().hra_codebook_step(ctypes.byref(self.dims), _ptr(hidden, torch.bfloat16, "hidden"),
+                                     _ptr(self.head_w, torch.bfloat16, "head_w"),
+                                     _ptr(self.code_emb, torch.bfloat16, "code_emb"),
+                                     _ptr(state, torch.int32, "state"),
+                                     _ptr(eoc_bias, torch.float32, "eoc_bias"), B,
+                                     _ptr(codes, torch.int32, "codes"),
+                                     _ptr(next_emb, torch.bfloat16, "next_emb"),
+                                     _ptr(done, torch.int32, "done"),
+                                     _ptr(logits, torch.float32, "logits"),
+                                     _ptr(ws, None, "workspace"), ws.numel(), _stream(stream))
+        _check(rc, "hra_codebook_step")
+        self.last_ws = ws
+        return codes, next_emb, done
+
+
+def hra_linear(a: torch.Tensor, w: torch.Tensor, epilogue: int = EPI_STORE,
+               out: Optional[torch.Tensor] = None, split_k: int = 0, stream=None) -> torch.Tensor:
+    """out = epilogue(a [M, K] @ w^T) through the tensor-core GEMM of the library."""
+    M, K = a.shape
+    N = w.shape[0] // 2 if epilogue == EPI_SWIGLU else w.shape[0]
+    if out is None:
+        dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+        out = torch.empty(M, N, dtype=dt, device=a.device)
+    need = lib().hra_linear_workspace_size(M, N, K, epilogue, split_k)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=a.device)
+    rc = lib().hra_linear(_ptr(a, torch.bfloat16, "a"), _ptr(w, torch.bfloat16, "w"), _ptr(out, None, "out"),
+                          M, N, K, epilogue, split_k, _ptr(ws, None, "workspace"), ws.numel(),
+                          _stream(stream))
+    _check(rc, "hra_linear")
+    err = lib().hra_device_error(_ptr(ws, None, "workspace"), _stream(stream))
+    if err != 0:
+        raise HraError(f"hra_linear device error bits {err}")
+    return out
+
+
+def hra_device_error(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the sticky device error bits of the last call on this workspace."""
+    return int(lib().hra_device_error(_ptr(workspace, None, "workspace"), _stream(stream)))

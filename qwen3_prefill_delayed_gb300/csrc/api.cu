@@ -1,0 +1,469 @@
+// api.cu -- the extern "C" entry points declared in include/hra.h.
+//
+// Host orchestration only: argument validation (before the first launch), the workspace plan,
+// and the stream-ordered kernel sequence of each operation.  No allocation, no synchronisation
+// (except hra_device_error, which exists to synchronise).
+//
+// Prefill per layer ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py", run(); "Stabilize
+// Higgs Audio termination and prefill", Summary):
+//   QKV GEMM -> q/k norm + RoPE + KV write -> causal attention -> o GEMM (+residual)
+//   -> RMSNorm -> gate/up GEMM (+SwiGLU) -> down GEMM (+residual) -> RMSNorm (next layer / final)
+// In the last layer only the rows that feed the last hidden are carried past the KV write
+// (attention of the last query, o-projection, MLP and final norm of B rows), unless
+// HRA_PREFILL_FULL_LAST_LAYER asks for every row.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "internal.h"
+
+using namespace hra;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Region {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += align_up(bytes);
+        return o;
+    }
+};
+
+// Offsets (bytes) of every buffer inside a caller workspace.
+struct Layout {
+    size_t err, row_seq, row_pos, cu, last_row, rope, r, y, qkv, q, att, h, rl, part, apart, total;
+    int attn_splits;
+};
+
+bool dims_ok(const hra_dims* d) {
+    if (d == nullptr) return false;
+    if (d->n_layers < 1 || d->hidden < 64 || d->hidden % 64 != 0) return false;
+    if (d->head_dim != 64 && d->head_dim != 128) return false;
+    if (d->n_q_heads < 1 || d->n_kv_heads < 1 || d->n_q_heads % d->n_kv_heads != 0) return false;
+    const int g = d->n_q_heads / d->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return false;
+    if ((d->n_q_heads * d->head_dim) % 64 != 0 || d->ffn < 64 || d->ffn % 64 != 0) return false;
+    if (d->vocab < 1) return false;
+    if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f)) return false;
+    return true;
+}
+
+bool audio_dims_ok(const hra_dims* d) {
+    if (d == nullptr || d->hidden < 64 || d->hidden % 64 != 0) return false;
+    if (d->n_codebooks < 1 || d->n_codebooks > 16) return false;
+    if (d->codebook_size < 2 || (d->n_codebooks * d->codebook_size) % 8 != 0) return false;
+    if (d->bos_id < 0 || d->bos_id >= d->codebook_size || d->eoc_id < 0 || d->eoc_id >= d->codebook_size)
+        return false;
+    return true;
+}
+
+// Shared plan of the backbone passes.  `rows` = packed rows that run the full layers, `last_rows`
+// = rows of the last-layer tail (batch), `rope_rows` = rows of the RoPE table.
+Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, int max_pos) {
+    const size_t H = d.hidden, hd = d.head_dim, Dq = (size_t)d.n_q_heads * hd;
+    const size_t Dqkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * hd, F = d.ffn;
+    const size_t T = (size_t)std::max(rows, batch);
+    Region g;
+    Layout L;
+    L.err = g.take(256);
+    L.row_seq = g.take(T * 4);
+    L.row_pos = g.take(T * 4);
+    L.cu = g.take((size_t)(batch + 1) * 4);
+    L.last_row = g.take((size_t)batch * 4);
+    L.rope = g.take((size_t)rope_rows * (hd / 2) * sizeof(float2));
+    L.r = g.take(T * H * 2);
+    L.y = g.take(T * H * 2);
+    L.qkv = g.take(T * Dqkv * 2);
+    L.q = g.take(T * Dq * 2);
+    L.att = g.take(T * Dq * 2);
+    L.h = g.take(T * F * 2);
+    L.rl = g.take((size_t)batch * H * 2);
+    const int m_split = std::min(std::max(rows, batch), 128);
+    size_t part = 0;
+    part = std::max(part, linear_partial_bound(m_split, (int)Dqkv, (int)H, EPI_STORE));
+    part = std::max(part, linear_partial_bound(m_split, (int)H, (int)Dq, EPI_RESIDUAL));
+    part = std::max(part, linear_partial_bound(m_split, (int)F, (int)H, EPI_SWIGLU));
+    part = std::max(part, linear_partial_bound(m_split, (int)H, (int)F, EPI_RESIDUAL));
+    L.part = g.take(part);
+    L.attn_splits = decode_attention_splits(batch, d.n_kv_heads, max_pos);
+    L.apart = g.take(decode_attention_scratch_bytes(batch, d.n_q_heads, d.head_dim, L.attn_splits));
+    L.total = g.off;
+    return L;
+}
+
+struct Ptrs {
+    uint8_t* base;
+    template <typename T>
+    T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return HRA_OK;
+    return HRA_ERR_CUDA;
+}
+
+#define HRA_TRY(expr)                               \
+    do {                                            \
+        cudaError_t e_ = (expr);                    \
+        if (e_ != cudaSuccess) return cuda_status(e_); \
+    } while (0)
+
+cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K, int epi, const Ptrs& P,
+                   const Layout& L, cudaStream_t st) {
+    LinearCall c{};
+    c.a = a;
+    c.w = reinterpret_cast<const bf16*>(w);
+    c.out = out;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.epi = epi;
+    c.split_req = 0;
+    c.partial = P.at<float>(L.part);
+    c.err = P.at<unsigned int>(L.err);
+    return launch_linear(c, st);
+}
+
+bool layer_ptrs_ok(const hra_layer_weights& l) {
+    return aligned16(l.attn_norm) && aligned16(l.w_qkv) && aligned16(l.q_norm) && aligned16(l.k_norm) &&
+           aligned16(l.w_o) && aligned16(l.mlp_norm) && aligned16(l.w_gate_up) && aligned16(l.w_down);
+}
+
+// One full layer (attention block + MLP) over `rows` packed rows; leaves the residual in r.
+// `attn_last_only` switches the tail to the B-row path (prefill's last layer).
+int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
+               int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
+               cudaStream_t st) {
+    const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
+    const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
+    const float eps = d.rms_eps;
+    bf16* r = P.at<bf16>(L.r);
+    bf16* y = P.at<bf16>(L.y);
+    bf16* qkv = P.at<bf16>(L.qkv);
+    bf16* q = P.at<bf16>(L.q);
+    bf16* att = P.at<bf16>(L.att);
+    bf16* h = P.at<bf16>(L.h);
+    bf16* rl = P.at<bf16>(L.rl);
+    const int32_t* row_seq = P.at<int32_t>(L.row_seq);
+    const int32_t* row_pos = P.at<int32_t>(L.row_pos);
+    const int32_t* last_row = P.at<int32_t>(L.last_row);
+    const size_t layer_elems = (size_t)kv.batch * 2 * nkv * (size_t)kv.n_slots * hd;
+
+    for (int l = 0; l < d.n_layers; ++l) {
+        const hra_layer_weights& lw = w.layers[l];
+        bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
+        const bool last = l == d.n_layers - 1;
+        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st));
+        QkRopeArgs qa{};
+        qa.qkv = qkv;
+        qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
+        qa.k_norm = reinterpret_cast<const bf16*>(lw.k_norm);
+        qa.rope = P.at<float2>(L.rope);
+        qa.row_seq = row_seq;
+        qa.row_pos = row_pos;
+        qa.rope_row_is_pos = prefill ? 1 : 0;
+        qa.q_out = q;
+        qa.kv_layer = kvl;
+        qa.n_slots = kv.n_slots;
+        qa.rows = rows;
+        qa.nq = nq;
+        qa.nkv = nkv;
+        qa.hd = hd;
+        qa.eps = eps;
+        HRA_TRY(launch_qk_rope_kv(qa, st));
+
+        const bool tail = prefill && last && !full_last;
+        if (!tail) {
+            if (prefill) {
+                PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), att, batch, max_len, kv.n_slots, nq, nkv, hd};
+                HRA_TRY(launch_prefill_attention(pa, st));
+            } else {
+                DecodeAttnArgs da{};
+                da.q = q;
+                da.kv_layer = kvl;
+                da.q_row = nullptr;
+                da.seq = row_seq;
+                da.pos = row_pos;
+                da.out = att;
+                da.part = P.at<float>(L.apart);
+                da.rows = rows;
+                da.max_pos = kv.n_slots - 1;
+                da.n_slots = kv.n_slots;
+                da.nq = nq;
+                da.nkv = nkv;
+                da.hd = hd;
+                da.splits = L.attn_splits;
+                HRA_TRY(launch_decode_attention(da, st));
+            }
+            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st));
+            HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(lw.mlp_norm), y, nullptr, rows, H, eps, st));
+            HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st));
+            HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st));
+            if (!last) {
+                HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(w.layers[l + 1].attn_norm), y,
+                                       nullptr, rows, H, eps, st));
+            } else {
+                HRA_TRY(launch_rmsnorm(r, prefill ? last_row : nullptr, reinterpret_cast<const bf16*>(w.final_norm),
+                                       out_hidden, nullptr, batch, H, eps, st));
+            }
+        } else {
+            // last prefill layer, rows that feed the last hidden only
+            DecodeAttnArgs da{};
+            da.q = q;
+            da.kv_layer = kvl;
+            da.q_row = last_row;
+            da.seq = row_seq;
+            da.pos = row_pos;
+            da.out = att;
+            da.part = P.at<float>(L.apart);
+            da.rows = batch;
+            da.max_pos = max_len - 1;
+            da.n_slots = kv.n_slots;
+            da.nq = nq;
+            da.nkv = nkv;
+            da.hd = hd;
+            da.splits = std::min(L.attn_splits, decode_attention_splits(batch, nkv, max_len - 1));
+            HRA_TRY(launch_decode_attention(da, st));
+            HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
+            HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st));
+            HRA_TRY(launch_rmsnorm(rl, nullptr, reinterpret_cast<const bf16*>(lw.mlp_norm), y, nullptr, batch, H, eps, st));
+            HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st));
+            HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st));
+            HRA_TRY(launch_rmsnorm(rl, nullptr, reinterpret_cast<const bf16*>(w.final_norm), out_hidden, nullptr,
+                                   batch, H, eps, st));
+        }
+    }
+    return HRA_OK;
+}
+
+bool weights_ok(const hra_dims& d, const hra_weights* w) {
+    if (w == nullptr || w->layers == nullptr || !aligned16(w->final_norm)) return false;
+    for (int l = 0; l < d.n_layers; ++l)
+        if (!layer_ptrs_ok(w->layers[l])) return false;
+    return true;
+}
+
+bool kv_ok(const hra_kv_cache* kv) {
+    return kv != nullptr && aligned16(kv->base) && kv->batch >= 1 && kv->n_slots >= 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hra_prefill_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
+    if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1) return 0;
+    return backbone_layout(*dims, batch, total_tokens, max_len, max_len - 1).total;
+}
+
+int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+    if (dims == nullptr || weights == nullptr || tokens_dev == nullptr || seq_lens == nullptr || kv == nullptr)
+        return HRA_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
+    const hra_dims& d = *dims;
+    if (batch < 1 || batch > kMaxBatch || max_len < 1) return HRA_ERR_INVALID_ARG;
+    if (!aligned16(weights->embed) || !weights_ok(d, weights) || !kv_ok(kv) || !aligned16(last_hidden_dev) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(tokens_dev) & 3u) != 0)
+        return HRA_ERR_INVALID_ARG;
+    if (batch > kv->batch) return HRA_ERR_INVALID_ARG;
+    SeqMeta meta{};
+    meta.batch = batch;
+    meta.mode = 0;
+    long long T = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int n = seq_lens[b];
+        if (n < 1 || n > max_len || n > kv->n_slots) return HRA_ERR_RANGE;
+        meta.vals[b] = (int32_t)T;
+        T += n;
+    }
+    meta.vals[batch] = (int32_t)T;
+    if (T > (1 << 30)) return HRA_ERR_RANGE;
+    const Layout L = backbone_layout(d, batch, (int)T, max_len, max_len - 1);
+    if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
+    HRA_TRY(cudaMemsetAsync(P.at<void>(L.err), 0, 4, st));
+    HRA_TRY(launch_build_rowmap(meta, (int)T, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), st));
+    HRA_TRY(launch_rope_table(max_len, nullptr, d.head_dim, (double)d.rope_theta, P.at<float2>(L.rope), st));
+    HRA_TRY(launch_embed_rmsnorm(tokens_dev, max_len, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
+                                 reinterpret_cast<const bf16*>(weights->embed), d.vocab,
+                                 reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.r),
+                                 P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
+    return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
+                      (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), st);
+}
+
+size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots) {
+    if (!dims_ok(dims) || batch < 1 || n_slots < 1) return 0;
+    return backbone_layout(*dims, batch, batch, batch, n_slots - 1).total;
+}
+
+int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev, const int32_t* pos,
+               int32_t batch, const hra_kv_cache* kv, void* hidden_dev, void* workspace, size_t workspace_bytes,
+               void* stream) {
+    if (dims == nullptr || weights == nullptr || in_emb_dev == nullptr || pos == nullptr || kv == nullptr)
+        return HRA_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
+    const hra_dims& d = *dims;
+    if (batch < 1 || batch > kMaxBatch) return HRA_ERR_INVALID_ARG;
+    if (!weights_ok(d, weights) || !kv_ok(kv) || !aligned16(in_emb_dev) || !aligned16(hidden_dev) ||
+        !aligned16(workspace))
+        return HRA_ERR_INVALID_ARG;
+    if (batch > kv->batch) return HRA_ERR_INVALID_ARG;
+    SeqMeta meta{};
+    meta.batch = batch;
+    meta.mode = 1;
+    for (int b = 0; b < batch; ++b) {
+        if (pos[b] < 0 || pos[b] >= kv->n_slots) return HRA_ERR_RANGE;
+        meta.vals[b] = pos[b];
+    }
+    const Layout L = backbone_layout(d, batch, batch, batch, kv->n_slots - 1);
+    if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
+    HRA_TRY(cudaMemsetAsync(P.at<void>(L.err), 0, 4, st));
+    HRA_TRY(launch_build_rowmap(meta, batch, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), st));
+    HRA_TRY(launch_rope_table(batch, P.at<int32_t>(L.row_pos), d.head_dim, (double)d.rope_theta,
+                              P.at<float2>(L.rope), st));
+    // r = input embedding, y = RMSNorm(r) with layer 0's attention gain
+    HRA_TRY(launch_rmsnorm(reinterpret_cast<const bf16*>(in_emb_dev), nullptr,
+                           reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.y),
+                           P.at<bf16>(L.r), batch, d.hidden, d.rms_eps, st));
+    return run_layers(d, *weights, *kv, P, L, batch, batch, 0, false, false, reinterpret_cast<bf16*>(hidden_dev),
+                      st);
+}
+
+size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch) {
+    if (!audio_dims_ok(dims) || batch < 1) return 0;
+    const int N = dims->n_codebooks * dims->codebook_size;
+    Region g;
+    g.take(256);
+    const size_t plane = (size_t)batch * N * sizeof(float);
+    g.take(std::max(plane, linear_partial_bound(std::min(batch, 128), N, dims->hidden, EPI_F32)));
+    return g.off;
+}
+
+int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev, const void* code_emb_dev,
+                      hra_delay_state* state_dev, const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
+                      void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    if (dims == nullptr || !audio_dims_ok(dims)) return dims == nullptr ? HRA_ERR_INVALID_ARG : HRA_ERR_UNSUPPORTED;
+    if (batch < 1 || batch > 1024) return HRA_ERR_INVALID_ARG;
+    if (!aligned16(hidden_dev) || !aligned16(head_w_dev) || !aligned16(code_emb_dev) || !aligned16(state_dev) ||
+        !aligned16(next_emb_dev) || !aligned16(workspace) || codes_dev == nullptr || done_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(codes_dev) & 3u) || (reinterpret_cast<uintptr_t>(done_dev) & 3u) ||
+        (eoc_bias_dev && (reinterpret_cast<uintptr_t>(eoc_bias_dev) & 3u)) ||
+        (logits_dev && (reinterpret_cast<uintptr_t>(logits_dev) & 3u)))
+        return HRA_ERR_INVALID_ARG;
+    if (workspace_bytes < hra_codebook_workspace_size(dims, batch)) return HRA_ERR_WORKSPACE;
+    const int K = dims->n_codebooks, Vc = dims->codebook_size, H = dims->hidden;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+    unsigned int* err = reinterpret_cast<unsigned int*>(base);
+    float* part = reinterpret_cast<float*>(base + 256);
+    HRA_TRY(cudaMemsetAsync(err, 0, 4, st));
+
+    int splits = 1;
+    LinearCall c{};
+    c.a = reinterpret_cast<const bf16*>(hidden_dev);
+    c.w = reinterpret_cast<const bf16*>(head_w_dev);
+    c.out = part;
+    c.M = batch;
+    c.N = K * Vc;
+    c.K = H;
+    c.epi = EPI_F32;
+    c.split_req = 0;
+    c.partial = part;
+    c.err = err;
+    c.partial_only = true;
+    c.splits_used = &splits;
+    HRA_TRY(launch_linear(c, st));
+
+    CodebookArgs a{};
+    a.partial = part;
+    a.splits = splits;
+    a.eoc_bias = eoc_bias_dev;
+    a.code_emb = reinterpret_cast<const bf16*>(code_emb_dev);
+    a.state = reinterpret_cast<int4*>(state_dev);
+    a.codes = codes_dev;
+    a.next_emb = reinterpret_cast<bf16*>(next_emb_dev);
+    a.done = done_dev;
+    a.logits_out = logits_dev;
+    a.err = err;
+    a.batch = batch;
+    a.K = K;
+    a.Vc = Vc;
+    a.H = H;
+    a.bos = dims->bos_id;
+    a.eoc = dims->eoc_id;
+    HRA_TRY(launch_codebook_finalize(a, st));
+    return HRA_OK;
+}
+
+size_t hra_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue, int32_t split_k) {
+    if (M < 1 || N < 8 || K < 64) return 0;
+    return 256 + align_up(linear_partial_bytes(M, N, K, epilogue, split_k));
+}
+
+int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
+               int32_t epilogue, int32_t split_k, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!aligned16(a_dev) || !aligned16(w_dev) || !aligned16(out_dev) || !aligned16(workspace))
+        return HRA_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || N % 8 != 0 || K < 64 || K % 64 != 0 || split_k < 0) return HRA_ERR_INVALID_ARG;
+    if (epilogue < EPI_STORE || epilogue > EPI_F32) return HRA_ERR_INVALID_ARG;
+    if (workspace_bytes < hra_linear_workspace_size(M, N, K, epilogue, split_k)) return HRA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+    HRA_TRY(cudaMemsetAsync(base, 0, 4, st));
+    LinearCall c{};
+    c.a = reinterpret_cast<const bf16*>(a_dev);
+    c.w = reinterpret_cast<const bf16*>(w_dev);
+    c.out = out_dev;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.epi = epilogue;
+    c.split_req = split_k;
+    c.partial = reinterpret_cast<float*>(base + 256);
+    c.err = reinterpret_cast<unsigned int*>(base);
+    HRA_TRY(launch_linear(c, st));
+    return HRA_OK;
+}
+
+int32_t hra_device_error(const void* workspace, void* stream) {
+    if (workspace == nullptr) return HRA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return HRA_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return HRA_ERR_CUDA;
+    return (int32_t)v;
+}
+
+const char* hra_status_string(int status) {
+    switch (status) {
+        case HRA_OK: return "ok";
+        case HRA_ERR_INVALID_ARG: return "invalid argument (null, misaligned or non-positive size)";
+        case HRA_ERR_UNSUPPORTED: return "unsupported dims";
+        case HRA_ERR_WORKSPACE: return "workspace too small";
+        case HRA_ERR_RANGE: return "sequence length or position outside the cache";
+        case HRA_ERR_CUDA: return "CUDA launch or driver error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

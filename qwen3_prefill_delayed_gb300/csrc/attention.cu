@@ -1,0 +1,392 @@
+// attention.cu -- causal GQA attention over the used keys of the KV cache.
+//
+// Semantics: row i of sequence b (position i) with q head h attends cache slots 0..i of kv head
+// h / (n_q / n_kv) with softmax(q.k / sqrt(hd)); slots past the sequence's length carry zero
+// weight and are never used ("fp8_chain.py", module docstring: attention "over exactly the used
+// keys (pads trail, so a used-key count carries the host's mask)"; causal here because the
+// backbone is a decoder).
+//
+// prefill_attn_kernel  flash-attention style: one CTA = 64 queries x one q head of one sequence,
+//                      4 warps x 16 query rows; K/V tiles of 64 keys double-buffered with cp.async
+//                      into XOR-swizzled shared memory; S = QK^T and O += PV on warp-level
+//                      bf16 MMA (m16n8k16) with fp32 online softmax; P is rounded to bf16 for PV.
+//                      Tiles above the causal diagonal are never loaded.
+// decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
+//                      across CTAs; each warp walks keys with 8-byte coalesced K/V loads, the
+//                      G = n_q / n_kv q heads of a kv head share every load; partial (m, l, o)
+//                      go to scratch and a combine kernel merges the splits.
+#include <math.h>
+
+#include "internal.h"
+
+namespace hra {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ prefill (many queries)
+
+constexpr int PQ = 64;    // queries per CTA
+constexpr int PK = 64;    // keys per tile
+
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    // byte offset of 16-byte chunk `chunk` of row `row` in a [rows][HD] bf16 tile
+    return (uint32_t)(row * HD * 2 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int HD>
+__device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* gbase, long long row_stride, int rows_valid,
+                                          int tid) {
+    constexpr int CH = HD / 8;   // 16-byte chunks per row
+    for (int idx = tid; idx < PK * CH; idx += 128) {
+        const int r = idx / CH, c = idx % CH;
+        const bool ok = r < rows_valid;
+        const bf16* src = gbase + (ok ? (long long)r * row_stride + c * 8 : 0);
+        cp_async16(sbase + swz<HD>(r, c), src, ok ? 16u : 0u);
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs a, float scale_log2) {
+    constexpr int KS = HD / 16;   // k-steps over the head dim
+    constexpr int DN = HD / 8;    // n-tiles of the output
+    extern __shared__ __align__(128) uint8_t sm[];
+    const uint32_t sQ = smem_u32(sm);
+    const uint32_t sK0 = sQ + PQ * HD * 2;
+    const uint32_t sV0 = sK0 + 2 * PK * HD * 2;
+
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int n_qt = (a.max_len + PQ - 1) / PQ;
+    const int qt = n_qt - 1 - (int)blockIdx.x;   // heaviest tiles first
+    const int cu0 = a.cu[b];
+    const int len = a.cu[b + 1] - cu0;
+    const int q0 = qt * PQ;
+    if (q0 >= len) return;
+    const int kvh = h / (a.nq / a.nkv);
+    const int kv_len = min(len, q0 + PQ);
+    const int n_kt = (kv_len + PK - 1) / PK;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long qstride = (long long)a.nq * HD;
+    const bf16* qbase = a.q + (long long)(cu0 + q0) * qstride + (long long)h * HD;
+    const long long hstride = (long long)a.n_slots * HD;
+    const bf16* kbase = a.kv_layer + ((long long)(b * 2) * a.nkv + kvh) * hstride;
+    const bf16* vbase = a.kv_layer + ((long long)(b * 2 + 1) * a.nkv + kvh) * hstride;
+
+    load_tile<HD>(sQ, qbase, qstride, min(PQ, len - q0), tid);
+    load_tile<HD>(sK0, kbase, HD, min(PK, kv_len), tid);
+    load_tile<HD>(sV0, vbase, HD, min(PK, kv_len), tid);
+    cp_async_commit();
+
+    uint32_t qf[KS][4];
+    float o[DN][4];
+#pragma unroll
+    for (int d = 0; d < DN; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    const int g = lane >> 2, tig = lane & 3;
+    const int qa = q0 + warp * 16 + g, qb = qa + 8;   // query positions of this thread's two rows
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < n_kt) {
+            const int j1 = (kt + 1) * PK;
+            load_tile<HD>(sK0 + (buf ^ 1) * PK * HD * 2, kbase + (long long)j1 * HD, HD, min(PK, kv_len - j1), tid);
+            load_tile<HD>(sV0 + (buf ^ 1) * PK * HD * 2, vbase + (long long)j1 * HD, HD, min(PK, kv_len - j1), tid);
+        }
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (kt == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+                ldmatrix_x4(qf[ks], sQ + swz<HD>(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)));
+        }
+        const uint32_t sK = sK0 + buf * PK * HD * 2;
+        const uint32_t sV = sV0 + buf * PK * HD * 2;
+        const int j0 = kt * PK;
+
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t kb[4];
+                ldmatrix_x4(kb, sK + swz<HD>(np * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
+                mma_bf16_16816(s[2 * np], qf[ks], kb[0], kb[1]);
+                mma_bf16_16816(s[2 * np + 1], qf[ks], kb[2], kb[3]);
+            }
+        }
+        // scale, causal + length mask
+        const bool need_mask = (j0 + PK > q0) || (j0 + PK > len);
+        float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int key = j0 + n * 8 + 2 * tig + (c & 1);
+                const int qp = c < 2 ? qa : qb;
+                float v = s[n][c] * scale_log2;
+                if (need_mask && (key > qp || key >= len)) v = -INFINITY;
+                s[n][c] = v;
+            }
+            mx_a = fmaxf(mx_a, fmaxf(s[n][0], s[n][1]));
+            mx_b = fmaxf(mx_b, fmaxf(s[n][2], s[n][3]));
+        }
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float al_a = exp2f(m_a - mn_a), al_b = exp2f(m_b - mn_b);
+        m_a = mn_a;
+        m_b = mn_b;
+        float rs_a = 0.f, rs_b = 0.f;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            s[n][0] = exp2f(s[n][0] - mn_a);
+            s[n][1] = exp2f(s[n][1] - mn_a);
+            s[n][2] = exp2f(s[n][2] - mn_b);
+            s[n][3] = exp2f(s[n][3] - mn_b);
+            rs_a += s[n][0] + s[n][1];
+            rs_b += s[n][2] + s[n][3];
+        }
+        l_a = l_a * al_a + rs_a;
+        l_b = l_b * al_b + rs_b;
+#pragma unroll
+        for (int d = 0; d < DN; ++d) {
+            o[d][0] *= al_a;
+            o[d][1] *= al_a;
+            o[d][2] *= al_b;
+            o[d][3] *= al_b;
+        }
+        // O += P V
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            uint32_t pa[4];
+            pa[0] = pack_bf2(s[2 * t][0], s[2 * t][1]);
+            pa[1] = pack_bf2(s[2 * t][2], s[2 * t][3]);
+            pa[2] = pack_bf2(s[2 * t + 1][0], s[2 * t + 1][1]);
+            pa[3] = pack_bf2(s[2 * t + 1][2], s[2 * t + 1][3]);
+#pragma unroll
+            for (int dp = 0; dp < DN / 2; ++dp) {
+                uint32_t vb[4];
+                ldmatrix_x4_trans(vb, sV + swz<HD>(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dp * 2 + (lane >> 4)));
+                mma_bf16_16816(o[2 * dp], pa, vb[0], vb[1]);
+                mma_bf16_16816(o[2 * dp + 1], pa, vb[2], vb[3]);
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    const float ia = 1.0f / l_a, ib = 1.0f / l_b;
+    bf16* oa = a.out + (long long)(cu0 + qa) * qstride + (long long)h * HD + 2 * tig;
+    bf16* ob = a.out + (long long)(cu0 + qb) * qstride + (long long)h * HD + 2 * tig;
+#pragma unroll
+    for (int d = 0; d < DN; ++d) {
+        if (qa < len)
+            *reinterpret_cast<__nv_bfloat162*>(oa + d * 8) = __floats2bfloat162_rn(o[d][0] * ia, o[d][1] * ia);
+        if (qb < len)
+            *reinterpret_cast<__nv_bfloat162*>(ob + d * 8) = __floats2bfloat162_rn(o[d][2] * ib, o[d][3] * ib);
+    }
+}
+
+// ------------------------------------------------------------------ single-query decode
+
+template <int HD, int G>
+__global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a, float scale_log2) {
+    constexpr int E = HD / 32;
+    const int i = blockIdx.z, j = blockIdx.y, sp = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qr = a.q_row ? a.q_row[i] : i;
+    const int seq = a.seq[qr], pos = a.pos[qr];
+    const int nkeys = pos + 1;
+    const int chunk = (nkeys + a.splits - 1) / a.splits;
+    const int k0 = sp * chunk, k1 = min(nkeys, k0 + chunk);
+
+    float q[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const bf16* qp = a.q + ((long long)qr * a.nq + j * G + g) * HD + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) q[g][e] = bf2f(qp[e]) * scale_log2;
+    }
+    const long long hstride = (long long)a.n_slots * HD;
+    const bf16* kb = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * hstride + lane * E;
+    const bf16* vb = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * hstride + lane * E;
+
+    float m[G], l[G], o[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[g][e] = 0.f;
+    }
+    for (int key = k0 + warp; key < k1; key += 4) {
+        float kf[E], vf[E];
+        if constexpr (E == 4) {
+            const uint2 ku = *reinterpret_cast<const uint2*>(kb + (long long)key * HD);
+            const uint2 vu = *reinterpret_cast<const uint2*>(vb + (long long)key * HD);
+            float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ku.x));
+            float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ku.y));
+            kf[0] = t0.x; kf[1] = t0.y; kf[2] = t1.x; kf[3] = t1.y;
+            t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vu.x));
+            t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vu.y));
+            vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
+        } else {
+            const float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kb + (long long)key * HD));
+            const float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vb + (long long)key * HD));
+            kf[0] = t0.x; kf[1] = t0.y;
+            vf[0] = t1.x; vf[1] = t1.y;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) d += q[g][e] * kf[e];
+            d = warp_sum(d);
+            const float mn = fmaxf(m[g], d);
+            const float al = exp2f(m[g] - mn);
+            const float p = exp2f(d - mn);
+            l[g] = l[g] * al + p;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[g][e] = o[g][e] * al + p * vf[e];
+            m[g] = mn;
+        }
+    }
+    // merge the 4 warps of this CTA
+    __shared__ float s_m[4][G], s_l[4][G];
+    __shared__ float s_o[4][G][HD];
+    if (lane == 0)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            s_m[warp][g] = m[g];
+            s_l[warp][g] = l[g];
+        }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < E; ++e) s_o[warp][g][lane * E + e] = o[g][e];
+    __syncthreads();
+    const int stride = (HD + 2);
+    for (int idx = threadIdx.x; idx < G * HD; idx += 128) {
+        const int g = idx / HD, d = idx % HD;
+        float M = -INFINITY;
+        for (int w = 0; w < 4; ++w) if (s_l[w][g] > 0.f) M = fmaxf(M, s_m[w][g]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY)
+            for (int w = 0; w < 4; ++w)
+                if (s_l[w][g] > 0.f) {
+                    const float f = exp2f(s_m[w][g] - M);
+                    L += s_l[w][g] * f;
+                    O += s_o[w][g][d] * f;
+                }
+        float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + g) * stride;
+        dst[d] = O;
+        if (d == 0) {
+            dst[HD] = M;
+            dst[HD + 1] = L;
+        }
+    }
+}
+
+template <int HD>
+__global__ void decode_combine_kernel(const DecodeAttnArgs a) {
+    const int i = blockIdx.y, h = blockIdx.x;
+    const int stride = HD + 2;
+    for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+        float M = -INFINITY;
+        for (int s = 0; s < a.splits; ++s) {
+            const float* p = a.part + (((long long)s * a.rows + i) * a.nq + h) * stride;
+            if (p[HD + 1] > 0.f) M = fmaxf(M, p[HD]);
+        }
+        float L = 0.f, O = 0.f;
+        for (int s = 0; s < a.splits; ++s) {
+            const float* p = a.part + (((long long)s * a.rows + i) * a.nq + h) * stride;
+            if (p[HD + 1] > 0.f) {
+                const float f = exp2f(p[HD] - M);
+                L += p[HD + 1] * f;
+                O += p[d] * f;
+            }
+        }
+        a.out[((long long)i * a.nq + h) * HD + d] = f2bf(O / L);
+    }
+}
+
+template <int HD>
+cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
+    const int smem = (PQ + 4 * PK) * HD * 2;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(prefill_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    dim3 grid((a.max_len + PQ - 1) / PQ, a.nq, a.batch);
+    const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
+    prefill_attn_kernel<HD><<<grid, 128, smem, st>>>(a, scale_log2);
+    return cudaGetLastError();
+}
+
+template <int HD, int G>
+cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
+    dim3 grid(a.splits, a.nkv, a.rows);
+    const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
+    decode_attn_kernel<HD, G><<<grid, 128, 0, st>>>(a, scale_log2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<HD><<<dim3(a.nq, a.rows), HD, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_decode_g(const DecodeAttnArgs& a, cudaStream_t st) {
+    switch (a.nq / a.nkv) {
+        case 1: return launch_decode_hd<HD, 1>(a, st);
+        case 2: return launch_decode_hd<HD, 2>(a, st);
+        case 4: return launch_decode_hd<HD, 4>(a, st);
+        case 8: return launch_decode_hd<HD, 8>(a, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st) {
+    if (a.hd == 128) return launch_prefill_hd<128>(a, st);
+    if (a.hd == 64) return launch_prefill_hd<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+int decode_attention_splits(int rows, int nkv, int max_pos) {
+    const int target = 2 * device_sm_count();
+    int s = (target + rows * nkv - 1) / (rows * nkv);
+    const int cap = max(1, (max_pos + 1) / 64);
+    s = min(s, cap);
+    s = min(s, 32);
+    return max(s, 1);
+}
+
+size_t decode_attention_scratch_bytes(int rows, int nq, int hd, int splits) {
+    return (size_t)splits * rows * nq * (hd + 2) * sizeof(float);
+}
+
+cudaError_t launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t st) {
+    if (a.hd == 128) return launch_decode_g<128>(a, st);
+    if (a.hd == 64) return launch_decode_g<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hra

@@ -1,0 +1,264 @@
+// elementwise.cu -- bandwidth-bound kernels of the prefill / decode chain.
+//
+//   build_rowmap      packed-row bookkeeping (sequence + position of each row) from the host lengths
+//   rope_table        cos/sin of pos * theta^(-2i/hd), evaluated in double, rounded to fp32
+//   embed_rmsnorm     embedding gather fused with the first RMSNorm ("Stabilize Higgs Audio
+//                     termination and prefill", Summary: embedding lookup)
+//   rmsnorm           RMSNorm of rows (optionally gathered), or a plain row gather
+//   qk_rope_kv        per-head q/k RMSNorm + rotate-half RoPE, q to scratch, K/V into the cache
+//                     (same page: "q/k norm + RoPE, and KV writes"; "fp8_chain.py": keys in host
+//                     rotate-half layout in the cache)
+// One warp per row (or per row x head); 16-byte vector loads; warp-shuffle reductions.
+#include "internal.h"
+
+namespace hra {
+
+namespace {
+
+__global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq, int32_t* row_pos,
+                                    int32_t* cu, int32_t* last_row) {
+    __shared__ int32_t s_vals[kMaxBatch + 1];
+    const int B = meta.batch;
+    const int nvals = meta.mode == 0 ? B + 1 : B;
+    for (int i = threadIdx.x; i < nvals; i += blockDim.x) s_vals[i] = meta.vals[i];
+    __syncthreads();
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (meta.mode == 0) {
+        if (r < T) {
+            int lo = 0, hi = B - 1;   // largest b with cu[b] <= r
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_vals[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            row_seq[r] = lo;
+            row_pos[r] = r - s_vals[lo];
+        }
+        if (blockIdx.x == 0)
+            for (int b = threadIdx.x; b <= B; b += blockDim.x) {
+                cu[b] = s_vals[b];
+                if (b < B) last_row[b] = s_vals[b + 1] - 1;
+            }
+    } else {
+        if (r < T) {
+            row_seq[r] = r;
+            row_pos[r] = s_vals[r];
+        }
+        if (blockIdx.x == 0)
+            for (int b = threadIdx.x; b < B; b += blockDim.x) {
+                cu[b] = b;
+                last_row[b] = b;
+            }
+    }
+}
+
+__global__ void rope_table_kernel(int n_rows, const int32_t* __restrict__ pos_of_row, int hd, double theta,
+                                  float2* __restrict__ table) {
+    const int half = hd / 2;
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_rows * half) return;
+    const int r = idx / half, i = idx % half;
+    const int pos = pos_of_row ? pos_of_row[r] : r;
+    const double inv_freq = pow(theta, -(2.0 * (double)i) / (double)hd);
+    double s, c;
+    sincos((double)pos * inv_freq, &s, &c);
+    table[idx] = make_float2((float)c, (float)s);
+}
+
+__global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok_ld,
+                                     const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_pos,
+                                     const bf16* __restrict__ embed, int vocab, const bf16* __restrict__ g,
+                                     bf16* __restrict__ r, bf16* __restrict__ y, int rows, int H, float eps,
+                                     unsigned int* err) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    int tok = tokens[(long long)row_seq[row] * tok_ld + row_pos[row]];
+    if (tok < 0 || tok >= vocab) {
+        if (lane == 0) raise_error(err, HRA_DEVERR_TOKEN_RANGE);
+        tok = tok < 0 ? 0 : vocab - 1;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(embed + (long long)tok * H);
+    uint4* dr = reinterpret_cast<uint4*>(r + (long long)row * H);
+    uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    const int nc = H >> 3;
+    float ss = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+        const uint4 u = src[c];
+        dr[c] = u;
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+    for (int c = lane; c < nc; c += 32) {
+        float f[8], w[8];
+        unpack8(src[c], f);
+        unpack8(gv[c], w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
+        dy[c] = pack8(f);
+    }
+}
+
+// g == nullptr: plain gather (copy_out must be set).
+__global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ idx,
+                               const bf16* __restrict__ g, bf16* __restrict__ y, bf16* __restrict__ copy_out,
+                               int rows, int H, float eps) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const long long src_row = idx ? idx[row] : row;
+    const uint4* src = reinterpret_cast<const uint4*>(x + src_row * H);
+    const int nc = H >> 3;
+    if (g == nullptr) {
+        uint4* dc = reinterpret_cast<uint4*>(copy_out + (long long)row * H);
+        for (int c = lane; c < nc; c += 32) dc[c] = src[c];
+        return;
+    }
+    float ss = 0.f;
+    for (int c = lane; c < nc; c += 32) {
+        const uint4 u = src[c];
+        if (copy_out) reinterpret_cast<uint4*>(copy_out + (long long)row * H)[c] = u;
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
+    for (int c = lane; c < nc; c += 32) {
+        float f[8], w[8];
+        unpack8(src[c], f);
+        unpack8(gv[c], w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
+        dy[c] = pack8(f);
+    }
+}
+
+// One warp per (row, head) over the nq + 2 nkv heads of the merged QKV row.  Lane l holds head
+// elements [l*E, l*E + E); the RoPE partner of element i < hd/2 is i + hd/2, held by lane l ^ 16.
+template <int HD>
+__global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
+    constexpr int E = HD / 32;
+    constexpr int HALF = HD / 2;
+    const int heads = a.nq + 2 * a.nkv;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)a.rows * heads) return;
+    const int row = (int)(gw / heads), hh = (int)(gw % heads);
+    const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + lane * E;
+    const int seq = a.row_seq[row], pos = a.row_pos[row];
+    const long long head_stride = (long long)a.n_slots * HD;
+
+    float x[E];
+    if constexpr (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+    } else {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src));
+        x[0] = f0.x; x[1] = f0.y;
+    }
+
+    if (hh >= a.nq + a.nkv) {   // V head: copied into the cache as is
+        const int j = hh - a.nq - a.nkv;
+        bf16* dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * head_stride + (long long)pos * HD + lane * E;
+        if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+        else *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+        return;
+    }
+    const bool is_q = hh < a.nq;
+    const bf16* gain = (is_q ? a.q_norm : a.k_norm) + lane * E;
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss += x[e] * x[e];
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+    float xn[E], pn[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) xn[e] = __fmul_rn(__fmul_rn(x[e], inv), bf2f(gain[e]));
+#pragma unroll
+    for (int e = 0; e < E; ++e) pn[e] = __shfl_xor_sync(0xffffffffu, xn[e], 16);
+    const int trow = a.rope_row_is_pos ? pos : row;
+    const float2* cs = a.rope + (long long)trow * HALF;
+    float out[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = (lane * E + e) % HALF;
+        const float2 c = cs[i];   // (cos, sin)
+        if (lane < 16)   // first half: a*cos - b*sin with a = own, b = partner
+            out[e] = __fsub_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
+        else             // second half: b*cos + a*sin with b = own, a = partner
+            out[e] = __fadd_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
+    }
+    bf16* dst;
+    if (is_q) {
+        dst = a.q_out + ((long long)row * a.nq + hh) * HD + lane * E;
+    } else {
+        const int j = hh - a.nq;
+        dst = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * head_stride + (long long)pos * HD + lane * E;
+    }
+    if constexpr (E == 4) {
+        uint2 u;
+        *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(out[0], out[1]);
+        *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(out[2], out[3]);
+        *reinterpret_cast<uint2*>(dst) = u;
+    } else {
+        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(out[0], out[1]);
+    }
+}
+
+inline unsigned blocks_for(long long threads, int per_block) {
+    return (unsigned)((threads + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
+                                int32_t* cu, int32_t* last_row, cudaStream_t st) {
+    const int threads = 256;
+    const unsigned blocks = blocks_for(total_rows > 0 ? total_rows : 1, threads);
+    build_rowmap_kernel<<<blocks, threads, 0, st>>>(meta, total_rows, row_seq, row_pos, cu, last_row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
+                              float2* table, cudaStream_t st) {
+    const long long n = (long long)n_rows * (head_dim / 2);
+    rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(n_rows, pos_of_row, head_dim, theta, table);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_t* row_seq,
+                                 const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
+                                 bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
+                                 cudaStream_t st) {
+    embed_rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(
+        tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf16* y, bf16* copy_out,
+                           int rows, int H, float eps, cudaStream_t st) {
+    rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(x, idx, g, y, copy_out, rows, H,
+                                                                        eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st) {
+    const long long warps = (long long)a.rows * (a.nq + 2 * a.nkv);
+    const unsigned blocks = blocks_for(warps * 32, 256);
+    if (a.hd == 128) qk_rope_kv_kernel<128><<<blocks, 256, 0, st>>>(a);
+    else if (a.hd == 64) qk_rope_kv_kernel<64><<<blocks, 256, 0, st>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace hra

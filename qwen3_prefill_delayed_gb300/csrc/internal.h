@@ -1,0 +1,128 @@
+// internal.h -- host-side declarations shared by the translation units of the hra library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace hra {
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+// ------------------------------------------------------------------ projection GEMM
+enum EpiMode : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
+
+// out = epilogue(a [M, K] . w^T); w has N rows (2N for EPI_SWIGLU, gate rows then up rows).
+// split_req: 0 = automatic, >= 1 forces that many K splits (only when M <= 128).
+struct LinearCall {
+    const bf16* a;
+    const bf16* w;
+    void* out;
+    int M, N, K;
+    int epi;
+    int split_req;
+    float* partial;        // fp32 scratch for split partials (>= linear_partial_bytes())
+    unsigned int* err;     // sticky device error word
+    bool partial_only;     // leave the split partials unreduced (EPI_F32 only; out == partial)
+    int* splits_used;      // optional: receives the number of K splits launched
+};
+size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req);
+cudaError_t launch_linear(const LinearCall& c, cudaStream_t st);
+// Largest partial buffer any automatic plan with M <= m_max rows and these N, K can ask for.
+size_t linear_partial_bound(int m_max, int N, int K, int epi);
+
+// ------------------------------------------------------------------ row bookkeeping + norms + RoPE
+constexpr int kMaxBatch = 512;
+
+// Host-built batch description passed by value to the row-map kernel.
+struct SeqMeta {
+    int32_t batch;
+    int32_t mode;           // 0: prefill (vals = cu_seqlens[0..batch]); 1: decode (vals = pos[0..batch))
+    int32_t vals[kMaxBatch + 1];
+};
+
+// Writes row_seq[T], row_pos[T] (sequence index and position of each packed row), and for prefill
+// cu[batch+1], last_row[batch]; for decode last_row[b] = b.
+cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
+                                int32_t* cu, int32_t* last_row, cudaStream_t st);
+
+// cos/sin table [n_rows][head_dim/2] (float2), row r at position pos_of_row[r] (or r when null).
+cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
+                              float2* table, cudaStream_t st);
+
+// r[row] = embed[tokens[row_seq*ld + row_pos]]; y = RMSNorm(r) * g.
+cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_t* row_seq,
+                                 const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
+                                 bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
+                                 cudaStream_t st);
+
+// y[i] = RMSNorm(x[idx ? idx[i] : i]) * g; when copy_out != null also copy_out[i] = x[idx[i]].
+cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf16* y, bf16* copy_out,
+                           int rows, int H, float eps, cudaStream_t st);
+
+// Per packed row: q heads and k heads get RMSNorm over head_dim (shared gains) + rotate-half RoPE
+// (table row = rope_row_is_pos ? row_pos[row] : row); q goes to q_out [rows, nq, hd]; k and v go to
+// cache slot row_pos[row] of cache sequence row_seq[row] of this layer.
+struct QkRopeArgs {
+    const bf16* qkv;
+    const bf16* q_norm;
+    const bf16* k_norm;
+    const float2* rope;
+    const int32_t* row_seq;
+    const int32_t* row_pos;
+    int rope_row_is_pos;
+    bf16* q_out;
+    bf16* kv_layer;     // this layer's cache block: [cache_batch][2][nkv][n_slots][hd]
+    int n_slots;
+    int rows, nq, nkv, hd;
+    float eps;
+};
+cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ attention
+// Causal prefill attention over the cache for every packed row.
+struct PrefillAttnArgs {
+    const bf16* q;          // [T, nq, hd]
+    const bf16* kv_layer;   // [cache_batch][2][nkv][n_slots][hd]
+    const int32_t* cu;      // [batch + 1] device
+    bf16* out;              // [T, nq * hd]
+    int batch, max_len, n_slots, nq, nkv, hd;
+};
+cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st);
+
+// Single-query attention: row i (sequence seq[i], query position pos[i]) attends slots 0..pos[i].
+struct DecodeAttnArgs {
+    const bf16* q;          // q rows [*, nq, hd]
+    const bf16* kv_layer;
+    const int32_t* q_row;   // [rows] q row of attention row i (null: i)
+    const int32_t* seq;     // cache sequence, indexed by q row
+    const int32_t* pos;     // query position, indexed by q row
+    bf16* out;              // [rows, nq * hd]
+    float* part;            // scratch: splits * rows * nq * (hd + 2) floats
+    int rows, max_pos, n_slots, nq, nkv, hd;
+    int splits;
+};
+int decode_attention_splits(int rows, int nkv, int max_pos);
+size_t decode_attention_scratch_bytes(int rows, int nq, int hd, int splits);
+cudaError_t launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ codebook step finalize
+struct CodebookArgs {
+    const float* partial;   // [splits][batch][K * Vc] fp32 logits partials
+    int splits;
+    const float* eoc_bias;  // [batch, K] or null
+    const bf16* code_emb;   // [K][Vc][H]
+    int4* state;            // hra_delay_state [batch]
+    int32_t* codes;         // [batch, K]
+    bf16* next_emb;         // [batch, H]
+    int32_t* done;          // [batch]
+    float* logits_out;      // [batch, K, Vc] or null
+    unsigned int* err;
+    int batch, K, Vc, H, bos, eoc;
+};
+cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st);
+
+}  // namespace hra

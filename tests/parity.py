@@ -1,0 +1,40 @@
+"""Comparison helpers shared by the GPU parity tests (no arithmetic of the method)."""
+import numpy as np
+import torch
+
+import oracle
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    """GPU/CPU tensor -> float64 numpy (bf16 values are exact)."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def ref_np(u16) -> np.ndarray:
+    return oracle.bf16_value(u16).astype(np.float64)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significand bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def cosine(a: np.ndarray, b: np.ndarray) -> float:
+    a, b = a.ravel(), b.ravel()
+    return float(np.dot(a, b) / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, max_abs: float, min_cos: float, what: str):
+    """The hidden-state / KV tolerance of the path: max |err| <= max_abs and cosine >= min_cos."""
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    cos = cosine(got, ref) if got.size else 1.0
+    assert err <= max_abs and cos >= min_cos, f"{what}: max|err| {err:.4g} (<= {max_abs}), cos {cos:.7f} (>= {min_cos})"
+    return err, cos
+
+
+HIDDEN_TOL = dict(max_abs=2e-2, min_cos=0.9999)   # hidden states and KV values
+LOGIT_TOL = 5e-2                                   # logits, max |err|
+ARGMAX_MARGIN = 0.1                                # argmax must agree above this top-1/top-2 margin

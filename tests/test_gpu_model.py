@@ -1,0 +1,163 @@
+"""GPU parity of hra_prefill / hra_decode / hra_codebook_step against the oracle on the tiny 2-layer
+model (whole outputs) and on the full-width single layer at P = 6 and P = 13."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity import ARGMAX_MARGIN, HIDDEN_TOL, LOGIT_TOL, assert_close, ref_np, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def hra():
+    import qwen3_prefill_delayed_gb300 as h
+    h.lib()
+    return h
+
+
+def _to_dev(w):
+    return {"embed": w["embed"].to(DEV), "final_norm": w["final_norm"].to(DEV),
+            "layers": [{k: v.to(DEV) for k, v in l.items()} for l in w["layers"]]}
+
+
+@pytest.fixture(scope="module")
+def tiny(hra):
+    wl = W.tiny_reference("cpu")
+    d = wl["dims"]
+    wl["bb"] = hra.Backbone(d, _to_dev(wl["weights"]))
+    wl["head"] = hra.AudioHead(d, wl["audio"]["head_w"].to(DEV), wl["audio"]["code_emb"].to(DEV))
+    wl["hw"] = oracle.host_weights_from(d, wl["weights"])
+    return wl
+
+
+def _check_kv(cache_gpu, kv_ref, lens, what):
+    g = cache_gpu.float().cpu().numpy()
+    for b, n in enumerate(lens):
+        assert_close(g[:, b, :, :, :n].astype(np.float64), ref_np(kv_ref[:, b, :, :, :n]), what=f"{what} seq {b}",
+                     **HIDDEN_TOL)
+        assert np.all(np.isnan(g[:, b, :, :, n:])), f"{what} seq {b}: slots past the length were written"
+
+
+@pytest.mark.parametrize("full_last", [False, True])
+def test_tiny_ragged_prefill(hra, tiny, full_last):
+    d, bb = tiny["dims"], tiny["bb"]
+    lens = [13, 5, 9, 1]
+    pr = W.make_prompts(11, len(lens), 1, 13, d.vocab)
+    tok = pr.tokens.clone()
+    tok[:, :] = d.vocab + 7                           # pads hold out-of-range ids: must never be read
+    for b, n in enumerate(lens):
+        tok[b, :n] = pr.tokens[b, :n] % d.vocab
+    cache = hra.new_kv_cache(d, len(lens), 32, DEV, fill=float("nan"))
+    hid = bb.prefill(tok.to(DEV), lens, cache, full_last_layer=full_last)
+    assert hra.hra_device_error(bb.last_ws) == 0
+    kv_o, hid_o = oracle.prefill(d, tiny["hw"], tok.numpy(), lens, 32)
+    assert_close(to_np(hid), ref_np(hid_o), what="last hidden", **HIDDEN_TOL)
+    _check_kv(cache, kv_o, lens, "kv")
+
+
+def test_token_out_of_range_sets_error_bit(hra, tiny):
+    d, bb = tiny["dims"], tiny["bb"]
+    tok = torch.tensor([[1, 2, d.vocab + 5, 3]], dtype=torch.int32, device=DEV)
+    cache = hra.new_kv_cache(d, 1, 8, DEV, fill=0.0)
+    bb.prefill(tok, [4], cache)
+    assert hra.hra_device_error(bb.last_ws) & hra.DEVERR_TOKEN_RANGE
+
+
+def test_bad_arguments_rejected_before_launch(hra, tiny):
+    d, bb = tiny["dims"], tiny["bb"]
+    tok = torch.zeros(1, 4, dtype=torch.int32, device=DEV)
+    cache = hra.new_kv_cache(d, 1, 8, DEV, fill=0.0)
+    with pytest.raises(hra.HraError, match="outside the cache"):
+        bb.prefill(tok, [9], cache)                   # longer than max_len / n_slots
+    with pytest.raises(hra.HraError, match="workspace"):
+        bb.prefill(tok, [4], cache, workspace=torch.empty(64, dtype=torch.uint8, device=DEV))
+
+
+def _argmax_agrees(gpu_codes, ref_codes, ref_logits, forced_mask):
+    """Codes must agree wherever the oracle's top-1/top-2 margin exceeds the threshold."""
+    B, K = ref_codes.shape
+    for b in range(B):
+        for k in range(K):
+            if forced_mask[b, k] or gpu_codes[b, k] == ref_codes[b, k]:
+                continue
+            top = np.sort(ref_logits[b, k])[-2:]
+            assert top[1] - top[0] <= ARGMAX_MARGIN, f"argmax differs at row {b} cb {k} with margin {top[1]-top[0]}"
+
+
+def test_tiny_ar_loop(hra, tiny):
+    """Prefill, then 6 frames of codebook step + decode pass; EOC bias on codebook 0 at frame 2."""
+    d, bb, head, p = tiny["dims"], tiny["bb"], tiny["head"], tiny["prompts"]
+    n_slots = tiny["n_slots"]
+    cache = hra.new_kv_cache(d, 1, n_slots, DEV, fill=float("nan"))
+    hid = bb.prefill(p.tokens.to(DEV), p.lengths, cache)
+    kv_o, hid_o = oracle.prefill(d, tiny["hw"], p.tokens.numpy(), p.lengths, n_slots)
+    head_u, tab_u = W.to_u16(tiny["audio"]["head_w"]), W.to_u16(tiny["audio"]["code_emb"])
+    state = torch.tensor([[0, -1, 0, 0]], dtype=torch.int32, device=DEV)
+    st_o = np.array([[0, -1, 0, 0]], np.int32)
+    K = d.n_codebooks
+    logits = torch.empty(1, K, d.codebook_size, dtype=torch.float32, device=DEV)
+    for t in range(tiny["frames"]):
+        bias = tiny["eoc_bias"][t]
+        st_before = state.cpu().numpy().copy()
+        codes, nxt, done = head.step(hid, state, eoc_bias=bias.to(DEV), logits=logits)
+        assert hra.hra_device_error(head.last_ws) == 0
+        c_o, n_o, d_o, lg_o = oracle.codebook_step(d, hid_o, head_u, tab_u, st_o, bias.numpy())
+        lg = logits.cpu().numpy()
+        assert np.max(np.abs(lg - lg_o)) <= LOGIT_TOL
+        # state machine bit-exact on the GPU's own logits
+        st_chk = st_before.copy()
+        c_chk, d_chk = oracle.delay_step(K, d.codebook_size, d.bos_id, d.eoc_id, lg, bias.numpy(), st_chk)
+        assert codes.cpu().numpy().tolist() == c_chk.tolist()
+        assert state.cpu().numpy().tolist() == st_chk.tolist() and done.cpu().numpy().tolist() == d_chk.tolist()
+        assert codes.cpu().numpy().tolist() == c_o.tolist(), f"frame {t}"
+        assert done.item() == int(t == 5) and state[0, 1].item() == (2 if t >= 2 else -1)
+        np.testing.assert_array_equal(W.to_u16(nxt.cpu()), n_o)
+        pos = p.lengths[0] + t
+        hid = bb.decode(nxt, [pos], cache)
+        hid_o = oracle.decode(d, tiny["hw"], n_o, [pos], kv_o, n_slots)
+        assert_close(to_np(hid), ref_np(hid_o), what=f"decode hidden frame {t}", **HIDDEN_TOL)
+    n = p.lengths[0] + tiny["frames"]
+    _check_kv(cache, kv_o, [n], "kv after decode")
+
+
+@pytest.fixture(scope="module")
+def single(hra):
+    wl = W.single_layer(13, "cpu")
+    d = wl["dims"]
+    wl["bb"] = hra.Backbone(d, _to_dev(wl["weights"]))
+    wl["hw"] = oracle.host_weights_from(d, wl["weights"])
+    return wl
+
+
+@pytest.mark.parametrize("P", [6, 13])
+@pytest.mark.parametrize("full_last", [False, True])
+def test_single_layer_prefill(hra, single, P, full_last):
+    d, bb = single["dims"], single["bb"]
+    pr = W.make_prompts(1, 1, P, P, d.vocab, fixed_len=P)
+    cache = hra.new_kv_cache(d, 1, 2048, DEV, fill=float("nan"))
+    hid = bb.prefill(pr.tokens.to(DEV), pr.lengths, cache, full_last_layer=full_last)
+    assert hra.hra_device_error(bb.last_ws) == 0
+    kv_o, hid_o = oracle.prefill(d, single["hw"], pr.tokens.numpy(), pr.lengths, 2048)
+    assert_close(to_np(hid), ref_np(hid_o), what="last hidden", **HIDDEN_TOL)
+    _check_kv(cache, kv_o, [P], "kv")
+
+
+def test_single_layer_decode(hra, single):
+    """Prefill 13, then 3 decode passes at batch 2 fed random embeddings."""
+    d, bb = single["dims"], single["bb"]
+    pr = W.make_prompts(5, 2, 13, 13, d.vocab, fixed_len=13)
+    cache = hra.new_kv_cache(d, 2, 64, DEV, fill=float("nan"))
+    bb.prefill(pr.tokens.to(DEV), pr.lengths, cache)
+    kv_o, _ = oracle.prefill(d, single["hw"], pr.tokens.numpy(), pr.lengths, 64)
+    g = torch.Generator().manual_seed(3)
+    for s in range(3):
+        emb = (torch.randn(2, d.hidden, generator=g) * 0.5).to(torch.bfloat16)
+        pos = [13 + s, 13 + s]
+        hid = bb.decode(emb.to(DEV), pos, cache)
+        hid_o = oracle.decode(d, single["hw"], W.to_u16(emb), pos, kv_o, 64)
+        assert_close(to_np(hid), ref_np(hid_o), what=f"decode {s}", **HIDDEN_TOL)
+    _check_kv(cache, kv_o, [16, 16], "kv")
