@@ -109,7 +109,7 @@ size_t hra_prefill_workspace_size(const hra_dims* dims, int32_t batch, int32_t t
 /* Batched prefill of `batch` ragged prompts.
  *   tokens_dev   int32 [batch, max_len] device; prompt b is tokens[b, 0 : seq_lens[b]]; the rest
  *                are pads and are never read.
- *   seq_lens     int32 [batch] HOST; each in [1, min(max_len, kv->n_slots)].  batch <= 1024 and
+ *   seq_lens     int32 [batch] HOST; each in [1, min(max_len, kv->n_slots)].  batch <= 512 and
  *                batch <= kv->batch.
  *   kv           cache; slots [0, seq_lens[b]) of sequence b are written in every layer.
  *   last_hidden_dev bf16 [batch, hidden]: final RMSNorm output at position seq_lens[b] - 1.
@@ -123,7 +123,7 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
 /* ---- decode pass ---------------------------------------------------------------------------- */
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots);
 
-/* One single-token pass through every layer for `batch` rows.
+/* One single-token pass through every layer for `batch` rows (batch <= 512).
  *   in_emb_dev  bf16 [batch, hidden]: the input embedding of each row (e.g. the summed codebook
  *               embedding from hra_codebook_step).
  *   pos         int32 [batch] HOST: the position of each row's token, in [0, kv->n_slots); the pass
@@ -172,6 +172,27 @@ size_t hra_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilog
 int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
                int32_t epilogue, int32_t split_k, void* workspace, size_t workspace_bytes,
                void* stream);
+
+/* ---- measurement ---------------------------------------------------------------------------- */
+/* Number of kernels the library has launched in this process (host-side count). */
+uint64_t hra_launch_counter(void);
+
+/* Kernel classes the event probe can bracket. */
+#define HRA_PROBE_NONE 0
+#define HRA_PROBE_QKV 1        /* QKV projection of full prefill layers                         */
+#define HRA_PROBE_O_PROJ 2     /* o-projection of full prefill layers                           */
+#define HRA_PROBE_GATE_UP 3    /* gate/up + SwiGLU projection of full prefill layers            */
+#define HRA_PROBE_DOWN 4       /* down projection of full prefill layers                        */
+#define HRA_PROBE_ATTENTION 5  /* causal prefill attention of full layers                       */
+#define HRA_PROBE_AUDIO_HEAD 6 /* audio-head projection of hra_codebook_step                    */
+
+/* While a class is selected, every launch of that class is bracketed by a CUDA event pair
+ * recorded on the launching stream (events are created on first use; do not select a class while
+ * a stream is being captured).  hra_probe_collect synchronises those events, returns the summed
+ * elapsed milliseconds, the number of launches and their summed algorithmic FLOPs, and clears
+ * them.  Returns HRA_OK or HRA_ERR_CUDA. */
+int hra_probe_select(int kernel_class);
+int hra_probe_collect(double* total_ms, int64_t* launches, double* total_flops);
 
 /* ---- errors --------------------------------------------------------------------------------- */
 /* Synchronise `stream` and return the sticky HRA_DEVERR_* bits of the last call that used this

@@ -81,6 +81,7 @@ def lib():
         for f in ("oracle_prefill", "oracle_decode", "oracle_codebook_step", "oracle_max_threads"):
             getattr(L, f).restype = ctypes.c_int
         L.oracle_set_threads.argtypes = [ctypes.c_int]
+        L.oracle_set_sum_order.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
 
@@ -95,6 +96,21 @@ def max_threads() -> int:
 
 def set_threads(n: int) -> None:
     lib().oracle_set_threads(int(n))
+
+
+class sum_order:
+    """Context manager: evaluate every linear dot product in descending k order inside the block."""
+
+    def __init__(self, descending: bool = True):
+        self.descending = descending
+
+    def __enter__(self):
+        lib().oracle_set_sum_order(1 if self.descending else 0)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_sum_order(0)
+        return False
 
 
 # ------------------------------------------------------------------ element-wise helpers

@@ -25,7 +25,8 @@
  * ascending index order; compiled with -ffp-contract=off so x86 and Arm builds agree bit for bit.
  *
  * Readings where the pages are silent (stated once here, used throughout):
- *   - RMSNorm: y = bf16((x * (1/sqrt(mean(x^2) + eps))) * g), one rounding;
+ *   - RMSNorm: y = bf16((x * (1/sqrt(ss/n + eps))) * g), one rounding, with ss the correctly
+ *     rounded fp32 sum of squares (so the result does not hinge on a reduction order);
  *   - q/k norm gains are shared across heads ([head_dim]); GQA maps q head h to kv head
  *     h / (n_q / n_kv); attention scale 1/sqrt(head_dim); no biases;
  *   - RoPE pairs (i, i + hd/2), inv_freq_i = theta^(-2i/hd), positions restart at 0 in each
@@ -91,15 +92,24 @@ void oracle_set_threads(int n) {
 
 /* ---------------------------------------------------------------- RMSNorm */
 
-/* y[r] = bf16((x[r] * (1/sqrt(mean(x[r]^2) + eps))) * g), per row of n.
+/* y[r] = bf16((x[r] * (1/sqrt(ss/n + eps))) * g), ss = sum_squares(x[r]), per row of n.
  * Source: RMSNorm before each projection and the final norm ("fp8_chain.py", run(): the final
  * hidden is fin * rsqrt(mean(fin^2) + eps) * final_w). */
+/* Sum of squares of n bf16 values as the fp32 rounding of the exact sum: each square of a bf16
+ * value is exact in double and the double sum carries ~2^-53 relative error, so the result does not
+ * depend on any summation order (the CUDA path reaches the same fp32 value by compensated
+ * summation).  This is the "mean(x^2)" of RMSNorm evaluated once, correctly rounded. */
+static float sum_squares(const uint16_t* x, int n) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += (double)bf(x[i]) * (double)bf(x[i]);
+    return (float)s;
+}
+
 void oracle_rmsnorm(const uint16_t* x, const uint16_t* g, int64_t rows, int n, float eps,
                     uint16_t* y) {
     for (int64_t r = 0; r < rows; ++r) {
         const uint16_t* xr = x + r * (int64_t)n;
-        float ss = 0.0f;
-        for (int i = 0; i < n; ++i) ss += bf(xr[i]) * bf(xr[i]);
+        float ss = sum_squares(xr, n);
         float inv = 1.0f / sqrtf(ss / (float)n + eps);
         for (int i = 0; i < n; ++i) y[r * (int64_t)n + i] = to_bf((bf(xr[i]) * inv) * bf(g[i]));
     }
@@ -108,31 +118,39 @@ void oracle_rmsnorm(const uint16_t* x, const uint16_t* g, int64_t rows, int n, f
 /* ---------------------------------------------------------------- linear */
 
 /* y[t][j] = sum_k x[t][k] * w[j][k] in fp32, k ascending; w row-major [N][K] (out, in).
- * The weight is transposed to fp32 once so the inner loop runs over j; each y[t][j] still sums
- * its K products in ascending k order. */
+ * Each output is one plain sequential dot product (ascending k unless oracle_set_sum_order(1)).  The loop runs over output features j on the
+ * outside and tokens t inside, so a weight row is read once per call whatever T is. */
+static int g_sum_descending = 0;
+
+/* Summation order of every linear dot product: ascending k (default) or descending k.  Both are
+ * plain evaluations of the same definition; running the oracle both ways measures how far two
+ * correct bf16 evaluations of this model drift apart (the comparison floor of any other
+ * implementation, whose fp32 sums take yet another order). */
+void oracle_set_sum_order(int descending) { g_sum_descending = descending != 0; }
+
 void oracle_linear(const uint16_t* x, const uint16_t* w, int T, int N, int K, float* y) {
-    float* wt = (float*)malloc(sizeof(float) * (size_t)K * (size_t)N);
-    #pragma omp parallel for schedule(static)
-    for (int j = 0; j < N; ++j)
-        for (int k = 0; k < K; ++k) wt[(size_t)k * N + j] = bf(w[(size_t)j * K + k]);
-    const int JB = 256;
-    int nblk = (N + JB - 1) / JB;
-    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
-    for (int t = 0; t < T; ++t) {
-        for (int jb = 0; jb < nblk; ++jb) {
-            int j0 = jb * JB, j1 = j0 + JB < N ? j0 + JB : N;
-            float acc[256];
-            for (int j = j0; j < j1; ++j) acc[j - j0] = 0.0f;
-            const uint16_t* xt = x + (size_t)t * K;
-            for (int k = 0; k < K; ++k) {
-                float xv = bf(xt[k]);
-                const float* wk = wt + (size_t)k * N;
-                for (int j = j0; j < j1; ++j) acc[j - j0] += xv * wk[j];
+    const int desc = g_sum_descending;
+    float* xf = (float*)malloc(sizeof(float) * (size_t)T * (size_t)K);
+    for (size_t i = 0; i < (size_t)T * (size_t)K; ++i) xf[i] = bf(x[i]);
+    #pragma omp parallel
+    {
+        float* wrow = (float*)malloc(sizeof(float) * (size_t)K);
+        #pragma omp for schedule(static)
+        for (int j = 0; j < N; ++j) {
+            for (int k = 0; k < K; ++k) wrow[k] = bf(w[(size_t)j * K + k]);
+            for (int t = 0; t < T; ++t) {
+                const float* xt = xf + (size_t)t * K;
+                float acc = 0.0f;
+                if (!desc)
+                    for (int k = 0; k < K; ++k) acc += xt[k] * wrow[k];
+                else
+                    for (int k = K - 1; k >= 0; --k) acc += xt[k] * wrow[k];
+                y[(size_t)t * N + j] = acc;
             }
-            for (int j = j0; j < j1; ++j) y[(size_t)t * N + j] = acc[j - j0];
         }
+        free(wrow);
     }
-    free(wt);
+    free(xf);
 }
 
 /* ---------------------------------------------------------------- RoPE */
@@ -156,8 +174,7 @@ void oracle_rope_table(int n_pos, int hd, double theta, float* cos_t, float* sin
 static void head_norm_rope(const uint16_t* x, const uint16_t* g, int hd, float eps,
                            const float* cos_p, const float* sin_p, uint16_t* out) {
     float xn[256];
-    float ss = 0.0f;
-    for (int i = 0; i < hd; ++i) ss += bf(x[i]) * bf(x[i]);
+    float ss = sum_squares(x, hd);
     float inv = 1.0f / sqrtf(ss / (float)hd + eps);
     for (int i = 0; i < hd; ++i) xn[i] = (bf(x[i]) * inv) * bf(g[i]);
     int half = hd / 2;

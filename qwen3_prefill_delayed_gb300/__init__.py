@@ -30,7 +30,9 @@ PREFILL_FULL_LAST_LAYER = 1
 
 EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_decode_workspace_size", "hra_decode",
             "hra_codebook_workspace_size", "hra_codebook_step", "hra_linear_workspace_size",
-            "hra_linear", "hra_device_error", "hra_status_string"]
+            "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
+            "hra_device_error", "hra_status_string"]
+PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6}
 
 
 class HraError(RuntimeError):
@@ -91,6 +93,13 @@ def lib() -> ctypes.CDLL:
         L.hra_linear_workspace_size.restype = sz
         L.hra_linear.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
         L.hra_linear.restype = ctypes.c_int
+        L.hra_launch_counter.argtypes = []
+        L.hra_launch_counter.restype = ctypes.c_uint64
+        L.hra_probe_select.argtypes = [ctypes.c_int]
+        L.hra_probe_select.restype = ctypes.c_int
+        L.hra_probe_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_double)]
+        L.hra_probe_collect.restype = ctypes.c_int
         L.hra_device_error.argtypes = [vp, vp]
         L.hra_device_error.restype = i32
         L.hra_status_string.argtypes = [ctypes.c_int]
@@ -289,3 +298,20 @@ def hra_linear(a: torch.Tensor, w: torch.Tensor, epilogue: int = EPI_STORE,
 def hra_device_error(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise and return the sticky device error bits of the last call on this workspace."""
     return int(lib().hra_device_error(_ptr(workspace, None, "workspace"), _stream(stream)))
+
+
+def hra_launch_counter() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().hra_launch_counter())
+
+
+def hra_probe_select(kernel_class: str) -> None:
+    """Bracket every launch of one kernel class with CUDA events (see PROBE for the names)."""
+    _check(lib().hra_probe_select(PROBE[kernel_class]), "hra_probe_select")
+
+
+def hra_probe_collect():
+    """(summed milliseconds, launches, summed algorithmic FLOPs) of the probed launches; clears them."""
+    ms, n, fl = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double()
+    _check(lib().hra_probe_collect(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl)), "hra_probe_collect")
+    return ms.value, n.value, fl.value

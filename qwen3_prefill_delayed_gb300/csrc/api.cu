@@ -15,6 +15,8 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -22,6 +24,37 @@
 using namespace hra;
 
 namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// Event probe: brackets launches of one kernel class with CUDA event pairs (see hra.h).
+struct Probe {
+    std::mutex mu;
+    int active = HRA_PROBE_NONE;
+    std::vector<cudaEvent_t> pool;                 // 2 events per slot
+    std::vector<std::pair<size_t, double>> used;   // (slot, flops)
+} g_probe;
+
+template <typename F>
+cudaError_t probed(int cls, double flops, cudaStream_t st, F&& launch) {
+    if (cls == HRA_PROBE_NONE || g_probe.active != cls) return launch();
+    std::lock_guard<std::mutex> lk(g_probe.mu);
+    const size_t slot = g_probe.used.size();
+    while (g_probe.pool.size() < 2 * (slot + 1)) {
+        cudaEvent_t e;
+        cudaError_t err = cudaEventCreate(&e);
+        if (err != cudaSuccess) return err;
+        g_probe.pool.push_back(e);
+    }
+    cudaError_t err = cudaEventRecord(g_probe.pool[2 * slot], st);
+    if (err != cudaSuccess) return err;
+    err = launch();
+    if (err != cudaSuccess) return err;
+    err = cudaEventRecord(g_probe.pool[2 * slot + 1], st);
+    if (err != cudaSuccess) return err;
+    g_probe.used.emplace_back(slot, flops);
+    return cudaSuccess;
+}
 
 constexpr size_t kAlign = 256;
 
@@ -118,7 +151,7 @@ int cuda_status(cudaError_t e) {
     } while (0)
 
 cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K, int epi, const Ptrs& P,
-                   const Layout& L, cudaStream_t st) {
+                   const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE) {
     LinearCall c{};
     c.a = a;
     c.w = reinterpret_cast<const bf16*>(w);
@@ -130,7 +163,8 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
     c.split_req = 0;
     c.partial = P.at<float>(L.part);
     c.err = P.at<unsigned int>(L.err);
-    return launch_linear(c, st);
+    const double flops = 2.0 * M * (double)K * (epi == EPI_SWIGLU ? 2.0 * N : (double)N);
+    return probed(probe_class, flops, st, [&] { return launch_linear(c, st); });
 }
 
 bool layer_ptrs_ok(const hra_layer_weights& l) {
@@ -142,7 +176,7 @@ bool layer_ptrs_ok(const hra_layer_weights& l) {
 // `attn_last_only` switches the tail to the B-row path (prefill's last layer).
 int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
                int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
-               cudaStream_t st) {
+               const int32_t* seq_lens_host, cudaStream_t st) {
     const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d.rms_eps;
@@ -157,12 +191,19 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
     const int32_t* row_pos = P.at<int32_t>(L.row_pos);
     const int32_t* last_row = P.at<int32_t>(L.last_row);
     const size_t layer_elems = (size_t)kv.batch * 2 * nkv * (size_t)kv.n_slots * hd;
+    double attn_flops = 0.0;   // causal QK^T + PV over the used keys: 4 nq hd sum_b len_b (len_b + 1) / 2
+    if (prefill) {
+        for (int b = 0; b < batch; ++b) {
+            const double n = (double)seq_lens_host[b];
+            attn_flops += 4.0 * nq * hd * n * (n + 1.0) / 2.0;
+        }
+    }
 
     for (int l = 0; l < d.n_layers; ++l) {
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
         const bool last = l == d.n_layers - 1;
-        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st));
+        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : 0));
         QkRopeArgs qa{};
         qa.qkv = qkv;
         qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
@@ -185,7 +226,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         if (!tail) {
             if (prefill) {
                 PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), att, batch, max_len, kv.n_slots, nq, nkv, hd};
-                HRA_TRY(launch_prefill_attention(pa, st));
+                HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_flops, st, [&] { return launch_prefill_attention(pa, st); }));
             } else {
                 DecodeAttnArgs da{};
                 da.q = q;
@@ -204,10 +245,11 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
                 da.splits = L.attn_splits;
                 HRA_TRY(launch_decode_attention(da, st));
             }
-            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st));
+            const int pc = prefill ? 1 : 0;
+            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_O_PROJ));
             HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(lw.mlp_norm), y, nullptr, rows, H, eps, st));
-            HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st));
-            HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st));
+            HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st, pc * HRA_PROBE_GATE_UP));
+            HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN));
             if (!last) {
                 HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(w.layers[l + 1].attn_norm), y,
                                        nullptr, rows, H, eps, st));
@@ -258,7 +300,38 @@ bool kv_ok(const hra_kv_cache* kv) {
 
 }  // namespace
 
+namespace hra {
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace hra
+
 extern "C" {
+
+uint64_t hra_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int hra_probe_select(int kernel_class) {
+    std::lock_guard<std::mutex> lk(g_probe.mu);
+    g_probe.active = kernel_class;
+    return HRA_OK;
+}
+
+int hra_probe_collect(double* total_ms, int64_t* launches, double* total_flops) {
+    std::lock_guard<std::mutex> lk(g_probe.mu);
+    double ms = 0.0, fl = 0.0;
+    for (const auto& u : g_probe.used) {
+        if (cudaEventSynchronize(g_probe.pool[2 * u.first + 1]) != cudaSuccess) return HRA_ERR_CUDA;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_probe.pool[2 * u.first], g_probe.pool[2 * u.first + 1]) != cudaSuccess)
+            return HRA_ERR_CUDA;
+        ms += t;
+        fl += u.second;
+    }
+    if (total_ms) *total_ms = ms;
+    if (launches) *launches = (int64_t)g_probe.used.size();
+    if (total_flops) *total_flops = fl;
+    g_probe.used.clear();
+    return HRA_OK;
+}
+
 
 size_t hra_prefill_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
     if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1) return 0;
@@ -303,7 +376,8 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
                                  reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.r),
                                  P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
     return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
-                      (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), st);
+                      (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), seq_lens,
+                      st);
 }
 
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots) {
@@ -345,7 +419,7 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                            reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.y),
                            P.at<bf16>(L.r), batch, d.hidden, d.rms_eps, st));
     return run_layers(d, *weights, *kv, P, L, batch, batch, 0, false, false, reinterpret_cast<bf16*>(hidden_dev),
-                      st);
+                      nullptr, st);
 }
 
 size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch) {
@@ -392,7 +466,7 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
     c.err = err;
     c.partial_only = true;
     c.splits_used = &splits;
-    HRA_TRY(launch_linear(c, st));
+    HRA_TRY(probed(HRA_PROBE_AUDIO_HEAD, 2.0 * batch * (double)K * Vc * H, st, [&] { return launch_linear(c, st); }));
 
     CodebookArgs a{};
     a.partial = part;

@@ -9,7 +9,8 @@
 // prefill_attn_kernel  flash-attention style: one CTA = 64 queries x one q head of one sequence,
 //                      4 warps x 16 query rows; K/V tiles of 64 keys double-buffered with cp.async
 //                      into XOR-swizzled shared memory; S = QK^T and O += PV on warp-level
-//                      bf16 MMA (m16n8k16) with fp32 online softmax; P is rounded to bf16 for PV.
+//                      bf16 MMA (m16n8k16) with fp32 online softmax; P enters PV as a bf16
+//                      hi + lo pair, so it is not rounded to 8 bits.
 //                      Tiles above the causal diagonal are never loaded.
 // decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
 //                      across CTAs; each warp walks keys with 8-byte coalesced K/V loads, the
@@ -28,6 +29,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ------------------------------------------------------------------ prefill (many queries)
 
 constexpr int PQ = 64;    // queries per CTA
+
+// (a, b) -> bf16 pairs hi = bf16(a, b) and lo = bf16(a - hi_a, b - hi_b).
+__device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_bf2(a - hf.x, b - hf.y);
+}
 constexpr int PK = 64;    // keys per tile
 
 template <int HD>
@@ -163,20 +172,23 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
             o[d][2] *= al_b;
             o[d][3] *= al_b;
         }
-        // O += P V
+        // O += P V with P carried as a bf16 pair P = hi + lo (about 16 significant bits), so the
+        // probabilities enter the product essentially unrounded.
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            uint32_t pa[4];
-            pa[0] = pack_bf2(s[2 * t][0], s[2 * t][1]);
-            pa[1] = pack_bf2(s[2 * t][2], s[2 * t][3]);
-            pa[2] = pack_bf2(s[2 * t + 1][0], s[2 * t + 1][1]);
-            pa[3] = pack_bf2(s[2 * t + 1][2], s[2 * t + 1][3]);
+            uint32_t ph[4], pl[4];
+            split_bf2(s[2 * t][0], s[2 * t][1], ph[0], pl[0]);
+            split_bf2(s[2 * t][2], s[2 * t][3], ph[1], pl[1]);
+            split_bf2(s[2 * t + 1][0], s[2 * t + 1][1], ph[2], pl[2]);
+            split_bf2(s[2 * t + 1][2], s[2 * t + 1][3], ph[3], pl[3]);
 #pragma unroll
             for (int dp = 0; dp < DN / 2; ++dp) {
                 uint32_t vb[4];
                 ldmatrix_x4_trans(vb, sV + swz<HD>(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dp * 2 + (lane >> 4)));
-                mma_bf16_16816(o[2 * dp], pa, vb[0], vb[1]);
-                mma_bf16_16816(o[2 * dp + 1], pa, vb[2], vb[3]);
+                mma_bf16_16816(o[2 * dp], ph, vb[0], vb[1]);
+                mma_bf16_16816(o[2 * dp + 1], ph, vb[2], vb[3]);
+                mma_bf16_16816(o[2 * dp], pl, vb[0], vb[1]);
+                mma_bf16_16816(o[2 * dp + 1], pl, vb[2], vb[3]);
             }
         }
         __syncthreads();
@@ -337,6 +349,7 @@ cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
     dim3 grid((a.max_len + PQ - 1) / PQ, a.nq, a.batch);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
     prefill_attn_kernel<HD><<<grid, 128, smem, st>>>(a, scale_log2);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -345,9 +358,11 @@ cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
     dim3 grid(a.splits, a.nkv, a.rows);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
     decode_attn_kernel<HD, G><<<grid, 128, 0, st>>>(a, scale_log2);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_combine_kernel<HD><<<dim3(a.nq, a.rows), HD, 0, st>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) codebook_finalize_kernel(const Codeb
 cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st) {
     if (a.K > kMaxCodebooks) return cudaErrorInvalidValue;
     codebook_finalize_kernel<<<a.batch, kThreads, 0, st>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,36 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Compensated fp32 sum of non-negative terms (Knuth TwoSum per add; compensation carried in c).
+// Used for the sum of squares of bf16 values (each square is exact in fp32), rounded once to
+// fp32 -- equal to the correctly rounded exact sum except in ~n * 2^-24 of rows -- so RMSNorm does
+// not depend on the order of its reduction.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    const float ap = __fsub_rn(s, bp);
+    e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+}
+__device__ __forceinline__ void csum_add(float& s, float& c, float x) {
+    float t, e;
+    two_sum(s, x, t, e);
+    s = t;
+    c = __fadd_rn(c, e);
+}
+// Warp-wide combination of per-lane (s, c) pairs; every lane gets fl(s + c) of the total.
+__device__ __forceinline__ float csum_warp(float s, float c) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, e;
+        two_sum(s, s2, t, e);
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, c2), e);
+    }
+    return __fadd_rn(s, c);
+}
+
 __device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit) {
     if (err != nullptr) atomicOr(err, bit);
 }

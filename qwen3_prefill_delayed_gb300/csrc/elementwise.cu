@@ -82,16 +82,16 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
     uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
     const uint4* gv = reinterpret_cast<const uint4*>(g);
     const int nc = H >> 3;
-    float ss = 0.f;
+    float ss = 0.f, sc = 0.f;
     for (int c = lane; c < nc; c += 32) {
         const uint4 u = src[c];
         dr[c] = u;
         float f[8];
         unpack8(u, f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+        for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
     }
-    ss = warp_sum(ss);
+    ss = csum_warp(ss, sc);
     const float inv = 1.0f / sqrtf(ss / (float)H + eps);
     for (int c = lane; c < nc; c += 32) {
         float f[8], w[8];
@@ -118,16 +118,16 @@ __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __rest
         for (int c = lane; c < nc; c += 32) dc[c] = src[c];
         return;
     }
-    float ss = 0.f;
+    float ss = 0.f, sc = 0.f;
     for (int c = lane; c < nc; c += 32) {
         const uint4 u = src[c];
         if (copy_out) reinterpret_cast<uint4*>(copy_out + (long long)row * H)[c] = u;
         float f[8];
         unpack8(u, f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+        for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
     }
-    ss = warp_sum(ss);
+    ss = csum_warp(ss, sc);
     const float inv = 1.0f / sqrtf(ss / (float)H + eps);
     const uint4* gv = reinterpret_cast<const uint4*>(g);
     uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
@@ -176,10 +176,10 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
     }
     const bool is_q = hh < a.nq;
     const bf16* gain = (is_q ? a.q_norm : a.k_norm) + lane * E;
-    float ss = 0.f;
+    float ss = 0.f, sc = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) ss += x[e] * x[e];
-    ss = warp_sum(ss);
+    for (int e = 0; e < E; ++e) csum_add(ss, sc, __fmul_rn(x[e], x[e]));
+    ss = csum_warp(ss, sc);
     const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
     float xn[E], pn[E];
 #pragma unroll
@@ -226,6 +226,7 @@ cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* ro
     const int threads = 256;
     const unsigned blocks = blocks_for(total_rows > 0 ? total_rows : 1, threads);
     build_rowmap_kernel<<<blocks, threads, 0, st>>>(meta, total_rows, row_seq, row_pos, cu, last_row);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -233,6 +234,7 @@ cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_di
                               float2* table, cudaStream_t st) {
     const long long n = (long long)n_rows * (head_dim / 2);
     rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(n_rows, pos_of_row, head_dim, theta, table);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -242,6 +244,7 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_
                                  cudaStream_t st) {
     embed_rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(
         tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -249,6 +252,7 @@ cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf1
                            int rows, int H, float eps, cudaStream_t st) {
     rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(x, idx, g, y, copy_out, rows, H,
                                                                         eps);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -258,6 +262,7 @@ cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st) {
     if (a.hd == 128) qk_rope_kv_kernel<128><<<blocks, 256, 0, st>>>(a);
     else if (a.hd == 64) qk_rope_kv_kernel<64><<<blocks, 256, 0, st>>>(a);
     else return cudaErrorInvalidValue;
+    count_launches(1);
     return cudaGetLastError();
 }
 

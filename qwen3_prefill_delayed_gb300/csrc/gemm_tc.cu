@@ -374,6 +374,7 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     }
     dim3 grid(pl.nt, pl.mt, pl.splits);
     gemm_bf16_tc_kernel<BN, SW><<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ma, mb, g);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -447,6 +448,7 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     const int threads = 256;
     splitk_reduce_kernel<<<(unsigned)((items + threads - 1) / threads), threads, 0, st>>>(
         c.partial, pl.splits, (long long)c.M * g.ldo, c.M, c.N, g.ldo, c.N, mode, c.out, c.N);
+    count_launches(1);
     return cudaGetLastError();
 }
 

