@@ -41,7 +41,39 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary sections")
+    ap.add_argument("--kernel-case", default=None, choices=["gate_up", "qkv", "down", "audio_head"],
+                    help="run only a few launches of one kernel at a profiling size, then exit")
     return ap.parse_args()
+
+
+def kernel_case(name):
+    """A few launches of one kernel on inputs larger than L2 (for an ncu capture of that kernel)."""
+    import torch
+
+    import qwen3_prefill_delayed_gb300 as hra
+    import workloads as W
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(7)
+    d = W.full_dims(1)
+    rnd = lambda *sh, std=1.0: (torch.randn(*sh, generator=g, device=dev) * std).to(torch.bfloat16)
+    if name == "audio_head":
+        wl = W.make_audio(d, g, dev)
+        head = hra.AudioHead(d, wl["head_w"], wl["code_emb"])
+        hid = rnd(64, d.hidden)
+        state = torch.zeros(64, 4, dtype=torch.int32, device=dev)
+        for _ in range(5):
+            head.step(hid, state)
+    else:
+        M = 8192
+        K, N, epi = {"gate_up": (d.hidden, d.ffn, hra.EPI_SWIGLU), "qkv": (d.hidden, d.qkv_rows, hra.EPI_STORE),
+                     "down": (d.ffn, d.hidden, hra.EPI_RESIDUAL)}[name]
+        a = rnd(M, K)
+        w = rnd(2 * N if epi == hra.EPI_SWIGLU else N, K, std=0.02)
+        out = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+        for _ in range(5):
+            hra.hra_linear(a, w, epi, out=out)
+    torch.cuda.synchronize()
+    print(f"kernel case {name} done")
 
 
 def load_peaks():
@@ -191,6 +223,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.kernel_case:
+        return kernel_case(args.kernel_case)
     if args.impl == "reference":
         return run_reference(args)
     import torch
