@@ -45,6 +45,8 @@ struct GemmArgs {
     int kb_per_split;
     int up_row0;              // SwiGLU: first up row in W (= F)
     int mode;
+    int mt, nt, splits;       // tile grid: M tiles, N tiles, K splits
+    int group;                // N tiles per raster band
 };
 
 template <int BN>
@@ -54,7 +56,8 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-    static constexpr uint32_t TMEM_COLS = BN;   // fp32 accumulator: one column per output column
+    // two fp32 accumulators of BN columns each: the epilogue drains one while the MMA fills the other
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
@@ -87,6 +90,21 @@ __device__ __forceinline__ void store_row_chunk(int mode, void* out, long long o
     }
 }
 
+// Work unit u -> (M tile, N tile, K split).  Tiles are rastered in bands of `group` N tiles with
+// the M tile varying fastest inside a band, so the CTAs resident at one time share a few weight
+// tiles (and the activation tiles stay in L2 across bands when they fit).
+__device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m_blk, int& n_blk, int& split) {
+    const int tiles = p.mt * p.nt;
+    split = u / tiles;
+    const int t = u - split * tiles;
+    const int band_units = p.group * p.mt;
+    const int band = t / band_units;
+    const int within = t - band * band_units;
+    m_blk = within % p.mt;
+    n_blk = band * p.group + within / p.mt;
+}
+
+// Persistent: each CTA walks work units blockIdx.x, blockIdx.x + gridDim.x, ...
 template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -95,20 +113,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 1);
+    // bars: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
+    int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM;
-    const int ntile = blockIdx.x;
-    const int kb0 = blockIdx.z * p.kb_per_split;
-    const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-    const int nk = kb1 - kb0;
+    const int units = p.mt * p.nt * p.splits;
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + C::STAGES + s); };
-    const uint32_t accum_bar = smem_u32(bars + 2 * C::STAGES);
+    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + b); };
+    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + 2 + b); };
     auto a_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
     auto b_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
 
@@ -117,9 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);   // one arrival per epilogue warp
+        }
         *abort_flag = 0;
         *issued_slot = 0;
+        *committed_slot = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
@@ -134,65 +155,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        int i = 0;
-        for (; i < nk; ++i) {
-            const int s = i % C::STAGES;
-            const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
-            if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
-                *abort_flag = 1;
-                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                break;
-            }
-            mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
-            const int kx = (kb0 + i) * BK;
-            tma_load_2d(a_tile(s), &tmA, full_bar(s), kx, m0);
-            if (SWIGLU) {
-                const int j0 = ntile * (BN / 2);
-                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, j0);
-                tma_load_2d(b_tile(s) + C::B_BYTES / 2, &tmB, full_bar(s), kx, p.up_row0 + j0);
-            } else {
-                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, ntile * BN);
+        // ---------------- TMA producer: one continuous stage ring across all of this CTA's units
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            int mb, nb, sp;
+            unit_coords(u, p, mb, nb, sp);
+            const int kb0 = sp * p.kb_per_split;
+            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+                const int kx = kb * BK;
+                tma_load_2d(a_tile(s), &tmA, full_bar(s), kx, mb * BM);
+                if (SWIGLU) {
+                    const int j0 = nb * (BN / 2);
+                    tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, j0);
+                    tma_load_2d(b_tile(s) + C::B_BYTES / 2, &tmB, full_bar(s), kx, p.up_row0 + j0);
+                } else {
+                    tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, nb * BN);
+                }
             }
         }
-        *issued_slot = i;
+        *issued_slot = it;
     } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer: accumulator buffer j % 2 for this CTA's j-th unit
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-        for (int i = 0; i < nk; ++i) {
-            const int s = i % C::STAGES;
-            const uint32_t ph = (uint32_t)(i / C::STAGES) & 1u;
-            if (!mbar_wait(full_bar(s), ph, abort_flag)) {
+        int it = 0, j = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+            int mb, nb, sp;
+            unit_coords(u, p, mb, nb, sp);
+            const int kb0 = sp * p.kb_per_split;
+            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            const int buf = j & 1;
+            const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+            if (!mbar_wait(tempty_bar(buf), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const uint64_t ad = sdesc_sw128(a_tile(s));
-            const uint64_t bd = sdesc_sw128(b_tile(s));
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+                if (!mbar_wait(full_bar(s), ph, abort_flag)) {
+                    *abort_flag = 1;
+                    raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sdesc_sw128(a_tile(s));
+                const uint64_t bd = sdesc_sw128(b_tile(s));
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-                tc_mma_bf16(tmem, ad + 2ull * k, bd + 2ull * k, idesc, (i > 0 || k > 0) ? 1u : 0u);
-            tc_commit(empty_bar(s));
+                for (int k = 0; k < BK / 16; ++k)
+                    tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                tc_commit(empty_bar(s));
+            }
+            tc_commit(tfull_bar(buf));
+            *committed_slot = j + 1;
         }
-        tc_commit(accum_bar);
     } else if (warp >= 2) {
-        // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+        // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (one row per thread)
         const int quad = warp & 3;
-        const int row = m0 + quad * 32 + lane;
-        const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
-        // warp-uniform decision: tcgen05.ld below is a .sync.aligned warp instruction
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, abort_flag));
-        if (!ok) {
-            *abort_flag = 1;
-            raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-        }
-        tc_fence_after();
-        if (ok) {
+        int j = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+            int mb, nb, sp;
+            unit_coords(u, p, mb, nb, sp);
+            const int buf = j & 1;
+            // warp-uniform decision: tcgen05.ld below is a .sync.aligned warp instruction
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+            const int row = mb * BM + quad * 32 + lane;
             const bool row_ok = row < p.M;
-            const long long split_off = (long long)blockIdx.z * p.split_stride;
+            const long long split_off = (long long)sp * p.split_stride;
             if (!SWIGLU) {
-                const int n0 = ntile * BN;
+                const int n0 = nb * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
@@ -203,27 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         min(32, p.n_valid - col));
                 }
             } else {
-                const int j0 = ntile * (BN / 2);
+                const int j0 = nb * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
-                    float g[32], u[32];
+                    float g[32], uu[32];
                     tmem_ld32(tq + c, g);
-                    tmem_ld32(tq + BN / 2 + c, u);
+                    tmem_ld32(tq + BN / 2 + c, uu);
                     const int col = j0 + c;
                     if (row_ok && col < p.n_valid) {
                         const int nv = min(32, p.n_valid - col);
                         if (p.mode == KM_PARTIAL) {
                             const long long base = split_off + (long long)row * p.ldo;
                             store_row_chunk(KM_PARTIAL, p.out, base + col, g, nv);
-                            store_row_chunk(KM_PARTIAL, p.out, base + p.up_row0 + col, u, nv);
+                            store_row_chunk(KM_PARTIAL, p.out, base + p.up_row0 + col, uu, nv);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) g[j] = silu_f(round_bf(g[j])) * round_bf(u[j]);
+                            for (int q = 0; q < 32; ++q) g[q] = silu_f(round_bf(g[q])) * round_bf(uu[q]);
                             store_row_chunk(KM_STORE, p.out, (long long)row * p.ldo + col, g, nv);
                         }
                     }
                 }
             }
+            // this warp is done reading accumulator `buf`: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
     }
 
@@ -231,13 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {
-        // Let every TMA load this CTA issued land before its shared memory is released.
+        // Let every TMA load and MMA this CTA issued land before its shared memory and TMEM go.
+        volatile int never = 0;
         const int issued = *issued_slot;
-        for (int i = max(0, issued - C::STAGES); i < issued; ++i) {
-            volatile int never = 0;
+        for (int i = max(0, issued - C::STAGES); i < issued; ++i)
             (void)mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, &never);
-        }
-        (void)mbar_wait(accum_bar, 0, abort_flag);
+        const int committed = *committed_slot;
+        for (int jj = max(0, committed - 2); jj < committed; ++jj)
+            (void)mbar_wait(tfull_bar(jj & 1), (uint32_t)(jj >> 1) & 1u, &never);
     }
     __syncthreads();
     if (warp == 1) {
@@ -325,9 +382,10 @@ struct Plan {
     int mt, nt;
 };
 
-// Choose the tile width and K split.  Per-CTA time ~ (K blocks) x BN (bytes streamed and MMA work
-// both scale with BN); the grid runs in ceil(CTAs / SMs) waves; splitting K is allowed for a
-// single M tile only and costs a reduction pass.
+// Choose the tile width and K split.  The kernel is persistent (one CTA per SM walking work
+// units), so the grid runs in ceil(units / SMs) rounds; per-unit time ~ (K blocks) x BN (bytes
+// streamed and MMA work both scale with BN) plus a fixed tile overhead.  Splitting K is allowed
+// for a single M tile only and costs a reduction pass.
 Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm) {
     const int n_kb = K / BK;
     const int mt = (M + BM - 1) / BM;
@@ -343,18 +401,15 @@ Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm) {
             if (split_req > 0 && s != std::min(split_req, max_split)) continue;
             const int kbps = (n_kb + s - 1) / s;
             const int splits = (n_kb + kbps - 1) / kbps;
-            const long long ctas = (long long)mt * nt * splits;
-            const long long waves = (ctas + nsm - 1) / nsm;
-            double cost = (double)waves * (kbps * (bn / 256.0) + 1.5);
+            const long long units = (long long)mt * nt * splits;
+            const long long rounds = (units + nsm - 1) / nsm;
+            double cost = (double)rounds * (kbps * (bn / 256.0) + 0.5);
             if (splits > 1) cost += 2.0;
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best = Plan{bn, splits, kbps, mt, nt};
             }
         }
-    }
-    if (split_req > 0 && mt > 1) {
-        best.splits = 1;
     }
     return best;
 }
@@ -372,7 +427,9 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    dim3 grid(pl.nt, pl.mt, pl.splits);
+    const long long units = (long long)pl.mt * pl.nt * pl.splits;
+    const int nsm = device_sm_count();
+    dim3 grid((unsigned)std::min<long long>(units, nsm));
     gemm_bf16_tc_kernel<BN, SW><<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ma, mb, g);
     count_launches(1);
     return cudaGetLastError();
@@ -423,6 +480,10 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     g.n_kb = c.K / BK;
     g.kb_per_split = pl.kbps;
     g.up_row0 = c.N;
+    g.mt = pl.mt;
+    g.nt = pl.nt;
+    g.splits = pl.splits;
+    g.group = 8;
     if (pl.splits > 1) {
         g.out = c.partial;
         g.mode = KM_PARTIAL;
