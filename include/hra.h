@@ -157,6 +157,28 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
                       void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* The same step for callers that cannot allocate device memory -- for instance a streaming-audio
+ * callback with a hard per-frame deadline (cudaMalloc may synchronise the device and take
+ * milliseconds), or a runtime whose device memory belongs to an allocator that forbids side
+ * allocations.  No pages' counterpart: it is an interface convenience, computing exactly what
+ * hra_codebook_step computes.  Instead of a caller workspace it uses a fixed 32 MiB scratch array
+ * that each GPU loading this library reserves once and holds until the process exits; it calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: accepted while hra_codebook_workspace_size(dims, batch) <= 32 MiB (batch <= 127 for
+ *     8 codebooks x 1026 entries at hidden 2560); larger requests return HRA_ERR_WORKSPACE and
+ *     enqueue nothing.
+ *   - The first call on a device looks up the scratch address for that device; make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one scratch array, which keeps the last call's contents;
+ *     the step clears its error word and overwrites every partial it reads.  Calls that overlap on
+ *     the GPU (different streams without ordering) race on the scratch and must be serialised by
+ *     the caller.
+ * Arguments and results are those of hra_codebook_step without the workspace. */
+int hra_codebook_step_noalloc(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev,
+                              const void* code_emb_dev, hra_delay_state* state_dev,
+                              const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
+                              void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* stream);
+
 /* ---- projection (diagnostic access to the tensor-core GEMM used by the path) ----------------- */
 #define HRA_EPI_STORE 0     /* out bf16 [M, N] = bf16(acc)                                        */
 #define HRA_EPI_RESIDUAL 1  /* out bf16 [M, N] = bf16(out + acc)   (in place)                      */

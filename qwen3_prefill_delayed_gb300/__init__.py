@@ -29,7 +29,8 @@ EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_F32 = 0, 1, 2, 3
 PREFILL_FULL_LAST_LAYER = 1
 
 EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_decode_workspace_size", "hra_decode",
-            "hra_codebook_workspace_size", "hra_codebook_step", "hra_linear_workspace_size",
+            "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_noalloc",
+            "hra_linear_workspace_size",
             "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
             "hra_device_error", "hra_status_string"]
 PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6}
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.hra_codebook_workspace_size.restype = sz
         L.hra_codebook_step.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
         L.hra_codebook_step.restype = ctypes.c_int
+        L.hra_codebook_step_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        L.hra_codebook_step_noalloc.restype = ctypes.c_int
         L.hra_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.hra_linear_workspace_size.restype = sz
         L.hra_linear.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
@@ -272,6 +275,35 @@ class AudioHead:
                                      _ptr(ws, None, "workspace"), ws.numel(), _stream(stream))
         _check(rc, "hra_codebook_step")
         self.last_ws = ws
+        return codes, next_emb, done
+
+    def step_noalloc(self, hidden: torch.Tensor, state: torch.Tensor, eoc_bias: Optional[torch.Tensor] = None,
+                     codes: Optional[torch.Tensor] = None, next_emb: Optional[torch.Tensor] = None,
+                     done: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None, stream=None):
+        """hra_codebook_step_noalloc: the same step for callers that cannot allocate device memory
+        (the library's fixed per-device scratch replaces the workspace).  The output tensors may be
+        passed in so that the call itself allocates nothing."""
+        B = hidden.shape[0]
+        K, H = self.d.n_codebooks, self.d.hidden
+        dev = hidden.device
+        if codes is None:
+            codes = torch.empty(B, K, dtype=torch.int32, device=dev)
+        if next_emb is None:
+            next_emb = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+        if done is None:
+            done = torch.empty(B, dtype=torch.int32, device=dev)
+        if state.dtype != torch.int32 or tuple(state.shape) != (B, 4):
+            raise HraError("state must be int32 [B, 4]")
+        rc = lib().hra_codebook_step_noalloc(ctypes.byref(self.dims), _ptr(hidden, torch.bfloat16, "hidden"),
+                                             _ptr(self.head_w, torch.bfloat16, "head_w"),
+                                             _ptr(self.code_emb, torch.bfloat16, "code_emb"),
+                                             _ptr(state, torch.int32, "state"),
+                                             _ptr(eoc_bias, torch.float32, "eoc_bias"), B,
+                                             _ptr(codes, torch.int32, "codes"),
+                                             _ptr(next_emb, torch.bfloat16, "next_emb"),
+                                             _ptr(done, torch.int32, "done"),
+                                             _ptr(logits, torch.float32, "logits"), _stream(stream))
+        _check(rc, "hra_codebook_step_noalloc")
         return codes, next_emb, done
 
 
