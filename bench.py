@@ -43,10 +43,11 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary sections")
     ap.add_argument("--kernel-case", default=None, choices=["gate_up", "qkv", "down", "audio_head"],
                     help="run only a few launches of one kernel at a profiling size, then exit")
+    ap.add_argument("--kernel-m", type=int, default=None, help="rows (tokens / batch) of the kernel case")
     return ap.parse_args()
 
 
-def kernel_case(name):
+def kernel_case(name, m=None):
     """A few launches of one kernel on inputs larger than L2 (for an ncu capture of that kernel)."""
     import torch
 
@@ -59,12 +60,13 @@ def kernel_case(name):
     if name == "audio_head":
         wl = W.make_audio(d, g, dev)
         head = hra.AudioHead(d, wl["head_w"], wl["code_emb"])
-        hid = rnd(64, d.hidden)
-        state = torch.zeros(64, 4, dtype=torch.int32, device=dev)
+        bsz = m or 64
+        hid = rnd(bsz, d.hidden)
+        state = torch.zeros(bsz, 4, dtype=torch.int32, device=dev)
         for _ in range(5):
             head.step(hid, state)
     else:
-        M = 8192
+        M = m or 8192
         K, N, epi = {"gate_up": (d.hidden, d.ffn, hra.EPI_SWIGLU), "qkv": (d.hidden, d.qkv_rows, hra.EPI_STORE),
                      "down": (d.ffn, d.hidden, hra.EPI_RESIDUAL)}[name]
         a = rnd(M, K)
@@ -224,7 +226,7 @@ def run_reference(args):
 def main():
     args = parse()
     if args.kernel_case:
-        return kernel_case(args.kernel_case)
+        return kernel_case(args.kernel_case, args.kernel_m)
     if args.impl == "reference":
         return run_reference(args)
     import torch

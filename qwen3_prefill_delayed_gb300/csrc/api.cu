@@ -126,6 +126,7 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     part = std::max(part, linear_partial_bound(m_split, (int)H, (int)Dq, EPI_RESIDUAL));
     part = std::max(part, linear_partial_bound(m_split, (int)F, (int)H, EPI_SWIGLU));
     part = std::max(part, linear_partial_bound(m_split, (int)H, (int)F, EPI_RESIDUAL));
+    if (std::max(rows, batch) > 128) part = std::max(part, linear_tail_bound());
     L.part = g.take(part);
     L.attn_splits = decode_attention_splits(batch, d.n_kv_heads, max_pos);
     L.apart = g.take(decode_attention_scratch_bytes(batch, d.n_q_heads, d.head_dim, L.attn_splits));
@@ -150,8 +151,12 @@ int cuda_status(cudaError_t e) {
         if (e_ != cudaSuccess) return cuda_status(e_); \
     } while (0)
 
+// norm_gain / norm_out: for EPI_RESIDUAL, the RMSNorm that follows (fused into a split-K reduction
+// when the plan splits; otherwise run as its own kernel here).
 cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K, int epi, const Ptrs& P,
-                   const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE) {
+                   const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE,
+                   const void* norm_gain = nullptr, bf16* norm_out = nullptr, float eps = 0.f,
+                   const int32_t* norm_rows = nullptr, int norm_nrows = 0) {
     LinearCall c{};
     c.a = a;
     c.w = reinterpret_cast<const bf16*>(w);
@@ -163,8 +168,18 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
     c.split_req = 0;
     c.partial = P.at<float>(L.part);
     c.err = P.at<unsigned int>(L.err);
+    bool norm_done = false;
+    if (norm_out != nullptr && norm_rows == nullptr) {
+        c.norm_gain = reinterpret_cast<const bf16*>(norm_gain);
+        c.norm_out = norm_out;
+        c.norm_eps = eps;
+        c.norm_done = &norm_done;
+    }
     const double flops = 2.0 * M * (double)K * (epi == EPI_SWIGLU ? 2.0 * N : (double)N);
-    return probed(probe_class, flops, st, [&] { return launch_linear(c, st); });
+    cudaError_t e = probed(probe_class, flops, st, [&] { return launch_linear(c, st); });
+    if (e != cudaSuccess || norm_out == nullptr || norm_done) return e;
+    return launch_rmsnorm(reinterpret_cast<const bf16*>(out), norm_rows, reinterpret_cast<const bf16*>(norm_gain),
+                          norm_out, nullptr, norm_rows ? norm_nrows : M, N, eps, st);
 }
 
 bool layer_ptrs_ok(const hra_layer_weights& l) {
@@ -246,16 +261,17 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
                 HRA_TRY(launch_decode_attention(da, st));
             }
             const int pc = prefill ? 1 : 0;
-            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_O_PROJ));
-            HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(lw.mlp_norm), y, nullptr, rows, H, eps, st));
+            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_O_PROJ, lw.mlp_norm,
+                           y, eps));
             HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st, pc * HRA_PROBE_GATE_UP));
-            HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN));
             if (!last) {
-                HRA_TRY(launch_rmsnorm(r, nullptr, reinterpret_cast<const bf16*>(w.layers[l + 1].attn_norm), y,
-                                       nullptr, rows, H, eps, st));
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN,
+                               w.layers[l + 1].attn_norm, y, eps));
+            } else if (!prefill) {
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps));
             } else {
-                HRA_TRY(launch_rmsnorm(r, prefill ? last_row : nullptr, reinterpret_cast<const bf16*>(w.final_norm),
-                                       out_hidden, nullptr, batch, H, eps, st));
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN,
+                               w.final_norm, out_hidden, eps, last_row, batch));
             }
         } else {
             // last prefill layer, rows that feed the last hidden only
@@ -276,12 +292,9 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             da.splits = std::min(L.attn_splits, decode_attention_splits(batch, nkv, max_len - 1));
             HRA_TRY(launch_decode_attention(da, st));
             HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
-            HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st));
-            HRA_TRY(launch_rmsnorm(rl, nullptr, reinterpret_cast<const bf16*>(lw.mlp_norm), y, nullptr, batch, H, eps, st));
+            HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps));
             HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st));
-            HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st));
-            HRA_TRY(launch_rmsnorm(rl, nullptr, reinterpret_cast<const bf16*>(w.final_norm), out_hidden, nullptr,
-                                   batch, H, eps, st));
+            HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps));
         }
     }
     return HRA_OK;
@@ -367,9 +380,8 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
-    HRA_TRY(cudaMemsetAsync(P.at<void>(L.err), 0, 4, st));
     HRA_TRY(launch_build_rowmap(meta, (int)T, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
-                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), st));
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<unsigned int>(L.err), st));
     HRA_TRY(launch_rope_table(max_len, nullptr, d.head_dim, (double)d.rope_theta, P.at<float2>(L.rope), st));
     HRA_TRY(launch_embed_rmsnorm(tokens_dev, max_len, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
                                  reinterpret_cast<const bf16*>(weights->embed), d.vocab,
@@ -409,9 +421,8 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
-    HRA_TRY(cudaMemsetAsync(P.at<void>(L.err), 0, 4, st));
     HRA_TRY(launch_build_rowmap(meta, batch, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
-                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), st));
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<unsigned int>(L.err), st));
     HRA_TRY(launch_rope_table(batch, P.at<int32_t>(L.row_pos), d.head_dim, (double)d.rope_theta,
                               P.at<float2>(L.rope), st));
     // r = input embedding, y = RMSNorm(r) with layer 0's attention gain
@@ -422,13 +433,30 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                       nullptr, st);
 }
 
+// Codebook-step workspace: error word and per-row counters (cleared by the GEMM), per-row argmax
+// candidates, then the fp32 logit partials.
+struct CbLayout {
+    size_t counters, cand, part;
+};
+CbLayout codebook_layout(const hra_dims* dims, int32_t batch) {
+    Region g;
+    CbLayout L;
+    g.take(4 + 4 * (size_t)batch);
+    L.counters = 4;
+    L.cand = g.take(4 * (size_t)batch * dims->n_codebooks);
+    L.part = g.off;
+    return L;
+}
+
 size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch) {
     if (!audio_dims_ok(dims) || batch < 1) return 0;
     const int N = dims->n_codebooks * dims->codebook_size;
     Region g;
-    g.take(256);
+    g.off = codebook_layout(dims, batch).part;
     const size_t plane = (size_t)batch * N * sizeof(float);
-    g.take(std::max(plane, linear_partial_bound(std::min(batch, 128), N, dims->hidden, EPI_F32)));
+    size_t part = std::max(plane, linear_partial_bound(std::min(batch, 128), N, dims->hidden, EPI_F32));
+    if (batch > 128) part = std::max(part, linear_tail_bound());
+    g.take(part);
     return g.off;
 }
 
@@ -448,9 +476,9 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
     const int K = dims->n_codebooks, Vc = dims->codebook_size, H = dims->hidden;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+    const CbLayout CL = codebook_layout(dims, batch);
     unsigned int* err = reinterpret_cast<unsigned int*>(base);
-    float* part = reinterpret_cast<float*>(base + 256);
-    HRA_TRY(cudaMemsetAsync(err, 0, 4, st));
+    float* part = reinterpret_cast<float*>(base + CL.part);
 
     int splits = 1;
     LinearCall c{};
@@ -466,10 +494,14 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
     c.err = err;
     c.partial_only = true;
     c.splits_used = &splits;
+    c.zero_ptr = err;                 // error word + per-row counters
+    c.zero_words = 1 + batch;
     HRA_TRY(probed(HRA_PROBE_AUDIO_HEAD, 2.0 * batch * (double)K * Vc * H, st, [&] { return launch_linear(c, st); }));
 
     CodebookArgs a{};
     a.partial = part;
+    a.counters = reinterpret_cast<int*>(base + CL.counters);
+    a.cand = reinterpret_cast<int*>(base + CL.cand);
     a.splits = splits;
     a.eoc_bias = eoc_bias_dev;
     a.code_emb = reinterpret_cast<const bf16*>(code_emb_dev);

@@ -13,9 +13,10 @@
 //                      hi + lo pair, so it is not rounded to 8 bits.
 //                      Tiles above the causal diagonal are never loaded.
 // decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
-//                      across CTAs; each warp walks keys with 8-byte coalesced K/V loads, the
-//                      G = n_q / n_kv q heads of a kv head share every load; partial (m, l, o)
-//                      go to scratch and a combine kernel merges the splits.
+//                      across CTAs and taken 128 at a time (one key per thread for the scores,
+//                      then coalesced V rows for PV); the G = n_q / n_kv q heads of a kv head
+//                      share every K/V load; partial (m, l, o) go to scratch and a combine kernel
+//                      merges the splits.
 #include <math.h>
 
 #include "internal.h"
@@ -59,6 +60,8 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* gbase, lon
 
 template <int HD>
 __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs a, float scale_log2) {
+    pdl_launch();
+    pdl_wait();
     constexpr int KS = HD / 16;   // k-steps over the head dim
     constexpr int DN = HD / 8;    // n-tiles of the output
     extern __shared__ __align__(128) uint8_t sm[];
@@ -213,106 +216,154 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
 
 // ------------------------------------------------------------------ single-query decode
 
+// One CTA = one (row, kv head, key split); keys are taken 128 at a time:
+//   phase 1  thread t scores key c0 + t against the G q heads (its K row is 16-byte loads; q is
+//            broadcast from shared memory) and stages that key's V row in shared memory;
+//   phase 2  warp g (per q head) takes the chunk max, turns scores into p = 2^(s - m), and updates
+//            the running max / sum;
+//   phase 3  warp g, lane l accumulates o[g][l*E .. l*E+E) += p_j v_j over the chunk from the
+//            staged V rows.
 template <int HD, int G>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a, float scale_log2) {
+    pdl_launch();
+    pdl_wait();
     constexpr int E = HD / 32;
+    constexpr int CH = 128;
     const int i = blockIdx.z, j = blockIdx.y, sp = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = a.q_row ? a.q_row[i] : i;
     const int seq = a.seq[qr], pos = a.pos[qr];
     const int nkeys = pos + 1;
     const int chunk = (nkeys + a.splits - 1) / a.splits;
     const int k0 = sp * chunk, k1 = min(nkeys, k0 + chunk);
 
-    float q[G][E];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const bf16* qp = a.q + ((long long)qr * a.nq + j * G + g) * HD + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) q[g][e] = bf2f(qp[e]) * scale_log2;
+    __shared__ float s_q[G][HD];
+    __shared__ float s_p[G][CH];
+    __shared__ uint4 s_v[CH][HD / 8];   // the chunk's V rows (bf16)
+    __shared__ float s_m[G], s_l[G], s_alpha[G];
+    for (int idx = tid; idx < G * HD; idx += 128) {
+        const int g = idx / HD, d = idx % HD;
+        s_q[g][d] = bf2f(a.q[((long long)qr * a.nq + j * G + g) * HD + d]) * scale_log2;
+    }
+    if (tid < G) {
+        s_m[tid] = -INFINITY;
+        s_l[tid] = 0.f;
     }
     const long long hstride = (long long)a.n_slots * HD;
-    const bf16* kb = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * hstride + lane * E;
-    const bf16* vb = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * hstride + lane * E;
-
-    float m[G], l[G], o[G][E];
+    const bf16* kb = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * hstride;
+    const bf16* vb = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * hstride;
+    float o[(G + 3) / 4][E];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
+    for (int r = 0; r < (G + 3) / 4; ++r)
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[g][e] = 0.f;
-    }
-    for (int key = k0 + warp; key < k1; key += 4) {
-        float kf[E], vf[E];
-        if constexpr (E == 4) {
-            const uint2 ku = *reinterpret_cast<const uint2*>(kb + (long long)key * HD);
-            const uint2 vu = *reinterpret_cast<const uint2*>(vb + (long long)key * HD);
-            float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ku.x));
-            float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ku.y));
-            kf[0] = t0.x; kf[1] = t0.y; kf[2] = t1.x; kf[3] = t1.y;
-            t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vu.x));
-            t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vu.y));
-            vf[0] = t0.x; vf[1] = t0.y; vf[2] = t1.x; vf[3] = t1.y;
-        } else {
-            const float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kb + (long long)key * HD));
-            const float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vb + (long long)key * HD));
-            kf[0] = t0.x; kf[1] = t0.y;
-            vf[0] = t1.x; vf[1] = t1.y;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) d += q[g][e] * kf[e];
-            d = warp_sum(d);
-            const float mn = fmaxf(m[g], d);
-            const float al = exp2f(m[g] - mn);
-            const float p = exp2f(d - mn);
-            l[g] = l[g] * al + p;
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[g][e] = o[g][e] * al + p * vf[e];
-            m[g] = mn;
-        }
-    }
-    // merge the 4 warps of this CTA
-    __shared__ float s_m[4][G], s_l[4][G];
-    __shared__ float s_o[4][G][HD];
-    if (lane == 0)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            s_m[warp][g] = m[g];
-            s_l[warp][g] = l[g];
-        }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < E; ++e) s_o[warp][g][lane * E + e] = o[g][e];
+        for (int e = 0; e < E; ++e) o[r][e] = 0.f;
     __syncthreads();
-    const int stride = (HD + 2);
-    for (int idx = threadIdx.x; idx < G * HD; idx += 128) {
-        const int g = idx / HD, d = idx % HD;
-        float M = -INFINITY;
-        for (int w = 0; w < 4; ++w) if (s_l[w][g] > 0.f) M = fmaxf(M, s_m[w][g]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY)
-            for (int w = 0; w < 4; ++w)
-                if (s_l[w][g] > 0.f) {
-                    const float f = exp2f(s_m[w][g] - M);
-                    L += s_l[w][g] * f;
-                    O += s_o[w][g][d] * f;
+
+    for (int c0 = k0; c0 < k1; c0 += CH) {
+        const int nc = min(CH, k1 - c0);
+        // phase 1: scores
+        {
+            float sc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
+            if (tid < nc) {
+                const uint4* kr = reinterpret_cast<const uint4*>(kb + (long long)(c0 + tid) * HD);
+                const uint4* vr = reinterpret_cast<const uint4*>(vb + (long long)(c0 + tid) * HD);
+                uint4 kv[HD / 8];
+#pragma unroll
+                for (int c = 0; c < HD / 8; ++c) kv[c] = kr[c];
+#pragma unroll
+                for (int c = 0; c < HD / 8; ++c) s_v[tid][c] = vr[c];   // V row of this key, for phase 3
+#pragma unroll
+                for (int g = 0; g < G; ++g) sc[g] = 0.f;
+#pragma unroll
+                for (int c = 0; c < HD / 8; ++c) {
+                    float f[8];
+                    unpack8(kv[c], f);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) sc[g] += s_q[g][c * 8 + e] * f[e];
                 }
-        float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + g) * stride;
-        dst[d] = O;
-        if (d == 0) {
-            dst[HD] = M;
-            dst[HD + 1] = L;
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) s_p[g][tid] = sc[g];
+        }
+        __syncthreads();
+        // phase 2: softmax bookkeeping, one warp per q head
+        for (int g = warp; g < G; g += 4) {
+            float mx = -INFINITY;
+            for (int t = lane; t < nc; t += 32) mx = fmaxf(mx, s_p[g][t]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_old = s_m[g];
+            const float m_new = fmaxf(m_old, mx);
+            float sum = 0.f;
+            for (int t = lane; t < nc; t += 32) {
+                const float pv = exp2f(s_p[g][t] - m_new);
+                s_p[g][t] = pv;
+                sum += pv;
+            }
+            sum = warp_sum(sum);
+            __syncwarp();
+            if (lane == 0) {
+                const float al = exp2f(m_old - m_new);
+                s_alpha[g] = al;
+                s_l[g] = s_l[g] * al + sum;
+                s_m[g] = m_new;
+            }
+        }
+        __syncthreads();
+        // phase 3: o = o * alpha + sum_j p_j v_j
+#pragma unroll
+        for (int r = 0; r < (G + 3) / 4; ++r) {
+            const int g = warp + 4 * r;
+            if (g < G) {
+                const float al = s_alpha[g];
+                float acc[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = o[r][e] * al;
+                const bf16* vp = reinterpret_cast<const bf16*>(&s_v[0][0]) + lane * E;
+#pragma unroll 4
+                for (int t = 0; t < nc; ++t) {
+                    const float pv = s_p[g][t];
+                    if constexpr (E == 4) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(vp + (long long)t * HD);
+                        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+                        acc[0] += pv * f0.x; acc[1] += pv * f0.y; acc[2] += pv * f1.x; acc[3] += pv * f1.y;
+                    } else {
+                        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp + (long long)t * HD));
+                        acc[0] += pv * f0.x; acc[1] += pv * f0.y;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[r][e] = acc[e];
+            }
+        }
+        __syncthreads();
+    }
+    // partial (o unnormalised, m, l) of this split
+    const int stride = HD + 2;
+#pragma unroll
+    for (int r = 0; r < (G + 3) / 4; ++r) {
+        const int g = warp + 4 * r;
+        if (g < G) {
+            float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + g) * stride;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[lane * E + e] = o[r][e];
+            if (lane == 0) {
+                dst[HD] = s_m[g];
+                dst[HD + 1] = s_l[g];
+            }
         }
     }
 }
 
 template <int HD>
 __global__ void decode_combine_kernel(const DecodeAttnArgs a) {
+    pdl_launch();
+    pdl_wait();
     const int i = blockIdx.y, h = blockIdx.x;
     const int stride = HD + 2;
     for (int d = threadIdx.x; d < HD; d += blockDim.x) {
@@ -348,8 +399,7 @@ cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
     }
     dim3 grid((a.max_len + PQ - 1) / PQ, a.nq, a.batch);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
-    prefill_attn_kernel<HD><<<grid, 128, smem, st>>>(a, scale_log2);
-    count_launches(1);
+    HRA_LAUNCH(prefill_attn_kernel<HD>, dim3(grid), dim3(128), smem, st, a, scale_log2);
     return cudaGetLastError();
 }
 
@@ -357,12 +407,10 @@ template <int HD, int G>
 cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
     dim3 grid(a.splits, a.nkv, a.rows);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
-    decode_attn_kernel<HD, G><<<grid, 128, 0, st>>>(a, scale_log2);
-    count_launches(1);
+    HRA_LAUNCH(decode_attn_kernel<HD, G>, dim3(grid), dim3(128), 0, st, a, scale_log2);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<HD><<<dim3(a.nq, a.rows), HD, 0, st>>>(a);
-    count_launches(1);
+    HRA_LAUNCH(decode_combine_kernel<HD>, dim3(dim3(a.nq, a.rows)), dim3(HD), 0, st, a);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,36 @@ __device__ __forceinline__ float csum_warp(float s, float c) {
     return __fadd_rn(s, c);
 }
 
+// Block-wide version (blockDim.x a multiple of 32, at most 1024): every thread gets fl(s + c).
+__device__ __forceinline__ float csum_block(float s, float c) {
+    __shared__ float sh_s[32], sh_c[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, e;
+        two_sum(s, s2, t, e);
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, c2), e);
+    }
+    if (lane == 0) {
+        sh_s[warp] = s;
+        sh_c[warp] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        s = lane < nw ? sh_s[lane] : 0.f;
+        c = lane < nw ? sh_c[lane] : 0.f;
+        const float tot = csum_warp(s, c);
+        if (lane == 0) sh_s[0] = tot;
+    }
+    __syncthreads();
+    const float r = sh_s[0];
+    __syncthreads();
+    return r;
+}
+
 __device__ __forceinline__ void raise_error(unsigned int* err, unsigned int bit) {
     if (err != nullptr) atomicOr(err, bit);
 }
@@ -86,6 +116,14 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
     return u;
 }
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialization: the next kernel
+// may be scheduled while this one runs, and each kernel waits (pdl_wait) before it touches memory
+// that an earlier kernel in the stream writes or reads.  pdl_launch lets the next kernel start its
+// own set-up as early as possible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------------ shared memory / mbarrier
 
@@ -239,6 +277,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Load 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // ------------------------------------------------------------------ legacy warp-level MMA helpers

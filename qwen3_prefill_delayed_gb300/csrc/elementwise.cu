@@ -6,9 +6,10 @@
 //                     termination and prefill", Summary: embedding lookup)
 //   rmsnorm           RMSNorm of rows (optionally gathered), or a plain row gather
 //   qk_rope_kv        per-head q/k RMSNorm + rotate-half RoPE, q to scratch, K/V into the cache
+//                     (half a warp per head)
 //                     (same page: "q/k norm + RoPE, and KV writes"; "fp8_chain.py": keys in host
 //                     rotate-half layout in the cache)
-// One warp per row (or per row x head); 16-byte vector loads; warp-shuffle reductions.
+// One warp per row (half a warp per row x head); 16-byte vector loads; shuffle reductions.
 #include "internal.h"
 
 namespace hra {
@@ -16,7 +17,10 @@ namespace hra {
 namespace {
 
 __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq, int32_t* row_pos,
-                                    int32_t* cu, int32_t* last_row) {
+                                    int32_t* cu, int32_t* last_row, unsigned int* err) {
+    pdl_launch();
+    pdl_wait();
+    if (err != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err = 0u;   // first kernel of a call
     __shared__ int32_t s_vals[kMaxBatch + 1];
     const int B = meta.batch;
     const int nvals = meta.mode == 0 ? B + 1 : B;
@@ -53,6 +57,8 @@ __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq,
 
 __global__ void rope_table_kernel(int n_rows, const int32_t* __restrict__ pos_of_row, int hd, double theta,
                                   float2* __restrict__ table) {
+    pdl_launch();
+    pdl_wait();
     const int half = hd / 2;
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_rows * half) return;
@@ -69,6 +75,8 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
                                      const bf16* __restrict__ embed, int vocab, const bf16* __restrict__ g,
                                      bf16* __restrict__ r, bf16* __restrict__ y, int rows, int H, float eps,
                                      unsigned int* err) {
+    pdl_launch();
+    pdl_wait();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -107,6 +115,8 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
 __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ idx,
                                const bf16* __restrict__ g, bf16* __restrict__ y, bf16* __restrict__ copy_out,
                                int rows, int H, float eps) {
+    pdl_launch();
+    pdl_wait();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -141,77 +151,93 @@ __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __rest
     }
 }
 
-// One warp per (row, head) over the nq + 2 nkv heads of the merged QKV row.  Lane l holds head
-// elements [l*E, l*E + E); the RoPE partner of element i < hd/2 is i + hd/2, held by lane l ^ 16.
+// Half a warp per (row, head) over the nq + 2 nkv heads of the merged QKV row.  Lane l of a
+// half-warp holds head elements [l*E, l*E + E) (E = hd/16, one 16- or 8-byte load); the RoPE partner
+// of element i < hd/2 is i + hd/2, held by lane l ^ 8 of the same half-warp.
 template <int HD>
 __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
-    constexpr int E = HD / 32;
+    pdl_launch();
+    pdl_wait();
+    constexpr int E = HD / 16;
     constexpr int HALF = HD / 2;
     const int heads = a.nq + 2 * a.nkv;
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (gw >= (long long)a.rows * heads) return;
-    const int row = (int)(gw / heads), hh = (int)(gw % heads);
-    const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + lane * E;
-    const int seq = a.row_seq[row], pos = a.row_pos[row];
-    const long long head_stride = (long long)a.n_slots * HD;
+    const long long total = (long long)a.rows * heads;
+    const long long hw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+    const int sub = threadIdx.x & 15;
+    const bool valid = hw < total;
+    const int row = valid ? (int)(hw / heads) : 0;
+    const int hh = valid ? (int)(hw % heads) : 0;
+    const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + sub * E;
 
     float x[E];
-    if constexpr (E == 4) {
-        const uint2 u = *reinterpret_cast<const uint2*>(src);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-        x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+    if (valid) {
+        if constexpr (E == 8) {
+            unpack8(*reinterpret_cast<const uint4*>(src), x);
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(src);
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+            const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+            x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
+        }
     } else {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src));
-        x[0] = f0.x; x[1] = f0.y;
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = 0.f;
     }
-
-    if (hh >= a.nq + a.nkv) {   // V head: copied into the cache as is
-        const int j = hh - a.nq - a.nkv;
-        bf16* dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * head_stride + (long long)pos * HD + lane * E;
-        if constexpr (E == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
-        else *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
-        return;
-    }
+    const int seq = valid ? a.row_seq[row] : 0, pos = valid ? a.row_pos[row] : 0;
+    const long long head_stride = (long long)a.n_slots * HD;
+    const bool is_v = hh >= a.nq + a.nkv;
     const bool is_q = hh < a.nq;
-    const bf16* gain = (is_q ? a.q_norm : a.k_norm) + lane * E;
+
+    // compensated sum of squares over the 16 lanes of this half-warp (all lanes take part)
     float ss = 0.f, sc = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) csum_add(ss, sc, __fmul_rn(x[e], x[e]));
-    ss = csum_warp(ss, sc);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, ss, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, sc, o);
+        float t, er;
+        two_sum(ss, s2, t, er);
+        ss = t;
+        sc = __fadd_rn(__fadd_rn(sc, c2), er);
+    }
+    ss = __fadd_rn(ss, sc);
     const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+    const bf16* gain = (is_q ? a.q_norm : a.k_norm) + sub * E;
     float xn[E], pn[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) xn[e] = __fmul_rn(__fmul_rn(x[e], inv), bf2f(gain[e]));
+    for (int e = 0; e < E; ++e) xn[e] = is_v ? 0.f : __fmul_rn(__fmul_rn(x[e], inv), bf2f(gain[e]));
 #pragma unroll
-    for (int e = 0; e < E; ++e) pn[e] = __shfl_xor_sync(0xffffffffu, xn[e], 16);
+    for (int e = 0; e < E; ++e) pn[e] = __shfl_xor_sync(0xffffffffu, xn[e], 8);
+    if (!valid) return;
+    bf16* dst;
+    if (is_v) {
+        dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride + (long long)pos * HD + sub * E;
+        if constexpr (E == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+        return;
+    }
     const int trow = a.rope_row_is_pos ? pos : row;
     const float2* cs = a.rope + (long long)trow * HALF;
     float out[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        const int i = (lane * E + e) % HALF;
+        const int i = (sub * E + e) % HALF;
         const float2 c = cs[i];   // (cos, sin)
-        if (lane < 16)   // first half: a*cos - b*sin with a = own, b = partner
+        if (sub < 8)   // first half: a*cos - b*sin with a = own, b = partner
             out[e] = __fsub_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
-        else             // second half: b*cos + a*sin with b = own, a = partner
+        else           // second half: b*cos + a*sin with b = own, a = partner
             out[e] = __fadd_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
     }
-    bf16* dst;
-    if (is_q) {
-        dst = a.q_out + ((long long)row * a.nq + hh) * HD + lane * E;
+    if (is_q) dst = a.q_out + ((long long)row * a.nq + hh) * HD + sub * E;
+    else dst = a.kv_layer + ((long long)(seq * 2) * a.nkv + (hh - a.nq)) * head_stride + (long long)pos * HD + sub * E;
+    if constexpr (E == 8) {
+        *reinterpret_cast<uint4*>(dst) = pack8(out);
     } else {
-        const int j = hh - a.nq;
-        dst = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * head_stride + (long long)pos * HD + lane * E;
-    }
-    if constexpr (E == 4) {
         uint2 u;
         *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(out[0], out[1]);
         *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(out[2], out[3]);
         *reinterpret_cast<uint2*>(dst) = u;
-    } else {
-        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(out[0], out[1]);
     }
 }
 
@@ -222,19 +248,18 @@ inline unsigned blocks_for(long long threads, int per_block) {
 }  // namespace
 
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
-                                int32_t* cu, int32_t* last_row, cudaStream_t st) {
+                                int32_t* cu, int32_t* last_row, unsigned int* err, cudaStream_t st) {
     const int threads = 256;
     const unsigned blocks = blocks_for(total_rows > 0 ? total_rows : 1, threads);
-    build_rowmap_kernel<<<blocks, threads, 0, st>>>(meta, total_rows, row_seq, row_pos, cu, last_row);
-    count_launches(1);
+    HRA_LAUNCH(build_rowmap_kernel, dim3(blocks), dim3(threads), 0, st, meta, total_rows, row_seq, row_pos, cu, last_row,
+               err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
                               float2* table, cudaStream_t st) {
     const long long n = (long long)n_rows * (head_dim / 2);
-    rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(n_rows, pos_of_row, head_dim, theta, table);
-    count_launches(1);
+    HRA_LAUNCH(rope_table_kernel, dim3(blocks_for(n, 256)), dim3(256), 0, st, n_rows, pos_of_row, head_dim, theta, table);
     return cudaGetLastError();
 }
 
@@ -242,28 +267,25 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_
                                  const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
                                  bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
                                  cudaStream_t st) {
-    embed_rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(
+    HRA_LAUNCH(embed_rmsnorm_kernel, dim3(blocks_for((long long)rows * 32, 256)), dim3(256), 0, st, 
         tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err);
-    count_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf16* y, bf16* copy_out,
                            int rows, int H, float eps, cudaStream_t st) {
-    rmsnorm_kernel<<<blocks_for((long long)rows * 32, 256), 256, 0, st>>>(x, idx, g, y, copy_out, rows, H,
+    HRA_LAUNCH(rmsnorm_kernel, dim3(blocks_for((long long)rows * 32, 256)), dim3(256), 0, st, x, idx, g, y, copy_out, rows, H,
                                                                         eps);
-    count_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st) {
-    const long long warps = (long long)a.rows * (a.nq + 2 * a.nkv);
-    const unsigned blocks = blocks_for(warps * 32, 256);
-    if (a.hd == 128) qk_rope_kv_kernel<128><<<blocks, 256, 0, st>>>(a);
-    else if (a.hd == 64) qk_rope_kv_kernel<64><<<blocks, 256, 0, st>>>(a);
+    const long long halves = (long long)a.rows * (a.nq + 2 * a.nkv);
+    const unsigned blocks = blocks_for(halves * 16, 256);
+    if (a.hd == 128) HRA_LAUNCH(qk_rope_kv_kernel<128>, dim3(blocks), dim3(256), 0, st, a);
+    else if (a.hd == 64) HRA_LAUNCH(qk_rope_kv_kernel<64>, dim3(blocks), dim3(256), 0, st, a);
     else return cudaErrorInvalidValue;
-    count_launches(1);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace hra

@@ -21,6 +21,7 @@
 #include <algorithm>
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <unordered_map>
 
 #include "internal.h"
 
@@ -47,6 +48,12 @@ struct GemmArgs {
     int mode;
     int mt, nt, splits;       // tile grid: M tiles, N tiles, K splits
     int group;                // N tiles per raster band
+    // last-round split: tiles [head_units, mt*nt) run as tail_splits K pieces each, written as fp32
+    // tile partials [piece][tile - head_units][BM][BN] to tail_part (0 tail tiles = off)
+    int head_units, tail_tiles, tail_splits, kb_per_tail;
+    float* tail_part;
+    unsigned int* zero_ptr;   // CTA 0 clears zero_words words here once earlier kernels are done
+    int zero_words;
 };
 
 template <int BN>
@@ -104,12 +111,41 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m_blk
     n_blk = band * p.group + within / p.mt;
 }
 
+// Linear tile index of (mb, nb) in the raster order of unit_coords.
+__device__ __forceinline__ int tile_linear(int mb, int nb, const GemmArgs& p) {
+    const int band = nb / p.group;
+    return band * p.group * p.mt + (nb - band * p.group) * p.mt + mb;
+}
+__device__ __forceinline__ int tail_index(int mb, int nb, const GemmArgs& p) {
+    return tile_linear(mb, nb, p) - p.head_units;
+}
+
+// Work unit u -> tile, K-block range and (for last-round pieces) the piece index (-1 otherwise).
+__device__ __forceinline__ void unit_work(int u, const GemmArgs& p, int& mb, int& nb, int& kb0, int& kb1,
+                                          int& piece) {
+    if (p.tail_tiles > 0 && u >= p.head_units) {
+        const int v = u - p.head_units;
+        piece = v / p.tail_tiles;
+        int sp;
+        unit_coords(p.head_units + (v - piece * p.tail_tiles), p, mb, nb, sp);
+        kb0 = piece * p.kb_per_tail;
+        kb1 = min(p.n_kb, kb0 + p.kb_per_tail);
+        return;
+    }
+    int sp;
+    unit_coords(u, p, mb, nb, sp);
+    piece = -1;
+    kb0 = sp * p.kb_per_split;
+    kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+}
+
 // Persistent: each CTA walks work units blockIdx.x, blockIdx.x + gridDim.x, ...
 template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
     using C = Cfg<BN>;
+    pdl_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -120,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = p.mt * p.nt * p.splits;
+    const int units = p.tail_tiles > 0 ? p.head_units + p.tail_tiles * p.tail_splits : p.mt * p.nt * p.splits;
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + C::STAGES + s); };
@@ -156,45 +192,58 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer: one continuous stage ring across all of this CTA's units
+        auto load_w = [&](int s, int kx, int nb) {
+            if (SWIGLU) {
+                const int j0 = nb * (BN / 2);
+                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, j0);
+                tma_load_2d(b_tile(s) + C::B_BYTES / 2, &tmB, full_bar(s), kx, p.up_row0 + j0);
+            } else {
+                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, nb * BN);
+            }
+        };
+        // Weight tiles of the first ring stages do not depend on earlier kernels: fetch them before
+        // waiting for those kernels (the activation half of each stage follows after the wait).
+        int pre = 0;
+        for (int u = blockIdx.x; u < units && pre < C::STAGES; u += gridDim.x) {
+            int mb, nb, kb0, kb1, piece;
+            unit_work(u, p, mb, nb, kb0, kb1, piece);
+            for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+                mbar_expect_tx(full_bar(pre), C::STAGE_BYTES);
+                load_w(pre, kb * BK, nb);
+            }
+        }
+        pdl_wait();
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int mb, nb, sp;
-            unit_coords(u, p, mb, nb, sp);
-            const int kb0 = sp * p.kb_per_split;
-            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            int mb, nb, kb0, kb1, piece;
+            unit_work(u, p, mb, nb, kb0, kb1, piece);
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
-                    *abort_flag = 1;
-                    raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
                 const int kx = kb * BK;
-                tma_load_2d(a_tile(s), &tmA, full_bar(s), kx, mb * BM);
-                if (SWIGLU) {
-                    const int j0 = nb * (BN / 2);
-                    tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, j0);
-                    tma_load_2d(b_tile(s) + C::B_BYTES / 2, &tmB, full_bar(s), kx, p.up_row0 + j0);
-                } else {
-                    tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, nb * BN);
+                if (it >= pre) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    load_w(s, kx, nb);
                 }
+                tma_load_2d(a_tile(s), &tmA, full_bar(s), kx, mb * BM);
             }
         }
-        *issued_slot = it;
+        *issued_slot = ok ? it : max(it, pre);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer: accumulator buffer j % 2 for this CTA's j-th unit
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
         int it = 0, j = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
-            int mb, nb, sp;
-            unit_coords(u, p, mb, nb, sp);
-            const int kb0 = sp * p.kb_per_split;
-            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            int mb, nb, kb0, kb1, piece;
+            unit_work(u, p, mb, nb, kb0, kb1, piece);
             const int buf = j & 1;
             const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
             if (!mbar_wait(tempty_bar(buf), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -225,11 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 2) {
         // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (one row per thread)
+        pdl_wait();
+        if (blockIdx.x == 0 && warp == 2)
+            for (int i = lane; i < p.zero_words; i += 32) p.zero_ptr[i] = 0u;
         const int quad = warp & 3;
         int j = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
-            int mb, nb, sp;
-            unit_coords(u, p, mb, nb, sp);
+            int mb, nb, kb0, kb1, piece;
+            unit_work(u, p, mb, nb, kb0, kb1, piece);
+            const int sp = piece < 0 ? u / (p.mt * p.nt) : 0;
             const int buf = j & 1;
             // warp-uniform decision: tcgen05.ld below is a .sync.aligned warp instruction
             const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
@@ -243,7 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = mb * BM + quad * 32 + lane;
             const bool row_ok = row < p.M;
             const long long split_off = (long long)sp * p.split_stride;
-            if (!SWIGLU) {
+            if (piece >= 0) {
+                // last-round K piece: raw fp32 tile [BM][BN] for the fix-up pass
+                float* dst = p.tail_part +
+                             ((long long)piece * p.tail_tiles + tail_index(mb, nb, p)) * (BM * BN) +
+                             (long long)(quad * 32 + lane) * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld32(tq + c, v);
+                    float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            } else if (!SWIGLU) {
                 const int n0 = nb * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
@@ -304,9 +370,304 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ small M: weights as the MMA rows
+// For M <= 64 activation rows the operands swap roles: a 128-row weight tile is the tcgen05 A
+// operand and the (zero-padded) activation rows are its N = NB columns, so no shared memory is
+// spent on empty activation rows and ~10 stages of weight tiles stay in flight per SM.  The
+// accumulator D[weight row][activation row] (NB columns) is written back transposed; a warp's
+// stores cover 32 consecutive output columns.  SwiGLU tiles hold 64 gate and 64 up rows and always
+// go through fp32 partials (the reduction applies the activation).
+template <int NB>
+struct SwCfg {
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = NB * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr uint32_t TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
+};
+
+struct SwArgs {
+    void* out;
+    unsigned int* err;
+    long long split_stride;
+    int M;           // activation rows (<= NB)
+    int n_valid;     // valid output columns (N, or F for SwiGLU)
+    int ldo;
+    int n_kb, kb_per_split;
+    int up_row0;     // SwiGLU: first up row in W (= F)
+    int mode;        // KM_STORE / KM_RESIDUAL / KM_F32 / KM_PARTIAL
+    int nt, splits;
+    unsigned int* zero_ptr;
+    int zero_words;
+};
+
+template <int NB, bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const SwArgs p) {
+    using C = SwCfg<NB>;
+    pdl_launch();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
+    int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = p.nt * p.splits;
+
+    auto full_bar = [&](int s) { return smem_u32(bars + s); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + C::STAGES + s); };
+    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + b); };
+    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + 2 + b); };
+    auto a_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
+    auto b_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);
+        }
+        *abort_flag = 0;
+        *issued_slot = 0;
+        *committed_slot = 0;
+        mbar_fence_init();
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        auto load_w = [&](int s, int kx, int nb) {
+            if (SWIGLU) {
+                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * 64);
+                tma_load_2d(a_tile(s) + C::A_BYTES / 2, &tmW, full_bar(s), kx, p.up_row0 + nb * 64);
+            } else {
+                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * 128);
+            }
+        };
+        // weight tiles of the first ring stages before waiting for earlier kernels
+        int pre = 0;
+        for (int u = blockIdx.x; u < units && pre < C::STAGES; u += gridDim.x) {
+            const int sp = u / p.nt, nb = u - sp * p.nt;
+            const int kb0 = sp * p.kb_per_split;
+            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+                mbar_expect_tx(full_bar(pre), C::STAGE_BYTES);
+                load_w(pre, kb * BK, nb);
+            }
+        }
+        pdl_wait();
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int sp = u / p.nt, nb = u - sp * p.nt;
+            const int kb0 = sp * p.kb_per_split;
+            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+                const int kx = kb * BK;
+                if (it >= pre) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    load_w(s, kx, nb);
+                }
+                tma_load_2d(b_tile(s), &tmX, full_bar(s), kx, 0);
+            }
+        }
+        *issued_slot = ok ? it : max(it, pre);
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
+        int it = 0, j = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+            const int sp = u / p.nt;
+            const int kb0 = sp * p.kb_per_split;
+            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+            const int buf = j & 1;
+            const uint32_t d_tmem = tmem + (uint32_t)(buf * NB);
+            if (!mbar_wait(tempty_bar(buf), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
+                *abort_flag = 1;
+                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+                if (!mbar_wait(full_bar(s), ph, abort_flag)) {
+                    *abort_flag = 1;
+                    raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sdesc_sw128(a_tile(s));
+                const uint64_t bd = sdesc_sw128(b_tile(s));
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                tc_commit(empty_bar(s));
+            }
+            tc_commit(tfull_bar(buf));
+            *committed_slot = j + 1;
+        }
+    } else if (warp >= 2) {
+        pdl_wait();
+        if (blockIdx.x == 0 && warp == 2)
+            for (int i = lane; i < p.zero_words; i += 32) p.zero_ptr[i] = 0u;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;   // weight row inside the tile
+        int j = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+            const int sp = u / p.nt, nb = u - sp * p.nt;
+            const int buf = j & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            int col;
+            bool col_ok;
+            if (SWIGLU) {
+                const int jj = nb * 64 + (r & 63);
+                col_ok = jj < p.n_valid;
+                col = r < 64 ? jj : p.up_row0 + jj;
+            } else {
+                col = nb * 128 + r;
+                col_ok = col < p.n_valid;
+            }
+            const long long split_off = (long long)sp * p.split_stride;
+            const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * NB);
+#pragma unroll
+            for (int c = 0; c < NB; c += 16) {
+                float v[16];
+                tmem_ld16(tq + c, v);
+                if (col_ok) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int b = c + q;
+                        if (b < p.M) {
+                            const long long off = (long long)b * p.ldo + col;
+                            if (p.mode == KM_PARTIAL || p.mode == KM_F32) {
+                                reinterpret_cast<float*>(p.out)[split_off + off] = v[q];
+                            } else if (p.mode == KM_RESIDUAL) {
+                                bf16* o = reinterpret_cast<bf16*>(p.out) + off;
+                                *o = f2bf(bf2f(*o) + v[q]);
+                            } else {
+                                reinterpret_cast<bf16*>(p.out)[off] = f2bf(v[q]);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane == 0) {
+        volatile int never = 0;
+        const int issued = *issued_slot;
+        for (int i = max(0, issued - C::STAGES); i < issued; ++i)
+            (void)mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, &never);
+        const int committed = *committed_slot;
+        for (int jj = max(0, committed - 2); jj < committed; ++jj)
+            (void)mbar_wait(tfull_bar(jj & 1), (uint32_t)(jj >> 1) & 1u, &never);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// Fix-up of the last-round K pieces: sum the pieces of each tail tile in piece order, then apply
+// the tile's epilogue.  One thread per 8 D-columns of one row (SwiGLU: 8 gate + the 8 matching up).
+__global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
+                                  int mt, int group, int BNt, int swiglu, int M, int n_valid, int ldo, int mode,
+                                  void* out) {
+    pdl_launch();
+    pdl_wait();
+    const int gw = swiglu ? BNt / 16 : BNt / 8;
+    const long long per_tile = (long long)BM * gw;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= per_tile * tail_tiles) return;
+    const int t = (int)(idx / per_tile);
+    const int rem = (int)(idx - (long long)t * per_tile);
+    const int r = rem / gw, cg = (rem - r * gw) * 8;
+    // tile (mb, nb) from the raster order
+    const int lin = head_units + t;
+    const int band_units = group * mt;
+    const int band = lin / band_units;
+    const int within = lin - band * band_units;
+    const int mb = within % mt, nb = band * group + within / mt;
+    const int row = mb * BM + r;
+    if (row >= M) return;
+    float a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int pc = 0; pc < pieces; ++pc) {
+        const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)r * BNt + cg;
+        const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
+        a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w; a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+        if (swiglu) {
+            const float4 y0 = *reinterpret_cast<const float4*>(src + BNt / 2);
+            const float4 y1 = *reinterpret_cast<const float4*>(src + BNt / 2 + 4);
+            u[0] += y0.x; u[1] += y0.y; u[2] += y0.z; u[3] += y0.w; u[4] += y1.x; u[5] += y1.y; u[6] += y1.z; u[7] += y1.w;
+        }
+    }
+    const int col = swiglu ? nb * (BNt / 2) + cg : nb * BNt + cg;
+    if (col >= n_valid) return;
+    const long long o = (long long)row * ldo + col;
+    if (mode == KM_F32) {
+        float4* q = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o);
+        q[0] = make_float4(a[0], a[1], a[2], a[3]);
+        q[1] = make_float4(a[4], a[5], a[6], a[7]);
+        return;
+    }
+    uint4* q = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(out) + o);
+    if (swiglu) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = silu_f(round_bf(a[j])) * round_bf(u[j]);
+    } else if (mode == KM_RESIDUAL) {
+        float rr[8];
+        unpack8(*q, rr);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = rr[j] + a[j];
+    }
+    *q = pack8(a);
+}
+
 // Sum of split partials in split order, then the epilogue.  One thread per 8 output columns.
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long split_stride,
                                      int M, int n_out, int ldp, int up_off, int mode, void* out, int ldo) {
+    pdl_launch();
+    pdl_wait();
     const int groups = n_out >> 3;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)M * groups) return;
@@ -347,6 +708,64 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
     *q = pack8(a);
 }
 
+// Split-K reduction fused with the residual add and the RMSNorm that follows it (small M): one CTA
+// per row, one thread per group of 8 columns (blockDim = groups rounded up to a warp), all split
+// loads issued before the sum (split order kept); writes r = bf16(r + acc), then y = RMSNorm(r) * g
+// with the compensated sum of squares of the rounded residual.
+constexpr int kNormMaxThreads = 1024;
+constexpr int kNormMaxSplits = 8;
+__global__ void __launch_bounds__(kNormMaxThreads) splitk_residual_norm_kernel(
+    const float* __restrict__ part, int splits, long long split_stride, int N, bf16* __restrict__ r,
+    const bf16* __restrict__ gain, bf16* __restrict__ y, float eps) {
+    pdl_launch();
+    pdl_wait();
+    const int row = blockIdx.x;
+    const int groups = N >> 3;
+    const int gi = threadIdx.x;
+    const bool active = gi < groups;
+    const int col = gi * 8;
+    float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float ss = 0.f, sc = 0.f;
+    if (active) {
+        float4 x0[kNormMaxSplits], x1[kNormMaxSplits];
+#pragma unroll
+        for (int s = 0; s < kNormMaxSplits; ++s) {
+            if (s < splits) {
+                const float* p = part + s * split_stride + (long long)row * N + col;
+                x0[s] = *reinterpret_cast<const float4*>(p);
+                x1[s] = *reinterpret_cast<const float4*>(p + 4);
+            }
+        }
+        uint4* rp = reinterpret_cast<uint4*>(r + (long long)row * N + col);
+        float rr[8];
+        unpack8(*rp, rr);
+        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int s = 0; s < kNormMaxSplits; ++s) {
+            if (s < splits) {
+                a[0] += x0[s].x; a[1] += x0[s].y; a[2] += x0[s].z; a[3] += x0[s].w;
+                a[4] += x1[s].x; a[5] += x1[s].y; a[6] += x1[s].z; a[7] += x1[s].w;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = rr[e] + a[e];
+        const uint4 packed = pack8(a);
+        *rp = packed;
+        unpack8(packed, v);   // the bf16-rounded residual is what the norm sees
+#pragma unroll
+        for (int e = 0; e < 8; ++e) csum_add(ss, sc, __fmul_rn(v[e], v[e]));
+    }
+    const float tot = csum_block(ss, sc);
+    const float inv = 1.0f / sqrtf(tot / (float)N + eps);
+    if (active) {
+        float w[8];
+        unpack8(*reinterpret_cast<const uint4*>(gain + col), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (v[e] * inv) * w[e];
+        *reinterpret_cast<uint4*>(y + (long long)row * N + col) = pack8(v);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -365,7 +784,7 @@ bool get_encoder() {
 }
 
 // Row-major bf16 matrix [rows, cols] viewed as a 2-D tensor (cols innermost), boxes of 64 x box_rows.
-bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+bool encode_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
@@ -375,12 +794,65 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps describe only (address, shape, box), so an encoded map is reused whenever the same
+// matrix is seen again (weights every call, workspace buffers every layer).
+struct MapKey {
+    const void* base;
+    int rows, cols, box_rows;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        size_t h = std::hash<const void*>()(k.base);
+        h ^= (size_t)k.rows * 0x9E3779B97F4A7C15ull + (size_t)k.cols * 0xC2B2AE3D27D4EB4Full + (size_t)k.box_rows;
+        return h;
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    const MapKey key{base, rows, cols, box_rows};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *m = it->second;
+            return true;
+        }
+    }
+    if (!encode_map(m, base, rows, cols, box_rows)) return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 8192) g_maps.clear();
+    g_maps.emplace(key, *m);
+    return true;
+}
+
 struct Plan {
     int bn;
     int splits;
     int kbps;
     int mt, nt;
+    int head_units = 0, tail_tiles = 0, tail_splits = 1, kb_per_tail = 0;
 };
+
+// Last-round split: when the final round of tiles fills at most half the SMs, each of its tiles is
+// cut into up to 4 K pieces that run on the SMs that would otherwise idle.
+void plan_tail(Plan& pl, int n_kb, int nsm) {
+    const long long units = (long long)pl.mt * pl.nt;
+    const long long rounds = (units + nsm - 1) / nsm;
+    const long long tail = units - (rounds - 1) * nsm;
+    if (pl.splits != 1 || rounds < 2 || tail * 2 > nsm) return;
+    int S = (int)std::min<long long>(4, nsm / tail);
+    while (S > 1 && n_kb < 2 * S) --S;
+    if (S < 2) return;
+    pl.head_units = (int)((rounds - 1) * nsm);
+    pl.tail_tiles = (int)tail;
+    pl.tail_splits = S;
+    pl.kb_per_tail = (n_kb + S - 1) / S;
+}
 
 // Choose the tile width and K split.  The kernel is persistent (one CTA per SM walking work
 // units), so the grid runs in ceil(units / SMs) rounds; per-unit time ~ (K blocks) x BN (bytes
@@ -403,11 +875,19 @@ Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm) {
             const int splits = (n_kb + kbps - 1) / kbps;
             const long long units = (long long)mt * nt * splits;
             const long long rounds = (units + nsm - 1) / nsm;
-            double cost = (double)rounds * (kbps * (bn / 256.0) + 0.5);
+            // K-block cost relative to a 256-wide tile: with one M tile the unit streams weights
+            // (cost ~ BN); with several, the 128-wide tile is bound by operand traffic into shared
+            // memory (measured 0.83 of the 256-wide tile's time for half its MMA work).
+            const double c_kb = bn == 256 ? 1.0 : (mt == 1 ? 0.5 : 0.83);
+            Plan cand{bn, splits, kbps, mt, nt};
+            plan_tail(cand, n_kb, nsm);
+            const double eff_rounds = cand.tail_tiles > 0 ? (double)(rounds - 1) + 1.0 / cand.tail_splits + 0.1
+                                                          : (double)rounds;
+            double cost = eff_rounds * (kbps * c_kb + 0.5);
             if (splits > 1) cost += 2.0;
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
-                best = Plan{bn, splits, kbps, mt, nt};
+                best = cand;
             }
         }
     }
@@ -430,9 +910,117 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     const long long units = (long long)pl.mt * pl.nt * pl.splits;
     const int nsm = device_sm_count();
     dim3 grid((unsigned)std::min<long long>(units, nsm));
-    gemm_bf16_tc_kernel<BN, SW><<<grid, kThreads, Cfg<BN>::SMEM, st>>>(ma, mb, g);
-    count_launches(1);
+    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ma, mb, g);
     return cudaGetLastError();
+}
+
+
+// ---- small-M (swap-AB) plan: units = N tiles x K splits over persistent CTAs; the per-SM critical
+// path is ceil(units / SMs) x (K blocks per unit), plus a small cost per extra split (partials).
+constexpr int kSmallM = 64;
+
+struct SmallPlan {
+    int nb;          // padded activation rows: 16, 32 or 64
+    int nt, splits, kbps;
+};
+
+SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) {
+    const int n_kb = K / BK;
+    const int per_tile = epi == EPI_SWIGLU ? 64 : 128;
+    const int nt = (N + per_tile - 1) / per_tile;
+    SmallPlan best{M <= 16 ? 16 : M <= 32 ? 32 : 64, nt, 1, n_kb};
+    double best_cost = 1e30;
+    for (int s = 1; s <= std::min(8, n_kb); ++s) {
+        if (split_req > 0 && s != std::min(split_req, std::min(8, n_kb))) continue;
+        const int kbps = (n_kb + s - 1) / s;
+        const int splits = (n_kb + kbps - 1) / kbps;
+        const long long units = (long long)nt * splits;
+        const long long rounds = (units + nsm - 1) / nsm;
+        const double cost = (double)rounds * (kbps + 0.75) + 0.05 * (splits - 1) * ((M + 15) / 16);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best.splits = splits;
+            best.kbps = kbps;
+        }
+    }
+    return best;
+}
+
+template <int NB, bool SW>
+cudaError_t launch_small(const CUtensorMap& mw, const CUtensorMap& mx, const SwArgs& a, int units, cudaStream_t st) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(gemm_smallm_kernel<NB, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SwCfg<NB>::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    dim3 grid((unsigned)std::min(units, device_sm_count()));
+    HRA_LAUNCH(gemm_smallm_kernel<NB, SW>, dim3(grid), dim3(kThreads), SwCfg<NB>::SMEM, st, mw, mx, a);
+    return cudaGetLastError();
+}
+
+// Reduction / epilogue pass shared by both GEMM paths once fp32 partials exist.
+cudaError_t reduce_partials(const LinearCall& c, int splits, int ldp, cudaStream_t st) {
+    const int mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : c.epi == EPI_SWIGLU ? KM_SWIGLU : KM_F32;
+    if (mode == KM_RESIDUAL && c.norm_out != nullptr && c.N <= 8 * kNormMaxThreads && splits <= kNormMaxSplits) {
+        const int threads = ((c.N / 8 + 31) / 32) * 32;
+        HRA_LAUNCH(splitk_residual_norm_kernel, dim3(c.M), dim3(threads), 0, st, c.partial, splits, (long long)c.M * ldp, c.N,
+                                                              reinterpret_cast<bf16*>(c.out), c.norm_gain,
+                                                              c.norm_out, c.norm_eps);
+        if (c.norm_done) *c.norm_done = true;
+        return cudaGetLastError();
+    }
+    const long long items = (long long)c.M * (c.N / 8);
+    const int threads = 256;
+    HRA_LAUNCH(splitk_reduce_kernel, dim3((unsigned)((items + threads - 1) / threads)), dim3(threads), 0, st, 
+        c.partial, splits, (long long)c.M * ldp, c.M, c.N, ldp, c.N, mode, c.out, c.N);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
+    const SmallPlan pl = make_small_plan(c.M, c.N, c.K, c.epi, c.split_req, device_sm_count());
+    const bool sw = c.epi == EPI_SWIGLU;
+    const int w_rows = sw ? 2 * c.N : c.N;
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, c.w, w_rows, c.K, sw ? 64 : 128)) return cudaErrorInvalidValue;
+    if (!make_map(&mx, c.a, c.M, c.K, pl.nb)) return cudaErrorInvalidValue;
+    // SwiGLU and every split go through fp32 partials; otherwise the epilogue writes the output.
+    const bool use_partial = sw || pl.splits > 1;
+    SwArgs a;
+    a.err = c.err;
+    a.M = c.M;
+    a.n_valid = c.N;
+    a.n_kb = c.K / BK;
+    a.kb_per_split = pl.kbps;
+    a.up_row0 = c.N;
+    a.nt = pl.nt;
+    a.splits = pl.splits;
+    a.zero_ptr = c.zero_ptr;
+    a.zero_words = c.zero_ptr ? c.zero_words : 0;
+    const int ldp = sw ? 2 * c.N : c.N;
+    if (use_partial) {
+        a.out = c.partial;
+        a.mode = KM_PARTIAL;
+        a.ldo = ldp;
+        a.split_stride = (long long)c.M * ldp;
+    } else {
+        a.out = c.out;
+        a.mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : KM_F32;
+        a.ldo = c.N;
+        a.split_stride = 0;
+    }
+    const int units = pl.nt * pl.splits;
+    cudaError_t e;
+    if (pl.nb == 16) e = sw ? launch_small<16, true>(mw, mx, a, units, st) : launch_small<16, false>(mw, mx, a, units, st);
+    else if (pl.nb == 32) e = sw ? launch_small<32, true>(mw, mx, a, units, st) : launch_small<32, false>(mw, mx, a, units, st);
+    else e = sw ? launch_small<64, true>(mw, mx, a, units, st) : launch_small<64, false>(mw, mx, a, units, st);
+    if (c.splits_used) *c.splits_used = use_partial ? pl.splits : 1;
+    if (e != cudaSuccess || !use_partial || c.partial_only) return e;
+    return reduce_partials(c, pl.splits, ldp, st);
 }
 
 }  // namespace
@@ -450,11 +1038,20 @@ int device_sm_count() {
 }
 
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req) {
+    if (M <= kSmallM) {
+        const SmallPlan sp = make_small_plan(M, N, K, epi, split_req, device_sm_count());
+        if (sp.splits <= 1 && epi != EPI_SWIGLU) return 0;
+        const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
+        return (size_t)sp.splits * (size_t)M * ldp * sizeof(float);
+    }
     const Plan pl = make_plan(M, N, K, epi, split_req, device_sm_count());
+    if (pl.tail_tiles > 0) return (size_t)pl.tail_splits * pl.tail_tiles * BM * pl.bn * sizeof(float);
     if (pl.splits <= 1) return 0;
     const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
     return (size_t)pl.splits * (size_t)M * ldp * sizeof(float);
 }
+
+size_t linear_tail_bound() { return (size_t)device_sm_count() * BM * 256 * sizeof(float); }
 
 size_t linear_partial_bound(int m_max, int N, int K, int epi) {
     if (m_max > BM) m_max = BM;
@@ -464,8 +1061,10 @@ size_t linear_partial_bound(int m_max, int N, int K, int epi) {
 
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     if (!get_encoder()) return cudaErrorNotSupported;
+    if (c.M <= kSmallM) return launch_linear_small(c, st);
     const int nsm = device_sm_count();
-    const Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm);
+    Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm);
+    if (c.partial_only) pl.tail_tiles = 0;   // the caller reads one output plane from the partial buffer
     const bool sw = c.epi == EPI_SWIGLU;
     const int w_rows = sw ? 2 * c.N : c.N;
 
@@ -484,6 +1083,13 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     g.nt = pl.nt;
     g.splits = pl.splits;
     g.group = 8;
+    g.head_units = pl.head_units;
+    g.tail_tiles = pl.tail_tiles;
+    g.tail_splits = pl.tail_splits;
+    g.kb_per_tail = pl.kb_per_tail;
+    g.tail_part = c.partial;
+    g.zero_ptr = c.zero_ptr;
+    g.zero_words = c.zero_ptr ? c.zero_words : 0;
     if (pl.splits > 1) {
         g.out = c.partial;
         g.mode = KM_PARTIAL;
@@ -502,14 +1108,29 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     else
         e = sw ? launch_tile<128, true>(ma, mb, g, pl, st) : launch_tile<128, false>(ma, mb, g, pl, st);
     if (c.splits_used) *c.splits_used = pl.splits;
+    if (e == cudaSuccess && pl.tail_tiles > 0) {
+        const int gw = sw ? pl.bn / 16 : pl.bn / 8;
+        const long long items = (long long)pl.tail_tiles * BM * gw;
+        HRA_LAUNCH(tail_fixup_kernel, dim3((unsigned)((items + 255) / 256)), dim3(256), 0, st, 
+            c.partial, pl.tail_splits, pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, sw ? 1 : 0, c.M, c.N, c.N,
+            g.mode, c.out);
+        return cudaGetLastError();
+    }
     if (e != cudaSuccess || pl.splits <= 1 || c.partial_only) return e;
 
     const int mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : c.epi == EPI_SWIGLU ? KM_SWIGLU : KM_F32;
+    if (mode == KM_RESIDUAL && c.norm_out != nullptr && c.N <= 8 * kNormMaxThreads && pl.splits <= kNormMaxSplits) {
+        const int threads = ((c.N / 8 + 31) / 32) * 32;
+        HRA_LAUNCH(splitk_residual_norm_kernel, dim3(c.M), dim3(threads), 0, st, c.partial, pl.splits, (long long)c.M * g.ldo, c.N,
+                                                              reinterpret_cast<bf16*>(c.out), c.norm_gain,
+                                                              c.norm_out, c.norm_eps);
+        if (c.norm_done) *c.norm_done = true;
+        return cudaGetLastError();
+    }
     const long long items = (long long)c.M * (c.N / 8);
     const int threads = 256;
-    splitk_reduce_kernel<<<(unsigned)((items + threads - 1) / threads), threads, 0, st>>>(
+    HRA_LAUNCH(splitk_reduce_kernel, dim3((unsigned)((items + threads - 1) / threads)), dim3(threads), 0, st, 
         c.partial, pl.splits, (long long)c.M * g.ldo, c.M, c.N, g.ldo, c.N, mode, c.out, c.N);
-    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace hra {
@@ -14,6 +16,31 @@ int device_sm_count();
 
 // Host-side count of kernel launches issued by the library.
 void count_launches(int n);
+
+// Launch with programmatic stream serialization (see pdl_wait / pdl_launch in common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launches(1);
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Launch through launch_pdl and return the error from the enclosing function if it fails.
+#define HRA_LAUNCH(...)                                  \
+    do {                                                 \
+        cudaError_t hra_e_ = ::hra::launch_pdl(__VA_ARGS__); \
+        if (hra_e_ != cudaSuccess) return hra_e_;        \
+    } while (0)
 
 // ------------------------------------------------------------------ projection GEMM
 enum EpiMode : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
@@ -31,11 +58,22 @@ struct LinearCall {
     unsigned int* err;     // sticky device error word
     bool partial_only;     // leave the split partials unreduced (EPI_F32 only; out == partial)
     int* splits_used;      // optional: receives the number of K splits launched
+    // EPI_RESIDUAL only: when the plan splits K, the reduction also writes
+    // norm_out = RMSNorm(out) * norm_gain (one CTA per row) and sets *norm_done.
+    const bf16* norm_gain;
+    bf16* norm_out;
+    float norm_eps;
+    bool* norm_done;
+    // CTA 0 clears zero_words words at zero_ptr after earlier kernels finished (0 = none)
+    unsigned int* zero_ptr;
+    int zero_words;
 };
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req);
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st);
 // Largest partial buffer any automatic plan with M <= m_max rows and these N, K can ask for.
 size_t linear_partial_bound(int m_max, int N, int K, int epi);
+// Largest last-round piece buffer any plan with more than one M tile can ask for.
+size_t linear_tail_bound();
 
 // ------------------------------------------------------------------ row bookkeeping + norms + RoPE
 constexpr int kMaxBatch = 512;
@@ -48,9 +86,9 @@ struct SeqMeta {
 };
 
 // Writes row_seq[T], row_pos[T] (sequence index and position of each packed row), and for prefill
-// cu[batch+1], last_row[batch]; for decode last_row[b] = b.
+// cu[batch+1], last_row[batch]; for decode last_row[b] = b.  Also clears the call's error word.
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
-                                int32_t* cu, int32_t* last_row, cudaStream_t st);
+                                int32_t* cu, int32_t* last_row, unsigned int* err, cudaStream_t st);
 
 // cos/sin table [n_rows][head_dim/2] (float2), row r at position pos_of_row[r] (or r when null).
 cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
@@ -115,6 +153,8 @@ cudaError_t launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t st);
 // ------------------------------------------------------------------ codebook step finalize
 struct CodebookArgs {
     const float* partial;   // [splits][batch][K * Vc] fp32 logits partials
+    int* counters;          // [batch], zero on entry: CTAs of a row that have finished their argmax
+    int* cand;              // [batch][K] argmax of each codebook
     int splits;
     const float* eoc_bias;  // [batch, K] or null
     const bf16* code_emb;   // [K][Vc][H]

@@ -31,11 +31,17 @@ CASES = [
     (1000, 1040, 512, "store", 0),
     (1, 6144, 2560, "store", 3),
     (8, 2560, 2560, "residual", 5),
+    (100, 2560, 2560, "residual", 3),
+    (33, 1040, 640, "store", 0),
+    (48, 768, 256, "swiglu", 2),
     (64, 2560, 4096, "residual", 0),
     (517, 2560, 9728, "residual", 0),
     (300, 768, 256, "swiglu", 0),
     (8, 9728, 2560, "swiglu", 0),
     (130, 1000, 512, "swiglu", 0),
+    (4255, 2560, 2560, "residual", 0),     # 340 tiles: the last round runs as 4 K pieces per tile
+    (4255, 2560, 1024, "swiglu", 0),       # 680 tiles: last round in 2 K pieces
+    (4255, 2560, 640, "store", 0),
     (3, 4104, 256, "f32", 0),
     (64, 8208, 2560, "f32", 0),
     (64, 8208, 2560, "f32", 7),
