@@ -79,7 +79,7 @@ struct Layout {
 
 bool dims_ok(const hra_dims* d) {
     if (d == nullptr) return false;
-    if (d->n_layers < 1 || d->hidden < 64 || d->hidden % 64 != 0) return false;
+    if (d->n_layers < 1 || d->hidden < 64 || d->hidden > 4096 || d->hidden % 64 != 0) return false;
     if (d->head_dim != 64 && d->head_dim != 128) return false;
     if (d->n_q_heads < 1 || d->n_kv_heads < 1 || d->n_q_heads % d->n_kv_heads != 0) return false;
     const int g = d->n_q_heads / d->n_kv_heads;
@@ -191,7 +191,7 @@ bool layer_ptrs_ok(const hra_layer_weights& l) {
 // `attn_last_only` switches the tail to the B-row path (prefill's last layer).
 int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
                int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
-               const int32_t* seq_lens_host, cudaStream_t st) {
+               const int32_t* seq_lens_host, int max_pos, cudaStream_t st) {
     const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d.rms_eps;
@@ -252,12 +252,12 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
                 da.out = att;
                 da.part = P.at<float>(L.apart);
                 da.rows = rows;
-                da.max_pos = kv.n_slots - 1;
+                da.max_pos = max_pos;
                 da.n_slots = kv.n_slots;
                 da.nq = nq;
                 da.nkv = nkv;
                 da.hd = hd;
-                da.splits = L.attn_splits;
+                da.splits = std::min(L.attn_splits, decode_attention_splits(rows, nkv, max_pos));
                 HRA_TRY(launch_decode_attention(da, st));
             }
             const int pc = prefill ? 1 : 0;
@@ -389,7 +389,7 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
                                  P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
     return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
                       (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), seq_lens,
-                      st);
+                      max_len - 1, st);
 }
 
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots) {
@@ -412,9 +412,11 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
     SeqMeta meta{};
     meta.batch = batch;
     meta.mode = 1;
+    int max_pos = 0;
     for (int b = 0; b < batch; ++b) {
         if (pos[b] < 0 || pos[b] >= kv->n_slots) return HRA_ERR_RANGE;
         meta.vals[b] = pos[b];
+        max_pos = std::max(max_pos, (int)pos[b]);
     }
     const Layout L = backbone_layout(d, batch, batch, batch, kv->n_slots - 1);
     if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
@@ -430,7 +432,7 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                            reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.y),
                            P.at<bf16>(L.r), batch, d.hidden, d.rms_eps, st));
     return run_layers(d, *weights, *kv, P, L, batch, batch, 0, false, false, reinterpret_cast<bf16*>(hidden_dev),
-                      nullptr, st);
+                      nullptr, max_pos, st);
 }
 
 // Codebook-step workspace: error word and per-row counters (cleared by the GEMM), per-row argmax

@@ -343,12 +343,17 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a
         }
         __syncthreads();
     }
-    // partial (o unnormalised, m, l) of this split
+    // one split: the normalised output directly; several: partial (o unnormalised, m, l)
     const int stride = HD + 2;
 #pragma unroll
     for (int r = 0; r < (G + 3) / 4; ++r) {
         const int g = warp + 4 * r;
-        if (g < G) {
+        if (g < G && a.splits == 1) {
+            const float il = 1.0f / s_l[g];
+            bf16* dst = a.out + ((long long)i * a.nq + j * G + g) * HD + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[e] = f2bf(o[r][e] * il);
+        } else if (g < G) {
             float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + g) * stride;
 #pragma unroll
             for (int e = 0; e < E; ++e) dst[lane * E + e] = o[r][e];
@@ -408,8 +413,7 @@ cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
     dim3 grid(a.splits, a.nkv, a.rows);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
     HRA_LAUNCH(decode_attn_kernel<HD, G>, dim3(grid), dim3(128), 0, st, a, scale_log2);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (a.splits == 1) return cudaSuccess;
     HRA_LAUNCH(decode_combine_kernel<HD>, dim3(dim3(a.nq, a.rows)), dim3(HD), 0, st, a);
     return cudaGetLastError();
 }
@@ -433,6 +437,7 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st) 
     return cudaErrorInvalidValue;
 }
 
+// Enough (row, kv head, split) CTAs for two per SM, with at least 64 keys per split.
 int decode_attention_splits(int rows, int nkv, int max_pos) {
     const int target = 2 * device_sm_count();
     int s = (target + rows * nkv - 1) / (rows * nkv);

@@ -9,7 +9,9 @@
 //                     (half a warp per head)
 //                     (same page: "q/k norm + RoPE, and KV writes"; "fp8_chain.py": keys in host
 //                     rotate-half layout in the cache)
-// One warp per row (half a warp per row x head); 16-byte vector loads; shuffle reductions.
+// One warp per row (a CTA per row for q/k/v heads); 16-byte vector loads; shuffle reductions.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace hra {
@@ -70,6 +72,41 @@ __global__ void rope_table_kernel(int n_rows, const int32_t* __restrict__ pos_of
     table[idx] = make_float2((float)c, (float)s);
 }
 
+// Row RMSNorm helpers: a warp holds its whole row in registers (up to kMaxChunks 16-byte chunks per
+// lane, H <= 32 * 8 * kMaxChunks), so every load of the row is in flight at once.
+constexpr int kMaxChunks = 16;
+
+__device__ __forceinline__ void norm_row_from_regs(const uint4 (&u)[kMaxChunks], int nc, int lane,
+                                                   const bf16* __restrict__ g, bf16* __restrict__ yrow, int H,
+                                                   float eps) {
+    float ss = 0.f, sc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxChunks; ++q) {
+        if (lane + 32 * q < nc) {
+            float f[8];
+            unpack8(u[q], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
+        }
+    }
+    ss = csum_warp(ss, sc);
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    uint4* dy = reinterpret_cast<uint4*>(yrow);
+#pragma unroll
+    for (int q = 0; q < kMaxChunks; ++q) {
+        const int c = lane + 32 * q;
+        if (c < nc) {
+            float f[8], w[8];
+            unpack8(u[q], f);
+            unpack8(gv[c], w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
+            dy[c] = pack8(f);
+        }
+    }
+}
+
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok_ld,
                                      const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_pos,
                                      const bf16* __restrict__ embed, int vocab, const bf16* __restrict__ g,
@@ -87,28 +124,15 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
     }
     const uint4* src = reinterpret_cast<const uint4*>(embed + (long long)tok * H);
     uint4* dr = reinterpret_cast<uint4*>(r + (long long)row * H);
-    uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
-    const uint4* gv = reinterpret_cast<const uint4*>(g);
     const int nc = H >> 3;
-    float ss = 0.f, sc = 0.f;
-    for (int c = lane; c < nc; c += 32) {
-        const uint4 u = src[c];
-        dr[c] = u;
-        float f[8];
-        unpack8(u, f);
+    uint4 u[kMaxChunks];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
-    }
-    ss = csum_warp(ss, sc);
-    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-    for (int c = lane; c < nc; c += 32) {
-        float f[8], w[8];
-        unpack8(src[c], f);
-        unpack8(gv[c], w);
+    for (int q = 0; q < kMaxChunks; ++q)
+        if (lane + 32 * q < nc) u[q] = src[lane + 32 * q];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
-        dy[c] = pack8(f);
-    }
+    for (int q = 0; q < kMaxChunks; ++q)
+        if (lane + 32 * q < nc) dr[lane + 32 * q] = u[q];
+    norm_row_from_regs(u, nc, lane, g, y + (long long)row * H, H, eps);
 }
 
 // g == nullptr: plain gather (copy_out must be set).
@@ -123,54 +147,46 @@ __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __rest
     const long long src_row = idx ? idx[row] : row;
     const uint4* src = reinterpret_cast<const uint4*>(x + src_row * H);
     const int nc = H >> 3;
-    if (g == nullptr) {
+    uint4 u[kMaxChunks];
+#pragma unroll
+    for (int q = 0; q < kMaxChunks; ++q)
+        if (lane + 32 * q < nc) u[q] = src[lane + 32 * q];
+    if (copy_out) {
         uint4* dc = reinterpret_cast<uint4*>(copy_out + (long long)row * H);
-        for (int c = lane; c < nc; c += 32) dc[c] = src[c];
-        return;
-    }
-    float ss = 0.f, sc = 0.f;
-    for (int c = lane; c < nc; c += 32) {
-        const uint4 u = src[c];
-        if (copy_out) reinterpret_cast<uint4*>(copy_out + (long long)row * H)[c] = u;
-        float f[8];
-        unpack8(u, f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
+        for (int q = 0; q < kMaxChunks; ++q)
+            if (lane + 32 * q < nc) dc[lane + 32 * q] = u[q];
     }
-    ss = csum_warp(ss, sc);
-    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-    const uint4* gv = reinterpret_cast<const uint4*>(g);
-    uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * H);
-    for (int c = lane; c < nc; c += 32) {
-        float f[8], w[8];
-        unpack8(src[c], f);
-        unpack8(gv[c], w);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
-        dy[c] = pack8(f);
-    }
+    if (g == nullptr) return;
+    norm_row_from_regs(u, nc, lane, g, y + (long long)row * H, H, eps);
 }
 
-// Half a warp per (row, head) over the nq + 2 nkv heads of the merged QKV row.  Lane l of a
-// half-warp holds head elements [l*E, l*E + E) (E = hd/16, one 16- or 8-byte load); the RoPE partner
-// of element i < hd/2 is i + hd/2, held by lane l ^ 8 of the same half-warp.
+// One CTA per (row, group of 8 heads); half a warp per head of the merged QKV row.  The row's
+// cos/sin are staged in shared memory once per CTA.  Lane l of a half-warp holds head elements [l*E, l*E + E) (E = hd/16, one 16- or 8-byte
+// load); the RoPE partner of element i < hd/2 is i + hd/2, held by lane l ^ 8 of the same half-warp.
 template <int HD>
 __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
     pdl_launch();
     pdl_wait();
     constexpr int E = HD / 16;
     constexpr int HALF = HD / 2;
+    __shared__ float2 s_cs[HALF];
     const int heads = a.nq + 2 * a.nkv;
-    const long long total = (long long)a.rows * heads;
-    const long long hw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+    const int row = blockIdx.x;
     const int sub = threadIdx.x & 15;
-    const bool valid = hw < total;
-    const int row = valid ? (int)(hw / heads) : 0;
-    const int hh = valid ? (int)(hw % heads) : 0;
-    const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + sub * E;
-
-    float x[E];
-    if (valid) {
+    const int nhw = blockDim.x >> 4;
+    const int hw0 = (threadIdx.x >> 4) + blockIdx.y * nhw;   // this CTA's group of heads
+    const int seq = a.row_seq[row], pos = a.row_pos[row];
+    const int trow = a.rope_row_is_pos ? pos : row;
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) s_cs[i] = a.rope[(long long)trow * HALF + i];
+    __syncthreads();
+    const long long head_stride = (long long)a.n_slots * HD;
+    {
+        const int hh_raw = hw0;
+        const bool valid = hh_raw < heads;       // half-warp uniform
+        const int hh = valid ? hh_raw : 0;
+        const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + sub * E;
+        float x[E];
         if constexpr (E == 8) {
             unpack8(*reinterpret_cast<const uint4*>(src), x);
         } else {
@@ -179,65 +195,57 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
             const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
             x[0] = f0.x; x[1] = f0.y; x[2] = f1.x; x[3] = f1.y;
         }
-    } else {
+        const bool is_v = hh >= a.nq + a.nkv;
+        const bool is_q = hh < a.nq;
+        // compensated sum of squares over the 16 lanes of this half-warp (all lanes take part)
+        float ss = 0.f, sc = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = 0.f;
-    }
-    const int seq = valid ? a.row_seq[row] : 0, pos = valid ? a.row_pos[row] : 0;
-    const long long head_stride = (long long)a.n_slots * HD;
-    const bool is_v = hh >= a.nq + a.nkv;
-    const bool is_q = hh < a.nq;
-
-    // compensated sum of squares over the 16 lanes of this half-warp (all lanes take part)
-    float ss = 0.f, sc = 0.f;
+        for (int e = 0; e < E; ++e) csum_add(ss, sc, __fmul_rn(x[e], x[e]));
 #pragma unroll
-    for (int e = 0; e < E; ++e) csum_add(ss, sc, __fmul_rn(x[e], x[e]));
+        for (int o = 8; o > 0; o >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, ss, o);
+            const float c2 = __shfl_xor_sync(0xffffffffu, sc, o);
+            float t, er;
+            two_sum(ss, s2, t, er);
+            ss = t;
+            sc = __fadd_rn(__fadd_rn(sc, c2), er);
+        }
+        ss = __fadd_rn(ss, sc);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+        const bf16* gain = (is_q ? a.q_norm : a.k_norm) + sub * E;
+        float xn[E], pn[E];
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-        const float s2 = __shfl_xor_sync(0xffffffffu, ss, o);
-        const float c2 = __shfl_xor_sync(0xffffffffu, sc, o);
-        float t, er;
-        two_sum(ss, s2, t, er);
-        ss = t;
-        sc = __fadd_rn(__fadd_rn(sc, c2), er);
-    }
-    ss = __fadd_rn(ss, sc);
-    const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
-    const bf16* gain = (is_q ? a.q_norm : a.k_norm) + sub * E;
-    float xn[E], pn[E];
+        for (int e = 0; e < E; ++e) xn[e] = is_v ? 0.f : __fmul_rn(__fmul_rn(x[e], inv), bf2f(gain[e]));
 #pragma unroll
-    for (int e = 0; e < E; ++e) xn[e] = is_v ? 0.f : __fmul_rn(__fmul_rn(x[e], inv), bf2f(gain[e]));
+        for (int e = 0; e < E; ++e) pn[e] = __shfl_xor_sync(0xffffffffu, xn[e], 8);
+        if (!valid) return;
+        bf16* dst;
+        if (is_v) {
+            dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride +
+                  (long long)pos * HD + sub * E;
+            if constexpr (E == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+            else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+            return;
+        }
+        float out[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) pn[e] = __shfl_xor_sync(0xffffffffu, xn[e], 8);
-    if (!valid) return;
-    bf16* dst;
-    if (is_v) {
-        dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride + (long long)pos * HD + sub * E;
-        if constexpr (E == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-        else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
-        return;
-    }
-    const int trow = a.rope_row_is_pos ? pos : row;
-    const float2* cs = a.rope + (long long)trow * HALF;
-    float out[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const int i = (sub * E + e) % HALF;
-        const float2 c = cs[i];   // (cos, sin)
-        if (sub < 8)   // first half: a*cos - b*sin with a = own, b = partner
-            out[e] = __fsub_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
-        else           // second half: b*cos + a*sin with b = own, a = partner
-            out[e] = __fadd_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
-    }
-    if (is_q) dst = a.q_out + ((long long)row * a.nq + hh) * HD + sub * E;
-    else dst = a.kv_layer + ((long long)(seq * 2) * a.nkv + (hh - a.nq)) * head_stride + (long long)pos * HD + sub * E;
-    if constexpr (E == 8) {
-        *reinterpret_cast<uint4*>(dst) = pack8(out);
-    } else {
-        uint2 u;
-        *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(out[0], out[1]);
-        *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(out[2], out[3]);
-        *reinterpret_cast<uint2*>(dst) = u;
+        for (int e = 0; e < E; ++e) {
+            const float2 c = s_cs[(sub * E + e) % HALF];   // (cos, sin)
+            if (sub < 8)   // first half: a*cos - b*sin with a = own, b = partner
+                out[e] = __fsub_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
+            else           // second half: b*cos + a*sin with b = own, a = partner
+                out[e] = __fadd_rn(__fmul_rn(xn[e], c.x), __fmul_rn(pn[e], c.y));
+        }
+        if (is_q) dst = a.q_out + ((long long)row * a.nq + hh) * HD + sub * E;
+        else dst = a.kv_layer + ((long long)(seq * 2) * a.nkv + (hh - a.nq)) * head_stride + (long long)pos * HD + sub * E;
+        if constexpr (E == 8) {
+            *reinterpret_cast<uint4*>(dst) = pack8(out);
+        } else {
+            uint2 u;
+            *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(out[0], out[1]);
+            *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(out[2], out[3]);
+            *reinterpret_cast<uint2*>(dst) = u;
+        }
     }
 }
 
@@ -280,10 +288,11 @@ cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf1
 }
 
 cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st) {
-    const long long halves = (long long)a.rows * (a.nq + 2 * a.nkv);
-    const unsigned blocks = blocks_for(halves * 16, 256);
-    if (a.hd == 128) HRA_LAUNCH(qk_rope_kv_kernel<128>, dim3(blocks), dim3(256), 0, st, a);
-    else if (a.hd == 64) HRA_LAUNCH(qk_rope_kv_kernel<64>, dim3(blocks), dim3(256), 0, st, a);
+    const int heads = a.nq + 2 * a.nkv;
+    constexpr int kHeadsPerCta = 8;
+    const dim3 grid(a.rows, (heads + kHeadsPerCta - 1) / kHeadsPerCta);
+    if (a.hd == 128) HRA_LAUNCH(qk_rope_kv_kernel<128>, grid, dim3(kHeadsPerCta * 16), 0, st, a);
+    else if (a.hd == 64) HRA_LAUNCH(qk_rope_kv_kernel<64>, grid, dim3(kHeadsPerCta * 16), 0, st, a);
     else return cudaErrorInvalidValue;
     return cudaSuccess;
 }
