@@ -59,8 +59,7 @@ extern "C" {
 
 /* ---- model description ---------------------------------------------------------------------- */
 /* Backbone and audio-head shape.  Supported: head_dim in {64, 128}; n_q_heads % n_kv_heads == 0;
- * hidden, n_q_heads * head_dim and ffn multiples of 64 (hidden <= 4096 for the backbone entry
- * points); 1 <= n_codebooks <= 16;
+ * hidden, n_q_heads * head_dim and ffn multiples of 64; 1 <= n_codebooks <= 16;
  * codebook_size >= 2 with bos_id, eoc_id < codebook_size. */
 typedef struct hra_dims {
     int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;

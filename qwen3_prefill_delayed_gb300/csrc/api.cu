@@ -79,7 +79,7 @@ struct Layout {
 
 bool dims_ok(const hra_dims* d) {
     if (d == nullptr) return false;
-    if (d->n_layers < 1 || d->hidden < 64 || d->hidden > 4096 || d->hidden % 64 != 0) return false;
+    if (d->n_layers < 1 || d->hidden < 64 || d->hidden % 64 != 0) return false;
     if (d->head_dim != 64 && d->head_dim != 128) return false;
     if (d->n_q_heads < 1 || d->n_kv_heads < 1 || d->n_q_heads % d->n_kv_heads != 0) return false;
     const int g = d->n_q_heads / d->n_kv_heads;
@@ -156,8 +156,11 @@ int cuda_status(cudaError_t e) {
 cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K, int epi, const Ptrs& P,
                    const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE,
                    const void* norm_gain = nullptr, bf16* norm_out = nullptr, float eps = 0.f,
-                   const int32_t* norm_rows = nullptr, int norm_nrows = 0) {
+                   const int32_t* norm_rows = nullptr, int norm_nrows = 0, const QkRopeArgs* qk = nullptr,
+                   bool* qk_done = nullptr) {
     LinearCall c{};
+    c.qk = qk;
+    c.qk_done = qk_done;
     c.a = a;
     c.w = reinterpret_cast<const bf16*>(w);
     c.out = out;
@@ -218,12 +221,12 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
         const bool last = l == d.n_layers - 1;
-        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : 0));
         QkRopeArgs qa{};
         qa.qkv = qkv;
         qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
         qa.k_norm = reinterpret_cast<const bf16*>(lw.k_norm);
         qa.rope = P.at<float2>(L.rope);
+        qa.rope_rows = prefill ? max_len : batch;
         qa.row_seq = row_seq;
         qa.row_pos = row_pos;
         qa.rope_row_is_pos = prefill ? 1 : 0;
@@ -235,7 +238,10 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         qa.nkv = nkv;
         qa.hd = hd;
         qa.eps = eps;
-        HRA_TRY(launch_qk_rope_kv(qa, st));
+        bool qk_done = false;
+        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : 0, nullptr,
+                       nullptr, 0.f, nullptr, 0, &qa, &qk_done));
+        if (!qk_done) HRA_TRY(launch_qk_rope_kv(qa, st));
 
         const bool tail = prefill && last && !full_last;
         if (!tail) {

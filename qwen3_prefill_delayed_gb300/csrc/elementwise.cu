@@ -64,7 +64,7 @@ __global__ void rope_table_kernel(int n_rows, const int32_t* __restrict__ pos_of
     const int half = hd / 2;
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_rows * half) return;
-    const int r = idx / half, i = idx % half;
+    const int i = idx / n_rows, r = idx % n_rows;   // transposed: entry (r, i) at i * n_rows + r
     const int pos = pos_of_row ? pos_of_row[r] : r;
     const double inv_freq = pow(theta, -(2.0 * (double)i) / (double)hd);
     double s, c;
@@ -72,33 +72,54 @@ __global__ void rope_table_kernel(int n_rows, const int32_t* __restrict__ pos_of
     table[idx] = make_float2((float)c, (float)s);
 }
 
-// Row RMSNorm helpers: a warp holds its whole row in registers (up to kMaxChunks 16-byte chunks per
-// lane, H <= 32 * 8 * kMaxChunks), so every load of the row is in flight at once.
-constexpr int kMaxChunks = 16;
-
-__device__ __forceinline__ void norm_row_from_regs(const uint4 (&u)[kMaxChunks], int nc, int lane,
-                                                   const bf16* __restrict__ g, bf16* __restrict__ yrow, int H,
-                                                   float eps) {
+// Row RMSNorm: a warp holds its whole row in registers (NC 16-byte chunks per lane, H = 256 * NC),
+// so every load of the row is in flight at once; NC = 0 takes H at run time in two passes.
+template <int NC>
+__device__ __forceinline__ void norm_row(const uint4* __restrict__ src, uint4* __restrict__ copy, int lane,
+                                         const bf16* __restrict__ g, bf16* __restrict__ yrow, int H, float eps) {
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    uint4* dy = reinterpret_cast<uint4*>(yrow);
     float ss = 0.f, sc = 0.f;
+    if constexpr (NC > 0) {
+        uint4 u[NC];
 #pragma unroll
-    for (int q = 0; q < kMaxChunks; ++q) {
-        if (lane + 32 * q < nc) {
+        for (int q = 0; q < NC; ++q) u[q] = src[lane + 32 * q];
+#pragma unroll
+        for (int q = 0; q < NC; ++q) {
+            if (copy) copy[lane + 32 * q] = u[q];
             float f[8];
             unpack8(u[q], f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
         }
-    }
-    ss = csum_warp(ss, sc);
-    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-    const uint4* gv = reinterpret_cast<const uint4*>(g);
-    uint4* dy = reinterpret_cast<uint4*>(yrow);
+        ss = csum_warp(ss, sc);
+        if (g == nullptr) return;
+        const float inv = 1.0f / sqrtf(ss / (float)H + eps);
 #pragma unroll
-    for (int q = 0; q < kMaxChunks; ++q) {
-        const int c = lane + 32 * q;
-        if (c < nc) {
+        for (int q = 0; q < NC; ++q) {
             float f[8], w[8];
             unpack8(u[q], f);
+            unpack8(gv[lane + 32 * q], w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
+            dy[lane + 32 * q] = pack8(f);
+        }
+    } else {
+        const int nc = H >> 3;
+        for (int c = lane; c < nc; c += 32) {
+            const uint4 u = src[c];
+            if (copy) copy[c] = u;
+            float f[8];
+            unpack8(u, f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
+        }
+        ss = csum_warp(ss, sc);
+        if (g == nullptr) return;
+        const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+        for (int c = lane; c < nc; c += 32) {
+            float f[8], w[8];
+            unpack8(src[c], f);
             unpack8(gv[c], w);
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
@@ -107,6 +128,7 @@ __device__ __forceinline__ void norm_row_from_regs(const uint4 (&u)[kMaxChunks],
     }
 }
 
+template <int NC>
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok_ld,
                                      const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_pos,
                                      const bf16* __restrict__ embed, int vocab, const bf16* __restrict__ g,
@@ -122,20 +144,12 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
         if (lane == 0) raise_error(err, HRA_DEVERR_TOKEN_RANGE);
         tok = tok < 0 ? 0 : vocab - 1;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(embed + (long long)tok * H);
-    uint4* dr = reinterpret_cast<uint4*>(r + (long long)row * H);
-    const int nc = H >> 3;
-    uint4 u[kMaxChunks];
-#pragma unroll
-    for (int q = 0; q < kMaxChunks; ++q)
-        if (lane + 32 * q < nc) u[q] = src[lane + 32 * q];
-#pragma unroll
-    for (int q = 0; q < kMaxChunks; ++q)
-        if (lane + 32 * q < nc) dr[lane + 32 * q] = u[q];
-    norm_row_from_regs(u, nc, lane, g, y + (long long)row * H, H, eps);
+    norm_row<NC>(reinterpret_cast<const uint4*>(embed + (long long)tok * H),
+                 reinterpret_cast<uint4*>(r + (long long)row * H), lane, g, y + (long long)row * H, H, eps);
 }
 
 // g == nullptr: plain gather (copy_out must be set).
+template <int NC>
 __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ idx,
                                const bf16* __restrict__ g, bf16* __restrict__ y, bf16* __restrict__ copy_out,
                                int rows, int H, float eps) {
@@ -145,20 +159,9 @@ __global__ void rmsnorm_kernel(const bf16* __restrict__ x, const int32_t* __rest
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const long long src_row = idx ? idx[row] : row;
-    const uint4* src = reinterpret_cast<const uint4*>(x + src_row * H);
-    const int nc = H >> 3;
-    uint4 u[kMaxChunks];
-#pragma unroll
-    for (int q = 0; q < kMaxChunks; ++q)
-        if (lane + 32 * q < nc) u[q] = src[lane + 32 * q];
-    if (copy_out) {
-        uint4* dc = reinterpret_cast<uint4*>(copy_out + (long long)row * H);
-#pragma unroll
-        for (int q = 0; q < kMaxChunks; ++q)
-            if (lane + 32 * q < nc) dc[lane + 32 * q] = u[q];
-    }
-    if (g == nullptr) return;
-    norm_row_from_regs(u, nc, lane, g, y + (long long)row * H, H, eps);
+    norm_row<NC>(reinterpret_cast<const uint4*>(x + src_row * H),
+                 copy_out ? reinterpret_cast<uint4*>(copy_out + (long long)row * H) : nullptr, lane, g,
+                 y + (long long)row * H, H, eps);
 }
 
 // One CTA per (row, group of 8 heads); half a warp per head of the merged QKV row.  The row's
@@ -178,7 +181,7 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
     const int hw0 = (threadIdx.x >> 4) + blockIdx.y * nhw;   // this CTA's group of heads
     const int seq = a.row_seq[row], pos = a.row_pos[row];
     const int trow = a.rope_row_is_pos ? pos : row;
-    for (int i = threadIdx.x; i < HALF; i += blockDim.x) s_cs[i] = a.rope[(long long)trow * HALF + i];
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) s_cs[i] = a.rope[(long long)i * a.rope_rows + trow];
     __syncthreads();
     const long long head_stride = (long long)a.n_slots * HD;
     {
@@ -275,16 +278,24 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_
                                  const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
                                  bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
                                  cudaStream_t st) {
-    HRA_LAUNCH(embed_rmsnorm_kernel, dim3(blocks_for((long long)rows * 32, 256)), dim3(256), 0, st, 
-        tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err);
-    return cudaGetLastError();
+    const dim3 grid(blocks_for((long long)rows * 32, 256));
+    switch (H) {
+        case 256: HRA_LAUNCH(embed_rmsnorm_kernel<1>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
+        case 2560: HRA_LAUNCH(embed_rmsnorm_kernel<10>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
+        default: HRA_LAUNCH(embed_rmsnorm_kernel<0>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf16* y, bf16* copy_out,
                            int rows, int H, float eps, cudaStream_t st) {
-    HRA_LAUNCH(rmsnorm_kernel, dim3(blocks_for((long long)rows * 32, 256)), dim3(256), 0, st, x, idx, g, y, copy_out, rows, H,
-                                                                        eps);
-    return cudaGetLastError();
+    const dim3 grid(blocks_for((long long)rows * 32, 256));
+    switch (H) {
+        case 256: HRA_LAUNCH(rmsnorm_kernel<1>, grid, dim3(256), 0, st, x, idx, g, y, copy_out, rows, H, eps); break;
+        case 2560: HRA_LAUNCH(rmsnorm_kernel<10>, grid, dim3(256), 0, st, x, idx, g, y, copy_out, rows, H, eps); break;
+        default: HRA_LAUNCH(rmsnorm_kernel<0>, grid, dim3(256), 0, st, x, idx, g, y, copy_out, rows, H, eps); break;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st) {

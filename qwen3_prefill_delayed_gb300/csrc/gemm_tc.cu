@@ -33,7 +33,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
 
-enum KMode : int { KM_STORE = 0, KM_RESIDUAL = 1, KM_SWIGLU = 2, KM_F32 = 3, KM_PARTIAL = 4 };
+enum KMode : int { KM_STORE = 0, KM_RESIDUAL = 1, KM_SWIGLU = 2, KM_F32 = 3, KM_PARTIAL = 4, KM_QKROPE = 5 };
 
 struct GemmArgs {
     void* out;
@@ -54,6 +54,7 @@ struct GemmArgs {
     float* tail_part;
     unsigned int* zero_ptr;   // CTA 0 clears zero_words words here once earlier kernels are done
     int zero_words;
+    QkRopeArgs qk;            // KM_QKROPE: per-head q/k norm + RoPE + K/V cache write in the epilogue
 };
 
 template <int BN>
@@ -109,6 +110,85 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m_blk
     const int within = t - band * band_units;
     m_blk = within % p.mt;
     n_blk = band * p.group + within / p.mt;
+}
+
+// KM_QKROPE epilogue: the tile's columns [n0, n0 + BN) are whole heads of the merged QKV row
+// (BN a multiple of HD).  Per head: round the fp32 accumulators to bf16 (the QKV output rounding),
+// then V heads go to the cache as is; q / k heads get RMSNorm over HD (compensated sum of squares,
+// shared gains) and rotate-half RoPE at the row's position, rounded once, to q_out or the K cache.
+// One row (token) per thread; the RoPE partner i + HD/2 is in the same thread.
+template <int BN, int HD>
+__device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row, bool row_ok, const QkRopeArgs& a) {
+    constexpr int HALF = HD / 2;
+    const int seq = row_ok ? a.row_seq[row] : 0;
+    const int pos = row_ok ? a.row_pos[row] : 0;
+    const float2* cs = a.rope + (a.rope_row_is_pos ? pos : row);   // pair i at cs[i * rope_rows]
+    const long long head_stride = (long long)a.n_slots * HD;
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += HD) {
+        float x[HD];
+#pragma unroll
+        for (int c = 0; c < HD; c += 32) {
+            float v[32];
+            tmem_ld32(tq + h0 + c, v);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) x[c + q] = round_bf(v[q]);
+        }
+        const int hh = (n0 + h0) / HD;   // head index in the merged row
+        if (!row_ok || hh >= a.nq + 2 * a.nkv) continue;
+        if (hh >= a.nq + a.nkv) {         // V head: cache as is
+            bf16* dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride +
+                        (long long)pos * HD;
+#pragma unroll
+            for (int c = 0; c < HD; c += 8) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = x[c + e];
+                *reinterpret_cast<uint4*>(dst + c) = pack8(f);
+            }
+            continue;
+        }
+        const bool is_q = hh < a.nq;
+        const bf16* gain = is_q ? a.q_norm : a.k_norm;
+        // four interleaved compensated sums (short dependency chains), combined compensated
+        float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < HD; ++e) csum_add(s4[e & 3], c4[e & 3], __fmul_rn(x[e], x[e]));
+        float ss = s4[0], sc = c4[0];
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+            float t, er;
+            two_sum(ss, s4[q], t, er);
+            ss = t;
+            sc = __fadd_rn(__fadd_rn(sc, c4[q]), er);
+        }
+        ss = __fadd_rn(ss, sc);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+        bf16* dst = is_q ? a.q_out + ((long long)row * a.nq + hh) * HD
+                         : a.kv_layer + ((long long)(seq * 2) * a.nkv + (hh - a.nq)) * head_stride + (long long)pos * HD;
+#pragma unroll
+        for (int c = 0; c < HALF; c += 8) {
+            float lo[8], hi[8], g_lo[8], g_hi[8];
+            unpack8(*reinterpret_cast<const uint4*>(gain + c), g_lo);
+            unpack8(*reinterpret_cast<const uint4*>(gain + HALF + c), g_hi);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float xa = __fmul_rn(__fmul_rn(x[c + e], inv), g_lo[e]);
+                const float xb = __fmul_rn(__fmul_rn(x[c + e + HALF], inv), g_hi[e]);
+                const float2 t = cs[(long long)(c + e) * a.rope_rows];   // (cos, sin)
+                lo[e] = __fsub_rn(__fmul_rn(xa, t.x), __fmul_rn(xb, t.y));
+                hi[e] = __fadd_rn(__fmul_rn(xb, t.x), __fmul_rn(xa, t.y));
+            }
+            *reinterpret_cast<uint4*>(dst + c) = pack8(lo);
+            *reinterpret_cast<uint4*>(dst + HALF + c) = pack8(hi);
+        }
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ void qk_rope_epilogue(uint32_t tq, int n0, int row, bool row_ok, const QkRopeArgs& a) {
+    if (a.hd == 128) qk_rope_epilogue_hd<BN, 128>(tq, n0, row, row_ok, a);
+    else qk_rope_epilogue_hd<BN, 64>(tq, n0, row, row_ok, a);
 }
 
 // Linear tile index of (mb, nb) in the raster order of unit_coords.
@@ -309,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
+            } else if (!SWIGLU && p.mode == KM_QKROPE) {
+                qk_rope_epilogue<BN>(tq, nb * BN, row, row_ok, p.qk);
             } else if (!SWIGLU) {
                 const int n0 = nb * BN;
 #pragma unroll 1
@@ -1065,6 +1147,8 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     const int nsm = device_sm_count();
     Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm);
     if (c.partial_only) pl.tail_tiles = 0;   // the caller reads one output plane from the partial buffer
+    const bool fuse_qk = c.qk != nullptr && c.epi == EPI_STORE && pl.splits == 1 && pl.bn % c.qk->hd == 0;
+    if (fuse_qk) pl.tail_tiles = 0;
     const bool sw = c.epi == EPI_SWIGLU;
     const int w_rows = sw ? 2 * c.N : c.N;
 
@@ -1100,6 +1184,11 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
         g.mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : c.epi == EPI_SWIGLU ? KM_SWIGLU : KM_F32;
         g.ldo = c.N;
         g.split_stride = 0;
+    }
+    if (fuse_qk) {
+        g.mode = KM_QKROPE;
+        g.qk = *c.qk;
+        if (c.qk_done) *c.qk_done = true;
     }
 
     cudaError_t e;

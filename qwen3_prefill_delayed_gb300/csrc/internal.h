@@ -42,6 +42,24 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
         if (hra_e_ != cudaSuccess) return hra_e_;        \
     } while (0)
 
+// Per packed row: q heads and k heads get RMSNorm over head_dim (shared gains) + rotate-half RoPE
+// (table row = rope_row_is_pos ? row_pos[row] : row); q goes to q_out [rows, nq, hd]; k and v go to
+// cache slot row_pos[row] of cache sequence row_seq[row] of this layer.
+struct QkRopeArgs {
+    const bf16* qkv;
+    const bf16* q_norm;
+    const bf16* k_norm;
+    const float2* rope;     // transposed table: (row r, pair i) at i * rope_rows + r
+    int rope_rows;
+    const int32_t* row_seq;
+    const int32_t* row_pos;
+    int rope_row_is_pos;
+    bf16* q_out;
+    bf16* kv_layer;     // this layer's cache block: [cache_batch][2][nkv][n_slots][hd]
+    int n_slots;
+    int rows, nq, nkv, hd;
+    float eps;
+};
 // ------------------------------------------------------------------ projection GEMM
 enum EpiMode : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
 
@@ -67,6 +85,10 @@ struct LinearCall {
     // CTA 0 clears zero_words words at zero_ptr after earlier kernels finished (0 = none)
     unsigned int* zero_ptr;
     int zero_words;
+    // EPI_STORE of the merged QKV projection: when set and the large-M path runs, the epilogue does the
+    // per-head q/k norm + RoPE + K/V cache write itself (out is not written) and sets *qk_done.
+    const QkRopeArgs* qk;
+    bool* qk_done;
 };
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req);
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st);
@@ -90,7 +112,8 @@ struct SeqMeta {
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
                                 int32_t* cu, int32_t* last_row, unsigned int* err, cudaStream_t st);
 
-// cos/sin table [n_rows][head_dim/2] (float2), row r at position pos_of_row[r] (or r when null).
+// cos/sin table, transposed: entry (row r, pair i) at i * n_rows + r (float2), for position
+// pos_of_row[r] (or r when null).
 cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
                               float2* table, cudaStream_t st);
 
@@ -104,23 +127,6 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_
 cudaError_t launch_rmsnorm(const bf16* x, const int32_t* idx, const bf16* g, bf16* y, bf16* copy_out,
                            int rows, int H, float eps, cudaStream_t st);
 
-// Per packed row: q heads and k heads get RMSNorm over head_dim (shared gains) + rotate-half RoPE
-// (table row = rope_row_is_pos ? row_pos[row] : row); q goes to q_out [rows, nq, hd]; k and v go to
-// cache slot row_pos[row] of cache sequence row_seq[row] of this layer.
-struct QkRopeArgs {
-    const bf16* qkv;
-    const bf16* q_norm;
-    const bf16* k_norm;
-    const float2* rope;
-    const int32_t* row_seq;
-    const int32_t* row_pos;
-    int rope_row_is_pos;
-    bf16* q_out;
-    bf16* kv_layer;     // this layer's cache block: [cache_batch][2][nkv][n_slots][hd]
-    int n_slots;
-    int rows, nq, nkv, hd;
-    float eps;
-};
 cudaError_t launch_qk_rope_kv(const QkRopeArgs& a, cudaStream_t st);
 
 // ------------------------------------------------------------------ attention
