@@ -482,6 +482,9 @@ struct SwArgs {
     int nt, splits;
     unsigned int* zero_ptr;
     int zero_words;
+    int rpu;         // > 0: unit u covers weight rows [u*rpu, u*rpu + rpu) over the whole K (rpu < 128;
+                     // the tile rows past rpu stay zero); 0: 128-row tiles
+    int w_box_bytes; // bytes of one weight box (rpu or 128 rows x 128 B)
 };
 
 template <int NB, bool SWIGLU>
@@ -524,6 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmW);
         tma_prefetch_map(&tmX);
     }
+    if (p.rpu > 0) {   // rows [rpu, 128) of every weight tile are never loaded: make them zero once
+        for (int s = 0; s < C::STAGES; ++s) {
+            uint4* t = reinterpret_cast<uint4*>(smem + s * C::STAGE_BYTES + p.rpu * 128);
+            const int n16 = (128 - p.rpu) * 128 / 16;
+            for (int i = threadIdx.x; i < n16; i += blockDim.x) t[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -532,10 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int stage_tx = p.w_box_bytes + C::B_BYTES;
 
     if (warp == 0 && lane == 0) {
         auto load_w = [&](int s, int kx, int nb) {
-            if (SWIGLU) {
+            if (p.rpu > 0) {
+                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * p.rpu);
+            } else if (SWIGLU) {
                 tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * 64);
                 tma_load_2d(a_tile(s) + C::A_BYTES / 2, &tmW, full_bar(s), kx, p.up_row0 + nb * 64);
             } else {
@@ -549,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb0 = sp * p.kb_per_split;
             const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
             for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
-                mbar_expect_tx(full_bar(pre), C::STAGE_BYTES);
+                mbar_expect_tx(full_bar(pre), stage_tx);
                 load_w(pre, kb * BK, nb);
             }
         }
@@ -571,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    mbar_expect_tx(full_bar(s), stage_tx);
                     load_w(s, kx, nb);
                 }
                 tma_load_2d(b_tile(s), &tmX, full_bar(s), kx, 0);
@@ -637,6 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int jj = nb * 64 + (r & 63);
                 col_ok = jj < p.n_valid;
                 col = r < 64 ? jj : p.up_row0 + jj;
+            } else if (p.rpu > 0) {
+                col = nb * p.rpu + r;
+                col_ok = r < p.rpu && col < p.n_valid;
             } else {
                 col = nb * 128 + r;
                 col_ok = col < p.n_valid;
@@ -1004,6 +1021,7 @@ constexpr int kSmallM = 64;
 struct SmallPlan {
     int nb;          // padded activation rows: 16, 32 or 64
     int nt, splits, kbps;
+    int rpu = 0;     // > 0: row-range units of rpu weight rows over the whole K (nt = units)
 };
 
 SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) {
@@ -1023,6 +1041,33 @@ SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) 
             best_cost = cost;
             best.splits = splits;
             best.kbps = kbps;
+        }
+    }
+    // Row ranges: units of rpu whole weight rows (rpu <= 128) times s K splits, sized so the units
+    // cover the SMs about once.  A stage then carries rpu x 128 B of weights; with fewer than ~96 KB
+    // of weights in flight per SM the stream is latency-bound, so such plans are charged for it.
+    if (epi != EPI_SWIGLU && split_req == 0) {
+        const int nb_pad = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+        const int stage_bytes = 128 * BK * 2 + nb_pad * BK * 2;
+        const int stages = std::min(12, (200 * 1024) / stage_bytes);
+        for (int s = 1; s <= std::min(8, n_kb); ++s) {
+            const int rpu = (int)(((long long)N * s + nsm - 1) / nsm);
+            if (rpu < 8 || rpu > 128) continue;
+            const int kbps = (n_kb + s - 1) / s;
+            const int splits = (n_kb + kbps - 1) / kbps;
+            const double inflight = (double)rpu * 128 * stages;
+            const double latency_factor = std::min(1.0, inflight / (96.0 * 1024));
+            const long long units = (long long)((N + rpu - 1) / rpu) * splits;
+            const long long rounds = (units + nsm - 1) / nsm;
+            const double cost = rounds * (kbps * (rpu / 128.0) / latency_factor + 0.75) +
+                                0.05 * (splits - 1) * ((M + 15) / 16);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.rpu = rpu;
+                best.nt = (N + rpu - 1) / rpu;
+                best.splits = splits;
+                best.kbps = kbps;
+            }
         }
     }
     return best;
@@ -1068,7 +1113,8 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
     const bool sw = c.epi == EPI_SWIGLU;
     const int w_rows = sw ? 2 * c.N : c.N;
     CUtensorMap mw, mx;
-    if (!make_map(&mw, c.w, w_rows, c.K, sw ? 64 : 128)) return cudaErrorInvalidValue;
+    const int w_box = pl.rpu > 0 ? pl.rpu : (sw ? 64 : 128);
+    if (!make_map(&mw, c.w, w_rows, c.K, w_box)) return cudaErrorInvalidValue;
     if (!make_map(&mx, c.a, c.M, c.K, pl.nb)) return cudaErrorInvalidValue;
     // SwiGLU and every split go through fp32 partials; otherwise the epilogue writes the output.
     const bool use_partial = sw || pl.splits > 1;
@@ -1081,6 +1127,8 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
     a.up_row0 = c.N;
     a.nt = pl.nt;
     a.splits = pl.splits;
+    a.rpu = pl.rpu;
+    a.w_box_bytes = (pl.rpu > 0 ? pl.rpu : 128) * BK * 2;
     a.zero_ptr = c.zero_ptr;
     a.zero_words = c.zero_ptr ? c.zero_words : 0;
     const int ldp = sw ? 2 * c.N : c.N;

@@ -43,6 +43,9 @@ CASES = [
     (4255, 2560, 1024, "swiglu", 0),       # 680 tiles: last round in 2 K pieces
     (4255, 2560, 640, "store", 0),
     (3, 4104, 256, "f32", 0),
+    (1, 8208, 2560, "f32", 0),             # row ranges of 54 weight rows per CTA, whole K
+    (8, 6144, 2560, "store", 0),           # row ranges of 41 rows
+    (16, 6144, 2560, "residual", 0),
     (64, 8208, 2560, "f32", 0),
     (64, 8208, 2560, "f32", 7),
 ]
