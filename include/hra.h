@@ -207,14 +207,17 @@ uint64_t hra_launch_counter(void);
 #define HRA_PROBE_DOWN 4       /* down projection of full prefill layers                        */
 #define HRA_PROBE_ATTENTION 5  /* causal prefill attention of full layers                       */
 #define HRA_PROBE_AUDIO_HEAD 6 /* audio-head projection of hra_codebook_step                    */
+#define HRA_PROBE_DECODE_ATTENTION 7 /* single-query attention (+ split combine) of hra_decode    */
+#define HRA_PROBE_DECODE_LINEAR 8    /* every projection of hra_decode, with its split-K reduction */
 
 /* While a class is selected, every launch of that class is bracketed by a CUDA event pair
  * recorded on the launching stream (events are created on first use; do not select a class while
  * a stream is being captured).  hra_probe_collect synchronises those events, returns the summed
- * elapsed milliseconds, the number of launches and their summed algorithmic FLOPs, and clears
- * them.  Returns HRA_OK or HRA_ERR_CUDA. */
+ * elapsed milliseconds, the number of launches and their summed algorithmic work, and clears
+ * them.  The work is FLOPs for classes 1-6 and bytes for the HBM-bound classes 7 (K/V bytes read)
+ * and 8 (weight bytes read).  Returns HRA_OK or HRA_ERR_CUDA. */
 int hra_probe_select(int kernel_class);
-int hra_probe_collect(double* total_ms, int64_t* launches, double* total_flops);
+int hra_probe_collect(double* total_ms, int64_t* launches, double* total_work);
 
 /* ---- errors --------------------------------------------------------------------------------- */
 /* Synchronise `stream` and return the sticky HRA_DEVERR_* bits of the last call that used this

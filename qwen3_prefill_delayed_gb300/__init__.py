@@ -33,7 +33,8 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_decode_workspace_s
             "hra_linear_workspace_size",
             "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
             "hra_device_error", "hra_status_string"]
-PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6}
+PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6,
+         "decode_attention": 7, "decode_linear": 8}
 
 
 class HraError(RuntimeError):
@@ -343,7 +344,9 @@ def hra_probe_select(kernel_class: str) -> None:
 
 
 def hra_probe_collect():
-    """(summed milliseconds, launches, summed algorithmic FLOPs) of the probed launches; clears them."""
+    """(summed milliseconds, launches, summed algorithmic work) of the probed launches; clears them.
+
+    The work is FLOPs for the prefill and audio-head classes and bytes for the two decode classes."""
     ms, n, fl = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double()
     _check(lib().hra_probe_collect(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl)), "hra_probe_collect")
     return ms.value, n.value, fl.value

@@ -157,8 +157,9 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
                    const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE,
                    const void* norm_gain = nullptr, bf16* norm_out = nullptr, float eps = 0.f,
                    const int32_t* norm_rows = nullptr, int norm_nrows = 0, const QkRopeArgs* qk = nullptr,
-                   bool* qk_done = nullptr) {
+                   bool* qk_done = nullptr, bool shallow_ring = false) {
     LinearCall c{};
+    c.shallow_ring = shallow_ring;
     c.qk = qk;
     c.qk_done = qk_done;
     c.a = a;
@@ -178,8 +179,9 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
         c.norm_eps = eps;
         c.norm_done = &norm_done;
     }
-    const double flops = 2.0 * M * (double)K * (epi == EPI_SWIGLU ? 2.0 * N : (double)N);
-    cudaError_t e = probed(probe_class, flops, st, [&] { return launch_linear(c, st); });
+    const double n_w = epi == EPI_SWIGLU ? 2.0 * N : (double)N;   // weight rows
+    const double work = probe_class == HRA_PROBE_DECODE_LINEAR ? 2.0 * K * n_w : 2.0 * M * (double)K * n_w;
+    cudaError_t e = probed(probe_class, work, st, [&] { return launch_linear(c, st); });
     if (e != cudaSuccess || norm_out == nullptr || norm_done) return e;
     return launch_rmsnorm(reinterpret_cast<const bf16*>(out), norm_rows, reinterpret_cast<const bf16*>(norm_gain),
                           norm_out, nullptr, norm_rows ? norm_nrows : M, N, eps, st);
@@ -209,13 +211,14 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
     const int32_t* row_pos = P.at<int32_t>(L.row_pos);
     const int32_t* last_row = P.at<int32_t>(L.last_row);
     const size_t layer_elems = (size_t)kv.batch * 2 * nkv * (size_t)kv.n_slots * hd;
-    double attn_flops = 0.0;   // causal QK^T + PV over the used keys: 4 nq hd sum_b len_b (len_b + 1) / 2
-    if (prefill) {
-        for (int b = 0; b < batch; ++b) {
-            const double n = (double)seq_lens_host[b];
-            attn_flops += 4.0 * nq * hd * n * (n + 1.0) / 2.0;
-        }
+    // prefill: causal QK^T + PV FLOPs over the used keys, 4 nq hd sum_b len_b (len_b + 1) / 2;
+    // decode (seq_lens_host = positions): K/V bytes read, 4 nkv hd sum_b (pos_b + 1)
+    double attn_work = 0.0;
+    for (int b = 0; b < batch && seq_lens_host != nullptr; ++b) {
+        const double n = (double)seq_lens_host[b];
+        attn_work += prefill ? 4.0 * nq * hd * n * (n + 1.0) / 2.0 : 4.0 * nkv * hd * (n + 1.0);
     }
+    const int lin_probe = prefill ? 0 : HRA_PROBE_DECODE_LINEAR;
 
     for (int l = 0; l < d.n_layers; ++l) {
         const hra_layer_weights& lw = w.layers[l];
@@ -239,7 +242,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         qa.hd = hd;
         qa.eps = eps;
         bool qk_done = false;
-        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : 0, nullptr,
+        HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : lin_probe, nullptr,
                        nullptr, 0.f, nullptr, 0, &qa, &qk_done));
         if (!qk_done) HRA_TRY(launch_qk_rope_kv(qa, st));
 
@@ -247,7 +250,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         if (!tail) {
             if (prefill) {
                 PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), att, batch, max_len, kv.n_slots, nq, nkv, hd};
-                HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_flops, st, [&] { return launch_prefill_attention(pa, st); }));
+                HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] { return launch_prefill_attention(pa, st); }));
             } else {
                 DecodeAttnArgs da{};
                 da.q = q;
@@ -264,19 +267,22 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
                 da.nkv = nkv;
                 da.hd = hd;
                 da.splits = std::min(L.attn_splits, decode_attention_splits(rows, nkv, max_pos));
-                HRA_TRY(launch_decode_attention(da, st));
+                HRA_TRY(probed(HRA_PROBE_DECODE_ATTENTION, attn_work, st,
+                               [&] { return launch_decode_attention(da, st); }));
             }
-            const int pc = prefill ? 1 : 0;
-            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_O_PROJ, lw.mlp_norm,
-                           y, eps));
-            HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st, pc * HRA_PROBE_GATE_UP));
+            HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st,
+                           prefill ? HRA_PROBE_O_PROJ : lin_probe, lw.mlp_norm, y, eps, nullptr, 0, nullptr,
+                           nullptr, /*shallow_ring=*/!prefill));
+            HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st,
+                           prefill ? HRA_PROBE_GATE_UP : lin_probe));
             if (!last) {
-                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN,
-                               w.layers[l + 1].attn_norm, y, eps));
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st,
+                               prefill ? HRA_PROBE_DOWN : lin_probe, w.layers[l + 1].attn_norm, y, eps));
             } else if (!prefill) {
-                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps));
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, lin_probe, w.final_norm,
+                               out_hidden, eps));
             } else {
-                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, pc * HRA_PROBE_DOWN,
+                HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, HRA_PROBE_DOWN,
                                w.final_norm, out_hidden, eps, last_row, batch));
             }
         } else {
@@ -298,7 +304,8 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             da.splits = std::min(L.attn_splits, decode_attention_splits(batch, nkv, max_len - 1));
             HRA_TRY(launch_decode_attention(da, st));
             HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
-            HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps));
+            HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps, nullptr, 0,
+                           nullptr, nullptr, /*shallow_ring=*/true));
             HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st));
             HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps));
         }
@@ -333,7 +340,7 @@ int hra_probe_select(int kernel_class) {
     return HRA_OK;
 }
 
-int hra_probe_collect(double* total_ms, int64_t* launches, double* total_flops) {
+int hra_probe_collect(double* total_ms, int64_t* launches, double* total_work) {
     std::lock_guard<std::mutex> lk(g_probe.mu);
     double ms = 0.0, fl = 0.0;
     for (const auto& u : g_probe.used) {
@@ -346,7 +353,7 @@ int hra_probe_collect(double* total_ms, int64_t* launches, double* total_flops) 
     }
     if (total_ms) *total_ms = ms;
     if (launches) *launches = (int64_t)g_probe.used.size();
-    if (total_flops) *total_flops = fl;
+    if (total_work) *total_work = fl;
     g_probe.used.clear();
     return HRA_OK;
 }
@@ -438,7 +445,7 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                            reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.y),
                            P.at<bf16>(L.r), batch, d.hidden, d.rms_eps, st));
     return run_layers(d, *weights, *kv, P, L, batch, batch, 0, false, false, reinterpret_cast<bf16*>(hidden_dev),
-                      nullptr, max_pos, st);
+                      pos, max_pos, st);
 }
 
 // Codebook-step workspace: error word and per-row counters (cleared by the GEMM), per-row argmax
@@ -531,7 +538,7 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
 
 size_t hra_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue, int32_t split_k) {
     if (M < 1 || N < 8 || K < 64) return 0;
-    return 256 + align_up(linear_partial_bytes(M, N, K, epilogue, split_k));
+    return 256 + align_up(linear_partial_bytes(M, N, K, epilogue, split_k, false));
 }
 
 int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, int32_t N, int32_t K,

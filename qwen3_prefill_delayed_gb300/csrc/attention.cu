@@ -13,10 +13,10 @@
 //                      hi + lo pair, so it is not rounded to 8 bits.
 //                      Tiles above the causal diagonal are never loaded.
 // decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
-//                      across CTAs and taken 128 at a time (one key per thread for the scores,
-//                      then coalesced V rows for PV); the G = n_q / n_kv q heads of a kv head
-//                      share every K/V load; partial (m, l, o) go to scratch and a combine kernel
-//                      merges the splits.
+//                      across CTAs and stream through a 3-stage cp.async ring; the G = n_q / n_kv
+//                      q heads of a kv head are the rows of one MMA tile, so they share every K/V
+//                      load; partial (m, l, o) go to scratch and a combine kernel merges the
+//                      splits (skipped when a row takes one split).
 #include <math.h>
 
 #include "internal.h"
@@ -216,150 +216,189 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
 
 // ------------------------------------------------------------------ single-query decode
 
-// One CTA = one (row, kv head, key split); keys are taken 128 at a time:
-//   phase 1  thread t scores key c0 + t against the G q heads (its K row is 16-byte loads; q is
-//            broadcast from shared memory) and stages that key's V row in shared memory;
-//   phase 2  warp g (per q head) takes the chunk max, turns scores into p = 2^(s - m), and updates
-//            the running max / sum;
-//   phase 3  warp g, lane l accumulates o[g][l*E .. l*E+E) += p_j v_j over the chunk from the
-//            staged V rows.
+constexpr int DS = 3;     // K/V stages in flight per CTA
+
+// One CTA = one (row, kv head, key split); 4 warps.  The split's keys stream through a ring of DS
+// shared-memory stages of PK keys (coalesced cp.async, zero-filled past the last key).  The G q
+// heads of the kv head are the rows of a 16-row MMA tile (rows G..15 are zero), so S = QK^T and
+// O += PV run on the same m16n8k16 fragments as the prefill kernel.  Warp w owns keys
+// w*16 .. w*16+15 of every stage and keeps its own online-softmax state; the four warps merge
+// through shared memory at the end.
 template <int HD, int G>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a, float scale_log2) {
+    static_assert(G <= 8, "the q heads of one kv head fill at most the upper half of the MMA tile");
     pdl_launch();
     pdl_wait();
-    constexpr int E = HD / 32;
-    constexpr int CH = 128;
+    constexpr int KS = HD / 16;
+    constexpr int DN = HD / 8;
+    constexpr uint32_t TILE = PK * HD * 2;   // bytes of one K (or V) stage
+    extern __shared__ __align__(128) uint8_t sm[];
+    const uint32_t sQ = smem_u32(sm);
+    const uint32_t sK0 = sQ + 16 * HD * 2;
+    const uint32_t sV0 = sK0 + DS * TILE;
+
     const int i = blockIdx.z, j = blockIdx.y, sp = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = a.q_row ? a.q_row[i] : i;
     const int seq = a.seq[qr], pos = a.pos[qr];
     const int nkeys = pos + 1;
-    const int chunk = (nkeys + a.splits - 1) / a.splits;
+    const int per = (nkeys + a.splits - 1) / a.splits;
+    const int chunk = (per + PK - 1) / PK * PK;
     const int k0 = sp * chunk, k1 = min(nkeys, k0 + chunk);
+    const int n_t = k1 > k0 ? (k1 - k0 + PK - 1) / PK : 0;
 
-    __shared__ float s_q[G][HD];
-    __shared__ float s_p[G][CH];
-    __shared__ uint4 s_v[CH][HD / 8];   // the chunk's V rows (bf16)
-    __shared__ float s_m[G], s_l[G], s_alpha[G];
-    for (int idx = tid; idx < G * HD; idx += 128) {
-        const int g = idx / HD, d = idx % HD;
-        s_q[g][d] = bf2f(a.q[((long long)qr * a.nq + j * G + g) * HD + d]) * scale_log2;
-    }
-    if (tid < G) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
-    }
     const long long hstride = (long long)a.n_slots * HD;
-    const bf16* kb = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * hstride;
-    const bf16* vb = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * hstride;
-    float o[(G + 3) / 4][E];
+    const bf16* kbase = a.kv_layer + ((long long)(seq * 2) * a.nkv + j) * hstride + (long long)k0 * HD;
+    const bf16* vbase = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + j) * hstride + (long long)k0 * HD;
+    const bf16* qbase = a.q + ((long long)qr * a.nq + j * G) * HD;
+
+    // q rows 0..G-1 (the G heads), rows G..15 zero-filled
+    for (int idx = tid; idx < 16 * (HD / 8); idx += 128) {
+        const int r = idx / (HD / 8), c = idx % (HD / 8);
+        const bool ok = r < G;
+        cp_async16(sQ + swz<HD>(r, c), qbase + (ok ? (long long)r * HD + c * 8 : 0), ok ? 16u : 0u);
+    }
 #pragma unroll
-    for (int r = 0; r < (G + 3) / 4; ++r)
+    for (int t = 0; t < DS - 1; ++t) {
+        if (t < n_t) {
+            const int rv = min(PK, k1 - k0 - t * PK);
+            load_tile<HD>(sK0 + t * TILE, kbase + (long long)t * PK * HD, HD, rv, tid);
+            load_tile<HD>(sV0 + t * TILE, vbase + (long long)t * PK * HD, HD, rv, tid);
+        }
+        cp_async_commit();
+    }
+
+    uint32_t qf[KS][4];
+    float o[DN][4];
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[r][e] = 0.f;
+    for (int d = 0; d < DN; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    float m_a = -INFINITY, l_a = 0.f;
+    const int tig = lane & 3;
+
+    for (int t = 0; t < n_t; ++t) {
+        {
+            const int tn = t + DS - 1;
+            if (tn < n_t) {
+                const int rv = min(PK, k1 - k0 - tn * PK);
+                load_tile<HD>(sK0 + (tn % DS) * TILE, kbase + (long long)tn * PK * HD, HD, rv, tid);
+                load_tile<HD>(sV0 + (tn % DS) * TILE, vbase + (long long)tn * PK * HD, HD, rv, tid);
+            }
+            cp_async_commit();
+        }
+        cp_async_wait<DS - 1>();
+        __syncthreads();
+        if (t == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) ldmatrix_x4(qf[ks], sQ + swz<HD>(lane & 15, ks * 2 + (lane >> 4)));
+        }
+        const uint32_t sK = sK0 + (t % DS) * TILE;
+        const uint32_t sV = sV0 + (t % DS) * TILE;
+        const int kw = k0 + t * PK + warp * 16;   // first key of this warp's 16
+
+        float s[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t kb[4];
+            ldmatrix_x4(kb, sK + swz<HD>(warp * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
+            mma_bf16_16816(s[0], qf[ks], kb[0], kb[1]);
+            mma_bf16_16816(s[1], qf[ks], kb[2], kb[3]);
+        }
+        // rows 8..15 are padding: their probabilities are zero.  Keys past k1 get zero weight.
+        float mx = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int key = kw + n * 8 + 2 * tig + c;
+                const float v = key < k1 ? s[n][c] * scale_log2 : -INFINITY;
+                s[n][c] = v;
+                mx = fmaxf(mx, v);
+            }
+            s[n][2] = s[n][3] = 0.f;
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_a, mx);
+        const float mref = mn == -INFINITY ? 0.f : mn;   // a warp with no key yet keeps p = 0
+        const float al = exp2f(m_a - mref);
+        m_a = mn;
+        float rs = 0.f;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            s[n][0] = exp2f(s[n][0] - mref);
+            s[n][1] = exp2f(s[n][1] - mref);
+            rs += s[n][0] + s[n][1];
+        }
+        l_a = l_a * al + rs;
+#pragma unroll
+        for (int d = 0; d < DN; ++d) {
+            o[d][0] *= al;
+            o[d][1] *= al;
+        }
+        uint32_t ph[4], pl[4];
+        split_bf2(s[0][0], s[0][1], ph[0], pl[0]);
+        split_bf2(s[0][2], s[0][3], ph[1], pl[1]);
+        split_bf2(s[1][0], s[1][1], ph[2], pl[2]);
+        split_bf2(s[1][2], s[1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int dp = 0; dp < DN / 2; ++dp) {
+            uint32_t vb[4];
+            ldmatrix_x4_trans(vb, sV + swz<HD>(warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dp * 2 + (lane >> 4)));
+            mma_bf16_16816(o[2 * dp], ph, vb[0], vb[1]);
+            mma_bf16_16816(o[2 * dp + 1], ph, vb[2], vb[3]);
+            mma_bf16_16816(o[2 * dp], pl, vb[0], vb[1]);
+            mma_bf16_16816(o[2 * dp + 1], pl, vb[2], vb[3]);
+        }
+        __syncthreads();   // the stage is refilled by the next iteration's loads
+    }
+    cp_async_wait<0>();
     __syncthreads();
 
-    for (int c0 = k0; c0 < k1; c0 += CH) {
-        const int nc = min(CH, k1 - c0);
-        // phase 1: scores
-        {
-            float sc[G];
+    // merge the four warps: per warp and head, (m, l) and the unnormalised o row
+    float* s_o = reinterpret_cast<float*>(sm + 16 * HD * 2);   // [4][G][HD], over the stages
+    float* s_ml = s_o + 4 * G * HD;                             // [4][G][2]
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    const int g = lane >> 2;
+    if (g < G) {
+        float* dst = s_o + (warp * G + g) * HD + 2 * tig;
 #pragma unroll
-            for (int g = 0; g < G; ++g) sc[g] = -INFINITY;
-            if (tid < nc) {
-                const uint4* kr = reinterpret_cast<const uint4*>(kb + (long long)(c0 + tid) * HD);
-                const uint4* vr = reinterpret_cast<const uint4*>(vb + (long long)(c0 + tid) * HD);
-                uint4 kv[HD / 8];
-#pragma unroll
-                for (int c = 0; c < HD / 8; ++c) kv[c] = kr[c];
-#pragma unroll
-                for (int c = 0; c < HD / 8; ++c) s_v[tid][c] = vr[c];   // V row of this key, for phase 3
-#pragma unroll
-                for (int g = 0; g < G; ++g) sc[g] = 0.f;
-#pragma unroll
-                for (int c = 0; c < HD / 8; ++c) {
-                    float f[8];
-                    unpack8(kv[c], f);
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) sc[g] += s_q[g][c * 8 + e] * f[e];
-                }
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) s_p[g][tid] = sc[g];
+        for (int d = 0; d < DN; ++d) {
+            dst[d * 8] = o[d][0];
+            dst[d * 8 + 1] = o[d][1];
         }
-        __syncthreads();
-        // phase 2: softmax bookkeeping, one warp per q head
-        for (int g = warp; g < G; g += 4) {
-            float mx = -INFINITY;
-            for (int t = lane; t < nc; t += 32) mx = fmaxf(mx, s_p[g][t]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_old = s_m[g];
-            const float m_new = fmaxf(m_old, mx);
-            float sum = 0.f;
-            for (int t = lane; t < nc; t += 32) {
-                const float pv = exp2f(s_p[g][t] - m_new);
-                s_p[g][t] = pv;
-                sum += pv;
-            }
-            sum = warp_sum(sum);
-            __syncwarp();
-            if (lane == 0) {
-                const float al = exp2f(m_old - m_new);
-                s_alpha[g] = al;
-                s_l[g] = s_l[g] * al + sum;
-                s_m[g] = m_new;
-            }
+        if (tig == 0) {
+            s_ml[(warp * G + g) * 2] = m_a;
+            s_ml[(warp * G + g) * 2 + 1] = l_a;
         }
-        __syncthreads();
-        // phase 3: o = o * alpha + sum_j p_j v_j
-#pragma unroll
-        for (int r = 0; r < (G + 3) / 4; ++r) {
-            const int g = warp + 4 * r;
-            if (g < G) {
-                const float al = s_alpha[g];
-                float acc[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] = o[r][e] * al;
-                const bf16* vp = reinterpret_cast<const bf16*>(&s_v[0][0]) + lane * E;
-#pragma unroll 4
-                for (int t = 0; t < nc; ++t) {
-                    const float pv = s_p[g][t];
-                    if constexpr (E == 4) {
-                        const uint2 u = *reinterpret_cast<const uint2*>(vp + (long long)t * HD);
-                        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-                        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-                        acc[0] += pv * f0.x; acc[1] += pv * f0.y; acc[2] += pv * f1.x; acc[3] += pv * f1.y;
-                    } else {
-                        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp + (long long)t * HD));
-                        acc[0] += pv * f0.x; acc[1] += pv * f0.y;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < E; ++e) o[r][e] = acc[e];
-            }
-        }
-        __syncthreads();
     }
-    // one split: the normalised output directly; several: partial (o unnormalised, m, l)
-    const int stride = HD + 2;
+    __syncthreads();
+    for (int idx = tid; idx < G * HD; idx += 128) {
+        const int hg = idx / HD, dc = idx % HD;
+        float M = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < (G + 3) / 4; ++r) {
-        const int g = warp + 4 * r;
-        if (g < G && a.splits == 1) {
-            const float il = 1.0f / s_l[g];
-            bf16* dst = a.out + ((long long)i * a.nq + j * G + g) * HD + lane * E;
+        for (int w = 0; w < 4; ++w)
+            if (s_ml[(w * G + hg) * 2 + 1] > 0.f) M = fmaxf(M, s_ml[(w * G + hg) * 2]);
+        float L = 0.f, O = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) dst[e] = f2bf(o[r][e] * il);
-        } else if (g < G) {
-            float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + g) * stride;
-#pragma unroll
-            for (int e = 0; e < E; ++e) dst[lane * E + e] = o[r][e];
-            if (lane == 0) {
-                dst[HD] = s_m[g];
-                dst[HD + 1] = s_l[g];
+        for (int w = 0; w < 4; ++w) {
+            const float lw = s_ml[(w * G + hg) * 2 + 1];
+            if (lw > 0.f) {
+                const float f = exp2f(s_ml[(w * G + hg) * 2] - M);
+                L += lw * f;
+                O += s_o[(w * G + hg) * HD + dc] * f;
+            }
+        }
+        if (a.splits == 1) {
+            a.out[((long long)i * a.nq + j * G + hg) * HD + dc] = f2bf(O / L);
+        } else {
+            float* dst = a.part + (((long long)sp * a.rows + i) * a.nq + j * G + hg) * (HD + 2);
+            dst[dc] = O;
+            if (dc == 0) {
+                dst[HD] = M;
+                dst[HD + 1] = L;
             }
         }
     }
@@ -410,9 +449,20 @@ cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
 
 template <int HD, int G>
 cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
+    constexpr int smem = 16 * HD * 2 + 2 * DS * PK * HD * 2;
+    static_assert(4 * G * HD * 4 + 4 * G * 2 * 4 <= 2 * DS * PK * HD * 2, "merge area fits over the stages");
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(decode_attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
     dim3 grid(a.splits, a.nkv, a.rows);
     const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
-    HRA_LAUNCH(decode_attn_kernel<HD, G>, dim3(grid), dim3(128), 0, st, a, scale_log2);
+    HRA_LAUNCH(decode_attn_kernel<HD, G>, dim3(grid), dim3(128), smem, st, a, scale_log2);
     if (a.splits == 1) return cudaSuccess;
     HRA_LAUNCH(decode_combine_kernel<HD>, dim3(dim3(a.nq, a.rows)), dim3(HD), 0, st, a);
     return cudaGetLastError();
@@ -437,12 +487,12 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st) 
     return cudaErrorInvalidValue;
 }
 
-// Enough (row, kv head, split) CTAs for two per SM, with at least 64 keys per split.
+// At most one wave of (row, kv head, split) CTAs (two per SM), with at least 128 keys per split:
+// short rows take one split and skip the combine.
 int decode_attention_splits(int rows, int nkv, int max_pos) {
     const int target = 2 * device_sm_count();
-    int s = (target + rows * nkv - 1) / (rows * nkv);
-    const int cap = max(1, (max_pos + 1) / 64);
-    s = min(s, cap);
+    int s = target / max(1, rows * nkv);
+    s = min(s, (max_pos + 1) / 128);
     s = min(s, 32);
     return max(s, 1);
 }

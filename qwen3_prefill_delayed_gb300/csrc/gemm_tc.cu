@@ -459,13 +459,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // accumulator D[weight row][activation row] (NB columns) is written back transposed; a warp's
 // stores cover 32 consecutive output columns.  SwiGLU tiles hold 64 gate and 64 up rows and always
 // go through fp32 partials (the reduction applies the activation).
+// Weight ring of the small-M kernel, chosen per launch.  Deep (about 200 KB): enough bytes in
+// flight for a long weight stream.  Shallow (about 100 KB): two CTAs fit on an SM, so a launch that
+// follows an attention or GEMM kernel starts streaming its weights while that kernel drains.
+constexpr int kSmallRingDeep = 200 * 1024;
+constexpr int kSmallRingShallow = 100 * 1024;
+constexpr int kSwigluXchBytes = 64 * 17 * 4;   // up-row accumulators handed to the gate rows
+
 template <int NB>
 struct SwCfg {
     static constexpr int A_BYTES = 128 * BK * 2;
     static constexpr int B_BYTES = NB * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int MAX_STAGES = kSmallRingDeep / STAGE_BYTES > 12 ? 12 : kSmallRingDeep / STAGE_BYTES;
+    static constexpr int stages_for(int ring_bytes) {
+        return ring_bytes / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : ring_bytes / STAGE_BYTES;
+    }
+    // ring, alignment slack, barriers and slots, SwiGLU exchange
+    static constexpr int smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 256 + kSwigluXchBytes; }
     static constexpr uint32_t TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
 };
 
@@ -478,14 +489,28 @@ struct SwArgs {
     int ldo;
     int n_kb, kb_per_split;
     int up_row0;     // SwiGLU: first up row in W (= F)
-    int mode;        // KM_STORE / KM_RESIDUAL / KM_F32 / KM_PARTIAL
+    int mode;        // KM_STORE / KM_RESIDUAL / KM_SWIGLU (one K split) / KM_F32 / KM_PARTIAL
     int nt, splits;
     unsigned int* zero_ptr;
     int zero_words;
     int rpu;         // > 0: unit u covers weight rows [u*rpu, u*rpu + rpu) over the whole K (rpu < 128;
                      // the tile rows past rpu stay zero); 0: 128-row tiles
     int w_box_bytes; // bytes of one weight box (rpu or 128 rows x 128 B)
+    int stages;      // ring depth of this launch (<= SwCfg::MAX_STAGES)
 };
+
+// OR of `v` over the four epilogue warps (named barrier 1, 128 threads); every one of them gets
+// the same answer.
+__device__ __forceinline__ bool bar_or_epilogue(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, 128, pi;\n"
+        " selp.u32 %0, 1, 0, po;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
 
 template <int NB, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -493,26 +518,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const SwArgs p) {
     using C = SwCfg<NB>;
     pdl_launch();
+    const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
     int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
+    float* xch = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES + 256);   // [64][17]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.nt * p.splits;
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
-    auto empty_bar = [&](int s) { return smem_u32(bars + C::STAGES + s); };
-    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + b); };
-    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * C::STAGES + 2 + b); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
+    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * S + b); };
+    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
     auto a_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
     auto b_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmX);
     }
     if (p.rpu > 0) {   // rows [rpu, 128) of every weight tile are never loaded: make them zero once
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             uint4* t = reinterpret_cast<uint4*>(smem + s * C::STAGE_BYTES + p.rpu * 128);
             const int n16 = (128 - p.rpu) * 128 / 16;
             for (int i = threadIdx.x; i < n16; i += blockDim.x) t[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -558,25 +585,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // weight tiles of the first ring stages before waiting for earlier kernels
         int pre = 0;
-        for (int u = blockIdx.x; u < units && pre < C::STAGES; u += gridDim.x) {
+        for (int u = blockIdx.x; u < units && pre < S; u += gridDim.x) {
             const int sp = u / p.nt, nb = u - sp * p.nt;
             const int kb0 = sp * p.kb_per_split;
             const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-            for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+            for (int kb = kb0; kb < kb1 && pre < S; ++kb, ++pre) {
                 mbar_expect_tx(full_bar(pre), stage_tx);
                 load_w(pre, kb * BK, nb);
             }
         }
         pdl_wait();
-        int it = 0;
+        int it = 0, s = 0;          // ring slot of iteration it, and that slot's phase
+        uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int sp = u / p.nt, nb = u - sp * p.nt;
             const int kb0 = sp * p.kb_per_split;
             const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+            for (int kb = kb0; kb < kb1; ++kb, ++it, s = s + 1 == S ? 0 : s + 1, ph ^= (s == 0 ? 1u : 0u)) {
                 const int kx = kb * BK;
                 if (it >= pre) {
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -594,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *issued_slot = ok ? it : max(it, pre);
     } else if (warp == 1 && lane == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
-        int it = 0, j = 0;
+        int it = 0, j = 0, s = 0;   // ring slot of iteration it, and that slot's phase
+        uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
             const int sp = u / p.nt;
@@ -608,9 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+            for (int kb = kb0; kb < kb1; ++kb, ++it, s = s + 1 == S ? 0 : s + 1, ph ^= (s == 0 ? 1u : 0u)) {
                 if (!mbar_wait(full_bar(s), ph, abort_flag)) {
                     *abort_flag = 1;
                     raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
@@ -638,13 +663,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             const int sp = u / p.nt, nb = u - sp * p.nt;
             const int buf = j & 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
+            bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
+            // the SwiGLU hand-off below synchronises the four epilogue warps, so they agree first
+            if (SWIGLU && p.mode == KM_SWIGLU) ok = !bar_or_epilogue(!ok);
             if (!ok) {
                 *abort_flag = 1;
                 raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
                 break;
             }
             tc_fence_after();
+            const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * NB);
+            if (SWIGLU && p.mode == KM_SWIGLU) {
+                // tile rows 0..63 are gate rows and 64..127 the matching up rows: quads 2 and 3 hand
+                // their accumulators to quads 0 and 1 (same lane) through shared memory, 16 columns
+                // at a time, and the gate threads write h = bf16(silu(bf16(g)) * bf16(u)).
+                const int jj = nb * 64 + (r & 63);
+                const bool ok_col = jj < p.n_valid;
+#pragma unroll
+                for (int c = 0; c < NB; c += 16) {
+                    float v[16];
+                    tmem_ld16(tq + c, v);
+                    if (quad >= 2) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) xch[(r - 64) * 17 + q] = v[q];
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (quad < 2 && ok_col) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int b = c + q;
+                            if (b < p.M)
+                                reinterpret_cast<bf16*>(p.out)[(long long)b * p.ldo + jj] =
+                                    f2bf(silu_f(round_bf(v[q])) * round_bf(xch[r * 17 + q]));
+                        }
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                continue;
+            }
             int col;
             bool col_ok;
             if (SWIGLU) {
@@ -659,7 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 col_ok = col < p.n_valid;
             }
             const long long split_off = (long long)sp * p.split_stride;
-            const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * NB);
 #pragma unroll
             for (int c = 0; c < NB; c += 16) {
                 float v[16];
@@ -693,8 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag && warp == 0 && lane == 0) {
         volatile int never = 0;
         const int issued = *issued_slot;
-        for (int i = max(0, issued - C::STAGES); i < issued; ++i)
-            (void)mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, &never);
+        for (int i = max(0, issued - S); i < issued; ++i)
+            (void)mbar_wait(full_bar(i % S), (uint32_t)(i / S) & 1u, &never);
         const int committed = *committed_slot;
         for (int jj = max(0, committed - 2); jj < committed; ++jj)
             (void)mbar_wait(tfull_bar(jj & 1), (uint32_t)(jj >> 1) & 1u, &never);
@@ -1024,7 +1082,12 @@ struct SmallPlan {
     int rpu = 0;     // > 0: row-range units of rpu weight rows over the whole K (nt = units)
 };
 
-SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) {
+// Cost of one extra launch (a split-K reduction and its kernel boundary) in the plan's unit, one
+// 128-row weight k-block per SM round (about 0.3 us at full bandwidth).
+constexpr double kReduceLaunchCost = 10.0;
+
+SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm, bool reduce_free) {
+    const double reduce_cost = reduce_free ? 0.0 : kReduceLaunchCost;
     const int n_kb = K / BK;
     const int per_tile = epi == EPI_SWIGLU ? 64 : 128;
     const int nt = (N + per_tile - 1) / per_tile;
@@ -1036,7 +1099,8 @@ SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) 
         const int splits = (n_kb + kbps - 1) / kbps;
         const long long units = (long long)nt * splits;
         const long long rounds = (units + nsm - 1) / nsm;
-        const double cost = (double)rounds * (kbps + 0.75) + 0.05 * (splits - 1) * ((M + 15) / 16);
+        const double cost = (double)rounds * (kbps + 0.75) + 0.05 * (splits - 1) * ((M + 15) / 16) +
+                            (splits > 1 ? reduce_cost : 0.0);
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best.splits = splits;
@@ -1049,7 +1113,7 @@ SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) 
     if (epi != EPI_SWIGLU && split_req == 0) {
         const int nb_pad = M <= 16 ? 16 : M <= 32 ? 32 : 64;
         const int stage_bytes = 128 * BK * 2 + nb_pad * BK * 2;
-        const int stages = std::min(12, (200 * 1024) / stage_bytes);
+        const int stages = std::min(12, kSmallRingDeep / stage_bytes);
         for (int s = 1; s <= std::min(8, n_kb); ++s) {
             const int rpu = (int)(((long long)N * s + nsm - 1) / nsm);
             if (rpu < 8 || rpu > 128) continue;
@@ -1060,7 +1124,7 @@ SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) 
             const long long units = (long long)((N + rpu - 1) / rpu) * splits;
             const long long rounds = (units + nsm - 1) / nsm;
             const double cost = rounds * (kbps * (rpu / 128.0) / latency_factor + 0.75) +
-                                0.05 * (splits - 1) * ((M + 15) / 16);
+                                0.05 * (splits - 1) * ((M + 15) / 16) + (splits > 1 ? reduce_cost : 0.0);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.rpu = rpu;
@@ -1074,19 +1138,22 @@ SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm) 
 }
 
 template <int NB, bool SW>
-cudaError_t launch_small(const CUtensorMap& mw, const CUtensorMap& mx, const SwArgs& a, int units, cudaStream_t st) {
+cudaError_t launch_small(const CUtensorMap& mw, const CUtensorMap& mx, SwArgs a, int units, int ring_bytes,
+                         cudaStream_t st) {
+    using C = SwCfg<NB>;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
         e = cudaFuncSetAttribute(gemm_smallm_kernel<NB, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SwCfg<NB>::SMEM);
+                                 C::smem_bytes(C::MAX_STAGES));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    a.stages = C::stages_for(ring_bytes);
     dim3 grid((unsigned)std::min(units, device_sm_count()));
-    HRA_LAUNCH(gemm_smallm_kernel<NB, SW>, dim3(grid), dim3(kThreads), SwCfg<NB>::SMEM, st, mw, mx, a);
+    HRA_LAUNCH(gemm_smallm_kernel<NB, SW>, dim3(grid), dim3(kThreads), C::smem_bytes(a.stages), st, mw, mx, a);
     return cudaGetLastError();
 }
 
@@ -1109,15 +1176,15 @@ cudaError_t reduce_partials(const LinearCall& c, int splits, int ldp, cudaStream
 }
 
 cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
-    const SmallPlan pl = make_small_plan(c.M, c.N, c.K, c.epi, c.split_req, device_sm_count());
+    const SmallPlan pl = make_small_plan(c.M, c.N, c.K, c.epi, c.split_req, device_sm_count(), c.partial_only);
     const bool sw = c.epi == EPI_SWIGLU;
     const int w_rows = sw ? 2 * c.N : c.N;
     CUtensorMap mw, mx;
     const int w_box = pl.rpu > 0 ? pl.rpu : (sw ? 64 : 128);
     if (!make_map(&mw, c.w, w_rows, c.K, w_box)) return cudaErrorInvalidValue;
     if (!make_map(&mx, c.a, c.M, c.K, pl.nb)) return cudaErrorInvalidValue;
-    // SwiGLU and every split go through fp32 partials; otherwise the epilogue writes the output.
-    const bool use_partial = sw || pl.splits > 1;
+    // Every split goes through fp32 partials; otherwise the epilogue writes the output.
+    const bool use_partial = pl.splits > 1;
     SwArgs a;
     a.err = c.err;
     a.M = c.M;
@@ -1139,15 +1206,19 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
         a.split_stride = (long long)c.M * ldp;
     } else {
         a.out = c.out;
-        a.mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : KM_F32;
+        a.mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : sw ? KM_SWIGLU : KM_F32;
         a.ldo = c.N;
         a.split_stride = 0;
     }
+    const int ring = c.shallow_ring ? kSmallRingShallow : kSmallRingDeep;
     const int units = pl.nt * pl.splits;
     cudaError_t e;
-    if (pl.nb == 16) e = sw ? launch_small<16, true>(mw, mx, a, units, st) : launch_small<16, false>(mw, mx, a, units, st);
-    else if (pl.nb == 32) e = sw ? launch_small<32, true>(mw, mx, a, units, st) : launch_small<32, false>(mw, mx, a, units, st);
-    else e = sw ? launch_small<64, true>(mw, mx, a, units, st) : launch_small<64, false>(mw, mx, a, units, st);
+    if (pl.nb == 16)
+        e = sw ? launch_small<16, true>(mw, mx, a, units, ring, st) : launch_small<16, false>(mw, mx, a, units, ring, st);
+    else if (pl.nb == 32)
+        e = sw ? launch_small<32, true>(mw, mx, a, units, ring, st) : launch_small<32, false>(mw, mx, a, units, ring, st);
+    else
+        e = sw ? launch_small<64, true>(mw, mx, a, units, ring, st) : launch_small<64, false>(mw, mx, a, units, ring, st);
     if (c.splits_used) *c.splits_used = use_partial ? pl.splits : 1;
     if (e != cudaSuccess || !use_partial || c.partial_only) return e;
     return reduce_partials(c, pl.splits, ldp, st);
@@ -1167,10 +1238,10 @@ int device_sm_count() {
     return cached[dev];
 }
 
-size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req) {
+size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool partial_only) {
     if (M <= kSmallM) {
-        const SmallPlan sp = make_small_plan(M, N, K, epi, split_req, device_sm_count());
-        if (sp.splits <= 1 && epi != EPI_SWIGLU) return 0;
+        const SmallPlan sp = make_small_plan(M, N, K, epi, split_req, device_sm_count(), partial_only);
+        if (sp.splits <= 1) return 0;
         const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
         return (size_t)sp.splits * (size_t)M * ldp * sizeof(float);
     }

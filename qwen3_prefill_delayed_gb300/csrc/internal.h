@@ -89,8 +89,11 @@ struct LinearCall {
     // per-head q/k norm + RoPE + K/V cache write itself (out is not written) and sets *qk_done.
     const QkRopeArgs* qk;
     bool* qk_done;
+    // small-M path: stream the weights through the shallow ring, so that the launch fits on an SM
+    // beside a kernel that still holds much shared memory (the attention before the o-projection)
+    bool shallow_ring;
 };
-size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req);
+size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool partial_only);
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st);
 // Largest partial buffer any automatic plan with M <= m_max rows and these N, K can ask for.
 size_t linear_partial_bound(int m_max, int N, int K, int epi);

@@ -48,6 +48,12 @@ CASES = [
     (16, 6144, 2560, "residual", 0),
     (64, 8208, 2560, "f32", 0),
     (64, 8208, 2560, "f32", 7),
+    # small M, one K split: SwiGLU applied in the GEMM epilogue (gate and up halves of the tile)
+    (1, 9728, 2560, "swiglu", 0),
+    (32, 9728, 2560, "swiglu", 1),
+    (64, 1000, 512, "swiglu", 0),          # ragged last tile: 1000 = 15 x 64 + 40
+    (17, 200, 256, "swiglu", 1),
+    (32, 768, 256, "swiglu", 3),           # partials + reduction
 ]
 
 
