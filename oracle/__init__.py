@@ -68,6 +68,9 @@ def lib():
         L.oracle_prefill.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
                                      _u16p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, _u16p,
                                      ctypes.c_int, ctypes.c_int, _u16p]
+        L.oracle_prefill_chunk.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
+                                           _u16p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, _u16p,
+                                           ctypes.c_int, ctypes.c_int, _u16p]
         L.oracle_decode.argtypes = [ctypes.POINTER(OracleDims), ctypes.POINTER(OracleLayer), _u16p,
                                     _u16p, _i32p, ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int,
                                     _u16p]
@@ -78,7 +81,8 @@ def lib():
         L.oracle_codebook_step.argtypes = [ctypes.POINTER(OracleDims), _u16p, _u16p, _u16p, _i32p,
                                            ctypes.c_void_p, ctypes.c_int, _i32p, _u16p, _i32p,
                                            ctypes.c_void_p]
-        for f in ("oracle_prefill", "oracle_decode", "oracle_codebook_step", "oracle_max_threads"):
+        for f in ("oracle_prefill", "oracle_prefill_chunk", "oracle_decode", "oracle_codebook_step",
+                  "oracle_max_threads"):
             getattr(L, f).restype = ctypes.c_int
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_set_sum_order.argtypes = [ctypes.c_int]
@@ -220,6 +224,24 @@ def prefill(d, w: HostWeights, tokens: np.ndarray, lens, n_slots: int,
     if rc != 0:
         raise ValueError("oracle_prefill rejected its arguments")
     return kv, last
+
+
+def prefill_chunk(d, w: HostWeights, tokens: np.ndarray, lens, starts, kv: np.ndarray, n_slots: int):
+    """One chunk per sequence at positions starts[b] .. starts[b] + lens[b] - 1 after the cached ones.
+
+    kv [L, B, 2, nkv, n_slots, hd] uint16 is read below each start and written in place; returns
+    last_hidden [B, H] uint16."""
+    tokens = _c(tokens, np.int32)
+    lens = _c(lens, np.int32)
+    starts = _c(starts, np.int32)
+    B, P = tokens.shape
+    last = np.empty((B, d.hidden), np.uint16)
+    dims = make_dims(d)
+    rc = lib().oracle_prefill_chunk(ctypes.byref(dims), w.embed, w.table, w.final_norm, tokens, lens, starts,
+                                    B, P, kv, kv.shape[1], n_slots, last)
+    if rc != 0:
+        raise ValueError("oracle_prefill_chunk rejected its arguments")
+    return last
 
 
 def decode(d, w: HostWeights, in_emb: np.ndarray, pos, kv: np.ndarray, n_slots: int) -> np.ndarray:

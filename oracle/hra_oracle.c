@@ -6,7 +6,8 @@
  * library and includes none of it.
  *
  * What it computes (each function cites its source):
- *   - batched prefill of a Qwen3-style decoder backbone: embedding lookup, RMSNorm, merged QKV
+ *   - batched prefill of a Qwen3-style decoder backbone (from position 0, or one chunk per
+ *     sequence after the positions already in the cache): embedding lookup, RMSNorm, merged QKV
  *     projection, per-head q/k RMSNorm + rotate-half RoPE with the KV-cache write, causal GQA
  *     attention over the used keys, o-projection + residual, RMSNorm, SwiGLU MLP + residual,
  *     final RMSNorm at the last used position ("Stabilize Higgs Audio termination and prefill",
@@ -328,37 +329,53 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
     free(r); free(y); free(qkv); free(qr); free(att); free(hmid); free(acc); free(ct); free(st);
 }
 
-/* Batched prefill.  tokens [B][P_max] with trailing pads (never read); seq_lens[B] in [1, n_slots].
- * kv [L][kv_batch][2][nkv][n_slots][hd]: slots 0..len-1 of sequence b are written, others untouched.
- * last_hidden [B][H] = final RMSNorm of position len_b - 1.  Returns 0, or -1 on a bad argument.
+/* Prefill of one chunk per sequence after the positions already in the cache.  Sequence b's
+ * seq_lens[b] tokens tokens[b][0..len) sit at positions starts[b] .. starts[b] + len - 1 (starts
+ * NULL: all 0).  Cache slots 0..starts[b]-1 hold that sequence's earlier keys and values and are
+ * read, never written; slots starts[b] .. starts[b]+len-1 are written; the rest stay untouched.
+ * Each new position attends every slot up to itself.  last_hidden [B][H] = final RMSNorm of
+ * position starts[b] + len_b - 1.  Returns 0, or -1 on a bad argument.
  * Source: batched prefill with KV writes ("Stabilize Higgs Audio termination and prefill",
- * Summary); pads trail and only the used keys are attended ("fp8_chain.py", module docstring). */
-int oracle_prefill(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
-                   const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
-                   int B, int P_max, uint16_t* kv, int kv_batch, int n_slots, uint16_t* last_hidden) {
+ * Summary); pads trail and only the used keys are attended ("fp8_chain.py", module docstring);
+ * mixed batches of prefill chunks and single-token steps under one launch bound taken from the
+ * real batch (vLLM-Omni PR #8226, Purpose). */
+int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                         const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
+                         const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
+                         uint16_t* last_hidden) {
     const int H = d->hidden;
     const size_t blk = (size_t)2 * d->n_kv_heads * n_slots * d->head_dim;
     if (B < 1 || B > kv_batch) return -1;
     for (int b = 0; b < B; ++b) {
-        int n = seq_lens[b];
-        if (n < 1 || n > P_max || n > n_slots) return -1;
+        const int n = seq_lens[b], s0 = starts ? starts[b] : 0;
+        if (n < 1 || n > P_max || s0 < 0 || s0 + n > n_slots) return -1;
         for (int i = 0; i < n; ++i)
             if (tokens[(size_t)b * P_max + i] < 0 || tokens[(size_t)b * P_max + i] >= d->vocab) return -1;
     }
     for (int b = 0; b < B; ++b) {
-        int n = seq_lens[b];
+        const int n = seq_lens[b], s0 = starts ? starts[b] : 0;
         uint16_t* x = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
         uint16_t* hid = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * H);
         for (int i = 0; i < n; ++i)
             memcpy(x + (size_t)i * H, embed + (size_t)tokens[(size_t)b * P_max + i] * H,
                    sizeof(uint16_t) * H);
-        forward_rows(d, layers, final_norm, x, 0, n, kv + (size_t)b * blk, (size_t)kv_batch * blk,
+        forward_rows(d, layers, final_norm, x, s0, n, kv + (size_t)b * blk, (size_t)kv_batch * blk,
                      n_slots, hid);
         memcpy(last_hidden + (size_t)b * H, hid + (size_t)(n - 1) * H, sizeof(uint16_t) * H);
         free(x);
         free(hid);
     }
     return 0;
+}
+
+/* Batched prefill from position 0: tokens [B][P_max] with trailing pads (never read); seq_lens[B]
+ * in [1, n_slots].  kv [L][kv_batch][2][nkv][n_slots][hd]: slots 0..len-1 of sequence b are
+ * written, others untouched.  last_hidden [B][H] = final RMSNorm of position len_b - 1. */
+int oracle_prefill(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                   const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
+                   int B, int P_max, uint16_t* kv, int kv_batch, int n_slots, uint16_t* last_hidden) {
+    return oracle_prefill_chunk(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch,
+                                n_slots, last_hidden);
 }
 
 /* Single-token decode pass: row b is the embedding in_emb[b] at position pos[b]; it writes cache

@@ -75,6 +75,64 @@ def test_decode_extends_prefill(orc, tiny):
     np.testing.assert_array_equal(kv_a, kv_b)
 
 
+def test_chunked_prefill_equals_whole(orc, tiny):
+    """A batch mixing a first chunk (start 0), a single-token step and a multi-token chunk after
+    cached positions reproduces, bit for bit, the prefill of each whole sequence."""
+    d, _, hw = tiny
+    rng = np.random.default_rng(5)
+    lens = [13, 10, 12]
+    tok = _tokens(rng, lens, d.vocab)
+    kv_w, last_w = orc.prefill(d, hw, tok, lens, 32)
+    cut = [0, 9, 5]                      # positions already in the cache before the chunk
+    kv = np.full(orc.kv_shape(d, 3, 32), 0x7fc1, np.uint16)
+    first = list(cut)
+    pre = [b for b in range(3) if first[b] > 0]
+    t_pre = np.zeros((len(pre), max(first)), np.int32)
+    for j, b in enumerate(pre):
+        t_pre[j, :first[b]] = tok[b, :first[b]]
+    kv_pre, _ = orc.prefill(d, hw, t_pre, [first[b] for b in pre], 32)
+    for j, b in enumerate(pre):
+        kv[:, b, :, :, :first[b]] = kv_pre[:, j, :, :, :first[b]]
+    before = kv.copy()
+    n_new = [lens[b] - cut[b] for b in range(3)]
+    n_new[1] = 1                          # sequence 1 takes one token (a decode-like step)
+    t_new = np.full((3, max(n_new)), d.vocab + 5, np.int32)   # trailing pads: out-of-range ids, never read
+    for b in range(3):
+        t_new[b, :n_new[b]] = tok[b, cut[b]:cut[b] + n_new[b]]
+    last = orc.prefill_chunk(d, hw, t_new, n_new, cut, kv, 32)
+    for b in (0, 2):
+        np.testing.assert_array_equal(last[b], last_w[b])
+        np.testing.assert_array_equal(kv[:, b, :, :, :lens[b]], kv_w[:, b, :, :, :lens[b]])
+    # sequence 1 stopped after cut + 1 positions: equal to the whole prefill of that prefix
+    kv_1, last_1 = orc.prefill(d, hw, tok[1:2, :cut[1] + 1], [cut[1] + 1], 32)
+    np.testing.assert_array_equal(last[1], last_1[0])
+    np.testing.assert_array_equal(kv[:, 1, :, :, :cut[1] + 1], kv_1[:, 0, :, :, :cut[1] + 1])
+    # cached slots are read only; slots past each chunk stay untouched
+    for b in range(3):
+        np.testing.assert_array_equal(kv[:, b, :, :, :cut[b]], before[:, b, :, :, :cut[b]])
+        assert np.all(kv[:, b, :, :, cut[b] + n_new[b]:] == 0x7fc1)
+
+
+def test_chunk_reads_the_cached_prefix(orc, tiny):
+    """The chunk attends the cached keys: perturbing one cached key changes its output, perturbing
+    a slot past the chunk does not; a start that runs past the cache is rejected."""
+    d, _, hw = tiny
+    rng = np.random.default_rng(6)
+    tok = _tokens(rng, [10], d.vocab)
+    kv0, _ = orc.prefill(d, hw, tok[:, :6], [6], 32)
+    base = orc.prefill_chunk(d, hw, tok[:, 6:], [4], [6], kv0.copy(), 32)
+    kv1 = kv0.copy()
+    kv1[0, 0, 0, 0, 3, :] ^= 0x0040              # key of position 3, layer 0, kv head 0
+    moved = orc.prefill_chunk(d, hw, tok[:, 6:], [4], [6], kv1, 32)
+    assert np.any(moved != base)
+    kv2 = kv0.copy()
+    kv2[..., 20, :] = 0x7fc1                     # a slot no position of the chunk reaches
+    same = orc.prefill_chunk(d, hw, tok[:, 6:], [4], [6], kv2, 32)
+    np.testing.assert_array_equal(same, base)
+    with pytest.raises(ValueError):
+        orc.prefill_chunk(d, hw, tok[:, 6:], [4], [29], kv0.copy(), 32)
+
+
 def _one_layer(d, w, **override):
     d1 = W.Dims(**{**d.__dict__, "n_layers": 1})
     lay = {k: v.clone() for k, v in w["layers"][0].items()}
