@@ -405,6 +405,12 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
         out["codebook_decode"] = bench_codebook(hra, W, torch, dev, hbm, peaks_kind)
     except Exception as ex:
         out["codebook_decode"] = {"error": repr(ex)}
+    # ---- the ragged batch prefilled in two chunks (the second reads the first from the cache)
+    try:
+        out["chunked_prefill"] = bench_chunked(hra, W, torch, dev, w_backbone)
+    except Exception as ex:
+        out["chunked_prefill"] = {"error": repr(ex)}
+    torch.cuda.empty_cache()
     # ---- long prompts + 64 AR frames
     try:
         out["long_prompts"] = bench_long(hra, W, torch, dev, w_backbone)
@@ -466,6 +472,45 @@ def bench_codebook(hra, W, torch, dev, hbm, peaks_kind):
     res["note"] = (f"200 chained steps in one CUDA graph; hbm_cold rotates 4 weight copies (336 MB > L2); "
                    f"hbm_frac is of the {peaks_kind} copy bandwidth")
     return res
+
+
+def bench_chunked(hra, W, torch, dev, w_backbone):
+    """The 32 ragged prompts as two chunks per sequence: the first ceil(len/2) tokens from position
+    0, then the rest after them (hra_prefill_chunk), against the whole prompts in one call."""
+    d = W.full_dims(36)
+    p = W.make_prompts(2, 32, 16, 256, d.vocab)       # the ragged batch's prompts
+    bb = hra.Backbone(d, w_backbone)
+    B = len(p.lengths)
+    lens = list(p.lengths)
+    first = [(n + 1) // 2 for n in lens]
+    rest = [n - f for n, f in zip(lens, first)]
+    tok = p.tokens.to(dev)
+    tok1 = p.tokens[:, :max(first)].contiguous().to(dev)
+    tok2 = torch.zeros(B, max(rest), dtype=torch.int32)
+    for b in range(B):
+        tok2[b, :rest[b]] = p.tokens[b, first[b]:lens[b]]
+    tok2 = tok2.to(dev)
+    cache = hra.new_kv_cache(d, B, 2048, dev)
+    out = torch.empty(B, d.hidden, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(bb.prefill_workspace_size(B, sum(lens), max(lens)),
+                         bb.prefill_chunk_workspace_size(B, sum(rest), max(rest), max(lens))),
+                     dtype=torch.uint8, device=dev)
+    whole = lambda: bb.prefill(tok, lens, cache, out=out, workspace=ws)
+    c1 = lambda: bb.prefill(tok1, first, cache, out=out, workspace=ws)
+    c2 = lambda: bb.prefill(tok2, rest, cache, out=out, workspace=ws, start_pos=first)
+    for f in (whole, c1, c2):
+        for _ in range(2):
+            f()
+    torch.cuda.synchronize()
+    ms_whole = events_time(whole, 5, torch) / 5
+    ms_c1 = events_time(c1, 5, torch) / 5
+    c1()
+    ms_c2 = events_time(c2, 5, torch) / 5
+    del cache
+    return {"whole_tokens_per_s": sum(lens) / (ms_whole / 1e3), "whole_ms": ms_whole,
+            "chunk1_ms": ms_c1, "chunk2_ms": ms_c2, "chunk2_tokens": sum(rest),
+            "chunk2_tokens_per_s": sum(rest) / (ms_c2 / 1e3),
+            "two_chunks_tokens_per_s": sum(lens) / ((ms_c1 + ms_c2) / 1e3)}
 
 
 def bench_long(hra, W, torch, dev, w_backbone):

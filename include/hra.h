@@ -120,6 +120,30 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
                 void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags,
                 void* stream);
 
+/* Prefill of one chunk per sequence after the positions already in its cache: a later piece of a
+ * long prompt (chunked prefill), a single token of a running sequence, or a mix of both in one
+ * launch -- the mixed prefill batches whose launch bound must come from the real batch
+ * (vLLM-Omni PR #8226, Purpose).  Same arguments as hra_prefill, plus:
+ *   start_pos    host int32 [batch]: sequence b's seq_lens[b] tokens sit at positions
+ *                start_pos[b] .. start_pos[b] + seq_lens[b] - 1; 0 <= start_pos[b] and
+ *                start_pos[b] + seq_lens[b] <= kv->n_slots (else HRA_ERR_RANGE).
+ *   tokens_dev   int32 [batch, max_len]: row b holds the chunk's tokens (not the whole prompt).
+ *   kv           slots [0, start_pos[b]) of sequence b must hold that sequence's earlier keys and
+ *                values (from earlier calls); they are read, never written.  Slots
+ *                [start_pos[b], start_pos[b] + seq_lens[b]) are written; the rest stay untouched.
+ *   last_hidden_dev bf16 [batch, hidden]: final RMSNorm output at position
+ *                start_pos[b] + seq_lens[b] - 1.
+ *   workspace    at least hra_prefill_chunk_workspace_size() bytes, with max_end the largest
+ *                start_pos[b] + seq_lens[b].
+ * With every start_pos[b] = 0 this is hra_prefill.  Returns HRA_OK or a negative status (nothing
+ * enqueued); start_pos == NULL is HRA_ERR_INVALID_ARG. */
+size_t hra_prefill_chunk_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens,
+                                        int32_t max_len, int32_t max_end);
+int hra_prefill_chunk(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                      const int32_t* seq_lens, const int32_t* start_pos, int32_t batch, int32_t max_len,
+                      const hra_kv_cache* kv, void* last_hidden_dev, void* workspace,
+                      size_t workspace_bytes, uint32_t flags, void* stream);
+
 /* ---- decode pass ---------------------------------------------------------------------------- */
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots);
 

@@ -123,10 +123,11 @@ void oracle_rmsnorm(const uint16_t* x, const uint16_t* g, int64_t rows, int n, f
  * outside and tokens t inside, so a weight row is read once per call whatever T is. */
 static int g_sum_descending = 0;
 
-/* Summation order of every linear dot product: ascending k (default) or descending k.  Both are
- * plain evaluations of the same definition; running the oracle both ways measures how far two
- * correct bf16 evaluations of this model drift apart (the comparison floor of any other
- * implementation, whose fp32 sums take yet another order). */
+/* Summation order of every dot product and sum whose order the method leaves open -- the linear
+ * projections and attention's q.k, softmax-denominator and p.v sums: ascending (default) or
+ * descending.  Both are plain evaluations of the same definition; running the oracle both ways
+ * measures how far two correct bf16 evaluations of this model drift apart (the comparison floor
+ * of any other implementation, whose fp32 sums take yet another order). */
 void oracle_set_sum_order(int descending) { g_sum_descending = descending != 0; }
 
 void oracle_linear(const uint16_t* x, const uint16_t* w, int T, int N, int K, float* y) {
@@ -224,21 +225,28 @@ void oracle_attend(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, in
             const uint16_t* kh = kc + (size_t)kvh * n_slots * hd;
             const uint16_t* vh = vc + (size_t)kvh * n_slots * hd;
             float* s = (float*)malloc(sizeof(float) * (size_t)(pos + 1));
+            /* summation order of the three sums (q.k over the head dim, the softmax denominator
+             * and p.v over the keys): ascending, or descending under oracle_set_sum_order(1) */
+            const int desc = g_sum_descending;
             float m = -INFINITY;
             for (int j = 0; j <= pos; ++j) {
                 float dot = 0.0f;
-                for (int e = 0; e < hd; ++e) dot += bf(qi[e]) * bf(kh[(size_t)j * hd + e]);
+                for (int t = 0; t < hd; ++t) {
+                    const int e = desc ? hd - 1 - t : t;
+                    dot += bf(qi[e]) * bf(kh[(size_t)j * hd + e]);
+                }
                 s[j] = dot * scale;
                 if (s[j] > m) m = s[j];
             }
             float l = 0.0f;
-            for (int j = 0; j <= pos; ++j) {
-                s[j] = expf(s[j] - m);
-                l += s[j];
-            }
+            for (int j = 0; j <= pos; ++j) s[j] = expf(s[j] - m);
+            for (int t = 0; t <= pos; ++t) l += s[desc ? pos - t : t];
             for (int e = 0; e < hd; ++e) {
                 float acc = 0.0f;
-                for (int j = 0; j <= pos; ++j) acc += s[j] * bf(vh[(size_t)j * hd + e]);
+                for (int t = 0; t <= pos; ++t) {
+                    const int j = desc ? pos - t : t;
+                    acc += s[j] * bf(vh[(size_t)j * hd + e]);
+                }
                 out[(size_t)i * nq * hd + (size_t)h * hd + e] = to_bf(acc / l);
             }
             if (probs) {

@@ -6,7 +6,8 @@ This module is a thin ctypes binding of the in-tree CUDA library ``libhra.so`` (
 path runs in the library's kernels.  There is no CPU fallback -- calling anything here without the
 built library, or with tensors not on a CUDA device, raises.
 
-Entry points (same names as the C ABI): ``hra_prefill``, ``hra_decode``, ``hra_codebook_step``,
+Entry points (same names as the C ABI): ``hra_prefill`` (and ``hra_prefill_chunk`` through
+``Backbone.prefill(..., start_pos=...)``), ``hra_decode``, ``hra_codebook_step``,
 ``hra_linear``, ``hra_device_error``; convenience wrappers ``Backbone`` and ``AudioHead`` keep the
 weight tables and workspaces.
 """
@@ -28,7 +29,8 @@ DEVERR_TOKEN_RANGE, DEVERR_WAIT_TIMEOUT, DEVERR_CODE_RANGE = 1, 2, 4
 EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_F32 = 0, 1, 2, 3
 PREFILL_FULL_LAST_LAYER = 1
 
-EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_decode_workspace_size", "hra_decode",
+EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_workspace_size", "hra_prefill_chunk",
+            "hra_decode_workspace_size", "hra_decode",
             "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_noalloc",
             "hra_linear_workspace_size",
             "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
@@ -82,6 +84,12 @@ def lib() -> ctypes.CDLL:
         L.hra_prefill.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32, i32,
                                   ctypes.POINTER(HraKvCache), vp, vp, sz, u32, vp]
         L.hra_prefill.restype = ctypes.c_int
+        L.hra_prefill_chunk_workspace_size.argtypes = [dp, i32, i32, i32, i32]
+        L.hra_prefill_chunk_workspace_size.restype = sz
+        L.hra_prefill_chunk.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32), i32, i32, ctypes.POINTER(HraKvCache), vp, vp, sz,
+                                        u32, vp]
+        L.hra_prefill_chunk.restype = ctypes.c_int
         L.hra_decode_workspace_size.argtypes = [dp, i32, i32]
         L.hra_decode_workspace_size.restype = sz
         L.hra_decode.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32,
@@ -190,23 +198,42 @@ class Backbone:
     def prefill_workspace_size(self, batch, total, max_len) -> int:
         return lib().hra_prefill_workspace_size(ctypes.byref(self.dims), batch, total, max_len)
 
+    def prefill_chunk_workspace_size(self, batch, total, max_len, max_end) -> int:
+        return lib().hra_prefill_chunk_workspace_size(ctypes.byref(self.dims), batch, total, max_len, max_end)
+
     def prefill(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor,
                 out: Optional[torch.Tensor] = None, full_last_layer: bool = False,
-                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """hra_prefill: tokens int32 [B, P_max] (CUDA), seq_lens host ints -> last hidden [B, H]."""
+                workspace: Optional[torch.Tensor] = None, stream=None,
+                start_pos: Optional[Sequence[int]] = None) -> torch.Tensor:
+        """hra_prefill: tokens int32 [B, P_max] (CUDA), seq_lens host ints -> last hidden [B, H].
+
+        With start_pos (host ints), hra_prefill_chunk: row b's tokens sit at positions
+        start_pos[b] .. start_pos[b] + seq_lens[b] - 1 after the ones already in the cache."""
         B, P = tokens.shape
         lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens])
         if out is None:
             out = torch.empty(B, self.d.hidden, dtype=torch.bfloat16, device=tokens.device)
-        need = self.prefill_workspace_size(B, int(sum(seq_lens)), P)
-        ws = workspace if workspace is not None else self.ws.get(need, tokens.device)
+        flags = PREFILL_FULL_LAST_LAYER if full_last_layer else 0
         kv = self.kv(cache)
-        rc = lib().hra_prefill(ctypes.byref(self.dims), ctypes.byref(self.table),
-                               _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
-                               _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
-                               ws.numel(), PREFILL_FULL_LAST_LAYER if full_last_layer else 0,
-                               _stream(stream))
-        _check(rc, "hra_prefill")
+        if start_pos is None:
+            need = self.prefill_workspace_size(B, int(sum(seq_lens)), P)
+        else:
+            starts = (ctypes.c_int32 * B)(*[int(x) for x in start_pos])
+            max_end = max(int(a) + int(n) for a, n in zip(start_pos, seq_lens))
+            need = self.prefill_chunk_workspace_size(B, int(sum(seq_lens)), P, max(max_end, P))
+        ws = workspace if workspace is not None else self.ws.get(need, tokens.device)
+        if start_pos is None:
+            rc = lib().hra_prefill(ctypes.byref(self.dims), ctypes.byref(self.table),
+                                   _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
+                                   _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
+                                   ws.numel(), flags, _stream(stream))
+            _check(rc, "hra_prefill")
+        else:
+            rc = lib().hra_prefill_chunk(ctypes.byref(self.dims), ctypes.byref(self.table),
+                                         _ptr(tokens, torch.int32, "tokens"), lens, starts, B, P,
+                                         ctypes.byref(kv), _ptr(out, torch.bfloat16, "last_hidden"),
+                                         _ptr(ws, None, "workspace"), ws.numel(), flags, _stream(stream))
+            _check(rc, "hra_prefill_chunk")
         self.last_ws = ws
         return out
 

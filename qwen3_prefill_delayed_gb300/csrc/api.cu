@@ -73,7 +73,7 @@ struct Region {
 
 // Offsets (bytes) of every buffer inside a caller workspace.
 struct Layout {
-    size_t err, row_seq, row_pos, cu, last_row, rope, r, y, qkv, q, att, h, rl, part, apart, total;
+    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, total;
     int attn_splits;
 };
 
@@ -112,6 +112,7 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     L.row_pos = g.take(T * 4);
     L.cu = g.take((size_t)(batch + 1) * 4);
     L.last_row = g.take((size_t)batch * 4);
+    L.start = g.take((size_t)batch * 4);
     L.rope = g.take((size_t)rope_rows * (hd / 2) * sizeof(float2));
     L.r = g.take(T * H * 2);
     L.y = g.take(T * H * 2);
@@ -196,7 +197,8 @@ bool layer_ptrs_ok(const hra_layer_weights& l) {
 // `attn_last_only` switches the tail to the B-row path (prefill's last layer).
 int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
                int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
-               const int32_t* seq_lens_host, int max_pos, cudaStream_t st) {
+               const int32_t* seq_lens_host, int max_pos, cudaStream_t st, int rope_rows = 0,
+               const int32_t* start_host = nullptr) {
     const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d.rms_eps;
@@ -211,12 +213,14 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
     const int32_t* row_pos = P.at<int32_t>(L.row_pos);
     const int32_t* last_row = P.at<int32_t>(L.last_row);
     const size_t layer_elems = (size_t)kv.batch * 2 * nkv * (size_t)kv.n_slots * hd;
-    // prefill: causal QK^T + PV FLOPs over the used keys, 4 nq hd sum_b len_b (len_b + 1) / 2;
+    // prefill: causal QK^T + PV FLOPs over the used keys, 4 nq hd sum_b (len_b s_b + len_b (len_b + 1) / 2)
+    // with s_b the cached positions before the sequence's rows;
     // decode (seq_lens_host = positions): K/V bytes read, 4 nkv hd sum_b (pos_b + 1)
     double attn_work = 0.0;
     for (int b = 0; b < batch && seq_lens_host != nullptr; ++b) {
         const double n = (double)seq_lens_host[b];
-        attn_work += prefill ? 4.0 * nq * hd * n * (n + 1.0) / 2.0 : 4.0 * nkv * hd * (n + 1.0);
+        const double s0 = start_host ? (double)start_host[b] : 0.0;
+        attn_work += prefill ? 4.0 * nq * hd * (n * s0 + n * (n + 1.0) / 2.0) : 4.0 * nkv * hd * (n + 1.0);
     }
     const int lin_probe = prefill ? 0 : HRA_PROBE_DECODE_LINEAR;
 
@@ -229,7 +233,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
         qa.k_norm = reinterpret_cast<const bf16*>(lw.k_norm);
         qa.rope = P.at<float2>(L.rope);
-        qa.rope_rows = prefill ? max_len : batch;
+        qa.rope_rows = prefill ? rope_rows : batch;
         qa.row_seq = row_seq;
         qa.row_pos = row_pos;
         qa.rope_row_is_pos = prefill ? 1 : 0;
@@ -249,7 +253,8 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         const bool tail = prefill && last && !full_last;
         if (!tail) {
             if (prefill) {
-                PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), att, batch, max_len, kv.n_slots, nq, nkv, hd};
+                PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), P.at<int32_t>(L.start), att, batch, max_len,
+                                   kv.n_slots, nq, nkv, hd};
                 HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] { return launch_prefill_attention(pa, st); }));
             } else {
                 DecodeAttnArgs da{};
@@ -296,12 +301,12 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             da.out = att;
             da.part = P.at<float>(L.apart);
             da.rows = batch;
-            da.max_pos = max_len - 1;
+            da.max_pos = max_pos;
             da.n_slots = kv.n_slots;
             da.nq = nq;
             da.nkv = nkv;
             da.hd = hd;
-            da.splits = std::min(L.attn_splits, decode_attention_splits(batch, nkv, max_len - 1));
+            da.splits = std::min(L.attn_splits, decode_attention_splits(batch, nkv, max_pos));
             HRA_TRY(launch_decode_attention(da, st));
             HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
             HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps, nullptr, 0,
@@ -360,13 +365,20 @@ int hra_probe_collect(double* total_ms, int64_t* launches, double* total_work) {
 
 
 size_t hra_prefill_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
-    if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1) return 0;
-    return backbone_layout(*dims, batch, total_tokens, max_len, max_len - 1).total;
+    return hra_prefill_chunk_workspace_size(dims, batch, total_tokens, max_len, max_len);
 }
 
-int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
-                const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
-                void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+size_t hra_prefill_chunk_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len,
+                                        int32_t max_end) {
+    if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1 || max_end < max_len) return 0;
+    return backbone_layout(*dims, batch, total_tokens, max_end, max_end - 1).total;
+}
+
+namespace {
+
+int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev, const int32_t* seq_lens,
+                 const int32_t* start_pos, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                 void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
     if (dims == nullptr || weights == nullptr || tokens_dev == nullptr || seq_lens == nullptr || kv == nullptr)
         return HRA_ERR_INVALID_ARG;
     if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
@@ -380,29 +392,52 @@ int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t*
     meta.batch = batch;
     meta.mode = 0;
     long long T = 0;
+    int max_end = 1;
     for (int b = 0; b < batch; ++b) {
         const int n = seq_lens[b];
-        if (n < 1 || n > max_len || n > kv->n_slots) return HRA_ERR_RANGE;
+        const int s0 = start_pos ? start_pos[b] : 0;
+        if (n < 1 || n > max_len || s0 < 0 || (long long)s0 + n > kv->n_slots) return HRA_ERR_RANGE;
         meta.vals[b] = (int32_t)T;
+        meta.start[b] = s0;
         T += n;
+        max_end = std::max(max_end, s0 + n);
     }
     meta.vals[batch] = (int32_t)T;
     if (T > (1 << 30)) return HRA_ERR_RANGE;
-    const Layout L = backbone_layout(d, batch, (int)T, max_len, max_len - 1);
+    const Layout L = backbone_layout(d, batch, (int)T, max_end, max_end - 1);
     if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
     HRA_TRY(launch_build_rowmap(meta, (int)T, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
-                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<unsigned int>(L.err), st));
-    HRA_TRY(launch_rope_table(max_len, nullptr, d.head_dim, (double)d.rope_theta, P.at<float2>(L.rope), st));
-    HRA_TRY(launch_embed_rmsnorm(tokens_dev, max_len, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<int32_t>(L.start),
+                                P.at<unsigned int>(L.err), st));
+    HRA_TRY(launch_rope_table(max_end, nullptr, d.head_dim, (double)d.rope_theta, P.at<float2>(L.rope), st));
+    HRA_TRY(launch_embed_rmsnorm(tokens_dev, max_len, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.cu),
                                  reinterpret_cast<const bf16*>(weights->embed), d.vocab,
                                  reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.r),
                                  P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
     return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
                       (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), seq_lens,
-                      max_len - 1, st);
+                      max_end - 1, st, max_end, start_pos);
+}
+
+}  // namespace
+
+int hra_prefill(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+    return prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last_hidden_dev, workspace,
+                        workspace_bytes, flags, stream);
+}
+
+int hra_prefill_chunk(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                      const int32_t* seq_lens, const int32_t* start_pos, int32_t batch, int32_t max_len,
+                      const hra_kv_cache* kv, void* last_hidden_dev, void* workspace, size_t workspace_bytes,
+                      uint32_t flags, void* stream) {
+    if (start_pos == nullptr) return HRA_ERR_INVALID_ARG;
+    return prefill_impl(dims, weights, tokens_dev, seq_lens, start_pos, batch, max_len, kv, last_hidden_dev,
+                        workspace, workspace_bytes, flags, stream);
 }
 
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots) {
@@ -437,7 +472,8 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
     HRA_TRY(launch_build_rowmap(meta, batch, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
-                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<unsigned int>(L.err), st));
+                                P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), nullptr, P.at<unsigned int>(L.err),
+                                st));
     HRA_TRY(launch_rope_table(batch, P.at<int32_t>(L.row_pos), d.head_dim, (double)d.rope_theta,
                               P.at<float2>(L.rope), st));
     // r = input embedding, y = RMSNorm(r) with layer 0's attention gain

@@ -6,7 +6,8 @@
 // keys (pads trail, so a used-key count carries the host's mask)"; causal here because the
 // backbone is a decoder).
 //
-// prefill_attn_kernel  flash-attention style: one CTA = 64 queries x one q head of one sequence,
+// prefill_attn_kernel  flash-attention style: one CTA = 64 queries x one q head of one sequence
+//                      (whose rows may follow positions already in the cache: they attend those too),
 //                      4 warps x 16 query rows; K/V tiles of 64 keys double-buffered with cp.async
 //                      into XOR-swizzled shared memory; S = QK^T and O += PV on warp-level
 //                      bf16 MMA (m16n8k16) with fp32 online softmax; P enters PV as a bf16
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     const int q0 = qt * PQ;
     if (q0 >= len) return;
     const int kvh = h / (a.nq / a.nkv);
-    const int kv_len = min(len, q0 + PQ);
+    const int s0 = a.start ? a.start[b] : 0;          // cached positions before this sequence's rows
+    const int kv_len = s0 + min(len, q0 + PQ);        // keys this query tile can reach
     const int n_kt = (kv_len + PK - 1) / PK;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     for (int d = 0; d < DN; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     const int g = lane >> 2, tig = lane & 3;
-    const int qa = q0 + warp * 16 + g, qb = qa + 8;   // query positions of this thread's two rows
+    const int qa = q0 + warp * 16 + g, qb = qa + 8;   // this thread's two query rows (within the sequence)
+    const int pa = s0 + qa, pb = s0 + qb;             // and their positions
 
     for (int kt = 0; kt < n_kt; ++kt) {
         const int buf = kt & 1;
@@ -133,16 +136,16 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
             }
         }
         // scale, causal + length mask
-        const bool need_mask = (j0 + PK > q0) || (j0 + PK > len);
+        const bool need_mask = (j0 + PK > s0 + q0) || (j0 + PK > s0 + len);
         float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int key = j0 + n * 8 + 2 * tig + (c & 1);
-                const int qp = c < 2 ? qa : qb;
+                const int qp = c < 2 ? pa : pb;
                 float v = s[n][c] * scale_log2;
-                if (need_mask && (key > qp || key >= len)) v = -INFINITY;
+                if (need_mask && (key > qp || key >= s0 + len)) v = -INFINITY;
                 s[n][c] = v;
             }
             mx_a = fmaxf(mx_a, fmaxf(s[n][0], s[n][1]));

@@ -19,7 +19,7 @@ namespace hra {
 namespace {
 
 __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq, int32_t* row_pos,
-                                    int32_t* cu, int32_t* last_row, unsigned int* err) {
+                                    int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err) {
     pdl_launch();
     pdl_wait();
     if (err != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err = 0u;   // first kernel of a call
@@ -37,12 +37,15 @@ __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq,
                 if (s_vals[mid] <= r) lo = mid; else hi = mid - 1;
             }
             row_seq[r] = lo;
-            row_pos[r] = r - s_vals[lo];
+            row_pos[r] = meta.start[lo] + r - s_vals[lo];
         }
         if (blockIdx.x == 0)
             for (int b = threadIdx.x; b <= B; b += blockDim.x) {
                 cu[b] = s_vals[b];
-                if (b < B) last_row[b] = s_vals[b + 1] - 1;
+                if (b < B) {
+                    last_row[b] = s_vals[b + 1] - 1;
+                    if (seq_start != nullptr) seq_start[b] = meta.start[b];
+                }
             }
     } else {
         if (r < T) {
@@ -130,7 +133,7 @@ __device__ __forceinline__ void norm_row(const uint4* __restrict__ src, uint4* _
 
 template <int NC>
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok_ld,
-                                     const int32_t* __restrict__ row_seq, const int32_t* __restrict__ row_pos,
+                                     const int32_t* __restrict__ row_seq, const int32_t* __restrict__ cu,
                                      const bf16* __restrict__ embed, int vocab, const bf16* __restrict__ g,
                                      bf16* __restrict__ r, bf16* __restrict__ y, int rows, int H, float eps,
                                      unsigned int* err) {
@@ -139,7 +142,8 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tokens, int tok
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    int tok = tokens[(long long)row_seq[row] * tok_ld + row_pos[row]];
+    const int seq = row_seq[row];
+    int tok = tokens[(long long)seq * tok_ld + (row - cu[seq])];   // the sequence's row-th new token
     if (tok < 0 || tok >= vocab) {
         if (lane == 0) raise_error(err, HRA_DEVERR_TOKEN_RANGE);
         tok = tok < 0 ? 0 : vocab - 1;
@@ -259,11 +263,12 @@ inline unsigned blocks_for(long long threads, int per_block) {
 }  // namespace
 
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
-                                int32_t* cu, int32_t* last_row, unsigned int* err, cudaStream_t st) {
+                                int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
+                                cudaStream_t st) {
     const int threads = 256;
     const unsigned blocks = blocks_for(total_rows > 0 ? total_rows : 1, threads);
     HRA_LAUNCH(build_rowmap_kernel, dim3(blocks), dim3(threads), 0, st, meta, total_rows, row_seq, row_pos, cu, last_row,
-               err);
+               seq_start, err);
     return cudaGetLastError();
 }
 
@@ -275,14 +280,14 @@ cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_di
 }
 
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_t* row_seq,
-                                 const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
+                                 const int32_t* cu, const bf16* embed, int vocab, const bf16* g,
                                  bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
                                  cudaStream_t st) {
     const dim3 grid(blocks_for((long long)rows * 32, 256));
     switch (H) {
-        case 256: HRA_LAUNCH(embed_rmsnorm_kernel<1>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
-        case 2560: HRA_LAUNCH(embed_rmsnorm_kernel<10>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
-        default: HRA_LAUNCH(embed_rmsnorm_kernel<0>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, row_pos, embed, vocab, g, r, y, rows, H, eps, err); break;
+        case 256: HRA_LAUNCH(embed_rmsnorm_kernel<1>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, cu, embed, vocab, g, r, y, rows, H, eps, err); break;
+        case 2560: HRA_LAUNCH(embed_rmsnorm_kernel<10>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, cu, embed, vocab, g, r, y, rows, H, eps, err); break;
+        default: HRA_LAUNCH(embed_rmsnorm_kernel<0>, grid, dim3(256), 0, st, tokens, tok_ld, row_seq, cu, embed, vocab, g, r, y, rows, H, eps, err); break;
     }
     return cudaSuccess;
 }

@@ -108,21 +108,24 @@ struct SeqMeta {
     int32_t batch;
     int32_t mode;           // 0: prefill (vals = cu_seqlens[0..batch]); 1: decode (vals = pos[0..batch))
     int32_t vals[kMaxBatch + 1];
+    int32_t start[kMaxBatch];   // prefill: position of each sequence's first new row (0 from scratch)
 };
 
 // Writes row_seq[T], row_pos[T] (sequence index and position of each packed row), and for prefill
 // cu[batch+1], last_row[batch]; for decode last_row[b] = b.  Also clears the call's error word.
+// Prefill also writes seq_start[batch] = meta.start (may be null for decode).
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
-                                int32_t* cu, int32_t* last_row, unsigned int* err, cudaStream_t st);
+                                int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
+                                cudaStream_t st);
 
 // cos/sin table, transposed: entry (row r, pair i) at i * n_rows + r (float2), for position
 // pos_of_row[r] (or r when null).
 cudaError_t launch_rope_table(int n_rows, const int32_t* pos_of_row, int head_dim, double theta,
                               float2* table, cudaStream_t st);
 
-// r[row] = embed[tokens[row_seq*ld + row_pos]]; y = RMSNorm(r) * g.
+// r[row] = embed[tokens[row_seq * ld + (row - cu[row_seq])]]; y = RMSNorm(r) * g.
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, int tok_ld, const int32_t* row_seq,
-                                 const int32_t* row_pos, const bf16* embed, int vocab, const bf16* g,
+                                 const int32_t* cu, const bf16* embed, int vocab, const bf16* g,
                                  bf16* r, bf16* y, int rows, int H, float eps, unsigned int* err,
                                  cudaStream_t st);
 
@@ -138,6 +141,7 @@ struct PrefillAttnArgs {
     const bf16* q;          // [T, nq, hd]
     const bf16* kv_layer;   // [cache_batch][2][nkv][n_slots][hd]
     const int32_t* cu;      // [batch + 1] device
+    const int32_t* start;   // [batch] device: position of each sequence's first row (cached keys below)
     bf16* out;              // [T, nq * hd]
     int batch, max_len, n_slots, nq, nkv, hd;
 };
