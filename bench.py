@@ -544,8 +544,24 @@ def bench_long(hra, W, torch, dev, w_backbone):
     hra.hra_probe_select("none")
     att_ms, att_n, att_flops = hra.hra_probe_collect()
     ms_ar = events_time(ar, 2, torch) / 2
+    # the same loop on device-resident state: all 64 frames captured once in a CUDA graph
+    prefill()
+    loop = hra.ARLoop(bb, head, cache, last.clone(), p.lengths, max(p.lengths) + frames)
+    hid0 = loop.hidden.clone()
+    loop.capture(frames)
+
+    def ar_graph():
+        loop.state.zero_()
+        loop.state[:, 1] = -1
+        loop.pos.copy_(torch.tensor(p.lengths, dtype=torch.int32))
+        loop.hidden.copy_(hid0)
+        loop.replay()
+
+    ar_graph()
+    torch.cuda.synchronize()
+    ms_graph = events_time(ar_graph, 3, torch) / 3
     return {"prefill_tokens_per_s": p.total / (ms_pf / 1e3), "prefill_ms": ms_pf, "tokens": p.total,
-            "ar_ms_per_frame": ms_ar / frames, "frames": frames,
+            "ar_ms_per_frame": ms_ar / frames, "ar_graph_ms_per_frame": ms_graph / frames, "frames": frames,
             "attention_tflops": att_flops / (att_ms / 1e3) / 1e12 if att_ms > 0 else None,
             "attention_ms_per_step": att_ms / 3}
 

@@ -56,6 +56,8 @@ extern "C" {
 #define HRA_DEVERR_TOKEN_RANGE 1u  /* a token id was outside [0, vocab); it was clamped          */
 #define HRA_DEVERR_WAIT_TIMEOUT 2u /* a pipeline wait inside a kernel gave up (kernel bug guard) */
 #define HRA_DEVERR_CODE_RANGE 4u   /* a code index outside [0, codebook_size) was clamped        */
+#define HRA_DEVERR_POS_RANGE 8u    /* a device-resident position was outside [0, n_slots); the row
+                                       ran at the nearest slot inside the cache                   */
 
 /* ---- model description ---------------------------------------------------------------------- */
 /* Backbone and audio-head shape.  Supported: head_dim in {64, 128}; n_q_heads % n_kv_heads == 0;
@@ -157,6 +159,23 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                const int32_t* pos, int32_t batch, const hra_kv_cache* kv, void* hidden_dev,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/* hra_decode with the positions in device memory, for loops captured once and replayed (a CUDA
+ * graph of the AR audio loop: host launch overhead was the per-frame limit, "Stabilize Higgs Audio
+ * termination and prefill", Performance; vLLM-Omni PR #8226, Step-overhead reductions).
+ *   pos_dev      device int32 [batch]: row b runs at position pos_dev[b] (read when the pass
+ *                starts).  A position outside [0, kv->n_slots) sets HRA_DEVERR_POS_RANGE and the
+ *                row runs at the nearest slot inside the cache (0 or n_slots - 1), overwriting it.
+ *   pos_bound    host upper bound of every position of this call, 0 <= pos_bound < kv->n_slots
+ *                (else HRA_ERR_RANGE); sizes the attention's key splits.  A captured graph passes
+ *                the largest position it will ever see.
+ *   advance      non-zero: every pos_dev[b] is incremented once it has been read, so replaying the
+ *                pass walks the positions forward with no host work.
+ * Other arguments as hra_decode. */
+int hra_decode_dev(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev,
+                   int32_t* pos_dev, int32_t pos_bound, int32_t advance, int32_t batch,
+                   const hra_kv_cache* kv, void* hidden_dev, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
 /* ---- delayed-codebook step ------------------------------------------------------------------ */
 size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch);
 
@@ -180,6 +199,25 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
                       const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
                       void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/* One frame of the AR audio loop, fully stream-ordered and free of host data dependencies (so a
+ * CUDA graph can capture it once and replay it per frame): hra_codebook_step on hidden_dev
+ * (codes, next embedding, done, delay state advanced), then hra_decode_dev on the next embedding
+ * at the device positions pos_dev (advanced by one), writing the next hidden back to hidden_dev.
+ * Sources: the per-frame codebook step and decode pass ("Stabilize Higgs Audio termination and
+ * prefill", Summary and Performance: AR decode ms/frame); graph-captured per-frame work
+ * (vLLM-Omni PR #8226, Purpose and Step-overhead reductions).
+ *   hidden_dev   bf16 [batch, hidden], in: this frame's backbone hidden; out: the next one.
+ *   backbone_ws  >= hra_decode_workspace_size(dims, batch, kv->n_slots) bytes;
+ *   codebook_ws  >= hra_codebook_workspace_size(dims, batch) bytes (two separate buffers, so
+ *                hra_device_error can read either call's error bits).
+ * Every argument of both steps is checked before anything is enqueued. */
+int hra_ar_frame(const hra_dims* dims, const hra_weights* weights, const void* head_w_dev,
+                 const void* code_emb_dev, hra_delay_state* state_dev, const float* eoc_bias_dev,
+                 void* hidden_dev, int32_t* pos_dev, int32_t pos_bound, int32_t batch,
+                 const hra_kv_cache* kv, int32_t* codes_dev, void* next_emb_dev, int32_t* done_dev,
+                 void* backbone_ws, size_t backbone_ws_bytes, void* codebook_ws,
+                 size_t codebook_ws_bytes, void* stream);
 
 /* The same step for callers that cannot allocate device memory -- for instance a streaming-audio
  * callback with a hard per-frame deadline (cudaMalloc may synchronise the device and take

@@ -25,12 +25,12 @@ LIB_PATH = os.path.join(_PKG, "libhra.so")
 HRA_OK = 0
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported dims", -3: "workspace too small",
           -4: "length or position outside the cache", -5: "CUDA error"}
-DEVERR_TOKEN_RANGE, DEVERR_WAIT_TIMEOUT, DEVERR_CODE_RANGE = 1, 2, 4
+DEVERR_TOKEN_RANGE, DEVERR_WAIT_TIMEOUT, DEVERR_CODE_RANGE, DEVERR_POS_RANGE = 1, 2, 4, 8
 EPI_STORE, EPI_RESIDUAL, EPI_SWIGLU, EPI_F32 = 0, 1, 2, 3
 PREFILL_FULL_LAST_LAYER = 1
 
 EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_workspace_size", "hra_prefill_chunk",
-            "hra_decode_workspace_size", "hra_decode",
+            "hra_decode_workspace_size", "hra_decode", "hra_decode_dev", "hra_ar_frame",
             "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_noalloc",
             "hra_linear_workspace_size",
             "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
@@ -95,6 +95,12 @@ def lib() -> ctypes.CDLL:
         L.hra_decode.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32,
                                  ctypes.POINTER(HraKvCache), vp, vp, sz, vp]
         L.hra_decode.restype = ctypes.c_int
+        L.hra_decode_dev.argtypes = [dp, ctypes.POINTER(HraWeights), vp, vp, i32, i32, i32,
+                                     ctypes.POINTER(HraKvCache), vp, vp, sz, vp]
+        L.hra_decode_dev.restype = ctypes.c_int
+        L.hra_ar_frame.argtypes = [dp, ctypes.POINTER(HraWeights), vp, vp, vp, vp, vp, vp, i32, i32,
+                                   ctypes.POINTER(HraKvCache), vp, vp, vp, vp, sz, vp, sz, vp]
+        L.hra_ar_frame.restype = ctypes.c_int
         L.hra_codebook_workspace_size.argtypes = [dp, i32]
         L.hra_codebook_workspace_size.restype = sz
         L.hra_codebook_step.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -237,6 +243,26 @@ class Backbone:
         self.last_ws = ws
         return out
 
+    def decode_dev(self, in_emb: torch.Tensor, pos: torch.Tensor, pos_bound: int, cache: torch.Tensor,
+                   advance: bool = True, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """hra_decode_dev: positions in the CUDA int32 tensor `pos` (advanced in place when
+        `advance`); pos_bound is a host upper bound of every position."""
+        B = in_emb.shape[0]
+        if out is None:
+            out = torch.empty(B, self.d.hidden, dtype=torch.bfloat16, device=in_emb.device)
+        need = self.decode_workspace_size(B, cache.shape[4])
+        ws = workspace if workspace is not None else self.ws.get(need, in_emb.device)
+        kv = self.kv(cache)
+        rc = lib().hra_decode_dev(ctypes.byref(self.dims), ctypes.byref(self.table),
+                                  _ptr(in_emb, torch.bfloat16, "in_emb"), _ptr(pos, torch.int32, "pos"),
+                                  int(pos_bound), 1 if advance else 0, B, ctypes.byref(kv),
+                                  _ptr(out, torch.bfloat16, "hidden"), _ptr(ws, None, "workspace"), ws.numel(),
+                                  _stream(stream))
+        _check(rc, "hra_decode_dev")
+        self.last_ws = ws
+        return out
+
     def decode_workspace_size(self, batch, n_slots) -> int:
         return lib().hra_decode_workspace_size(ctypes.byref(self.dims), batch, n_slots)
 
@@ -258,6 +284,78 @@ class Backbone:
         _check(rc, "hra_decode")
         self.last_ws = ws
         return out
+
+
+class ARLoop:
+    """The AR audio loop on device-resident state: each frame is one hra_ar_frame call (codebook
+    step on the current hidden, then the decode pass at the device positions, which advance by
+    one).  No frame depends on host data, so `capture(n)` records n frames into one CUDA graph and
+    `replay()` runs them with a single launch from the host.
+
+    pos0: host ints, the position of each row's first decoded frame (its prompt length); pos_bound
+    (host) must cover every position the loop will reach."""
+
+    def __init__(self, bb: "Backbone", head: "AudioHead", cache: torch.Tensor, hidden: torch.Tensor,
+                 pos0: Sequence[int], pos_bound: int, eoc_bias: Optional[torch.Tensor] = None):
+        self.bb, self.head, self.cache = bb, head, cache
+        d = bb.d
+        B = hidden.shape[0]
+        dev = hidden.device
+        self.B = B
+        self.hidden = hidden                      # in/out: the current backbone hidden
+        self.state = torch.zeros(B, 4, dtype=torch.int32, device=dev)
+        self.state[:, 1] = -1
+        self.pos = torch.tensor([int(x) for x in pos0], dtype=torch.int32, device=dev)
+        self.pos_bound = int(pos_bound)
+        self.eoc_bias = eoc_bias
+        self.codes = torch.empty(B, d.n_codebooks, dtype=torch.int32, device=dev)
+        self.next_emb = torch.empty(B, d.hidden, dtype=torch.bfloat16, device=dev)
+        self.done = torch.empty(B, dtype=torch.int32, device=dev)
+        self.bws = torch.empty(bb.decode_workspace_size(B, cache.shape[4]), dtype=torch.uint8, device=dev)
+        self.cws = torch.empty(head.workspace_size(B), dtype=torch.uint8, device=dev)
+        self.kv = bb.kv(cache)
+        self.graph = None
+
+    def frame(self, codes: Optional[torch.Tensor] = None, done: Optional[torch.Tensor] = None,
+              eoc_bias: Optional[torch.Tensor] = None, stream=None):
+        """Enqueue one frame; codes/done default to the loop's own buffers, eoc_bias (fp32 [B, K])
+        to the loop's.  Returns (codes, done)."""
+        codes = self.codes if codes is None else codes
+        done = self.done if done is None else done
+        bias = self.eoc_bias if eoc_bias is None else eoc_bias
+        rc = lib().hra_ar_frame(ctypes.byref(self.bb.dims), ctypes.byref(self.bb.table),
+                                _ptr(self.head.head_w, torch.bfloat16, "head_w"),
+                                _ptr(self.head.code_emb, torch.bfloat16, "code_emb"),
+                                _ptr(self.state, torch.int32, "state"),
+                                _ptr(bias, torch.float32, "eoc_bias"),
+                                _ptr(self.hidden, torch.bfloat16, "hidden"), _ptr(self.pos, torch.int32, "pos"),
+                                self.pos_bound, self.B, ctypes.byref(self.kv),
+                                _ptr(codes, torch.int32, "codes"), _ptr(self.next_emb, torch.bfloat16, "next_emb"),
+                                _ptr(done, torch.int32, "done"), _ptr(self.bws, None, "backbone workspace"),
+                                self.bws.numel(), _ptr(self.cws, None, "codebook workspace"), self.cws.numel(),
+                                _stream(stream))
+        _check(rc, "hra_ar_frame")
+        return codes, done
+
+    def capture(self, n_frames: int, eoc_bias_seq: Optional[torch.Tensor] = None) -> None:
+        """Record n_frames frames into one CUDA graph; frame f writes codes_seq[f] and done_seq[f]
+        (and adds eoc_bias_seq[f], fp32 [n_frames, B, K], when given).  Capturing runs nothing: the
+        state, positions and hidden are untouched until replay()."""
+        dev = self.hidden.device
+        self.codes_seq = torch.empty(n_frames, self.B, self.bb.d.n_codebooks, dtype=torch.int32, device=dev)
+        self.done_seq = torch.empty(n_frames, self.B, dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for f in range(n_frames):
+                bias = None if eoc_bias_seq is None else eoc_bias_seq[f]
+                self.frame(self.codes_seq[f], self.done_seq[f], eoc_bias=bias, stream=side)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = g
+
+    def replay(self) -> None:
+        self.graph.replay()
 
 
 class AudioHead:

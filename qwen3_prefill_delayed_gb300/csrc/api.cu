@@ -445,29 +445,44 @@ size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_
     return backbone_layout(*dims, batch, batch, batch, n_slots - 1).total;
 }
 
-int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev, const int32_t* pos,
-               int32_t batch, const hra_kv_cache* kv, void* hidden_dev, void* workspace, size_t workspace_bytes,
-               void* stream) {
-    if (dims == nullptr || weights == nullptr || in_emb_dev == nullptr || pos == nullptr || kv == nullptr)
+namespace {
+
+// pos_host: host positions (validated here); otherwise pos_dev (device, checked on the device) with
+// pos_bound, a host upper bound of every position, for the attention split count.
+int decode_impl(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev, const int32_t* pos_host,
+                int32_t* pos_dev, int32_t pos_bound, int advance, int32_t batch, const hra_kv_cache* kv,
+                void* hidden_dev, void* workspace, size_t workspace_bytes, void* stream, bool validate_only = false) {
+    if (dims == nullptr || weights == nullptr || in_emb_dev == nullptr || kv == nullptr ||
+        (pos_host == nullptr && pos_dev == nullptr))
         return HRA_ERR_INVALID_ARG;
     if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
     const hra_dims& d = *dims;
     if (batch < 1 || batch > kMaxBatch) return HRA_ERR_INVALID_ARG;
     if (!weights_ok(d, weights) || !kv_ok(kv) || !aligned16(in_emb_dev) || !aligned16(hidden_dev) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (pos_dev != nullptr && (reinterpret_cast<uintptr_t>(pos_dev) & 3u) != 0))
         return HRA_ERR_INVALID_ARG;
     if (batch > kv->batch) return HRA_ERR_INVALID_ARG;
     SeqMeta meta{};
     meta.batch = batch;
-    meta.mode = 1;
     int max_pos = 0;
-    for (int b = 0; b < batch; ++b) {
-        if (pos[b] < 0 || pos[b] >= kv->n_slots) return HRA_ERR_RANGE;
-        meta.vals[b] = pos[b];
-        max_pos = std::max(max_pos, (int)pos[b]);
+    if (pos_host != nullptr) {
+        meta.mode = 1;
+        for (int b = 0; b < batch; ++b) {
+            if (pos_host[b] < 0 || pos_host[b] >= kv->n_slots) return HRA_ERR_RANGE;
+            meta.vals[b] = pos_host[b];
+            max_pos = std::max(max_pos, (int)pos_host[b]);
+        }
+    } else {
+        if (pos_bound < 0 || pos_bound >= kv->n_slots) return HRA_ERR_RANGE;
+        meta.mode = 2;
+        meta.pos_dev = pos_dev;
+        meta.n_slots = kv->n_slots;
+        meta.advance = advance ? 1 : 0;
+        max_pos = pos_bound;
     }
     const Layout L = backbone_layout(d, batch, batch, batch, kv->n_slots - 1);
     if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
+    if (validate_only) return HRA_OK;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
@@ -481,7 +496,25 @@ int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_
                            reinterpret_cast<const bf16*>(weights->layers[0].attn_norm), P.at<bf16>(L.y),
                            P.at<bf16>(L.r), batch, d.hidden, d.rms_eps, st));
     return run_layers(d, *weights, *kv, P, L, batch, batch, 0, false, false, reinterpret_cast<bf16*>(hidden_dev),
-                      pos, max_pos, st);
+                      pos_host, max_pos, st);
+}
+
+}  // namespace
+
+int hra_decode(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev, const int32_t* pos,
+               int32_t batch, const hra_kv_cache* kv, void* hidden_dev, void* workspace, size_t workspace_bytes,
+               void* stream) {
+    if (pos == nullptr) return HRA_ERR_INVALID_ARG;
+    return decode_impl(dims, weights, in_emb_dev, pos, nullptr, 0, 0, batch, kv, hidden_dev, workspace,
+                       workspace_bytes, stream);
+}
+
+int hra_decode_dev(const hra_dims* dims, const hra_weights* weights, const void* in_emb_dev, int32_t* pos_dev,
+                   int32_t pos_bound, int32_t advance, int32_t batch, const hra_kv_cache* kv, void* hidden_dev,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (pos_dev == nullptr) return HRA_ERR_INVALID_ARG;
+    return decode_impl(dims, weights, in_emb_dev, nullptr, pos_dev, pos_bound, advance, batch, kv, hidden_dev,
+                       workspace, workspace_bytes, stream);
 }
 
 // Codebook-step workspace: error word and per-row counters (cleared by the GEMM), per-row argmax
@@ -570,6 +603,23 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
     a.eoc = dims->eoc_id;
     HRA_TRY(launch_codebook_finalize(a, st));
     return HRA_OK;
+}
+
+int hra_ar_frame(const hra_dims* dims, const hra_weights* weights, const void* head_w_dev, const void* code_emb_dev,
+                 hra_delay_state* state_dev, const float* eoc_bias_dev, void* hidden_dev, int32_t* pos_dev,
+                 int32_t pos_bound, int32_t batch, const hra_kv_cache* kv, int32_t* codes_dev, void* next_emb_dev,
+                 int32_t* done_dev, void* backbone_ws, size_t backbone_ws_bytes, void* codebook_ws,
+                 size_t codebook_ws_bytes, void* stream) {
+    if (pos_dev == nullptr) return HRA_ERR_INVALID_ARG;
+    // the decode pass's arguments are checked before the codebook step is enqueued
+    int rc = decode_impl(dims, weights, next_emb_dev, nullptr, pos_dev, pos_bound, 1, batch, kv, hidden_dev,
+                         backbone_ws, backbone_ws_bytes, stream, /*validate_only=*/true);
+    if (rc != HRA_OK) return rc;
+    rc = hra_codebook_step(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, batch, codes_dev,
+                               next_emb_dev, done_dev, nullptr, codebook_ws, codebook_ws_bytes, stream);
+    if (rc != HRA_OK) return rc;
+    return decode_impl(dims, weights, next_emb_dev, nullptr, pos_dev, pos_bound, 1, batch, kv, hidden_dev,
+                       backbone_ws, backbone_ws_bytes, stream);
 }
 
 size_t hra_linear_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue, int32_t split_k) {

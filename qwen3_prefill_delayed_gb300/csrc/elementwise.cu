@@ -47,6 +47,23 @@ __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq,
                     if (seq_start != nullptr) seq_start[b] = meta.start[b];
                 }
             }
+    } else if (meta.mode == 2) {
+        // one CTA (the launcher makes it so): the error word was cleared above, before the barrier
+        for (int i = threadIdx.x; i < T; i += blockDim.x) {
+            const int p = meta.pos_dev[i];
+            int pc = p;
+            if (p < 0 || p >= meta.n_slots) {
+                raise_error(err, HRA_DEVERR_POS_RANGE);
+                pc = p < 0 ? 0 : meta.n_slots - 1;
+            }
+            row_seq[i] = i;
+            row_pos[i] = pc;
+            if (meta.advance) meta.pos_dev[i] = p + 1;
+        }
+        for (int b = threadIdx.x; b < B; b += blockDim.x) {
+            cu[b] = b;
+            last_row[b] = b;
+        }
     } else {
         if (r < T) {
             row_seq[r] = r;
@@ -266,7 +283,7 @@ cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* ro
                                 int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
                                 cudaStream_t st) {
     const int threads = 256;
-    const unsigned blocks = blocks_for(total_rows > 0 ? total_rows : 1, threads);
+    const unsigned blocks = meta.mode == 2 ? 1u : blocks_for(total_rows > 0 ? total_rows : 1, threads);
     HRA_LAUNCH(build_rowmap_kernel, dim3(blocks), dim3(threads), 0, st, meta, total_rows, row_seq, row_pos, cu, last_row,
                seq_start, err);
     return cudaGetLastError();

@@ -106,9 +106,15 @@ constexpr int kMaxBatch = 512;
 // Host-built batch description passed by value to the row-map kernel.
 struct SeqMeta {
     int32_t batch;
-    int32_t mode;           // 0: prefill (vals = cu_seqlens[0..batch]); 1: decode (vals = pos[0..batch))
+    int32_t mode;           // 0: prefill (vals = cu_seqlens[0..batch]); 1: decode (vals = pos[0..batch));
+                            // 2: decode with positions read from pos_dev (device)
     int32_t vals[kMaxBatch + 1];
     int32_t start[kMaxBatch];   // prefill: position of each sequence's first new row (0 from scratch)
+    int32_t* pos_dev;           // mode 2: [batch] positions; a position outside [0, n_slots) raises
+                                // HRA_DEVERR_POS_RANGE and is clamped; when advance != 0 each is
+                                // incremented after it is read
+    int32_t n_slots;
+    int32_t advance;
 };
 
 // Writes row_seq[T], row_pos[T] (sequence index and position of each packed row), and for prefill
