@@ -81,6 +81,19 @@ def lib():
         L.oracle_codebook_step.argtypes = [ctypes.POINTER(OracleDims), _u16p, _u16p, _u16p, _i32p,
                                            ctypes.c_void_p, ctypes.c_int, _i32p, _u16p, _i32p,
                                            ctypes.c_void_p]
+        _u32p = np.ctypeslib.ndpointer(np.uint32, flags="C_CONTIGUOUS")
+        _u64p = np.ctypeslib.ndpointer(np.uint64, flags="C_CONTIGUOUS")
+        L.oracle_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+        L.oracle_exponential.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.oracle_exponential.restype = ctypes.c_float
+        L.oracle_sample_step.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
+                                         ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_float, _u64p,
+                                         ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_sample_step.restype = ctypes.c_int
+        L.oracle_codebook_step_sampled.argtypes = [ctypes.POINTER(OracleDims), _u16p, _u16p, _u16p, _i32p,
+                                                   ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_float,
+                                                   _u64p, ctypes.c_int, _i32p, _u16p, _i32p, ctypes.c_void_p]
+        L.oracle_codebook_step_sampled.restype = ctypes.c_int
         for f in ("oracle_prefill", "oracle_prefill_chunk", "oracle_decode", "oracle_codebook_step",
                   "oracle_max_threads"):
             getattr(L, f).restype = ctypes.c_int
@@ -255,6 +268,62 @@ def decode(d, w: HostWeights, in_emb: np.ndarray, pos, kv: np.ndarray, n_slots: 
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return out
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 of counter (4 x uint32) under key (2 x uint32) -> 4 x uint32."""
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.empty(4, np.uint32)
+    lib().oracle_philox4x32_10(c, k, out)
+    return out
+
+
+def exponential(seed: int, t: int, k: int, v: int) -> float:
+    """The sampler's exponential noise of entry v, codebook k, frame t for a row seeded `seed`."""
+    return float(lib().oracle_exponential(ctypes.c_uint64(seed), t, k, v))
+
+
+def sample_step(K: int, Vc: int, bos: int, eoc: int, logits: np.ndarray, eoc_bias, temperature: float,
+                top_k: int, top_p: float, seeds, state: np.ndarray):
+    """Sampled state machine (state [B,4] int32 updated in place).
+    Returns (codes [B,K], done [B], margin [B,K], ambiguous [B,K])."""
+    logits = _c(logits, np.float32)
+    B = logits.shape[0]
+    assert state.dtype == np.int32 and state.flags.c_contiguous
+    seeds = np.ascontiguousarray(seeds, np.uint64)
+    codes = np.empty((B, K), np.int32)
+    done = np.empty((B,), np.int32)
+    margin = np.empty((B, K), np.float32)
+    amb = np.empty((B, K), np.int32)
+    bias = None if eoc_bias is None else _c(eoc_bias, np.float32)
+    rc = lib().oracle_sample_step(K, Vc, bos, eoc, logits, None if bias is None else bias.ctypes.data,
+                                  float(temperature), int(top_k), float(top_p), seeds, B, state, codes, done,
+                                  margin.ctypes.data, amb.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_sample_step rejected its arguments")
+    return codes, done, margin, amb
+
+
+def codebook_step_sampled(d, hidden: np.ndarray, head_w: np.ndarray, code_emb: np.ndarray, state: np.ndarray,
+                          eoc_bias, temperature: float, top_k: int, top_p: float, seeds):
+    """Returns (codes [B,K], next [B,H] uint16, done [B], logits [B,K,Vc] fp32)."""
+    hidden = _c(hidden, np.uint16)
+    B = hidden.shape[0]
+    K, Vc = d.n_codebooks, d.codebook_size
+    codes = np.empty((B, K), np.int32)
+    nxt = np.empty((B, d.hidden), np.uint16)
+    done = np.empty((B,), np.int32)
+    logits = np.empty((B, K, Vc), np.float32)
+    bias = None if eoc_bias is None else _c(eoc_bias, np.float32)
+    rc = lib().oracle_codebook_step_sampled(ctypes.byref(make_dims(d)), hidden, _c(head_w, np.uint16),
+                                            _c(code_emb, np.uint16), state,
+                                            None if bias is None else bias.ctypes.data, float(temperature),
+                                            int(top_k), float(top_p), np.ascontiguousarray(seeds, np.uint64), B,
+                                            codes, nxt, done, logits.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_codebook_step_sampled rejected its arguments")
+    return codes, nxt, done, logits
 
 
 def delay_step(K: int, Vc: int, bos: int, eoc: int, logits: np.ndarray, eoc_bias, state: np.ndarray):

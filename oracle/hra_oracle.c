@@ -15,7 +15,9 @@
  *   - the single-token decode pass through the same layers, fed an embedding;
  *   - the per-frame delayed-codebook step: audio-head logits, per-codebook argmax under the delay
  *     pattern with BOS/EOC handling and stop flags, and the sum of the K codebook embeddings
- *     ("Stabilize Higgs Audio termination and prefill", Summary and Root cause).
+ *     ("Stabilize Higgs Audio termination and prefill", Summary and Root cause);
+ *   - the same step with each codebook sampled (temperature, top-k, top-p, exponential race on
+ *     per-row seeded Philox4x32-10 noise; vLLM-Omni PR #8226, Purpose and Test Plan).
  *
  * Arithmetic: fp32 on bf16-rounded weights and activations.  Values are rounded to bf16
  * (round-to-nearest-even) at these points and nowhere else: every RMSNorm output, the QKV
@@ -406,64 +408,239 @@ int oracle_decode(const oracle_dims* d, const oracle_layer* layers, const uint16
 
 /* ---------------------------------------------------------------- delayed-codebook step */
 
-/* Delay-pattern state machine for B rows, from given fp32 logits [B][K][Vc].
- * state [B][4] = (frame t, eoc_frame e (-1 none), done, 0), updated in place; codes [B][K]; done [B].
- * Source: per-frame argmax with delay handling, and the delayed-EOC fix that makes EOC on any
+/* Delay-pattern state machine for one row, given a chooser for the codebooks that are neither
+ * forced to BOS nor to EOC.  state = (frame t, eoc_frame e (-1 none), done, 0), updated in place.
+ * Source: per-frame choice with delay handling, and the delayed-EOC fix that makes EOC on any
  * codebook terminate ("Stabilize Higgs Audio termination and prefill", Summary and Root cause).
- * Rule, per row (codebook k lags k frames; bias adds eoc_bias[b][k] to the EOC logit):
+ * Rule (codebook k lags k frames):
  *   t < k               -> BOS (codebook not started)
  *   e >= 0, t - k >= e  -> EOC (codebook past the end)
- *   otherwise           -> argmax over all Vc logits, lowest index on ties
- *   if e < 0 and some argmaxed codebook chose EOC: e = min over those k of (t - k), and every
- *   codebook with t >= k and t - k >= e is EOC in this frame too
+ *   otherwise           -> choose(k) (argmax, or a sample)
+ *   if e < 0 and some chosen codebook is EOC: e = min over those k of (t - k), and every codebook
+ *   with t >= k and t - k >= e is EOC in this frame too
  *   done |= e >= 0 and t >= e + K - 1; t += 1 (a done row keeps advancing and emits all EOC). */
+typedef int (*choose_fn)(void* ctx, int b, int k, int t);
+
+static void delay_row(int K, int bos, int eoc, int b, int32_t* st, int32_t* c, int32_t* done, choose_fn choose,
+                      void* ctx) {
+    int t = st[0], e = st[1], dn = st[2];
+    int forced[64];
+    for (int k = 0; k < K; ++k) {
+        if (t < k) {
+            c[k] = bos;
+            forced[k] = 1;
+        } else if (e >= 0 && t - k >= e) {
+            c[k] = eoc;
+            forced[k] = 1;
+        } else {
+            c[k] = choose(ctx, b, k, t);
+            forced[k] = 0;
+        }
+    }
+    if (e < 0) {
+        int cand = INT_MAX;
+        for (int k = 0; k < K; ++k)
+            if (!forced[k] && c[k] == eoc && t - k < cand) cand = t - k;
+        if (cand != INT_MAX) {
+            e = cand;
+            for (int k = 0; k < K; ++k)
+                if (t >= k && t - k >= e) c[k] = eoc;
+        }
+    }
+    if (e >= 0 && t >= e + K - 1) dn = 1;
+    st[0] = t + 1;
+    st[1] = e;
+    st[2] = dn;
+    st[3] = 0;
+    *done = dn;
+}
+
+typedef struct {
+    int K, Vc, eoc;
+    const float* logits;
+    const float* eoc_bias;
+} greedy_ctx;
+
+/* argmax over all Vc logits (eoc_bias[b][k] added to the EOC logit), lowest index on ties */
+static int choose_argmax(void* vctx, int b, int k, int t) {
+    (void)t;
+    const greedy_ctx* g = (const greedy_ctx*)vctx;
+    const float* lg = g->logits + ((size_t)b * g->K + k) * g->Vc;
+    int best = 0;
+    float bv = 0.0f;
+    for (int v = 0; v < g->Vc; ++v) {
+        float x = lg[v];
+        if (v == g->eoc && g->eoc_bias) x = x + g->eoc_bias[(size_t)b * g->K + k];
+        if (v == 0 || x > bv) {
+            bv = x;
+            best = v;
+        }
+    }
+    return best;
+}
+
+/* Greedy step for B rows from fp32 logits [B][K][Vc]; codes [B][K]; done [B]; state [B][4]. */
 void oracle_delay_step(int K, int Vc, int bos, int eoc, const float* logits, const float* eoc_bias,
                        int B, int32_t* state, int32_t* codes, int32_t* done) {
-    for (int b = 0; b < B; ++b) {
-        int32_t* st = state + (size_t)b * 4;
-        int t = st[0], e = st[1], dn = st[2];
-        int32_t* c = codes + (size_t)b * K;
-        int forced[64];
-        for (int k = 0; k < K; ++k) {
-            if (t < k) {
-                c[k] = bos;
-                forced[k] = 1;
-            } else if (e >= 0 && t - k >= e) {
-                c[k] = eoc;
-                forced[k] = 1;
-            } else {
-                const float* lg = logits + ((size_t)b * K + k) * Vc;
-                int best = 0;
-                float bv = 0.0f;
-                for (int v = 0; v < Vc; ++v) {
-                    float x = lg[v];
-                    if (v == eoc && eoc_bias) x = x + eoc_bias[(size_t)b * K + k];
-                    if (v == 0 || x > bv) {
-                        bv = x;
-                        best = v;
-                    }
-                }
-                c[k] = best;
-                forced[k] = 0;
-            }
+    greedy_ctx g = {K, Vc, eoc, logits, eoc_bias};
+    for (int b = 0; b < B; ++b)
+        delay_row(K, bos, eoc, b, state + (size_t)b * 4, codes + (size_t)b * K, done + b, choose_argmax, &g);
+}
+
+/* ---------------------------------------------------------------- sampled codebook step */
+
+/* Philox4x32-10 counter-based generator, from its published definition (Salmon, Moraes, Dror,
+ * Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011): ten rounds of
+ *   (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the key bumped by the Weyl constants (0x9E3779B9,
+ * 0xBB67AE85) between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
         }
-        if (e < 0) {
-            int cand = INT_MAX;
-            for (int k = 0; k < K; ++k)
-                if (!forced[k] && c[k] == eoc && t - k < cand) cand = t - k;
-            if (cand != INT_MAX) {
-                e = cand;
-                for (int k = 0; k < K; ++k)
-                    if (t >= k && t - k >= e) c[k] = eoc;
-            }
-        }
-        if (e >= 0 && t >= e + K - 1) dn = 1;
-        st[0] = t + 1;
-        st[1] = e;
-        st[2] = dn;
-        st[3] = 0;
-        done[b] = dn;
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
     }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* Exponential noise of entry v of codebook k at frame t for a row seeded with `seed` (the
+ * per-request seeded exponential noise of vLLM-Omni PR #8226, Purpose and Step-overhead
+ * reductions): word v & 3 of Philox4x32-10 at counter (v >> 2, k, t, 0) under key
+ * (seed low 32 bits, seed high 32 bits), as a uniform u = (x >> 8 + 1) / 2^24 in (0, 1], and
+ * E = -log(u) in fp32. */
+float oracle_exponential(uint64_t seed, int t, int k, int v) {
+    const uint32_t ctr[4] = {(uint32_t)v >> 2, (uint32_t)k, (uint32_t)t, 0u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    const float u = (float)((out[v & 3] >> 8) + 1u) * (1.0f / 16777216.0f);
+    return -logf(u);
+}
+
+typedef struct {
+    float z;
+    int v;
+} zv;
+
+/* descending z, then ascending index */
+static int cmp_zv(const void* a, const void* b) {
+    const zv* x = (const zv*)a;
+    const zv* y = (const zv*)b;
+    if (x->z > y->z) return -1;
+    if (x->z < y->z) return 1;
+    return x->v < y->v ? -1 : (x->v > y->v);
+}
+
+typedef struct {
+    int K, Vc, eoc;
+    const float* logits;
+    const float* eoc_bias;
+    float temperature, top_p;
+    int top_k;
+    const uint64_t* seeds;
+    float* margin;    /* [B][K] or NULL: relative gap of the two fastest race times (-1 if forced) */
+    int32_t* amb;     /* [B][K] or NULL: 1 where the top-p cut falls within 1e-4 of an entry's boundary */
+} sample_ctx;
+
+/* One sampled code (temperature, top-k, top-p, then the exponential race; vLLM-Omni PR #8226,
+ * Purpose and Test Plan: temperature 1, top-k 50, top-p 0.95, seeded exponential noise):
+ *   z_v = (logit_v (+ eoc_bias on the EOC entry)) / temperature, fp32;
+ *   order the Vc entries by z descending, ties by ascending index;
+ *   top-k (0 < top_k < Vc): keep every entry whose z is >= the top_k-th largest z;
+ *   top-p (top_p < 1): with p = softmax of z over the kept entries, keep an entry while the
+ *     probability of the kept entries before it in that order is < top_p (so the shortest prefix
+ *     reaching top_p, and at least the first entry);
+ *   exponential race: each kept entry's clock is E_v / q_v with q_v = exp(z_v - z_max) and E_v the
+ *     entry's exponential noise; the first clock to ring (smallest, lowest index on ties) is the
+ *     sample -- a draw from the kept entries with probability proportional to q_v.
+ * Floating point decides the code here, so the oracle takes the decisions in fp32 like the
+ * kernel: the comparisons of z are exact, the sums run in the sorted order above. */
+static int choose_sample(void* vctx, int b, int k, int t) {
+    const sample_ctx* s = (const sample_ctx*)vctx;
+    const int Vc = s->Vc;
+    const float* lg = s->logits + ((size_t)b * s->K + k) * Vc;
+    zv* e = (zv*)malloc(sizeof(zv) * (size_t)Vc);
+    for (int v = 0; v < Vc; ++v) {
+        float x = lg[v];
+        if (v == s->eoc && s->eoc_bias) x = x + s->eoc_bias[(size_t)b * s->K + k];
+        e[v].z = x / s->temperature;
+        e[v].v = v;
+    }
+    qsort(e, (size_t)Vc, sizeof(zv), cmp_zv);
+    int n = Vc;
+    if (s->top_k > 0 && s->top_k < Vc) {
+        const float zk = e[s->top_k - 1].z;
+        n = s->top_k;
+        while (n < Vc && e[n].z >= zk) ++n;
+    }
+    float* q = (float*)malloc(sizeof(float) * (size_t)n);
+    const float zmax = e[0].z;
+    float S = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        q[i] = expf(e[i].z - zmax);
+        S += q[i];
+    }
+    int amb = 0;
+    int m = n;
+    if (s->top_p < 1.0f) {
+        float cum = 0.0f;
+        m = 0;
+        for (int i = 0; i < n; ++i) {
+            if (fabsf(cum - s->top_p) < 1e-4f) amb = 1;
+            if (!(cum < s->top_p)) break;
+            m = i + 1;
+            cum += q[i] / S;
+        }
+        if (m == 0) m = 1;
+    }
+    const uint64_t seed = s->seeds[b];
+    int best = -1;
+    float bt = 0.0f, second = INFINITY;
+    for (int i = 0; i < m; ++i) {
+        const float tv = oracle_exponential(seed, t, k, e[i].v) / q[i];
+        if (best < 0 || tv < bt || (tv == bt && e[i].v < best)) {
+            if (best >= 0) second = fminf(second, bt);
+            bt = tv;
+            best = e[i].v;
+        } else {
+            second = fminf(second, tv);
+        }
+    }
+    if (s->margin) s->margin[(size_t)b * s->K + k] = m > 1 ? (float)(((double)second - bt) / (double)bt) : INFINITY;
+    if (s->amb) s->amb[(size_t)b * s->K + k] = amb;
+    free(q);
+    free(e);
+    return best;
+}
+
+/* Sampled step for B rows from fp32 logits [B][K][Vc]: the delay state machine with each
+ * non-forced codebook sampled by choose_sample with the row's seed seeds[b] and the row's frame t.
+ * margin / amb (optional, [B][K]): the near-tie diagnostics of each sampled codebook (margin -1
+ * and amb 0 where the slot was forced).  Returns 0, or -1 on a bad argument. */
+int oracle_sample_step(int K, int Vc, int bos, int eoc, const float* logits, const float* eoc_bias,
+                       float temperature, int top_k, float top_p, const uint64_t* seeds, int B,
+                       int32_t* state, int32_t* codes, int32_t* done, float* margin, int32_t* amb) {
+    if (B < 1 || K < 1 || K > 64 || Vc < 1 || !(temperature > 0.0f) || !(top_p > 0.0f)) return -1;
+    if (margin)
+        for (int i = 0; i < B * K; ++i) margin[i] = -1.0f;
+    if (amb)
+        for (int i = 0; i < B * K; ++i) amb[i] = 0;
+    sample_ctx c = {K, Vc, eoc, logits, eoc_bias, temperature, top_p, top_k, seeds, margin, amb};
+    for (int b = 0; b < B; ++b)
+        delay_row(K, bos, eoc, b, state + (size_t)b * 4, codes + (size_t)b * K, done + b, choose_sample, &c);
+    return 0;
 }
 
 /* next[b] = bf16(sum over k ascending of fp32 code_emb[k][codes[b][k]]).  code_emb [K][Vc][H].
@@ -493,4 +670,21 @@ int oracle_codebook_step(const oracle_dims* d, const uint16_t* hidden, const uin
     oracle_code_embed_sum(K, Vc, H, code_emb, codes, B, next);
     if (!logits_out) free(lg);
     return 0;
+}
+
+/* Sampled full step: the logits as in oracle_codebook_step, then oracle_sample_step, then the
+ * embedding sum of the sampled codes. */
+int oracle_codebook_step_sampled(const oracle_dims* d, const uint16_t* hidden, const uint16_t* head_w,
+                                 const uint16_t* code_emb, int32_t* state, const float* eoc_bias,
+                                 float temperature, int top_k, float top_p, const uint64_t* seeds, int B,
+                                 int32_t* codes, uint16_t* next, int32_t* done, float* logits_out) {
+    const int K = d->n_codebooks, Vc = d->codebook_size, H = d->hidden;
+    if (B < 1 || K < 1 || K > 64) return -1;
+    float* lg = logits_out ? logits_out : (float*)malloc(sizeof(float) * (size_t)B * K * Vc);
+    oracle_linear(hidden, head_w, B, K * Vc, H, lg);
+    const int rc = oracle_sample_step(K, Vc, d->bos_id, d->eoc_id, lg, eoc_bias, temperature, top_k, top_p, seeds,
+                                      B, state, codes, done, NULL, NULL);
+    if (rc == 0) oracle_code_embed_sum(K, Vc, H, code_emb, codes, B, next);
+    if (!logits_out) free(lg);
+    return rc;
 }
