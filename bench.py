@@ -438,15 +438,20 @@ def bench_codebook(hra, W, torch, dev, hbm, peaks_kind):
         ws = torch.empty(heads[0].workspace_size(B), dtype=torch.uint8, device=dev)
         stream = torch.cuda.Stream()
         result = {}
-        for mode, rot in (("l2_warm", 1), ("hbm_cold", 4)):
+        seeds = torch.arange(1, B + 1, dtype=torch.int64, device=dev) * 0x9E3779B97F4A7C1
+        # greedy with the head warm in L2 and cold (4 copies), then sampled (temperature 1, top-k 50,
+        # top-p 0.95: the pages' serving setting) cold
+        for mode, rot, sampling in (("l2_warm", 1, None), ("hbm_cold", 4, None),
+                                    ("sampled_hbm_cold", 4, (1.0, 50, 0.95))):
+            sk = {} if sampling is None else {"sampling": sampling, "seeds": seeds}
             with torch.cuda.stream(stream):
-                heads[0].step(chain.hidden[0], state.clone(), eoc_bias=chain.eoc_bias[0], workspace=ws)
+                heads[0].step(chain.hidden[0], state.clone(), eoc_bias=chain.eoc_bias[0], workspace=ws, **sk)
             torch.cuda.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 for s in range(steps):
                     heads[s % rot].step(chain.hidden[s], state, eoc_bias=chain.eoc_bias[s], codes=codes[s],
-                                        next_emb=nxt[s], done=done[s], workspace=ws)
+                                        next_emb=nxt[s], done=done[s], workspace=ws, **sk)
             for _ in range(3):
                 state.copy_(chain.state0)
                 graph.replay()
@@ -470,6 +475,7 @@ def bench_codebook(hra, W, torch, dev, hbm, peaks_kind):
             del graph
         res[f"B{B}"] = result
     res["note"] = (f"200 chained steps in one CUDA graph; hbm_cold rotates 4 weight copies (336 MB > L2); "
+                   f"sampled: temperature 1, top-k 50, top-p 0.95, per-row seeds; "
                    f"hbm_frac is of the {peaks_kind} copy bandwidth")
     return res
 

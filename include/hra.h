@@ -200,6 +200,36 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
                       void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* Sampling parameters of hra_codebook_step_sampled (one set for the whole batch). */
+typedef struct {
+    float temperature; /* > 0: logits are divided by it                                        */
+    int32_t top_k;     /* 0 = off; else keep the entries at or above the top_k-th largest       */
+    float top_p;       /* in (0, 1]; 1 = off; else keep the shortest prefix (z descending)       */
+                       /* whose probability reaches top_p                                        */
+} hra_sampling;
+
+/* hra_codebook_step with each non-forced codebook sampled instead of argmaxed (vLLM-Omni PR
+ * #8226, Purpose: temperature / top-k / top-p with per-request seeded exponential noise; Test
+ * Plan: temperature 1, top-k 50, top-p 0.95).  For row b and codebook k at frame t:
+ *   z_v = (logit_v (+ eoc_bias[b][k] on the EOC entry)) / temperature (fp32; NaN counts as -inf);
+ *   entries ordered by z descending, ties by ascending index; top-k keeps every entry whose z is
+ *   >= the top_k-th largest; top-p keeps an entry while the probability (softmax of z over the
+ *   kept entries) of the kept entries before it is < top_p;
+ *   the code is the kept entry with the smallest E_v / exp(z_v - z_max) (lowest index on ties),
+ *   E_v = -log(u), u = ((w >> 8) + 1) / 2^24 with w = word (v & 3) of Philox4x32-10 at counter
+ *   (v >> 2, k, t, 0) under key (seed_b low 32 bits, seed_b high 32 bits).
+ * The delay state machine, outputs and workspace are those of hra_codebook_step.
+ *   sampling     host parameters (NULL = HRA_ERR_INVALID_ARG); temperature must be finite and
+ *                > 0, top_k >= 0, 0 < top_p <= 1 (else HRA_ERR_INVALID_ARG).
+ *   seeds_dev    device uint64 [batch] (8-byte aligned): each row's seed, read every step.
+ * codebook_size must be <= 2048 (else HRA_ERR_UNSUPPORTED). */
+int hra_codebook_step_sampled(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev,
+                              const void* code_emb_dev, hra_delay_state* state_dev,
+                              const float* eoc_bias_dev, const hra_sampling* sampling,
+                              const uint64_t* seeds_dev, int32_t batch, int32_t* codes_dev,
+                              void* next_emb_dev, int32_t* done_dev, float* logits_dev,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /* One frame of the AR audio loop, fully stream-ordered and free of host data dependencies (so a
  * CUDA graph can capture it once and replay it per frame): hra_codebook_step on hidden_dev
  * (codes, next embedding, done, delay state advanced), then hra_decode_dev on the next embedding
@@ -211,9 +241,12 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
  *   backbone_ws  >= hra_decode_workspace_size(dims, batch, kv->n_slots) bytes;
  *   codebook_ws  >= hra_codebook_workspace_size(dims, batch) bytes (two separate buffers, so
  *                hra_device_error can read either call's error bits).
+ *   sampling, seeds_dev  NULL: the greedy step (hra_codebook_step); else the sampled step
+ *                (hra_codebook_step_sampled) with these parameters and per-row seeds.
  * Every argument of both steps is checked before anything is enqueued. */
 int hra_ar_frame(const hra_dims* dims, const hra_weights* weights, const void* head_w_dev,
                  const void* code_emb_dev, hra_delay_state* state_dev, const float* eoc_bias_dev,
+                 const hra_sampling* sampling, const uint64_t* seeds_dev,
                  void* hidden_dev, int32_t* pos_dev, int32_t pos_bound, int32_t batch,
                  const hra_kv_cache* kv, int32_t* codes_dev, void* next_emb_dev, int32_t* done_dev,
                  void* backbone_ws, size_t backbone_ws_bytes, void* codebook_ws,

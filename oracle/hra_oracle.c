@@ -575,7 +575,8 @@ static int choose_sample(void* vctx, int b, int k, int t) {
     for (int v = 0; v < Vc; ++v) {
         float x = lg[v];
         if (v == s->eoc && s->eoc_bias) x = x + s->eoc_bias[(size_t)b * s->K + k];
-        e[v].z = x / s->temperature;
+        const float z = x / s->temperature;
+        e[v].z = z != z ? -INFINITY : z;   /* a NaN logit counts as -inf */
         e[v].v = v;
     }
     qsort(e, (size_t)Vc, sizeof(zv), cmp_zv);
@@ -609,6 +610,7 @@ static int choose_sample(void* vctx, int b, int k, int t) {
     int best = -1;
     float bt = 0.0f, second = INFINITY;
     for (int i = 0; i < m; ++i) {
+        if (q[i] == 0.0f) continue;   /* probability 0 (underflow): its clock never rings */
         const float tv = oracle_exponential(seed, t, k, e[i].v) / q[i];
         if (best < 0 || tv < bt || (tv == bt && e[i].v < best)) {
             if (best >= 0) second = fminf(second, bt);

@@ -31,7 +31,8 @@ PREFILL_FULL_LAST_LAYER = 1
 
 EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_workspace_size", "hra_prefill_chunk",
             "hra_decode_workspace_size", "hra_decode", "hra_decode_dev", "hra_ar_frame",
-            "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_noalloc",
+            "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_sampled",
+            "hra_codebook_step_noalloc",
             "hra_linear_workspace_size",
             "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
             "hra_device_error", "hra_status_string"]
@@ -66,6 +67,11 @@ class HraKvCache(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("batch", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
 
 
+class HraSampling(ctypes.Structure):
+    """hra_sampling: temperature (> 0), top_k (0 = off), top_p (1 = off)."""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
 _lib = None
 
 
@@ -98,13 +104,16 @@ def lib() -> ctypes.CDLL:
         L.hra_decode_dev.argtypes = [dp, ctypes.POINTER(HraWeights), vp, vp, i32, i32, i32,
                                      ctypes.POINTER(HraKvCache), vp, vp, sz, vp]
         L.hra_decode_dev.restype = ctypes.c_int
-        L.hra_ar_frame.argtypes = [dp, ctypes.POINTER(HraWeights), vp, vp, vp, vp, vp, vp, i32, i32,
-                                   ctypes.POINTER(HraKvCache), vp, vp, vp, vp, sz, vp, sz, vp]
+        L.hra_ar_frame.argtypes = [dp, ctypes.POINTER(HraWeights), vp, vp, vp, vp, ctypes.POINTER(HraSampling), vp,
+                                   vp, vp, i32, i32, ctypes.POINTER(HraKvCache), vp, vp, vp, vp, sz, vp, sz, vp]
         L.hra_ar_frame.restype = ctypes.c_int
         L.hra_codebook_workspace_size.argtypes = [dp, i32]
         L.hra_codebook_workspace_size.restype = sz
         L.hra_codebook_step.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
         L.hra_codebook_step.restype = ctypes.c_int
+        L.hra_codebook_step_sampled.argtypes = [dp, vp, vp, vp, vp, vp, ctypes.POINTER(HraSampling), vp, i32, vp,
+                                                vp, vp, vp, vp, sz, vp]
+        L.hra_codebook_step_sampled.restype = ctypes.c_int
         L.hra_codebook_step_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
         L.hra_codebook_step_noalloc.restype = ctypes.c_int
         L.hra_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
@@ -296,8 +305,11 @@ class ARLoop:
     (host) must cover every position the loop will reach."""
 
     def __init__(self, bb: "Backbone", head: "AudioHead", cache: torch.Tensor, hidden: torch.Tensor,
-                 pos0: Sequence[int], pos_bound: int, eoc_bias: Optional[torch.Tensor] = None):
+                 pos0: Sequence[int], pos_bound: int, eoc_bias: Optional[torch.Tensor] = None,
+                 sampling=None, seeds: Optional[torch.Tensor] = None):
         self.bb, self.head, self.cache = bb, head, cache
+        self.sampling = None if sampling is None else HraSampling(*sampling)   # (temperature, top_k, top_p)
+        self.seeds = seeds                                                      # CUDA int64 [B] (uint64 bits)
         d = bb.d
         B = hidden.shape[0]
         dev = hidden.device
@@ -328,6 +340,8 @@ class ARLoop:
                                 _ptr(self.head.code_emb, torch.bfloat16, "code_emb"),
                                 _ptr(self.state, torch.int32, "state"),
                                 _ptr(bias, torch.float32, "eoc_bias"),
+                                ctypes.byref(self.sampling) if self.sampling is not None else None,
+                                _ptr(self.seeds, torch.int64, "seeds"),
                                 _ptr(self.hidden, torch.bfloat16, "hidden"), _ptr(self.pos, torch.int32, "pos"),
                                 self.pos_bound, self.B, ctypes.byref(self.kv),
                                 _ptr(codes, torch.int32, "codes"), _ptr(self.next_emb, torch.bfloat16, "next_emb"),
@@ -374,9 +388,13 @@ class AudioHead:
     def step(self, hidden: torch.Tensor, state: torch.Tensor, eoc_bias: Optional[torch.Tensor] = None,
              codes: Optional[torch.Tensor] = None, next_emb: Optional[torch.Tensor] = None,
              done: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None):
+             workspace: Optional[torch.Tensor] = None, stream=None, sampling=None,
+             seeds: Optional[torch.Tensor] = None):
         """hra_codebook_step: state int32 [B, 4] (frame, eoc_frame, done, 0), advanced in place.
-        Returns (codes int32 [B, K], next_emb bf16 [B, H], done int32 [B])."""
+        Returns (codes int32 [B, K], next_emb bf16 [B, H], done int32 [B]).
+
+        With sampling = (temperature, top_k, top_p) and seeds (CUDA uint64 [B], one per row; torch
+        int64 holding the same bits), hra_codebook_step_sampled."""
         B = hidden.shape[0]
         K, Vc, H = self.d.n_codebooks, self.d.codebook_size, self.d.hidden
         dev = hidden.device
@@ -389,6 +407,22 @@ class AudioHead:
         if state.dtype != torch.int32 or tuple(state.shape) != (B, 4):
             raise HraError("state must be int32 [B, 4]")
         ws = workspace if workspace is not None else self.ws.get(self.workspace_size(B), dev)
+        if sampling is not None:
+            sp = HraSampling(*sampling)
+            rc = lib().hra_codebook_step_sampled(ctypes.byref(self.dims), _ptr(hidden, torch.bfloat16, "hidden"),
+                                                 _ptr(self.head_w, torch.bfloat16, "head_w"),
+                                                 _ptr(self.code_emb, torch.bfloat16, "code_emb"),
+                                                 _ptr(state, torch.int32, "state"),
+                                                 _ptr(eoc_bias, torch.float32, "eoc_bias"), ctypes.byref(sp),
+                                                 _ptr(seeds, torch.int64, "seeds"), B,
+                                                 _ptr(codes, torch.int32, "codes"),
+                                                 _ptr(next_emb, torch.bfloat16, "next_emb"),
+                                                 _ptr(done, torch.int32, "done"),
+                                                 _ptr(logits, torch.float32, "logits"),
+                                                 _ptr(ws, None, "workspace"), ws.numel(), _stream(stream))
+            _check(rc, "hra_codebook_step_sampled")
+            self.last_ws = ws
+            return codes, next_emb, done
         rc = lib().hra_codebook_step(ctypes.byref(self.dims), _ptr(hidden, torch.bfloat16, "hidden"),
                                      _ptr(self.head_w, torch.bfloat16, "head_w"),
                                      _ptr(self.code_emb, torch.bfloat16, "code_emb"),

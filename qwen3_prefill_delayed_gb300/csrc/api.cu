@@ -14,6 +14,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cmath>
+
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -544,12 +546,23 @@ size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch) {
     return g.off;
 }
 
-int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev, const void* code_emb_dev,
-                      hra_delay_state* state_dev, const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
-                      void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+namespace {
+
+// The codebook step, greedy (sampling == nullptr) or sampled; validate_only checks the arguments
+// and returns without enqueueing anything.
+int codebook_impl(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev, const void* code_emb_dev,
+                  hra_delay_state* state_dev, const float* eoc_bias_dev, const hra_sampling* sampling,
+                  const uint64_t* seeds_dev, int32_t batch, int32_t* codes_dev, void* next_emb_dev, int32_t* done_dev,
+                  float* logits_dev, void* workspace, size_t workspace_bytes, void* stream, bool validate_only) {
     if (dims == nullptr || !audio_dims_ok(dims)) return dims == nullptr ? HRA_ERR_INVALID_ARG : HRA_ERR_UNSUPPORTED;
     if (batch < 1 || batch > 1024) return HRA_ERR_INVALID_ARG;
+    if (sampling != nullptr) {
+        if (!(sampling->temperature > 0.f) || !std::isfinite(sampling->temperature) || sampling->top_k < 0 ||
+            !(sampling->top_p > 0.f) || !(sampling->top_p <= 1.f) || seeds_dev == nullptr ||
+            (reinterpret_cast<uintptr_t>(seeds_dev) & 7u) != 0)
+            return HRA_ERR_INVALID_ARG;
+        if (dims->codebook_size > 2048) return HRA_ERR_UNSUPPORTED;
+    }
     if (!aligned16(hidden_dev) || !aligned16(head_w_dev) || !aligned16(code_emb_dev) || !aligned16(state_dev) ||
         !aligned16(next_emb_dev) || !aligned16(workspace) || codes_dev == nullptr || done_dev == nullptr ||
         (reinterpret_cast<uintptr_t>(codes_dev) & 3u) || (reinterpret_cast<uintptr_t>(done_dev) & 3u) ||
@@ -557,6 +570,7 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
         (logits_dev && (reinterpret_cast<uintptr_t>(logits_dev) & 3u)))
         return HRA_ERR_INVALID_ARG;
     if (workspace_bytes < hra_codebook_workspace_size(dims, batch)) return HRA_ERR_WORKSPACE;
+    if (validate_only) return HRA_OK;
     const int K = dims->n_codebooks, Vc = dims->codebook_size, H = dims->hidden;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
@@ -601,22 +615,52 @@ int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* 
     a.H = H;
     a.bos = dims->bos_id;
     a.eoc = dims->eoc_id;
+    if (sampling != nullptr) {
+        a.seeds = seeds_dev;
+        a.temperature = sampling->temperature;
+        a.top_k = sampling->top_k;
+        a.top_p = sampling->top_p;
+    }
     HRA_TRY(launch_codebook_finalize(a, st));
     return HRA_OK;
 }
 
+}  // namespace
+
+int hra_codebook_step(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev, const void* code_emb_dev,
+                      hra_delay_state* state_dev, const float* eoc_bias_dev, int32_t batch, int32_t* codes_dev,
+                      void* next_emb_dev, int32_t* done_dev, float* logits_dev, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return codebook_impl(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, nullptr, nullptr, batch,
+                         codes_dev, next_emb_dev, done_dev, logits_dev, workspace, workspace_bytes, stream, false);
+}
+
+int hra_codebook_step_sampled(const hra_dims* dims, const void* hidden_dev, const void* head_w_dev,
+                              const void* code_emb_dev, hra_delay_state* state_dev, const float* eoc_bias_dev,
+                              const hra_sampling* sampling, const uint64_t* seeds_dev, int32_t batch,
+                              int32_t* codes_dev, void* next_emb_dev, int32_t* done_dev, float* logits_dev,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    if (sampling == nullptr) return HRA_ERR_INVALID_ARG;
+    return codebook_impl(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, sampling, seeds_dev,
+                         batch, codes_dev, next_emb_dev, done_dev, logits_dev, workspace, workspace_bytes, stream,
+                         false);
+}
+
 int hra_ar_frame(const hra_dims* dims, const hra_weights* weights, const void* head_w_dev, const void* code_emb_dev,
-                 hra_delay_state* state_dev, const float* eoc_bias_dev, void* hidden_dev, int32_t* pos_dev,
-                 int32_t pos_bound, int32_t batch, const hra_kv_cache* kv, int32_t* codes_dev, void* next_emb_dev,
-                 int32_t* done_dev, void* backbone_ws, size_t backbone_ws_bytes, void* codebook_ws,
-                 size_t codebook_ws_bytes, void* stream) {
+                 hra_delay_state* state_dev, const float* eoc_bias_dev, const hra_sampling* sampling,
+                 const uint64_t* seeds_dev, void* hidden_dev, int32_t* pos_dev, int32_t pos_bound, int32_t batch,
+                 const hra_kv_cache* kv, int32_t* codes_dev, void* next_emb_dev, int32_t* done_dev, void* backbone_ws,
+                 size_t backbone_ws_bytes, void* codebook_ws, size_t codebook_ws_bytes, void* stream) {
     if (pos_dev == nullptr) return HRA_ERR_INVALID_ARG;
-    // the decode pass's arguments are checked before the codebook step is enqueued
+    // both steps' arguments are checked before anything is enqueued
     int rc = decode_impl(dims, weights, next_emb_dev, nullptr, pos_dev, pos_bound, 1, batch, kv, hidden_dev,
                          backbone_ws, backbone_ws_bytes, stream, /*validate_only=*/true);
     if (rc != HRA_OK) return rc;
-    rc = hra_codebook_step(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, batch, codes_dev,
-                               next_emb_dev, done_dev, nullptr, codebook_ws, codebook_ws_bytes, stream);
+    rc = codebook_impl(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, sampling, seeds_dev, batch,
+                       codes_dev, next_emb_dev, done_dev, nullptr, codebook_ws, codebook_ws_bytes, stream, true);
+    if (rc != HRA_OK) return rc;
+    rc = codebook_impl(dims, hidden_dev, head_w_dev, code_emb_dev, state_dev, eoc_bias_dev, sampling, seeds_dev, batch,
+                       codes_dev, next_emb_dev, done_dev, nullptr, codebook_ws, codebook_ws_bytes, stream, false);
     if (rc != HRA_OK) return rc;
     return decode_impl(dims, weights, next_emb_dev, nullptr, pos_dev, pos_bound, 1, batch, kv, hidden_dev,
                        backbone_ws, backbone_ws_bytes, stream);

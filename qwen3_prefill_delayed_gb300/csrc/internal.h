@@ -184,6 +184,10 @@ struct CodebookArgs {
     float* logits_out;      // [batch, K, Vc] or null
     unsigned int* err;
     int batch, K, Vc, H, bos, eoc;
+    // sampled step (seeds != null): temperature, top-k (0 = off), top-p (1 = off), per-row seeds
+    const uint64_t* seeds;  // [batch]
+    float temperature, top_p;
+    int top_k;
 };
 cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st);
 
