@@ -48,6 +48,11 @@ class OracleLayer(ctypes.Structure):
                 ("attn_norm", "w_qkv", "q_norm", "k_norm", "w_o", "mlp_norm", "w_gate_up", "w_down")]
 
 
+class OracleFp8Layer(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("w_scale", ctypes.c_float * 4), ("a_scale", ctypes.c_float * 4)]
+
+
 _lib = None
 
 
@@ -94,6 +99,21 @@ def lib():
                                                    ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_float,
                                                    _u64p, ctypes.c_int, _i32p, _u16p, _i32p, ctypes.c_void_p]
         L.oracle_codebook_step_sampled.restype = ctypes.c_int
+        _u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_decode.restype = ctypes.c_float
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_quantize_e4m3.argtypes = [_u16p, ctypes.c_int64, ctypes.c_float, _u8p]
+        L.oracle_quantize_weight_e4m3.argtypes = [_u16p, ctypes.c_int64, ctypes.POINTER(ctypes.c_float), _u8p]
+        L.oracle_linear_fp8.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _f32p]
+        L.oracle_prefill_fp8.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
+                                         ctypes.POINTER(OracleFp8Layer), _u16p, _i32p, _i32p, ctypes.c_int,
+                                         ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int, _u16p]
+        L.oracle_calibrate.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer), _u16p, _i32p,
+                                       _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
+        for f in ("oracle_prefill_fp8", "oracle_calibrate"):
+            getattr(L, f).restype = ctypes.c_int
         for f in ("oracle_prefill", "oracle_prefill_chunk", "oracle_decode", "oracle_codebook_step",
                   "oracle_max_threads"):
             getattr(L, f).restype = ctypes.c_int
@@ -324,6 +344,93 @@ def codebook_step_sampled(d, hidden: np.ndarray, head_w: np.ndarray, code_emb: n
     if rc != 0:
         raise ValueError("oracle_codebook_step_sampled rejected its arguments")
     return codes, nxt, done, logits
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, np.uint8).ravel()
+    return np.array([lib().oracle_e4m3_decode(int(x)) for x in c], np.float32).reshape(np.shape(codes))
+
+
+def e4m3_encode(x) -> np.ndarray:
+    a = np.asarray(x, np.float32).ravel()
+    return np.array([lib().oracle_e4m3_encode(float(v)) for v in a], np.uint8).reshape(np.shape(x))
+
+
+def quantize_e4m3(x_u16: np.ndarray, scale: float) -> np.ndarray:
+    x = _c(x_u16, np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    lib().oracle_quantize_e4m3(x, x.size, float(scale), out)
+    return out
+
+
+def quantize_weight_e4m3(w_u16: np.ndarray):
+    """(scale, E4M3 codes) with scale = max|w| / 448."""
+    w = _c(w_u16, np.uint16)
+    out = np.empty(w.shape, np.uint8)
+    sc = ctypes.c_float()
+    lib().oracle_quantize_weight_e4m3(w, w.size, ctypes.byref(sc), out)
+    return sc.value, out
+
+
+def linear_fp8(x8: np.ndarray, w8: np.ndarray, scale: float) -> np.ndarray:
+    x8 = np.ascontiguousarray(x8, np.uint8)
+    w8 = np.ascontiguousarray(w8, np.uint8)
+    T, K = x8.shape
+    N = w8.shape[0]
+    y = np.empty((T, N), np.float32)
+    lib().oracle_linear_fp8(x8, w8, T, N, K, float(scale), y)
+    return y
+
+
+class Fp8Weights:
+    """E4M3 copies of every layer's projections with per-tensor weight scales, plus the static
+    activation scales (a_scale [L, 4]: qkv, o, gate_up, down inputs)."""
+
+    def __init__(self, hw: "HostWeights", a_scale: np.ndarray):
+        self.w8, self.w_scale = [], []
+        for lay in hw.layers:
+            ws, ws8 = [], []
+            for name in ("w_qkv", "w_o", "w_gate_up", "w_down"):
+                sc, q = quantize_weight_e4m3(lay[name])
+                ws.append(sc)
+                ws8.append(q)
+            self.w8.append(ws8)
+            self.w_scale.append(ws)
+        self.a_scale = np.asarray(a_scale, np.float32)
+        self.table = (OracleFp8Layer * len(self.w8))()
+        for l, ws8 in enumerate(self.w8):
+            self.table[l].w_qkv, self.table[l].w_o, self.table[l].w_gate_up, self.table[l].w_down = \
+                [x.ctypes.data for x in ws8]
+            for i in range(4):
+                self.table[l].w_scale[i] = self.w_scale[l][i]
+                self.table[l].a_scale[i] = float(self.a_scale[l, i])
+
+
+def prefill_fp8(d, w: "HostWeights", f8: Fp8Weights, tokens: np.ndarray, lens, n_slots: int):
+    """Returns (kv, last_hidden) of the FP8 variant."""
+    tokens = _c(tokens, np.int32)
+    lens = _c(lens, np.int32)
+    B, P = tokens.shape
+    kv = np.zeros(kv_shape(d, B, n_slots), np.uint16)
+    last = np.empty((B, d.hidden), np.uint16)
+    rc = lib().oracle_prefill_fp8(ctypes.byref(make_dims(d)), w.embed, w.table, f8.table, w.final_norm, tokens,
+                                  lens, B, P, kv, B, n_slots, last)
+    if rc != 0:
+        raise ValueError("oracle_prefill_fp8 rejected its arguments")
+    return kv, last
+
+
+def calibrate(d, w: "HostWeights", tokens: np.ndarray, lens, n_slots: int) -> np.ndarray:
+    """amax [L, 4] of the qkv, o, gate_up and down inputs over a bf16 prefill of the batch."""
+    tokens = _c(tokens, np.int32)
+    lens = _c(lens, np.int32)
+    B, P = tokens.shape
+    amax = np.empty((d.n_layers, 4), np.float32)
+    rc = lib().oracle_calibrate(ctypes.byref(make_dims(d)), w.embed, w.table, w.final_norm, tokens, lens, B, P,
+                                n_slots, amax)
+    if rc != 0:
+        raise ValueError("oracle_calibrate rejected its arguments")
+    return amax
 
 
 def delay_step(K: int, Vc: int, bos: int, eoc: int, logits: np.ndarray, eoc_bias, state: np.ndarray):

@@ -17,7 +17,10 @@
  *     pattern with BOS/EOC handling and stop flags, and the sum of the K codebook embeddings
  *     ("Stabilize Higgs Audio termination and prefill", Summary and Root cause);
  *   - the same step with each codebook sampled (temperature, top-k, top-p, exponential race on
- *     per-row seeded Philox4x32-10 noise; vLLM-Omni PR #8226, Purpose and Test Plan).
+ *     per-row seeded Philox4x32-10 noise; vLLM-Omni PR #8226, Purpose and Test Plan);
+ *   - the static-FP8 variant of the prefill projections (E4M3 weights with per-tensor scales,
+ *     inputs quantized with calibrated static scales) and that calibration ("fp8_chain.py",
+ *     module docstring; "Stabilize Higgs Audio termination and prefill", Summary).
  *
  * Arithmetic: fp32 on bf16-rounded weights and activations.  Values are rounded to bf16
  * (round-to-nearest-even) at these points and nowhere else: every RMSNorm output, the QKV
@@ -260,6 +263,107 @@ void oracle_attend(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, in
     }
 }
 
+/* ---------------------------------------------------------------- FP8 (E4M3) variant */
+
+/* OCP FP8 E4M3 ("fn": no infinities): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ * Normal codes (exponent field E > 0): (1 + M/8) * 2^(E-7); subnormals (E == 0): M/8 * 2^-6;
+ * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.  Encoding rounds to the
+ * nearest code, ties to an even mantissa, and saturates finite overflow to +-448 (the satfinite
+ * conversion); NaN stays NaN.  Source: the static-FP8 chain's E4M3 weights and activations
+ * ("fp8_chain.py", module docstring: RMSNorm->FP8, FP8 GEMMs, FP8_MAX). */
+float oracle_e4m3_decode(uint8_t c) {
+    const int sgn = c >> 7, E = (c >> 3) & 15, M = c & 7;
+    if (E == 15 && M == 7) return NAN;
+    const double v = E == 0 ? (double)M / 8.0 * ldexp(1.0, -6) : (1.0 + (double)M / 8.0) * ldexp(1.0, E - 7);
+    return (float)(sgn ? -v : v);
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+    if (x != x) return 0x7F;
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sgn | 0x7E;                 /* satfinite */
+    /* quantum of the binade holding a (subnormal quantum below 2^-6) */
+    int e = a > 0.0 ? (int)floor(log2(a)) : -6;
+    if (e < -6) e = -6;
+    const double q = ldexp(1.0, e - 3);
+    double m = a / q;                                  /* exact: power-of-two scaling */
+    double f = floor(m);
+    const double frac = m - f;
+    if (frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) == 1.0)) f += 1.0;
+    const double r = f * q;
+    if (r >= 448.0) return sgn | 0x7E;
+    if (r == 0.0) return sgn;
+    if (r < ldexp(1.0, -6)) return sgn | (uint8_t)(r / ldexp(1.0, -9));   /* subnormal: M = r / 2^-9 */
+    const int er = (int)floor(log2(r));
+    const int M = (int)((r / ldexp(1.0, er) - 1.0) * 8.0);
+    return sgn | (uint8_t)((er + 7) << 3) | (uint8_t)M;
+}
+
+/* out[i] = e4m3(bf(x[i]) / scale), the division in fp32. */
+void oracle_quantize_e4m3(const uint16_t* x, int64_t n, float scale, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(bf(x[i]) / scale);
+}
+
+/* Per-tensor weight quantization: scale = max|w| / 448 (fp32; 1 when w is all zero), w8 = e4m3(w / scale). */
+void oracle_quantize_weight_e4m3(const uint16_t* w, int64_t n, float* scale_out, uint8_t* out) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf(bf(w[i]));
+        if (a > amax) amax = a;
+    }
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    *scale_out = scale;
+    oracle_quantize_e4m3(w, n, scale, out);
+}
+
+/* y[t][j] = (sum_k x8[t][k] * w8[j][k]) * scale in fp32 (the products of two E4M3 values are exact
+ * in fp32), k ascending (descending under oracle_set_sum_order(1)); w8 row-major [N][K]. */
+void oracle_linear_fp8(const uint8_t* x8, const uint8_t* w8, int T, int N, int K, float scale, float* y) {
+    const int desc = g_sum_descending;
+    float lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = oracle_e4m3_decode((uint8_t)c);
+    #pragma omp parallel for schedule(static)
+    for (int j = 0; j < N; ++j) {
+        const uint8_t* wr = w8 + (size_t)j * K;
+        for (int t = 0; t < T; ++t) {
+            const uint8_t* xr = x8 + (size_t)t * K;
+            float s = 0.0f;
+            for (int i = 0; i < K; ++i) {
+                const int k = desc ? K - 1 - i : i;
+                s += lut[xr[k]] * lut[wr[k]];
+            }
+            y[(size_t)t * N + j] = s * scale;
+        }
+    }
+}
+
+typedef struct {
+    const uint8_t *w_qkv, *w_o, *w_gate_up, *w_down;   /* E4M3 weights, shapes as the bf16 ones */
+    float w_scale[4];                                   /* qkv, o, gate_up, down */
+    float a_scale[4];                                   /* static scale of each projection's input */
+} oracle_fp8_layer;
+
+/* One projection: bf16 (w8 == NULL) or FP8 (the input quantized with the static scale as, the
+ * result scaled by as * ws).  amax (optional) receives the max |input| seen. */
+static void project(const uint16_t* x, const uint16_t* w, const uint8_t* w8, float ws, float as, int n, int N,
+                    int K, float* y, float* amax) {
+    if (amax) {
+        for (size_t i = 0; i < (size_t)n * K; ++i) {
+            const float a = fabsf(bf(x[i]));
+            if (a > *amax) *amax = a;
+        }
+    }
+    if (w8 == NULL) {
+        oracle_linear(x, w, n, N, K, y);
+        return;
+    }
+    uint8_t* x8 = (uint8_t*)malloc((size_t)n * K);
+    oracle_quantize_e4m3(x, (int64_t)n * K, as, x8);
+    oracle_linear_fp8(x8, w8, n, N, K, as * ws, y);
+    free(x8);
+}
+
 /* ---------------------------------------------------------------- decoder layers */
 
 static float silu(float x) { return x / (1.0f + expf(-x)); }
@@ -279,7 +383,7 @@ static float silu(float x) { return x / (1.0f + expf(-x)); }
  *   r = bf16(r + h W_down^T) */
 static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const uint16_t* final_norm,
                          const uint16_t* x_in, int start, int n, uint16_t* kv, size_t layer_stride,
-                         int n_slots, uint16_t* hidden) {
+                         int n_slots, uint16_t* hidden, const oracle_fp8_layer* fp8, float* amax) {
     const int H = d->hidden, nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim, F = d->ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d->rms_eps;
@@ -303,7 +407,8 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
         uint16_t* vc = kc + (size_t)nkv * n_slots * hd;
         /* attention block */
         oracle_rmsnorm(r, L->attn_norm, n, H, eps, y);
-        oracle_linear(y, L->w_qkv, n, Dqkv, H, acc);
+        project(y, L->w_qkv, fp8 ? fp8[l].w_qkv : NULL, fp8 ? fp8[l].w_scale[0] : 1.0f, fp8 ? fp8[l].a_scale[0] : 1.0f,
+                n, Dqkv, H, acc, amax ? amax + 4 * l : NULL);
         for (size_t i = 0; i < (size_t)n * Dqkv; ++i) qkv[i] = to_bf(acc[i]);
         for (int i = 0; i < n; ++i) {
             int pos = start + i;
@@ -321,18 +426,21 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
             }
         }
         oracle_attend(qr, kc, vc, n_slots, start, n, nq, nkv, hd, att, NULL, 0);
-        oracle_linear(att, L->w_o, n, H, Dq, acc);
+        project(att, L->w_o, fp8 ? fp8[l].w_o : NULL, fp8 ? fp8[l].w_scale[1] : 1.0f, fp8 ? fp8[l].a_scale[1] : 1.0f,
+                n, H, Dq, acc, amax ? amax + 4 * l + 1 : NULL);
         for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
         /* MLP block */
         oracle_rmsnorm(r, L->mlp_norm, n, H, eps, y);
-        oracle_linear(y, L->w_gate_up, n, 2 * F, H, acc);
+        project(y, L->w_gate_up, fp8 ? fp8[l].w_gate_up : NULL, fp8 ? fp8[l].w_scale[2] : 1.0f,
+                fp8 ? fp8[l].a_scale[2] : 1.0f, n, 2 * F, H, acc, amax ? amax + 4 * l + 2 : NULL);
         for (int i = 0; i < n; ++i)
             for (int j = 0; j < F; ++j) {
                 float g = bf(to_bf(acc[(size_t)i * 2 * F + j]));
                 float u = bf(to_bf(acc[(size_t)i * 2 * F + F + j]));
                 hmid[(size_t)i * F + j] = to_bf(silu(g) * u);
             }
-        oracle_linear(hmid, L->w_down, n, H, F, acc);
+        project(hmid, L->w_down, fp8 ? fp8[l].w_down : NULL, fp8 ? fp8[l].w_scale[3] : 1.0f,
+                fp8 ? fp8[l].a_scale[3] : 1.0f, n, H, F, acc, amax ? amax + 4 * l + 3 : NULL);
         for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
     }
     if (hidden) oracle_rmsnorm(r, final_norm, n, H, eps, hidden);
@@ -349,10 +457,10 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
  * Summary); pads trail and only the used keys are attended ("fp8_chain.py", module docstring);
  * mixed batches of prefill chunks and single-token steps under one launch bound taken from the
  * real batch (vLLM-Omni PR #8226, Purpose). */
-int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
-                         const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
-                         const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
-                         uint16_t* last_hidden) {
+static int prefill_impl(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                        const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
+                        const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
+                        uint16_t* last_hidden, const oracle_fp8_layer* fp8, float* amax) {
     const int H = d->hidden;
     const size_t blk = (size_t)2 * d->n_kv_heads * n_slots * d->head_dim;
     if (B < 1 || B > kv_batch) return -1;
@@ -370,12 +478,51 @@ int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const orac
             memcpy(x + (size_t)i * H, embed + (size_t)tokens[(size_t)b * P_max + i] * H,
                    sizeof(uint16_t) * H);
         forward_rows(d, layers, final_norm, x, s0, n, kv + (size_t)b * blk, (size_t)kv_batch * blk,
-                     n_slots, hid);
+                     n_slots, hid, fp8, amax);
         memcpy(last_hidden + (size_t)b * H, hid + (size_t)(n - 1) * H, sizeof(uint16_t) * H);
         free(x);
         free(hid);
     }
     return 0;
+}
+
+int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                         const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
+                         const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
+                         uint16_t* last_hidden) {
+    return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, starts, B, P_max, kv, kv_batch, n_slots,
+                        last_hidden, NULL, NULL);
+}
+
+/* FP8 variant of the prefill from position 0: every projection of every layer runs on E4M3 weights
+ * fp8[l] and on its input quantized with that layer's static activation scale, the result scaled
+ * by activation scale * weight scale; everything else is the bf16 prefill ("fp8_chain.py", module
+ * docstring: static-FP8 merged-QKV, output, gate/up and down GEMMs). */
+int oracle_prefill_fp8(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                       const oracle_fp8_layer* fp8, const uint16_t* final_norm, const int32_t* tokens,
+                       const int32_t* seq_lens, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
+                       uint16_t* last_hidden) {
+    if (fp8 == NULL) return -1;
+    return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch, n_slots,
+                        last_hidden, fp8, NULL);
+}
+
+/* Calibration of the static activation scales (FlashRT PR #141, Summary: FP8 activation scales
+ * from a fixed calibration prompt): the bf16 prefill of the calibration batch, recording per layer
+ * l the max |x| over every row of each projection's input -- amax[4l + 0..3] for the QKV, output,
+ * gate/up and down projections.  The scale of a projection is then amax / 448. */
+int oracle_calibrate(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                     const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens, int B, int P_max,
+                     int n_slots, float* amax) {
+    for (int i = 0; i < 4 * d->n_layers; ++i) amax[i] = 0.0f;
+    const size_t per = (size_t)d->n_layers * B * 2 * d->n_kv_heads * n_slots * d->head_dim;
+    uint16_t* kv = (uint16_t*)calloc(per, sizeof(uint16_t));
+    uint16_t* last = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * d->hidden);
+    const int rc = prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, B, n_slots,
+                                last, NULL, amax);
+    free(kv);
+    free(last);
+    return rc;
 }
 
 /* Batched prefill from position 0: tokens [B][P_max] with trailing pads (never read); seq_lens[B]
@@ -384,8 +531,8 @@ int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const orac
 int oracle_prefill(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
                    const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
                    int B, int P_max, uint16_t* kv, int kv_batch, int n_slots, uint16_t* last_hidden) {
-    return oracle_prefill_chunk(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch,
-                                n_slots, last_hidden);
+    return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch, n_slots,
+                        last_hidden, NULL, NULL);
 }
 
 /* Single-token decode pass: row b is the embedding in_emb[b] at position pos[b]; it writes cache
@@ -402,7 +549,7 @@ int oracle_decode(const oracle_dims* d, const oracle_layer* layers, const uint16
         if (pos[b] < 0 || pos[b] >= n_slots) return -1;
     for (int b = 0; b < B; ++b)
         forward_rows(d, layers, final_norm, in_emb + (size_t)b * H, pos[b], 1, kv + (size_t)b * blk,
-                     (size_t)kv_batch * blk, n_slots, hidden + (size_t)b * H);
+                     (size_t)kv_batch * blk, n_slots, hidden + (size_t)b * H, NULL, NULL);
     return 0;
 }
 
