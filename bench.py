@@ -411,6 +411,12 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
     except Exception as ex:
         out["chunked_prefill"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
+    # ---- the static-FP8 variant of the prefill projections on the same ragged batch
+    try:
+        out["fp8_prefill"] = bench_fp8(hra, W, torch, dev, w_backbone, peaks)
+    except Exception as ex:
+        out["fp8_prefill"] = {"error": repr(ex)}
+    torch.cuda.empty_cache()
     # ---- long prompts + 64 AR frames
     try:
         out["long_prompts"] = bench_long(hra, W, torch, dev, w_backbone)
@@ -517,6 +523,41 @@ def bench_chunked(hra, W, torch, dev, w_backbone):
             "chunk1_ms": ms_c1, "chunk2_ms": ms_c2, "chunk2_tokens": sum(rest),
             "chunk2_tokens_per_s": sum(rest) / (ms_c2 / 1e3),
             "two_chunks_tokens_per_s": sum(lens) / ((ms_c1 + ms_c2) / 1e3)}
+
+
+def bench_fp8(hra, W, torch, dev, w_backbone, peaks):
+    """FP8 (E4M3) projections with static activation scales calibrated on a fixed calibration batch
+    (4 prompts of 64 tokens, their own seed), then the ragged batch's prefill; the gate/up GEMM is
+    reported against the FP8 peak = the measured bf16 sustained peak x 2 (the nominal dense
+    FP8 / BF16 tensor-rate ratio of the part)."""
+    d = W.full_dims(36)
+    p = W.make_prompts(2, 32, 16, 256, d.vocab)
+    bb = hra.Backbone(d, w_backbone)
+    f8 = hra.Fp8Backbone(bb)
+    cal = W.make_prompts(99, 4, 64, 64, d.vocab, fixed_len=64)
+    cache = hra.new_kv_cache(d, 32, 2048, dev)
+    f8.calibrate(cal.tokens.to(dev), cal.lengths, cache)
+    tok = p.tokens.to(dev)
+    out = torch.empty(32, d.hidden, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(f8.prefill_workspace_size(32, p.total, p.max_len), dtype=torch.uint8, device=dev)
+    run = lambda: f8.prefill(tok, p.lengths, cache, out=out, workspace=ws)
+    run16 = lambda: bb.prefill(tok, p.lengths, cache, out=out)
+    for f in (run, run16):
+        for _ in range(2):
+            f()
+    torch.cuda.synchronize()
+    ms = events_time(run, 5, torch) / 5
+    ms16 = events_time(run16, 5, torch) / 5
+    hra.hra_probe_select("gate_up")
+    run()
+    hra.hra_probe_select("none")
+    gu_ms, gu_n, gu_flops = hra.hra_probe_collect()
+    peak8 = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    tf = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+    del cache, f8
+    return {"prefill_tokens_per_s": p.total / (ms / 1e3), "prefill_ms": ms, "bf16_prefill_ms": ms16,
+            "gate_up_tflops": tf, "gate_up_frac_of_fp8_peak": tf / peak8 if tf else None,
+            "fp8_peak_tflops": peak8, "calibration": "4 prompts x 64 tokens, seed 99"}
 
 
 def bench_long(hra, W, torch, dev, w_backbone):

@@ -290,6 +290,62 @@ int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, i
                int32_t epilogue, int32_t split_k, void* workspace, size_t workspace_bytes,
                void* stream);
 
+/* ---- static-FP8 variant of the prefill projections ------------------------------------------ */
+/* The FP8 band of the prefill chain ("fp8_chain.py", module docstring: RMSNorm->FP8, merged-QKV,
+ * output, gate/up and down FP8 GEMMs with static activation scales; "Stabilize Higgs Audio
+ * termination and prefill", Summary: activation scales calibrated on a fixed prompt):
+ *   weights      w8 = e4m3(w / s_w) with one per-tensor scale s_w = max|w| / 448;
+ *   activations  each projection's input x8 = e4m3(x / s_a) with a static per-layer, per-projection
+ *                scale s_a (from hra_fp8_calibrate: max|x| / 448);
+ *   GEMM         fp32 sum of the E4M3 products times s_a * s_w, then the bf16 path's epilogue.
+ * e4m3() rounds to nearest (ties to even) and saturates finite overflow to +-448 (OCP E4M3, "fn").
+ * Every other step (norms, RoPE, attention, SwiGLU, residuals, rounding points) is the bf16
+ * prefill's.  Scales are device fp32 scalars so that no call needs a host round trip. */
+typedef struct {
+    const void* w_qkv;      /* E4M3 [(nq + 2 nkv) hd, H] */
+    const void* w_o;        /* E4M3 [H, nq hd]            */
+    const void* w_gate_up;  /* E4M3 [2F, H]               */
+    const void* w_down;     /* E4M3 [H, F]                */
+    const float* w_scale;   /* device float [4]: s_w of qkv, o, gate_up, down */
+    const float* a_scale;   /* device float [4]: s_a of the inputs of the same four projections */
+} hra_fp8_layer;
+
+/* Weight preparation: w8_dev[i] = e4m3(w[i] / s_w) and *scale_dev = s_w = max|w| / 448 (1 for an
+ * all-zero tensor).  w_dev bf16 [n] (16-byte aligned), n a multiple of 8; w8_dev 8-byte aligned. */
+int hra_fp8_quantize_weight(const void* w_dev, int64_t n, void* w8_dev, float* scale_dev, void* stream);
+
+/* x8_dev[i] = e4m3(x[i] / *scale_dev) (IEEE division), n a multiple of 8. */
+int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void* x8_dev, void* stream);
+
+/* FP8 projection: out = epilogue((a8 . w8^T) * (*a_scale) * (*w_scale)), a8 E4M3 [M, K], w8 E4M3
+ * [N, K] (2N rows for EPI_SWIGLU), K a multiple of 128; epilogues as hra_linear. */
+size_t hra_linear_fp8_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue);
+int hra_linear_fp8(const void* a8_dev, const void* w8_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
+                   const float* a_scale_dev, const float* w_scale_dev, int32_t epilogue, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Calibration: the bf16 prefill of the calibration batch (every row through the last layer, the
+ * cache written as by hra_prefill), recording amax_dev[4 l + p] = max |input| of projection p
+ * (0 qkv, 1 o, 2 gate_up, 3 down) of layer l over all rows, and scale_dev[4 l + p] =
+ * amax / 448 (1 where amax is 0).  Both device float [4 n_layers].  Arguments as hra_prefill;
+ * the workspace holds hra_fp8_calibrate_workspace_size() bytes. */
+size_t hra_fp8_calibrate_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens,
+                                        int32_t max_len);
+int hra_fp8_calibrate(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                      const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                      float* amax_dev, float* scale_dev, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* hra_prefill with every projection of every layer in FP8 (fp8_layers: host array [n_layers]).
+ * weights still supplies the embedding, the norm gains and the final norm.  hidden, n_q_heads *
+ * head_dim and ffn must be multiples of 128 (else HRA_ERR_UNSUPPORTED). */
+size_t hra_prefill_fp8_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens,
+                                      int32_t max_len);
+int hra_prefill_fp8(const hra_dims* dims, const hra_weights* weights, const hra_fp8_layer* fp8_layers,
+                    const int32_t* tokens_dev, const int32_t* seq_lens, int32_t batch, int32_t max_len,
+                    const hra_kv_cache* kv, void* last_hidden_dev, void* workspace,
+                    size_t workspace_bytes, uint32_t flags, void* stream);
+
 /* ---- measurement ---------------------------------------------------------------------------- */
 /* Number of kernels the library has launched in this process (host-side count). */
 uint64_t hra_launch_counter(void);

@@ -34,7 +34,10 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_work
             "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_sampled",
             "hra_codebook_step_noalloc",
             "hra_linear_workspace_size",
-            "hra_linear", "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
+            "hra_linear", "hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_linear_fp8_workspace_size",
+            "hra_linear_fp8", "hra_fp8_calibrate_workspace_size", "hra_fp8_calibrate",
+            "hra_prefill_fp8_workspace_size", "hra_prefill_fp8",
+            "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
             "hra_device_error", "hra_status_string"]
 PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6,
          "decode_attention": 7, "decode_linear": 8}
@@ -65,6 +68,11 @@ class HraWeights(ctypes.Structure):
 
 class HraKvCache(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("batch", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
+
+
+class HraFp8Layer(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("w_scale", ctypes.c_void_p), ("a_scale", ctypes.c_void_p)]
 
 
 class HraSampling(ctypes.Structure):
@@ -116,6 +124,23 @@ def lib() -> ctypes.CDLL:
         L.hra_codebook_step_sampled.restype = ctypes.c_int
         L.hra_codebook_step_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
         L.hra_codebook_step_noalloc.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        L.hra_fp8_quantize_weight.argtypes = [vp, i64, vp, vp, vp]
+        L.hra_fp8_quantize.argtypes = [vp, i64, vp, vp, vp]
+        L.hra_linear_fp8_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.hra_linear_fp8_workspace_size.restype = sz
+        L.hra_linear_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp]
+        L.hra_fp8_calibrate_workspace_size.argtypes = [dp, i32, i32, i32]
+        L.hra_fp8_calibrate_workspace_size.restype = sz
+        L.hra_fp8_calibrate.argtypes = [dp, ctypes.POINTER(HraWeights), vp, ctypes.POINTER(i32), i32, i32,
+                                        ctypes.POINTER(HraKvCache), vp, vp, vp, sz, vp]
+        L.hra_prefill_fp8_workspace_size.argtypes = [dp, i32, i32, i32]
+        L.hra_prefill_fp8_workspace_size.restype = sz
+        L.hra_prefill_fp8.argtypes = [dp, ctypes.POINTER(HraWeights), ctypes.POINTER(HraFp8Layer), vp,
+                                      ctypes.POINTER(i32), i32, i32, ctypes.POINTER(HraKvCache), vp, vp, sz, u32, vp]
+        for f in ("hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_linear_fp8", "hra_fp8_calibrate",
+                  "hra_prefill_fp8"):
+            getattr(L, f).restype = ctypes.c_int
         L.hra_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.hra_linear_workspace_size.restype = sz
         L.hra_linear.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]
@@ -485,6 +510,107 @@ def hra_linear(a: torch.Tensor, w: torch.Tensor, epilogue: int = EPI_STORE,
     if err != 0:
         raise HraError(f"hra_linear device error bits {err}")
     return out
+
+
+def fp8_quantize_weight(w: torch.Tensor, stream=None):
+    """hra_fp8_quantize_weight: bf16 CUDA tensor -> (E4M3 codes uint8 same shape, scale float32 [1])."""
+    w8 = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(1, dtype=torch.float32, device=w.device)
+    _check(lib().hra_fp8_quantize_weight(_ptr(w, torch.bfloat16, "w"), w.numel(), _ptr(w8, torch.uint8, "w8"),
+                                         _ptr(sc, torch.float32, "scale"), _stream(stream)), "hra_fp8_quantize_weight")
+    return w8, sc
+
+
+def fp8_quantize(x: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:
+    """hra_fp8_quantize: e4m3(x / scale) as uint8 codes (scale: CUDA float32 scalar tensor)."""
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().hra_fp8_quantize(_ptr(x, torch.bfloat16, "x"), x.numel(), _ptr(scale, torch.float32, "scale"),
+                                  _ptr(x8, torch.uint8, "x8"), _stream(stream)), "hra_fp8_quantize")
+    return x8
+
+
+def hra_linear_fp8(a8: torch.Tensor, w8: torch.Tensor, a_scale: torch.Tensor, w_scale: torch.Tensor,
+                   epilogue: int = EPI_STORE, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """hra_linear_fp8: a8 [M, K] and w8 [N or 2N, K] E4M3 codes (uint8), per-tensor scales."""
+    M, K = a8.shape
+    rows = w8.shape[0]
+    N = rows // 2 if epilogue == EPI_SWIGLU else rows
+    if out is None:
+        dt = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+        out = torch.empty(M, N, dtype=dt, device=a8.device)
+    ws = torch.empty(lib().hra_linear_fp8_workspace_size(M, N, K, epilogue), dtype=torch.uint8, device=a8.device)
+    _check(lib().hra_linear_fp8(_ptr(a8, torch.uint8, "a8"), _ptr(w8, torch.uint8, "w8"), _ptr(out, None, "out"),
+                                M, N, K, _ptr(a_scale, torch.float32, "a_scale"),
+                                _ptr(w_scale, torch.float32, "w_scale"), epilogue, _ptr(ws, None, "workspace"),
+                                ws.numel(), _stream(stream)), "hra_linear_fp8")
+    return out
+
+
+class Fp8Backbone:
+    """The static-FP8 variant of a Backbone: E4M3 copies of every projection (hra_fp8_quantize_weight)
+    and static activation scales from hra_fp8_calibrate."""
+
+    NAMES = ("w_qkv", "w_o", "w_gate_up", "w_down")
+
+    def __init__(self, bb: "Backbone"):
+        self.bb = bb
+        d = bb.d
+        dev = bb.device
+        self.w8, self.w_scale = [], torch.empty(d.n_layers, 4, dtype=torch.float32, device=dev)
+        for l, lay in enumerate(bb.w["layers"]):
+            q = []
+            for i, name in enumerate(self.NAMES):
+                w8, sc = fp8_quantize_weight(lay[name])
+                q.append(w8)
+                self.w_scale[l, i] = sc[0]
+            self.w8.append(q)
+        self.amax = torch.zeros(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self.a_scale = torch.ones(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self._table()
+
+    def _table(self):
+        t = (HraFp8Layer * len(self.w8))()
+        for l, q in enumerate(self.w8):
+            t[l].w_qkv, t[l].w_o, t[l].w_gate_up, t[l].w_down = [x.data_ptr() for x in q]
+            t[l].w_scale = self.w_scale[l].data_ptr()
+            t[l].a_scale = self.a_scale[l].data_ptr()
+        self.table = t
+
+    def calibrate(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor, stream=None):
+        """hra_fp8_calibrate on a calibration batch: fills amax and a_scale [n_layers, 4]."""
+        B, P = tokens.shape
+        lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens])
+        need = lib().hra_fp8_calibrate_workspace_size(ctypes.byref(self.bb.dims), B, int(sum(seq_lens)), P)
+        ws = torch.empty(need, dtype=torch.uint8, device=tokens.device)
+        kv = self.bb.kv(cache)
+        _check(lib().hra_fp8_calibrate(ctypes.byref(self.bb.dims), ctypes.byref(self.bb.table),
+                                       _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
+                                       _ptr(self.amax, torch.float32, "amax"),
+                                       _ptr(self.a_scale, torch.float32, "a_scale"), _ptr(ws, None, "workspace"),
+                                       ws.numel(), _stream(stream)), "hra_fp8_calibrate")
+        return self.amax, self.a_scale
+
+    def prefill_workspace_size(self, batch, total, max_len) -> int:
+        return lib().hra_prefill_fp8_workspace_size(ctypes.byref(self.bb.dims), batch, total, max_len)
+
+    def prefill(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor,
+                out: Optional[torch.Tensor] = None, full_last_layer: bool = False,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """hra_prefill_fp8 -> last hidden [B, H] bf16."""
+        B, P = tokens.shape
+        lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens])
+        if out is None:
+            out = torch.empty(B, self.bb.d.hidden, dtype=torch.bfloat16, device=tokens.device)
+        need = self.prefill_workspace_size(B, int(sum(seq_lens)), P)
+        ws = workspace if workspace is not None else self.bb.ws.get(need, tokens.device)
+        kv = self.bb.kv(cache)
+        _check(lib().hra_prefill_fp8(ctypes.byref(self.bb.dims), ctypes.byref(self.bb.table), self.table,
+                                     _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
+                                     _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
+                                     ws.numel(), PREFILL_FULL_LAST_LAYER if full_last_layer else 0,
+                                     _stream(stream)), "hra_prefill_fp8")
+        self.last_ws = ws
+        return out
 
 
 def hra_device_error(workspace: torch.Tensor, stream=None) -> int:

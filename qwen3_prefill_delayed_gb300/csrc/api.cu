@@ -75,7 +75,7 @@ struct Region {
 
 // Offsets (bytes) of every buffer inside a caller workspace.
 struct Layout {
-    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, total;
+    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, total;
     int attn_splits;
 };
 
@@ -103,7 +103,7 @@ bool audio_dims_ok(const hra_dims* d) {
 
 // Shared plan of the backbone passes.  `rows` = packed rows that run the full layers, `last_rows`
 // = rows of the last-layer tail (batch), `rope_rows` = rows of the RoPE table.
-Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, int max_pos) {
+Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, int max_pos, bool fp8 = false) {
     const size_t H = d.hidden, hd = d.head_dim, Dq = (size_t)d.n_q_heads * hd;
     const size_t Dqkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * hd, F = d.ffn;
     const size_t T = (size_t)std::max(rows, batch);
@@ -133,6 +133,8 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     L.part = g.take(part);
     L.attn_splits = decode_attention_splits(batch, d.n_kv_heads, max_pos);
     L.apart = g.take(decode_attention_scratch_bytes(batch, d.n_q_heads, d.head_dim, L.attn_splits));
+    // FP8 variant: the E4M3 copy of the current projection's input (the widest input is the FFN's)
+    L.x8 = fp8 ? g.take(T * std::max(std::max(H, Dq), F)) : 0;
     L.total = g.off;
     return L;
 }
@@ -154,15 +156,42 @@ int cuda_status(cudaError_t e) {
         if (e_ != cudaSuccess) return cuda_status(e_); \
     } while (0)
 
+// FP8 variant / calibration of one layer's projections: `layers` (the E4M3 weights and scales) makes
+// every projection quantize its input into x8 and run the FP8 GEMM; `amax` records max |input| of
+// each projection (4 per layer: QKV, output, gate/up, down inputs).
+struct QuantCtx {
+    const hra_fp8_layer* layers;
+    float* amax;
+    uint8_t* x8;
+    int layer;
+};
+enum Proj : int { PROJ_QKV = 0, PROJ_O = 1, PROJ_GATE_UP = 2, PROJ_DOWN = 3 };
+
 // norm_gain / norm_out: for EPI_RESIDUAL, the RMSNorm that follows (fused into a split-K reduction
 // when the plan splits; otherwise run as its own kernel here).
 cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K, int epi, const Ptrs& P,
                    const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE,
                    const void* norm_gain = nullptr, bf16* norm_out = nullptr, float eps = 0.f,
                    const int32_t* norm_rows = nullptr, int norm_nrows = 0, const QkRopeArgs* qk = nullptr,
-                   bool* qk_done = nullptr, bool shallow_ring = false) {
+                   bool* qk_done = nullptr, bool shallow_ring = false, const QuantCtx* qc = nullptr,
+                   int proj = PROJ_QKV) {
     LinearCall c{};
     c.shallow_ring = shallow_ring;
+    if (qc != nullptr && qc->amax != nullptr) {
+        cudaError_t e = launch_absmax(a, (long long)M * K, qc->amax + 4 * qc->layer + proj, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (qc != nullptr && qc->layers != nullptr) {
+        const hra_fp8_layer& f = qc->layers[qc->layer];
+        const void* w8s[4] = {f.w_qkv, f.w_o, f.w_gate_up, f.w_down};
+        cudaError_t e = launch_fp8_quantize(a, (long long)M * K, f.a_scale + proj, qc->x8, st);
+        if (e != cudaSuccess) return e;
+        a = reinterpret_cast<const bf16*>(qc->x8);   // E4M3 codes from here on
+        w = w8s[proj];
+        c.fp8 = true;
+        c.a_scale = f.a_scale + proj;
+        c.w_scale = f.w_scale + proj;
+    }
     c.qk = qk;
     c.qk_done = qk_done;
     c.a = a;
@@ -200,7 +229,7 @@ bool layer_ptrs_ok(const hra_layer_weights& l) {
 int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
                int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
                const int32_t* seq_lens_host, int max_pos, cudaStream_t st, int rope_rows = 0,
-               const int32_t* start_host = nullptr) {
+               const int32_t* start_host = nullptr, const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr) {
     const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d.rms_eps;
@@ -230,6 +259,8 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
         const bool last = l == d.n_layers - 1;
+        const QuantCtx qc{fp8, amax, fp8 ? P.at<uint8_t>(L.x8) : nullptr, l};
+        const QuantCtx* qcp = (fp8 != nullptr || amax != nullptr) ? &qc : nullptr;
         QkRopeArgs qa{};
         qa.qkv = qkv;
         qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
@@ -249,7 +280,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         qa.eps = eps;
         bool qk_done = false;
         HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : lin_probe, nullptr,
-                       nullptr, 0.f, nullptr, 0, &qa, &qk_done));
+                       nullptr, 0.f, nullptr, 0, &qa, &qk_done, false, qcp, PROJ_QKV));
         if (!qk_done) HRA_TRY(launch_qk_rope_kv(qa, st));
 
         const bool tail = prefill && last && !full_last;
@@ -279,18 +310,21 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             }
             HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st,
                            prefill ? HRA_PROBE_O_PROJ : lin_probe, lw.mlp_norm, y, eps, nullptr, 0, nullptr,
-                           nullptr, /*shallow_ring=*/!prefill));
+                           nullptr, /*shallow_ring=*/!prefill, qcp, PROJ_O));
             HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st,
-                           prefill ? HRA_PROBE_GATE_UP : lin_probe));
+                           prefill ? HRA_PROBE_GATE_UP : lin_probe, nullptr, nullptr, 0.f, nullptr, 0, nullptr,
+                           nullptr, false, qcp, PROJ_GATE_UP));
             if (!last) {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st,
-                               prefill ? HRA_PROBE_DOWN : lin_probe, w.layers[l + 1].attn_norm, y, eps));
+                               prefill ? HRA_PROBE_DOWN : lin_probe, w.layers[l + 1].attn_norm, y, eps, nullptr, 0,
+                               nullptr, nullptr, false, qcp, PROJ_DOWN));
             } else if (!prefill) {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, lin_probe, w.final_norm,
-                               out_hidden, eps));
+                               out_hidden, eps, nullptr, 0, nullptr, nullptr, false, qcp, PROJ_DOWN));
             } else {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, HRA_PROBE_DOWN,
-                               w.final_norm, out_hidden, eps, last_row, batch));
+                               w.final_norm, out_hidden, eps, last_row, batch, nullptr, nullptr, false, qcp,
+                               PROJ_DOWN));
             }
         } else {
             // last prefill layer, rows that feed the last hidden only
@@ -312,9 +346,11 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             HRA_TRY(launch_decode_attention(da, st));
             HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
             HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps, nullptr, 0,
-                           nullptr, nullptr, /*shallow_ring=*/true));
-            HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st));
-            HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps));
+                           nullptr, nullptr, /*shallow_ring=*/true, qcp, PROJ_O));
+            HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st, 0, nullptr, nullptr, 0.f, nullptr, 0,
+                           nullptr, nullptr, false, qcp, PROJ_GATE_UP));
+            HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps,
+                           nullptr, 0, nullptr, nullptr, false, qcp, PROJ_DOWN));
         }
     }
     return HRA_OK;
@@ -378,9 +414,12 @@ size_t hra_prefill_chunk_workspace_size(const hra_dims* dims, int32_t batch, int
 
 namespace {
 
+constexpr int H_ALIGN_FP8(int k) { return k % 128; }
+
 int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev, const int32_t* seq_lens,
                  const int32_t* start_pos, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
-                 void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream) {
+                 void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream,
+                 const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr, bool validate_only = false) {
     if (dims == nullptr || weights == nullptr || tokens_dev == nullptr || seq_lens == nullptr || kv == nullptr)
         return HRA_ERR_INVALID_ARG;
     if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
@@ -406,8 +445,20 @@ int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t
     }
     meta.vals[batch] = (int32_t)T;
     if (T > (1 << 30)) return HRA_ERR_RANGE;
-    const Layout L = backbone_layout(d, batch, (int)T, max_end, max_end - 1);
+    if (fp8 != nullptr) {
+        if ((H_ALIGN_FP8(d.hidden) | H_ALIGN_FP8(d.n_q_heads * d.head_dim) | H_ALIGN_FP8(d.ffn)) != 0)
+            return HRA_ERR_UNSUPPORTED;   // FP8 K blocks are 128 elements
+        for (int l = 0; l < d.n_layers; ++l) {
+            const hra_fp8_layer& f = fp8[l];
+            if (!aligned16(f.w_qkv) || !aligned16(f.w_o) || !aligned16(f.w_gate_up) || !aligned16(f.w_down) ||
+                f.w_scale == nullptr || f.a_scale == nullptr || (reinterpret_cast<uintptr_t>(f.w_scale) & 3u) ||
+                (reinterpret_cast<uintptr_t>(f.a_scale) & 3u))
+                return HRA_ERR_INVALID_ARG;
+        }
+    }
+    const Layout L = backbone_layout(d, batch, (int)T, max_end, max_end - 1, fp8 != nullptr);
     if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
+    if (validate_only) return HRA_OK;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
@@ -421,7 +472,7 @@ int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t
                                  P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
     return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
                       (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), seq_lens,
-                      max_end - 1, st, max_end, start_pos);
+                      max_end - 1, st, max_end, start_pos, fp8, amax);
 }
 
 }  // namespace
@@ -440,6 +491,78 @@ int hra_prefill_chunk(const hra_dims* dims, const hra_weights* weights, const in
     if (start_pos == nullptr) return HRA_ERR_INVALID_ARG;
     return prefill_impl(dims, weights, tokens_dev, seq_lens, start_pos, batch, max_len, kv, last_hidden_dev,
                         workspace, workspace_bytes, flags, stream);
+}
+
+size_t hra_prefill_fp8_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
+    if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1) return 0;
+    return backbone_layout(*dims, batch, total_tokens, max_len, max_len - 1, true).total;
+}
+
+int hra_prefill_fp8(const hra_dims* dims, const hra_weights* weights, const hra_fp8_layer* fp8_layers,
+                    const int32_t* tokens_dev, const int32_t* seq_lens, int32_t batch, int32_t max_len,
+                    const hra_kv_cache* kv, void* last_hidden_dev, void* workspace, size_t workspace_bytes,
+                    uint32_t flags, void* stream) {
+    if (fp8_layers == nullptr) return HRA_ERR_INVALID_ARG;
+    return prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last_hidden_dev, workspace,
+                        workspace_bytes, flags, stream, fp8_layers, nullptr);
+}
+
+size_t hra_fp8_calibrate_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
+    const size_t pf = hra_prefill_workspace_size(dims, batch, total_tokens, max_len);
+    if (pf == 0) return 0;
+    return align_up(pf) + align_up((size_t)batch * dims->hidden * 2);
+}
+
+int hra_fp8_calibrate(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev,
+                      const int32_t* seq_lens, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
+                      float* amax_dev, float* scale_dev, void* workspace, size_t workspace_bytes, void* stream) {
+    if (dims == nullptr || seq_lens == nullptr || amax_dev == nullptr || scale_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(amax_dev) & 3u) || (reinterpret_cast<uintptr_t>(scale_dev) & 3u))
+        return HRA_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
+    if (batch < 1 || batch > kMaxBatch) return HRA_ERR_INVALID_ARG;
+    long long T = 0;
+    for (int b = 0; b < batch; ++b) T += seq_lens[b];
+    if (T < batch || T > (1 << 30)) return HRA_ERR_RANGE;
+    const size_t need = hra_fp8_calibrate_workspace_size(dims, batch, (int32_t)T, max_len);
+    if (need == 0) return HRA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return HRA_ERR_WORKSPACE;
+    const size_t pf = align_up(hra_prefill_workspace_size(dims, batch, (int32_t)T, max_len));
+    void* last = reinterpret_cast<uint8_t*>(workspace) + pf;
+    // the bf16 prefill with every row through the last layer, recording max |input| per projection
+    int rc = prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last, workspace, pf,
+                          HRA_PREFILL_FULL_LAST_LAYER, stream, nullptr, amax_dev, /*validate_only=*/true);
+    if (rc != HRA_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int n = 4 * dims->n_layers;
+    HRA_TRY(launch_zero_floats(amax_dev, n, st));
+    rc = prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last, workspace, pf,
+                      HRA_PREFILL_FULL_LAST_LAYER, stream, nullptr, amax_dev);
+    if (rc != HRA_OK) return rc;
+    HRA_TRY(launch_amax_to_scale(amax_dev, scale_dev, n, st));
+    return HRA_OK;
+}
+
+int hra_fp8_quantize_weight(const void* w_dev, int64_t n, void* w8_dev, float* scale_dev, void* stream) {
+    if (!aligned16(w_dev) || w8_dev == nullptr || (reinterpret_cast<uintptr_t>(w8_dev) & 7u) || scale_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(scale_dev) & 3u) || n < 8 || n % 8 != 0)
+        return HRA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    HRA_TRY(launch_zero_floats(scale_dev, 1, st));
+    HRA_TRY(launch_absmax(reinterpret_cast<const bf16*>(w_dev), n, scale_dev, st));
+    HRA_TRY(launch_amax_to_scale(scale_dev, scale_dev, 1, st));
+    HRA_TRY(launch_fp8_quantize(reinterpret_cast<const bf16*>(w_dev), n, scale_dev, reinterpret_cast<uint8_t*>(w8_dev),
+                                st));
+    return HRA_OK;
+}
+
+int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void* x8_dev, void* stream) {
+    if (!aligned16(x_dev) || x8_dev == nullptr || (reinterpret_cast<uintptr_t>(x8_dev) & 7u) || scale_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(scale_dev) & 3u) || n < 8 || n % 8 != 0)
+        return HRA_ERR_INVALID_ARG;
+    HRA_TRY(launch_fp8_quantize(reinterpret_cast<const bf16*>(x_dev), n, scale_dev, reinterpret_cast<uint8_t*>(x8_dev),
+                                reinterpret_cast<cudaStream_t>(stream)));
+    return HRA_OK;
 }
 
 size_t hra_decode_workspace_size(const hra_dims* dims, int32_t batch, int32_t n_slots) {
@@ -692,6 +815,43 @@ int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, i
     c.split_req = split_k;
     c.partial = reinterpret_cast<float*>(base + 256);
     c.err = reinterpret_cast<unsigned int*>(base);
+    HRA_TRY(launch_linear(c, st));
+    return HRA_OK;
+}
+
+size_t hra_linear_fp8_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue) {
+    if (M < 1 || N < 8 || K < 128) return 0;
+    size_t part = linear_partial_bound(M, N, K, epilogue);
+    if (M > 128) part = std::max(part, linear_tail_bound());
+    return 256 + align_up(part);
+}
+
+int hra_linear_fp8(const void* a8_dev, const void* w8_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
+                   const float* a_scale_dev, const float* w_scale_dev, int32_t epilogue, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    if (!aligned16(a8_dev) || !aligned16(w8_dev) || !aligned16(out_dev) || !aligned16(workspace) ||
+        a_scale_dev == nullptr || w_scale_dev == nullptr || (reinterpret_cast<uintptr_t>(a_scale_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(w_scale_dev) & 3u))
+        return HRA_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || N % 8 != 0 || K < 128 || K % 128 != 0) return HRA_ERR_INVALID_ARG;
+    if (epilogue < EPI_STORE || epilogue > EPI_F32) return HRA_ERR_INVALID_ARG;
+    if (workspace_bytes < hra_linear_fp8_workspace_size(M, N, K, epilogue)) return HRA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+    HRA_TRY(cudaMemsetAsync(base, 0, 4, st));
+    LinearCall c{};
+    c.a = reinterpret_cast<const bf16*>(a8_dev);
+    c.w = reinterpret_cast<const bf16*>(w8_dev);
+    c.out = out_dev;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.epi = epilogue;
+    c.partial = reinterpret_cast<float*>(base + 256);
+    c.err = reinterpret_cast<unsigned int*>(base);
+    c.fp8 = true;
+    c.a_scale = a_scale_dev;
+    c.w_scale = w_scale_dev;
     HRA_TRY(launch_linear(c, st));
     return HRA_OK;
 }

@@ -55,6 +55,9 @@ struct GemmArgs {
     unsigned int* zero_ptr;   // CTA 0 clears zero_words words here once earlier kernels are done
     int zero_words;
     QkRopeArgs qk;            // KM_QKROPE: per-head q/k norm + RoPE + K/V cache write in the epilogue
+    // FP8 operands: the accumulators are multiplied by (*a_scale) * (*w_scale) (device scalars)
+    const float* a_scale;
+    const float* w_scale;
 };
 
 template <int BN>
@@ -220,11 +223,14 @@ __device__ __forceinline__ void unit_work(int u, const GemmArgs& p, int& mb, int
 }
 
 // Persistent: each CTA walks work units blockIdx.x, blockIdx.x + gridDim.x, ...
-template <int BN, bool SWIGLU>
+// F8: both operands E4M3 (kind::f8f6f4): a 128-byte stage row holds 128 elements instead of 64,
+// and every accumulator is scaled by the two per-tensor scales before any store.
+template <int BN, bool SWIGLU, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
     using C = Cfg<BN>;
+    constexpr int KE = F8 ? 2 * BK : BK;   // elements per K block (one 128-byte row)
     pdl_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
                 mbar_expect_tx(full_bar(pre), C::STAGE_BYTES);
-                load_w(pre, kb * BK, nb);
+                load_w(pre, kb * KE, nb);
             }
         }
         pdl_wait();
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-                const int kx = kb * BK;
+                const int kx = kb * KE;
                 if (it >= pre) {
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *issued_slot = ok ? it : max(it, pre);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer: accumulator buffer j % 2 for this CTA's j-th unit
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
         int it = 0, j = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
@@ -345,8 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t ad = sdesc_sw128(a_tile(s));
                 const uint64_t bd = sdesc_sw128(b_tile(s));
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {   // 4 x 32 bytes of each 128-byte row
+                    if constexpr (F8)
+                        tc_mma_f8(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    else
+                        tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                }
                 tc_commit(empty_bar(s));
             }
             tc_commit(tfull_bar(buf));
@@ -358,6 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (blockIdx.x == 0 && warp == 2)
             for (int i = lane; i < p.zero_words; i += 32) p.zero_ptr[i] = 0u;
         const int quad = warp & 3;
+        float scale = 1.f;
+        if constexpr (F8) scale = (*p.a_scale) * (*p.w_scale);
+        auto scaled = [&](float (&v)[32]) {
+            if constexpr (F8) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] *= scale;
+            }
+        };
         int j = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             int mb, nb, kb0, kb1, piece;
@@ -385,11 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(tq + c, v);
+                    scaled(v);
                     float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
-            } else if (!SWIGLU && p.mode == KM_QKROPE) {
+            } else if (!SWIGLU && !F8 && p.mode == KM_QKROPE) {
                 qk_rope_epilogue<BN>(tq, nb * BN, row, row_ok, p.qk);
             } else if (!SWIGLU) {
                 const int n0 = nb * BN;
@@ -397,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(tq + c, v);
+                    scaled(v);
                     const int col = n0 + c;
                     if (row_ok && col < p.n_valid)
                         store_row_chunk(p.mode, p.out, split_off + (long long)row * p.ldo + col, v,
@@ -409,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float g[32], uu[32];
                     tmem_ld32(tq + c, g);
                     tmem_ld32(tq + BN / 2 + c, uu);
+                    scaled(g);
+                    scaled(uu);
                     const int col = j0 + c;
                     if (row_ok && col < p.n_valid) {
                         const int nv = min(32, p.n_valid - col);
@@ -940,13 +962,15 @@ bool get_encoder() {
     return g_encode != nullptr;
 }
 
-// Row-major bf16 matrix [rows, cols] viewed as a 2-D tensor (cols innermost), boxes of 64 x box_rows.
-bool encode_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+// Row-major matrix [rows, cols] of bf16 (esize 2) or one-byte E4M3 (esize 1) viewed as a 2-D
+// tensor (cols innermost), boxes of 128 bytes x box_rows.
+bool encode_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int esize) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+    return g_encode(m, esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -955,23 +979,24 @@ bool encode_map(CUtensorMap* m, const void* base, int rows, int cols, int box_ro
 // matrix is seen again (weights every call, workspace buffers every layer).
 struct MapKey {
     const void* base;
-    int rows, cols, box_rows;
+    int rows, cols, box_rows, esize;
     bool operator==(const MapKey& o) const {
-        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows;
+        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows && esize == o.esize;
     }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
         size_t h = std::hash<const void*>()(k.base);
-        h ^= (size_t)k.rows * 0x9E3779B97F4A7C15ull + (size_t)k.cols * 0xC2B2AE3D27D4EB4Full + (size_t)k.box_rows;
+        h ^= (size_t)k.rows * 0x9E3779B97F4A7C15ull + (size_t)k.cols * 0xC2B2AE3D27D4EB4Full + (size_t)k.box_rows +
+             ((size_t)k.esize << 40);
         return h;
     }
 };
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
-    const MapKey key{base, rows, cols, box_rows};
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int esize = 2) {
+    const MapKey key{base, rows, cols, box_rows, esize};
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_maps.find(key);
@@ -980,7 +1005,7 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows
             return true;
         }
     }
-    if (!encode_map(m, base, rows, cols, box_rows)) return false;
+    if (!encode_map(m, base, rows, cols, box_rows, esize)) return false;
     std::lock_guard<std::mutex> lk(g_map_mu);
     if (g_maps.size() > 8192) g_maps.clear();
     g_maps.emplace(key, *m);
@@ -1015,8 +1040,8 @@ void plan_tail(Plan& pl, int n_kb, int nsm) {
 // units), so the grid runs in ceil(units / SMs) rounds; per-unit time ~ (K blocks) x BN (bytes
 // streamed and MMA work both scale with BN) plus a fixed tile overhead.  Splitting K is allowed
 // for a single M tile only and costs a reduction pass.
-Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm) {
-    const int n_kb = K / BK;
+Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm, int ke = BK) {
+    const int n_kb = K / ke;
     const int mt = (M + BM - 1) / BM;
     const int dcols = epi == EPI_SWIGLU ? 2 * N : N;
     Plan best{256, 1, n_kb, mt, 0};
@@ -1051,7 +1076,7 @@ Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm) {
     return best;
 }
 
-template <int BN, bool SW>
+template <int BN, bool SW, bool F8>
 cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, const Plan& pl,
                         cudaStream_t st) {
     static bool configured[64] = {false};
@@ -1059,7 +1084,7 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, SW, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<BN>::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -1067,7 +1092,7 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     const long long units = (long long)pl.mt * pl.nt * pl.splits;
     const int nsm = device_sm_count();
     dim3 grid((unsigned)std::min<long long>(units, nsm));
-    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ma, mb, g);
+    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW, F8>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ma, mb, g);
     return cudaGetLastError();
 }
 
@@ -1262,24 +1287,30 @@ size_t linear_partial_bound(int m_max, int N, int K, int epi) {
 
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     if (!get_encoder()) return cudaErrorNotSupported;
-    if (c.M <= kSmallM) return launch_linear_small(c, st);
+    if (c.M <= kSmallM && !c.fp8) return launch_linear_small(c, st);   // FP8 always takes the tile path
     const int nsm = device_sm_count();
-    Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm);
+    const int ke = c.fp8 ? 2 * BK : BK;
+    if (c.fp8 && (c.K % ke != 0 || c.a_scale == nullptr || c.w_scale == nullptr)) return cudaErrorInvalidValue;
+    Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm, ke);
     if (c.partial_only) pl.tail_tiles = 0;   // the caller reads one output plane from the partial buffer
-    const bool fuse_qk = c.qk != nullptr && c.epi == EPI_STORE && pl.splits == 1 && pl.bn % c.qk->hd == 0;
+    const bool fuse_qk =
+        !c.fp8 && c.qk != nullptr && c.epi == EPI_STORE && pl.splits == 1 && pl.bn % c.qk->hd == 0;
     if (fuse_qk) pl.tail_tiles = 0;
     const bool sw = c.epi == EPI_SWIGLU;
     const int w_rows = sw ? 2 * c.N : c.N;
+    const int esize = c.fp8 ? 1 : 2;
 
     CUtensorMap ma, mb;
-    if (!make_map(&ma, c.a, c.M, c.K, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, c.w, w_rows, c.K, sw ? pl.bn / 2 : pl.bn)) return cudaErrorInvalidValue;
+    if (!make_map(&ma, c.a, c.M, c.K, BM, esize)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, c.w, w_rows, c.K, sw ? pl.bn / 2 : pl.bn, esize)) return cudaErrorInvalidValue;
 
-    GemmArgs g;
+    GemmArgs g{};
     g.err = c.err;
     g.M = c.M;
     g.n_valid = c.N;
-    g.n_kb = c.K / BK;
+    g.n_kb = c.K / ke;
+    g.a_scale = c.a_scale;
+    g.w_scale = c.w_scale;
     g.kb_per_split = pl.kbps;
     g.up_row0 = c.N;
     g.mt = pl.mt;
@@ -1311,10 +1342,16 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     }
 
     cudaError_t e;
-    if (pl.bn == 256)
-        e = sw ? launch_tile<256, true>(ma, mb, g, pl, st) : launch_tile<256, false>(ma, mb, g, pl, st);
-    else
-        e = sw ? launch_tile<128, true>(ma, mb, g, pl, st) : launch_tile<128, false>(ma, mb, g, pl, st);
+    if (c.fp8) {
+        if (pl.bn == 256)
+            e = sw ? launch_tile<256, true, true>(ma, mb, g, pl, st) : launch_tile<256, false, true>(ma, mb, g, pl, st);
+        else
+            e = sw ? launch_tile<128, true, true>(ma, mb, g, pl, st) : launch_tile<128, false, true>(ma, mb, g, pl, st);
+    } else if (pl.bn == 256) {
+        e = sw ? launch_tile<256, true, false>(ma, mb, g, pl, st) : launch_tile<256, false, false>(ma, mb, g, pl, st);
+    } else {
+        e = sw ? launch_tile<128, true, false>(ma, mb, g, pl, st) : launch_tile<128, false, false>(ma, mb, g, pl, st);
+    }
     if (c.splits_used) *c.splits_used = pl.splits;
     if (e == cudaSuccess && pl.tail_tiles > 0) {
         const int gw = sw ? pl.bn / 16 : pl.bn / 8;

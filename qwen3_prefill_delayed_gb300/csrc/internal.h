@@ -91,7 +91,11 @@ struct LinearCall {
     bool* qk_done;
     // small-M path: stream the weights through the shallow ring, so that the launch fits on an SM
     // beside a kernel that still holds much shared memory (the attention before the o-projection)
-    bool shallow_ring;
+    bool shallow_ring;    // FP8: a and w hold E4M3 codes (K a multiple of 128); the accumulators are scaled by
+    // (*a_scale) * (*w_scale), device scalars.  Always runs the tile kernel (any M).
+    bool fp8;
+    const float* a_scale;
+    const float* w_scale;
 };
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool partial_only);
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st);
@@ -190,5 +194,14 @@ struct CodebookArgs {
     int top_k;
 };
 cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ E4M3 quantization (fp8.cu)
+// out = e4m3(x / *scale), n a multiple of 8 (x 16-byte, out 8-byte aligned)
+cudaError_t launch_fp8_quantize(const bf16* x, long long n, const float* scale, uint8_t* out, cudaStream_t st);
+// *amax = max(*amax, max |x|), n a multiple of 8
+cudaError_t launch_absmax(const bf16* x, long long n, float* amax, cudaStream_t st);
+cudaError_t launch_zero_floats(float* v, int n, cudaStream_t st);
+// scale[i] = amax[i] > 0 ? amax[i] / 448 : 1
+cudaError_t launch_amax_to_scale(const float* amax, float* scale, int n, cudaStream_t st);
 
 }  // namespace hra

@@ -51,20 +51,48 @@ LOGIT_TOL = 5e-2                                   # logits, max |err|
 ARGMAX_MARGIN = 0.1                                # argmax must agree above this top-1/top-2 margin
 
 
-def parity_bar(ref: np.ndarray, alt: np.ndarray, factor: float = 2.0):
-    """Hidden/KV bar against the oracle.  `alt` is the oracle run with every dot product summed in
-    the opposite order (an equally valid evaluation).  The stated bar (max |err| <= 2e-2, cosine
-    >= 0.9999) holds wherever it is above the oracle's own reordering spread; where that spread is
-    larger (deep stacks amplify single bf16 rounding flips), the bar is `factor` x the spread."""
-    floor_abs = float(np.max(np.abs(ref - alt))) if ref.size else 0.0
-    floor_1mcos = 1.0 - cosine(ref, alt) if ref.size else 0.0
+def parity_bar(ref: np.ndarray, alt: np.ndarray, factor: float = 2.0, extra_alts=()):
+    """Hidden/KV bar against the oracle.  `alt` is the oracle run with every open sum taken in the
+    opposite order (an equally valid evaluation); `extra_alts` are further equally valid oracle
+    runs (the FP8 variant adds its static scales moved by one fp32 ulp).  The stated bar (max |err|
+    <= 2e-2, cosine >= 0.9999) holds wherever it is above the oracle's own spread across these
+    runs; where that spread is larger (deep stacks amplify single bf16 rounding flips; E4M3's
+    3-bit mantissa turns last-bit input differences into whole-step code flips), the bar is
+    `factor` x the largest spread."""
+    floor_abs, floor_1mcos = 0.0, 0.0
+    for a in (alt, *extra_alts):
+        if ref.size:
+            floor_abs = max(floor_abs, float(np.max(np.abs(ref - a))))
+            floor_1mcos = max(floor_1mcos, 1.0 - cosine(ref, a))
     max_abs = max(HIDDEN_TOL["max_abs"], factor * floor_abs)
     min_cos = min(HIDDEN_TOL["min_cos"], 1.0 - factor * floor_1mcos)
     return dict(max_abs=max_abs, min_cos=min_cos), (floor_abs, floor_1mcos)
 
 
-def assert_parity(got: np.ndarray, ref: np.ndarray, alt: np.ndarray, what: str):
-    bar, floor = parity_bar(ref, alt)
+def assert_parity(got: np.ndarray, ref: np.ndarray, alt: np.ndarray, what: str, extra_alts=()):
+    bar, floor = parity_bar(ref, alt, extra_alts=extra_alts)
     err, cos = assert_close(got, ref, what=f"{what} [oracle self-spread max {floor[0]:.3g}, 1-cos {floor[1]:.2g}]",
                             **bar)
     return err, cos, floor
+
+
+# E4M3 keeps 3 mantissa bits to bf16's 7: a one-step bf16 difference of a projection input crosses an
+# E4M3 rounding boundary about 2^-4 of the time and then moves the input by one E4M3 step (2^4 bf16
+# steps), so the bf16-level differences the bar above admits arrive ~2^2 larger in amplitude and
+# ~2^4 larger in 1 - cos after an FP8 projection.
+FP8_AMPLITUDE, FP8_ONE_MINUS_COS = 4.0, 16.0
+
+
+def assert_parity_fp8(got: np.ndarray, ref: np.ndarray, alts, ref_bf16: np.ndarray, what: str):
+    """FP8-variant bar: the bf16 parity bar over the oracle's spread (alts: equally valid oracle FP8
+    runs) widened by the E4M3 amplification, and the result must sit at least 4x closer (in
+    1 - cos) to the oracle's FP8 result than the oracle's bf16 result does, so that a projection
+    left in bf16 (or quantized twice) cannot pass."""
+    bar, floor = parity_bar(ref, alts[0], extra_alts=tuple(alts[1:]))
+    max_abs = FP8_AMPLITUDE * bar["max_abs"]
+    min_cos = 1.0 - FP8_ONE_MINUS_COS * (1.0 - bar["min_cos"])
+    err, cos = assert_close(got, ref, max_abs=max_abs, min_cos=min_cos,
+                            what=f"{what} [oracle self-spread max {floor[0]:.3g}, 1-cos {floor[1]:.2g}; fp8-widened]")
+    gap = 1.0 - cosine(ref_bf16, ref)
+    assert 1.0 - cos <= 0.25 * gap, f"{what}: 1-cos {1 - cos:.3g} not well inside the fp8-vs-bf16 gap {gap:.3g}"
+    return err, cos

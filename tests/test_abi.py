@@ -25,7 +25,7 @@ def hra():
 def _declared():
     with open(os.path.join(ROOT, "include", "hra.h")) as f:
         text = f.read()
-    return sorted(set(re.findall(r"\b(hra_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(hra_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(hra):
