@@ -47,11 +47,12 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(row * HD * 2 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int HD>
+// ROWS rows of HD bf16 into a swizzled tile, rows past rows_valid zero-filled (128 threads).
+template <int HD, int ROWS = PK>
 __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* gbase, long long row_stride, int rows_valid,
                                           int tid) {
     constexpr int CH = HD / 8;   // 16-byte chunks per row
-    for (int idx = tid; idx < PK * CH; idx += 128) {
+    for (int idx = tid; idx < ROWS * CH; idx += 128) {
         const int r = idx / CH, c = idx % CH;
         const bool ok = r < rows_valid;
         const bf16* src = gbase + (ok ? (long long)r * row_stride + c * 8 : 0);
@@ -59,8 +60,12 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* gbase, lon
     }
 }
 
+constexpr int AKT = 64;   // keys per K/V tile of the prefill kernel
+
+// Two CTAs per SM (80 KB of shared memory each) and the register budget that allows: measured on
+// short and long prompts, more CTAs with smaller key tiles or fewer registers were slower.
 template <int HD>
-__global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs a, float scale_log2) {
+__global__ void __launch_bounds__(128, 2) prefill_attn_kernel(const PrefillAttnArgs a, float scale_log2) {
     pdl_launch();
     pdl_wait();
     constexpr int KS = HD / 16;   // k-steps over the head dim
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     extern __shared__ __align__(128) uint8_t sm[];
     const uint32_t sQ = smem_u32(sm);
     const uint32_t sK0 = sQ + PQ * HD * 2;
-    const uint32_t sV0 = sK0 + 2 * PK * HD * 2;
+    const uint32_t sV0 = sK0 + 2 * AKT * HD * 2;
 
     const int b = blockIdx.z, h = blockIdx.y;
     const int n_qt = (a.max_len + PQ - 1) / PQ;
@@ -80,7 +85,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     const int kvh = h / (a.nq / a.nkv);
     const int s0 = a.start ? a.start[b] : 0;          // cached positions before this sequence's rows
     const int kv_len = s0 + min(len, q0 + PQ);        // keys this query tile can reach
-    const int n_kt = (kv_len + PK - 1) / PK;
+    const int n_kt = (kv_len + AKT - 1) / AKT;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long qstride = (long long)a.nq * HD;
@@ -89,9 +94,9 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     const bf16* kbase = a.kv_layer + ((long long)(b * 2) * a.nkv + kvh) * hstride;
     const bf16* vbase = a.kv_layer + ((long long)(b * 2 + 1) * a.nkv + kvh) * hstride;
 
-    load_tile<HD>(sQ, qbase, qstride, min(PQ, len - q0), tid);
-    load_tile<HD>(sK0, kbase, HD, min(PK, kv_len), tid);
-    load_tile<HD>(sV0, vbase, HD, min(PK, kv_len), tid);
+    load_tile<HD, PQ>(sQ, qbase, qstride, min(PQ, len - q0), tid);
+    load_tile<HD, AKT>(sK0, kbase, HD, min(AKT, kv_len), tid);
+    load_tile<HD, AKT>(sV0, vbase, HD, min(AKT, kv_len), tid);
     cp_async_commit();
 
     uint32_t qf[KS][4];
@@ -106,9 +111,11 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
     for (int kt = 0; kt < n_kt; ++kt) {
         const int buf = kt & 1;
         if (kt + 1 < n_kt) {
-            const int j1 = (kt + 1) * PK;
-            load_tile<HD>(sK0 + (buf ^ 1) * PK * HD * 2, kbase + (long long)j1 * HD, HD, min(PK, kv_len - j1), tid);
-            load_tile<HD>(sV0 + (buf ^ 1) * PK * HD * 2, vbase + (long long)j1 * HD, HD, min(PK, kv_len - j1), tid);
+            const int j1 = (kt + 1) * AKT;
+            load_tile<HD, AKT>(sK0 + (buf ^ 1) * AKT * HD * 2, kbase + (long long)j1 * HD, HD, min(AKT, kv_len - j1),
+                               tid);
+            load_tile<HD, AKT>(sV0 + (buf ^ 1) * AKT * HD * 2, vbase + (long long)j1 * HD, HD, min(AKT, kv_len - j1),
+                               tid);
         }
         cp_async_commit();
         cp_async_wait<1>();
@@ -118,17 +125,18 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
             for (int ks = 0; ks < KS; ++ks)
                 ldmatrix_x4(qf[ks], sQ + swz<HD>(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)));
         }
-        const uint32_t sK = sK0 + buf * PK * HD * 2;
-        const uint32_t sV = sV0 + buf * PK * HD * 2;
-        const int j0 = kt * PK;
+        const uint32_t sK = sK0 + buf * AKT * HD * 2;
+        const uint32_t sV = sV0 + buf * AKT * HD * 2;
+        const int j0 = kt * AKT;
 
-        float s[8][4];
+        constexpr int NT = AKT / 8;   // 8-key n-tiles of S
+        float s[NT][4];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
+            for (int np = 0; np < NT / 2; ++np) {
                 uint32_t kb[4];
                 ldmatrix_x4(kb, sK + swz<HD>(np * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
                 mma_bf16_16816(s[2 * np], qf[ks], kb[0], kb[1]);
@@ -136,10 +144,10 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
             }
         }
         // scale, causal + length mask
-        const bool need_mask = (j0 + PK > s0 + q0) || (j0 + PK > s0 + len);
+        const bool need_mask = (j0 + AKT > s0 + q0) || (j0 + AKT > s0 + len);
         float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
+        for (int n = 0; n < NT; ++n) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int key = j0 + n * 8 + 2 * tig + (c & 1);
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
         m_b = mn_b;
         float rs_a = 0.f, rs_b = 0.f;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
+        for (int n = 0; n < NT; ++n) {
             s[n][0] = exp2f(s[n][0] - mn_a);
             s[n][1] = exp2f(s[n][1] - mn_a);
             s[n][2] = exp2f(s[n][2] - mn_b);
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnArgs
         // O += P V with P carried as a bf16 pair P = hi + lo (about 16 significant bits), so the
         // probabilities enter the product essentially unrounded.
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < NT / 2; ++t) {
             uint32_t ph[4], pl[4];
             split_bf2(s[2 * t][0], s[2 * t][1], ph[0], pl[0]);
             split_bf2(s[2 * t][2], s[2 * t][3], ph[1], pl[1]);
@@ -434,7 +442,7 @@ __global__ void decode_combine_kernel(const DecodeAttnArgs a) {
 
 template <int HD>
 cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
-    const int smem = (PQ + 4 * PK) * HD * 2;
+    const int smem = (PQ + 4 * AKT) * HD * 2;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

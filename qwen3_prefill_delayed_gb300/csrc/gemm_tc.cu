@@ -127,36 +127,35 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row
     const int pos = row_ok ? a.row_pos[row] : 0;
     const float2* cs = a.rope + (a.rope_row_is_pos ? pos : row);   // pair i at cs[i * rope_rows]
     const long long head_stride = (long long)a.n_slots * HD;
+    // Two passes over each head's TMEM columns keep at most 64 values in registers: the first
+    // writes V heads and takes the sum of squares of q / k heads, the second applies the norm and
+    // RoPE to the pairs (c, c + HD/2).  tcgen05.ld is a warp instruction: every lane issues it.
 #pragma unroll 1
     for (int h0 = 0; h0 < BN; h0 += HD) {
-        float x[HD];
+        const int hh = (n0 + h0) / HD;   // head index in the merged row (uniform over the warp)
+        if (hh >= a.nq + 2 * a.nkv) break;
+        const bool is_v = hh >= a.nq + a.nkv;
+        bf16* vdst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride +
+                     (long long)pos * HD;
+        // four interleaved compensated sums (short dependency chains), combined compensated
+        float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < HD; c += 32) {
             float v[32];
             tmem_ld32(tq + h0 + c, v);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) x[c + q] = round_bf(v[q]);
-        }
-        const int hh = (n0 + h0) / HD;   // head index in the merged row
-        if (!row_ok || hh >= a.nq + 2 * a.nkv) continue;
-        if (hh >= a.nq + a.nkv) {         // V head: cache as is
-            bf16* dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride +
-                        (long long)pos * HD;
+            for (int q = 0; q < 32; ++q) v[q] = round_bf(v[q]);
+            if (is_v) {
+                if (row_ok) {
 #pragma unroll
-            for (int c = 0; c < HD; c += 8) {
-                float f[8];
+                    for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(vdst + c + e) = pack8(v + e);
+                }
+            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = x[c + e];
-                *reinterpret_cast<uint4*>(dst + c) = pack8(f);
+                for (int q = 0; q < 32; ++q) csum_add(s4[q & 3], c4[q & 3], __fmul_rn(v[q], v[q]));
             }
-            continue;
         }
-        const bool is_q = hh < a.nq;
-        const bf16* gain = is_q ? a.q_norm : a.k_norm;
-        // four interleaved compensated sums (short dependency chains), combined compensated
-        float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < HD; ++e) csum_add(s4[e & 3], c4[e & 3], __fmul_rn(x[e], x[e]));
+        if (is_v) continue;
         float ss = s4[0], sc = c4[0];
 #pragma unroll
         for (int q = 1; q < 4; ++q) {
@@ -167,23 +166,32 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row
         }
         ss = __fadd_rn(ss, sc);
         const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+        const bool is_q = hh < a.nq;
+        const bf16* gain = is_q ? a.q_norm : a.k_norm;
         bf16* dst = is_q ? a.q_out + ((long long)row * a.nq + hh) * HD
                          : a.kv_layer + ((long long)(seq * 2) * a.nkv + (hh - a.nq)) * head_stride + (long long)pos * HD;
 #pragma unroll
-        for (int c = 0; c < HALF; c += 8) {
-            float lo[8], hi[8], g_lo[8], g_hi[8];
-            unpack8(*reinterpret_cast<const uint4*>(gain + c), g_lo);
-            unpack8(*reinterpret_cast<const uint4*>(gain + HALF + c), g_hi);
+        for (int c = 0; c < HALF; c += 32) {
+            float xl[32], xh[32];
+            tmem_ld32(tq + h0 + c, xl);
+            tmem_ld32(tq + h0 + HALF + c, xh);
+            if (!row_ok) continue;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float xa = __fmul_rn(__fmul_rn(x[c + e], inv), g_lo[e]);
-                const float xb = __fmul_rn(__fmul_rn(x[c + e + HALF], inv), g_hi[e]);
-                const float2 t = cs[(long long)(c + e) * a.rope_rows];   // (cos, sin)
-                lo[e] = __fsub_rn(__fmul_rn(xa, t.x), __fmul_rn(xb, t.y));
-                hi[e] = __fadd_rn(__fmul_rn(xb, t.x), __fmul_rn(xa, t.y));
+            for (int e8 = 0; e8 < 32; e8 += 8) {
+                float lo[8], hi[8], g_lo[8], g_hi[8];
+                unpack8(*reinterpret_cast<const uint4*>(gain + c + e8), g_lo);
+                unpack8(*reinterpret_cast<const uint4*>(gain + HALF + c + e8), g_hi);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xa = __fmul_rn(__fmul_rn(round_bf(xl[e8 + e]), inv), g_lo[e]);
+                    const float xb = __fmul_rn(__fmul_rn(round_bf(xh[e8 + e]), inv), g_hi[e]);
+                    const float2 t = cs[(long long)(c + e8 + e) * a.rope_rows];   // (cos, sin)
+                    lo[e] = __fsub_rn(__fmul_rn(xa, t.x), __fmul_rn(xb, t.y));
+                    hi[e] = __fadd_rn(__fmul_rn(xb, t.x), __fmul_rn(xa, t.y));
+                }
+                *reinterpret_cast<uint4*>(dst + c + e8) = pack8(lo);
+                *reinterpret_cast<uint4*>(dst + HALF + c + e8) = pack8(hi);
             }
-            *reinterpret_cast<uint4*>(dst + c) = pack8(lo);
-            *reinterpret_cast<uint4*>(dst + HALF + c) = pack8(hi);
         }
     }
 }
