@@ -287,8 +287,10 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         if (!tail) {
             if (prefill) {
                 PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), P.at<int32_t>(L.start), att, batch, max_len,
-                                   kv.n_slots, nq, nkv, hd};
-                HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] { return launch_prefill_attention(pa, st); }));
+                                   kv.n_slots, nq, nkv, hd, rows, kv.batch, P.at<unsigned int>(L.err)};
+                HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] {
+                    return launch_prefill_attention_tc(pa, st);
+                }));
             } else {
                 DecodeAttnArgs da{};
                 da.q = q;

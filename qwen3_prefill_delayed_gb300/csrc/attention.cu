@@ -1,18 +1,11 @@
 // attention.cu -- causal GQA attention over the used keys of the KV cache.
 //
-// Semantics: row i of sequence b (position i) with q head h attends cache slots 0..i of kv head
+// Semantics: row i of sequence b (position p_i) with q head h attends cache slots 0..p_i of kv head
 // h / (n_q / n_kv) with softmax(q.k / sqrt(hd)); slots past the sequence's length carry zero
 // weight and are never used ("fp8_chain.py", module docstring: attention "over exactly the used
 // keys (pads trail, so a used-key count carries the host's mask)"; causal here because the
 // backbone is a decoder).
 //
-// prefill_attn_kernel  flash-attention style: one CTA = 64 queries x one q head of one sequence
-//                      (whose rows may follow positions already in the cache: they attend those too),
-//                      4 warps x 16 query rows; K/V tiles of 64 keys double-buffered with cp.async
-//                      into XOR-swizzled shared memory; S = QK^T and O += PV on warp-level
-//                      bf16 MMA (m16n8k16) with fp32 online softmax; P enters PV as a bf16
-//                      hi + lo pair, so it is not rounded to 8 bits.
-//                      Tiles above the causal diagonal are never loaded.
 // decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
 //                      across CTAs and stream through a 3-stage cp.async ring; the G = n_q / n_kv
 //                      q heads of a kv head are the rows of one MMA tile, so they share every K/V
@@ -28,9 +21,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// ------------------------------------------------------------------ prefill (many queries)
-
-constexpr int PQ = 64;    // queries per CTA
+// Prefill (many queries per kv head) runs on the tensor-core kernel in attention_tc.cu.
 
 // (a, b) -> bf16 pairs hi = bf16(a, b) and lo = bf16(a - hi_a, b - hi_b).
 __device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -57,171 +48,6 @@ __device__ __forceinline__ void load_tile(uint32_t sbase, const bf16* gbase, lon
         const bool ok = r < rows_valid;
         const bf16* src = gbase + (ok ? (long long)r * row_stride + c * 8 : 0);
         cp_async16(sbase + swz<HD>(r, c), src, ok ? 16u : 0u);
-    }
-}
-
-constexpr int AKT = 64;   // keys per K/V tile of the prefill kernel
-
-// Two CTAs per SM (80 KB of shared memory each) and the register budget that allows: measured on
-// short and long prompts, more CTAs with smaller key tiles or fewer registers were slower.
-template <int HD>
-__global__ void __launch_bounds__(128, 2) prefill_attn_kernel(const PrefillAttnArgs a, float scale_log2) {
-    pdl_launch();
-    pdl_wait();
-    constexpr int KS = HD / 16;   // k-steps over the head dim
-    constexpr int DN = HD / 8;    // n-tiles of the output
-    extern __shared__ __align__(128) uint8_t sm[];
-    const uint32_t sQ = smem_u32(sm);
-    const uint32_t sK0 = sQ + PQ * HD * 2;
-    const uint32_t sV0 = sK0 + 2 * AKT * HD * 2;
-
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int n_qt = (a.max_len + PQ - 1) / PQ;
-    const int qt = n_qt - 1 - (int)blockIdx.x;   // heaviest tiles first
-    const int cu0 = a.cu[b];
-    const int len = a.cu[b + 1] - cu0;
-    const int q0 = qt * PQ;
-    if (q0 >= len) return;
-    const int kvh = h / (a.nq / a.nkv);
-    const int s0 = a.start ? a.start[b] : 0;          // cached positions before this sequence's rows
-    const int kv_len = s0 + min(len, q0 + PQ);        // keys this query tile can reach
-    const int n_kt = (kv_len + AKT - 1) / AKT;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long qstride = (long long)a.nq * HD;
-    const bf16* qbase = a.q + (long long)(cu0 + q0) * qstride + (long long)h * HD;
-    const long long hstride = (long long)a.n_slots * HD;
-    const bf16* kbase = a.kv_layer + ((long long)(b * 2) * a.nkv + kvh) * hstride;
-    const bf16* vbase = a.kv_layer + ((long long)(b * 2 + 1) * a.nkv + kvh) * hstride;
-
-    load_tile<HD, PQ>(sQ, qbase, qstride, min(PQ, len - q0), tid);
-    load_tile<HD, AKT>(sK0, kbase, HD, min(AKT, kv_len), tid);
-    load_tile<HD, AKT>(sV0, vbase, HD, min(AKT, kv_len), tid);
-    cp_async_commit();
-
-    uint32_t qf[KS][4];
-    float o[DN][4];
-#pragma unroll
-    for (int d = 0; d < DN; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    const int g = lane >> 2, tig = lane & 3;
-    const int qa = q0 + warp * 16 + g, qb = qa + 8;   // this thread's two query rows (within the sequence)
-    const int pa = s0 + qa, pb = s0 + qb;             // and their positions
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < n_kt) {
-            const int j1 = (kt + 1) * AKT;
-            load_tile<HD, AKT>(sK0 + (buf ^ 1) * AKT * HD * 2, kbase + (long long)j1 * HD, HD, min(AKT, kv_len - j1),
-                               tid);
-            load_tile<HD, AKT>(sV0 + (buf ^ 1) * AKT * HD * 2, vbase + (long long)j1 * HD, HD, min(AKT, kv_len - j1),
-                               tid);
-        }
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (kt == 0) {
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-                ldmatrix_x4(qf[ks], sQ + swz<HD>(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)));
-        }
-        const uint32_t sK = sK0 + buf * AKT * HD * 2;
-        const uint32_t sV = sV0 + buf * AKT * HD * 2;
-        const int j0 = kt * AKT;
-
-        constexpr int NT = AKT / 8;   // 8-key n-tiles of S
-        float s[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-            for (int np = 0; np < NT / 2; ++np) {
-                uint32_t kb[4];
-                ldmatrix_x4(kb, sK + swz<HD>(np * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
-                mma_bf16_16816(s[2 * np], qf[ks], kb[0], kb[1]);
-                mma_bf16_16816(s[2 * np + 1], qf[ks], kb[2], kb[3]);
-            }
-        }
-        // scale, causal + length mask
-        const bool need_mask = (j0 + AKT > s0 + q0) || (j0 + AKT > s0 + len);
-        float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int key = j0 + n * 8 + 2 * tig + (c & 1);
-                const int qp = c < 2 ? pa : pb;
-                float v = s[n][c] * scale_log2;
-                if (need_mask && (key > qp || key >= s0 + len)) v = -INFINITY;
-                s[n][c] = v;
-            }
-            mx_a = fmaxf(mx_a, fmaxf(s[n][0], s[n][1]));
-            mx_b = fmaxf(mx_b, fmaxf(s[n][2], s[n][3]));
-        }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float al_a = exp2f(m_a - mn_a), al_b = exp2f(m_b - mn_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            s[n][0] = exp2f(s[n][0] - mn_a);
-            s[n][1] = exp2f(s[n][1] - mn_a);
-            s[n][2] = exp2f(s[n][2] - mn_b);
-            s[n][3] = exp2f(s[n][3] - mn_b);
-            rs_a += s[n][0] + s[n][1];
-            rs_b += s[n][2] + s[n][3];
-        }
-        l_a = l_a * al_a + rs_a;
-        l_b = l_b * al_b + rs_b;
-#pragma unroll
-        for (int d = 0; d < DN; ++d) {
-            o[d][0] *= al_a;
-            o[d][1] *= al_a;
-            o[d][2] *= al_b;
-            o[d][3] *= al_b;
-        }
-        // O += P V with P carried as a bf16 pair P = hi + lo (about 16 significant bits), so the
-        // probabilities enter the product essentially unrounded.
-#pragma unroll
-        for (int t = 0; t < NT / 2; ++t) {
-            uint32_t ph[4], pl[4];
-            split_bf2(s[2 * t][0], s[2 * t][1], ph[0], pl[0]);
-            split_bf2(s[2 * t][2], s[2 * t][3], ph[1], pl[1]);
-            split_bf2(s[2 * t + 1][0], s[2 * t + 1][1], ph[2], pl[2]);
-            split_bf2(s[2 * t + 1][2], s[2 * t + 1][3], ph[3], pl[3]);
-#pragma unroll
-            for (int dp = 0; dp < DN / 2; ++dp) {
-                uint32_t vb[4];
-                ldmatrix_x4_trans(vb, sV + swz<HD>(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dp * 2 + (lane >> 4)));
-                mma_bf16_16816(o[2 * dp], ph, vb[0], vb[1]);
-                mma_bf16_16816(o[2 * dp + 1], ph, vb[2], vb[3]);
-                mma_bf16_16816(o[2 * dp], pl, vb[0], vb[1]);
-                mma_bf16_16816(o[2 * dp + 1], pl, vb[2], vb[3]);
-            }
-        }
-        __syncthreads();
-    }
-    cp_async_wait<0>();
-
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    const float ia = 1.0f / l_a, ib = 1.0f / l_b;
-    bf16* oa = a.out + (long long)(cu0 + qa) * qstride + (long long)h * HD + 2 * tig;
-    bf16* ob = a.out + (long long)(cu0 + qb) * qstride + (long long)h * HD + 2 * tig;
-#pragma unroll
-    for (int d = 0; d < DN; ++d) {
-        if (qa < len)
-            *reinterpret_cast<__nv_bfloat162*>(oa + d * 8) = __floats2bfloat162_rn(o[d][0] * ia, o[d][1] * ia);
-        if (qb < len)
-            *reinterpret_cast<__nv_bfloat162*>(ob + d * 8) = __floats2bfloat162_rn(o[d][2] * ib, o[d][3] * ib);
     }
 }
 
@@ -440,24 +266,6 @@ __global__ void decode_combine_kernel(const DecodeAttnArgs a) {
     }
 }
 
-template <int HD>
-cudaError_t launch_prefill_hd(const PrefillAttnArgs& a, cudaStream_t st) {
-    const int smem = (PQ + 4 * AKT) * HD * 2;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
-    dim3 grid((a.max_len + PQ - 1) / PQ, a.nq, a.batch);
-    const float scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
-    HRA_LAUNCH(prefill_attn_kernel<HD>, dim3(grid), dim3(128), smem, st, a, scale_log2);
-    return cudaGetLastError();
-}
-
 template <int HD, int G>
 cudaError_t launch_decode_hd(const DecodeAttnArgs& a, cudaStream_t st) {
     constexpr int smem = 16 * HD * 2 + 2 * DS * PK * HD * 2;
@@ -491,12 +299,6 @@ cudaError_t launch_decode_g(const DecodeAttnArgs& a, cudaStream_t st) {
 }
 
 }  // namespace
-
-cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st) {
-    if (a.hd == 128) return launch_prefill_hd<128>(a, st);
-    if (a.hd == 64) return launch_prefill_hd<64>(a, st);
-    return cudaErrorInvalidValue;
-}
 
 // At most one wave of (row, kv head, split) CTAs (two per SM), with at least 128 keys per split:
 // short rows take one split and skip the combine.

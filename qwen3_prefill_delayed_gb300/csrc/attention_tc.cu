@@ -1,0 +1,480 @@
+// attention_tc.cu -- causal GQA prefill attention on the 5th-generation tensor cores.
+//
+// Semantics: row i of sequence b (position start_b + i) with
+// q head h attends cache slots 0 .. start_b + i of kv head h / (n_q / n_kv) with
+// softmax(q.k / sqrt(hd)) ("fp8_chain.py", module docstring: attention over exactly the used keys;
+// causal because the backbone is a decoder).
+//
+// A work item = one kv head of one sequence and QT = 128 / G consecutive query positions, for all
+// G = n_q / n_kv q heads of that kv head: the 128 rows of every tcgen05.mma are (position, head)
+// pairs, row r = (position r / G, head r % G), so each K/V tile is loaded once for the G heads.
+// The kernel is persistent (one CTA per SM walks the items, heaviest first) and its pipelines run
+// across items: the next item's Q and K/V stream in while this one's softmax and PV finish, and O
+// alternates between two TMEM accumulators so one item's epilogue overlaps the next item's MMAs.
+//   warp 0     TMA: lane 0 the Q tile (a 3-D box of 64 dims x G heads x QT positions per 64-dim
+//              half) and a 3-stage ring of 64-key K tiles, lane 1 the V ring, straight from the
+//              cache (K stages come free once S has read them, V stages once PV has);
+//   warp 1     allocates TMEM (S: two 64-column buffers, O: two hd-column accumulators) and issues
+//              the MMAs:
+//              S_j = Q K_j^T (K-major operands), then O += P_j V_j with P_j from shared memory
+//              (K-major) and V_j as the MN-major B operand;
+//   warps 2-5  one row per thread: online softmax of S_j in fp32 (scores in log2 units, causal and
+//              length mask on the tiles that need it), P_j written to one of two shared-memory buffers
+//              as a bf16 hi + lo pair (hi the top 16 bits, lo = bf16(p - hi), so the probabilities
+//              enter PV with about 16 significant bits), the O accumulator rescaled in
+//              TMEM when a row's running max moves (only then does the softmax wait for the previous
+//              PV), and the final O / l stored as bf16.
+// Key slots past the last valid key of a tile are zeroed in the V tile before PV, so stale cache
+// contents never reach the output (0 x NaN).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <math.h>
+
+#include "internal.h"
+
+namespace hra {
+
+namespace {
+
+constexpr int TROWS = 128;         // MMA rows: G heads x QT positions
+constexpr int TKT = 64;            // keys per K/V tile
+constexpr int NST = 3;             // K and V ring stages
+constexpr int kTcThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int HD>
+struct AttnCfg {
+    static constexpr int NSUB = HD / 64;                 // 64-dim (128-byte) halves of a head
+    static constexpr int Q_BYTES = NSUB * TROWS * 128;   // Q tile
+    static constexpr int KV_SUB = TKT * 128;             // one 64-key x 64-dim sub-tile
+    static constexpr int K_BYTES = NSUB * KV_SUB;
+    static constexpr int P_BYTES = TROWS * 128;          // 128 rows x 64 keys bf16
+    // Q | K stages | V stages | P buffer 0 (hi, lo) | P buffer 1 (hi, lo) | barriers
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NST * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NST * K_BYTES;
+    static constexpr int OFF_BAR = OFF_P + 4 * P_BYTES;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;           // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384)
+};
+
+struct TcAttnArgs {
+    const int32_t* cu;      // [batch + 1]
+    const int32_t* start;   // [batch]
+    bf16* out;              // [T, nq * hd]
+    unsigned int* err;
+    int batch, max_len, n_slots, nq, nkv, G, QT;
+    long long kv_rows_per_seq;   // 2 * nkv * n_slots: rows of one sequence in the cache's row view
+    float scale_log2;
+};
+
+// Work item i (heaviest query tiles first): q tile n_qt - 1 - i / (nkv * batch), sequence and kv
+// head from i % (nkv * batch).  Returns the item's key-tile count (0: the tile is past the sequence).
+__device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, int& b, int& j, int& cu0, int& len,
+                                         int& t0, int& s0, int& kv_len) {
+    const int per = p.nkv * p.batch;
+    const int qt = n_qt - 1 - i / per;
+    const int rem = i - (i / per) * per;
+    b = rem / p.nkv;
+    j = rem - b * p.nkv;
+    cu0 = p.cu[b];
+    len = p.cu[b + 1] - cu0;
+    t0 = qt * p.QT;
+    if (t0 >= len) return 0;
+    s0 = p.start ? p.start[b] : 0;
+    kv_len = s0 + min(len, t0 + p.QT);
+    return (kv_len + TKT - 1) / TKT;
+}
+
+// Persistent: each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x, ...  Every role walks
+// the same items and numbers the key tiles it handles across items (g), which fixes the K/V ring
+// stage (g % NST), the S and P buffer (g & 1) and each barrier's phase.
+template <int HD>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                           const TcAttnArgs p) {
+    using C = AttnCfg<HD>;
+    pdl_launch();
+    pdl_wait();   // the row map, Q and this layer's K/V all come from earlier kernels
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    // 0 q_full, 1 q_empty, 2-4 k_full, 5-7 v_full, 8-10 k_empty, 11-13 v_empty, 14-15 s_full,
+    // 16-17 s_free, 18-19 p_full, 20-21 pv_done, 22-23 o_free, 24 mma_idle.  Every barrier's
+    // consecutive completions are gated by the other side having seen the previous one, so no waiter
+    // can fall two phases behind.
+    uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 26);   // tmem, abort, issued K, V, Q
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+    const uint32_t sP0 = smem_u32(smem + C::OFF_P);   // buffer q: hi at sP0 + 2q P_BYTES, lo right after
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_qt = (p.max_len + p.QT - 1) / p.QT;
+    const int n_items = n_qt * p.nkv * p.batch;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 25; ++i) mbar_init(bar(i), (i >= 16 && i <= 19) || i == 22 || i == 23 ? 4 : 1);
+        *abort_flag = 0;
+        slots[2] = slots[3] = slots[4] = 0;
+        mbar_fence_init();
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmKV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(slots), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = slots[0];
+    int b, j, cu0, len, t0, s0, kv_len;
+
+    if (warp == 0 && lane < 2) {
+        // lane 0: Q and the K ring; lane 1: the V ring
+        const bool is_k = lane == 0;
+        const int full0 = is_k ? 2 : 5, empty0 = is_k ? 8 : 11;
+        const uint32_t ring = is_k ? sK : sV;
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            if (n_kt == 0) continue;
+            if (is_k) {
+                if (it >= 1 && !mbar_wait(bar(1), (uint32_t)(it - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(bar(0), C::Q_BYTES);
+#pragma unroll
+                for (int h = 0; h < C::NSUB; ++h)
+                    tma_load_3d(sQ + h * TROWS * 128, &tmQ, bar(0), 64 * h, j * p.G, cu0 + t0);
+                reinterpret_cast<volatile int*>(slots)[4] = it + 1;
+            }
+            const long long row0 = (long long)b * p.kv_rows_per_seq + (long long)j * p.n_slots +
+                                   (is_k ? 0LL : (long long)p.nkv * p.n_slots);
+            for (int t = 0; t < n_kt; ++t, ++g) {
+                const int st = g % NST;
+                if (g >= NST && !mbar_wait(bar(empty0 + st), (uint32_t)(g / NST - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(bar(full0 + st), C::K_BYTES);
+#pragma unroll
+                for (int h = 0; h < C::NSUB; ++h)
+                    tma_load_2d(ring + st * C::K_BYTES + h * C::KV_SUB, &tmKV, bar(full0 + st), 64 * h,
+                                (int)(row0 + (long long)t * TKT));
+                reinterpret_cast<volatile int*>(slots)[2 + lane] = g + 1;
+            }
+            ++it;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+        }
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(TROWS, TKT);
+        // PV: B = V is MN-major (transpose bit 16), N = HD
+        constexpr uint32_t idesc_o = idesc_bf16_f32(TROWS, HD) | (1u << 16);
+        auto issue_s = [&](int gs) -> bool {
+            const int sb = gs & 1, ks = gs % NST;
+            if (!mbar_wait(bar(2 + ks), (uint32_t)(gs / NST) & 1u, abort_flag)) return false;
+            if (gs >= 2 && !mbar_wait(bar(16 + sb), (uint32_t)((gs >> 1) - 1) & 1u, abort_flag)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * TROWS * 128) + 2ull * (kk & 3);
+                const uint64_t bd = sdesc_sw128(sK + ks * C::K_BYTES + (kk >> 2) * C::KV_SUB) + 2ull * (kk & 3);
+                tc_mma_bf16(tmem + sb * TKT, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar(14 + sb));   // S ready for the softmax
+            tc_commit(bar(8 + ks));    // K stage free again
+            return true;
+        };
+        int g = 0, it = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            if (n_kt == 0) continue;
+            const uint32_t tO = tmem + 2 * TKT + (uint32_t)((it & 1) * 128);
+            if (!mbar_wait(bar(0), (uint32_t)it & 1u, abort_flag) || !issue_s(g)) {
+                ok = false;
+                break;
+            }
+            if (n_kt == 1) tc_commit(bar(1));   // Q read by the item's last S
+            for (int t = 0; t < n_kt; ++t) {
+                const int gt = g + t;
+                if (t + 1 < n_kt) {
+                    if (!issue_s(gt + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (t + 2 == n_kt) tc_commit(bar(1));
+                }
+                if (!mbar_wait(bar(18 + (gt & 1)), (uint32_t)(gt >> 1) & 1u, abort_flag) ||
+                    !mbar_wait(bar(5 + gt % NST), (uint32_t)(gt / NST) & 1u, abort_flag) ||
+                    (t == 0 && it >= 2 &&
+                     !mbar_wait(bar(22 + (it & 1)), (uint32_t)((it >> 1) - 1) & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t v_base = sV + (gt % NST) * C::K_BYTES;
+                const uint32_t ph = sP0 + (uint32_t)(2 * (gt & 1) * C::P_BYTES), pl = ph + C::P_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < TKT / 16; ++ks) {
+                    const uint64_t bd = sdesc_sw128_mn(v_base + ks * 16 * 128, C::KV_SUB, 1024);
+                    tc_mma_bf16(tO, sdesc_sw128(ph) + 2ull * ks, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+                    tc_mma_bf16(tO, sdesc_sw128(pl) + 2ull * ks, bd, idesc_o, 1u);
+                }
+                tc_commit(bar(20 + (gt & 1)));   // P buffer gt & 1 (and O) free again
+                tc_commit(bar(11 + gt % NST));   // V stage free again
+            }
+            g += n_kt;
+            ++it;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+        }
+        tc_commit(bar(24));   // completes once every MMA this thread issued has finished
+    } else if (warp >= 2) {
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                 // MMA row = TMEM lane
+        const int tl = r / p.G, hg = r - (r / p.G) * p.G;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        int g = 0, it = 0, pv_seen = 0;   // PV(0) .. PV(pv_seen - 1) are known to be complete
+        bool ok = true;
+        auto wait_pv = [&](int need) {   // PV(x) completes barrier 20 + (x & 1) for the (x >> 1)-th time
+            while (ok && pv_seen <= need) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar(20 + (pv_seen & 1)), (uint32_t)(pv_seen >> 1) & 1u, abort_flag));
+                ++pv_seen;
+            }
+        };
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            if (n_kt == 0) continue;
+            const bool row_ok = t0 + tl < len;
+            const int qpos = s0 + t0 + tl;
+            const uint32_t tO = lane_base + 2 * TKT + (uint32_t)((it & 1) * 128);
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < n_kt && ok; ++t) {
+                const int gt = g + t;
+                const int sb = gt & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(14 + sb), (uint32_t)(gt >> 1) & 1u, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                float sv[TKT];
+                {
+                    float a[32], c[32];
+                    tmem_ld32(lane_base + sb * TKT, a);
+                    tmem_ld32(lane_base + sb * TKT + 32, c);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        sv[q] = a[q];
+                        sv[32 + q] = c[q];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(16 + sb));   // S buffer may be reused
+                const int j0 = t * TKT;
+                // causal / length mask only where this tile reaches past a row's position or the
+                // keys' end (the item's first row has the smallest position, s0 + t0)
+                if (j0 + TKT > s0 + t0 + 1 || j0 + TKT > kv_len) {
+#pragma unroll
+                    for (int q = 0; q < TKT; ++q) {
+                        const int key = j0 + q;
+                        if (key > qpos || key >= kv_len) sv[q] = -INFINITY;
+                    }
+                }
+                // row max in four independent chains (max is exact in any order), in log2 units
+                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+                for (int q = 4; q < TKT; ++q) mx4[q & 3] = fmaxf(mx4[q & 3], sv[q]);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+                const float mn = fmaxf(m, mx);
+                const float mref = mn == -INFINITY ? 0.f : mn;
+                const float alpha = exp2f(m - mref);
+                // p = 2^(s * scale - mref) (one rounding of the exponent), summed in four chains
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < TKT; ++q) {
+                    sv[q] = exp2f(fmaf(sv[q], p.scale_log2, -mref));
+                    rs4[q & 3] += sv[q];
+                }
+                l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+                m = mn;
+                // P buffer gt & 1 was last read by PV(gt - 2); O needs PV(gt - 1) done only when it is
+                // rescaled (once the running max settles, P writes and PV MMAs stream without waiting)
+                const bool rescale = t > 0 && !__all_sync(0xffffffffu, alpha == 1.f);
+                wait_pv(rescale ? gt - 1 : gt - 2);
+                if (!ok) break;
+                tc_fence_after();
+                if (rescale) {
+#pragma unroll 1
+                    for (int c = 0; c < HD; c += 32) {
+                        float o[32];
+                        tmem_ld32(tO + c, o);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                        tmem_st32(tO + c, o);
+                    }
+                }
+                // the item's last tile: zero the V rows of slots past the valid keys (stale cache)
+                const int valid_in_tile = kv_len - j0;
+                if (valid_in_tile < TKT) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(5 + gt % NST), (uint32_t)(gt / NST) & 1u, abort_flag));
+                    if (!ok) break;
+                    const int z_rows = TKT - valid_in_tile;
+                    uint8_t* vt = smem + C::OFF_V + (gt % NST) * C::K_BYTES;
+                    for (int idx = r; idx < C::NSUB * z_rows * 8; idx += TROWS) {
+                        const int h = idx / (z_rows * 8), rem = idx - h * z_rows * 8;
+                        const int row = valid_in_tile + rem / 8, chunk = rem & 7;
+                        *reinterpret_cast<uint4*>(vt + h * C::KV_SUB + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                // P as bf16 hi + lo, K-major with the 128-byte swizzle: row r, 16-byte chunk c at c ^ (r & 7)
+                {
+                    uint8_t* ph = smem + C::OFF_P + 2 * (gt & 1) * C::P_BYTES + r * 128;
+                    uint8_t* pl = ph + C::P_BYTES;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // hi = the top 16 bits (p truncated to bf16), lo = bf16(p - hi): p - hi is exact
+                            const uint32_t u0 = __float_as_uint(sv[c * 8 + 2 * e]) & 0xFFFF0000u;
+                            const uint32_t u1 = __float_as_uint(sv[c * 8 + 2 * e + 1]) & 0xFFFF0000u;
+                            hw[e] = (u0 >> 16) | u1;
+                            lw[e] = pack_bf2(sv[c * 8 + 2 * e] - __uint_as_float(u0),
+                                             sv[c * 8 + 2 * e + 1] - __uint_as_float(u1));
+                        }
+                        const int off = (c ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+                fence_proxy_async_smem();   // generic-proxy writes (P, zeroed V rows) before the MMA reads them
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(18 + (gt & 1)));
+            }
+            // the item's output: O / l once its last PV is done
+            wait_pv(g + n_kt - 1);
+            if (!ok) break;
+            tc_fence_after();
+            const float il = 1.0f / l;
+            bf16* dst = p.out + ((long long)(cu0 + t0 + tl) * p.nq + (long long)j * p.G + hg) * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                float o[32];
+                tmem_ld32(tO + c, o);
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        float f[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) f[q] = o[e + q] * il;
+                        *reinterpret_cast<uint4*>(dst + c + e) = pack8(f);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(22 + (it & 1)));   // O buffer free for item it + 2
+            g += n_kt;
+            ++it;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
+        }
+    }
+
+    // ---------------- teardown: on abort, let every issued TMA load and MMA land first
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane < 2) {
+        volatile int never = 0;
+        if (lane == 0) {
+            const int qi = reinterpret_cast<volatile int*>(slots)[4];
+            if (qi > 0) (void)mbar_wait(bar(0), (uint32_t)(qi - 1) & 1u, &never);
+        }
+        const int issued = reinterpret_cast<volatile int*>(slots)[2 + lane];
+        const int full0 = lane == 0 ? 2 : 5;
+        for (int t = max(0, issued - NST); t < issued; ++t)
+            (void)mbar_wait(bar(full0 + t % NST), (uint32_t)(t / NST) & 1u, &never);
+    }
+    if (warp == 1 && lane == 0) {
+        volatile int never = 0;
+        (void)mbar_wait(bar(24), 0u, &never);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int HD>
+cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
+    using C = AttnCfg<HD>;
+    const int G = a.nq / a.nkv;
+    const int QT = TROWS / G;
+    alignas(64) CUtensorMap mq, mkv;
+    // q [T, nq, hd] as (hd, nq, T); one box = 64 dims x G heads x QT positions (zero past T)
+    const uint64_t qdims[3] = {(uint64_t)HD, (uint64_t)a.nq, (uint64_t)a.total_rows};
+    const uint64_t qstr[2] = {(uint64_t)HD * 2, (uint64_t)a.nq * HD * 2};
+    const uint32_t qbox[3] = {64u, (uint32_t)G, (uint32_t)QT};
+    if (!encode_tensor_map(&mq, 3, a.q, qdims, qstr, qbox)) return cudaErrorInvalidValue;
+    // the layer's cache as rows of hd: [cache_batch * 2 * nkv * n_slots, hd]; box 64 dims x 64 keys
+    const uint64_t kvdims[2] = {(uint64_t)HD, (uint64_t)a.cache_batch * 2 * a.nkv * a.n_slots};
+    const uint64_t kvstr[1] = {(uint64_t)HD * 2};
+    const uint32_t kvbox[2] = {64u, (uint32_t)TKT};
+    if (!encode_tensor_map(&mkv, 2, a.kv_layer, kvdims, kvstr, kvbox)) return cudaErrorInvalidValue;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(prefill_attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    TcAttnArgs p{};
+    p.cu = a.cu;
+    p.start = a.start;
+    p.out = a.out;
+    p.err = a.err;
+    p.batch = a.batch;
+    p.max_len = a.max_len;
+    p.n_slots = a.n_slots;
+    p.nq = a.nq;
+    p.nkv = a.nkv;
+    p.G = G;
+    p.QT = QT;
+    p.kv_rows_per_seq = 2LL * a.nkv * a.n_slots;
+    p.scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
+    const long long items = (long long)((a.max_len + QT - 1) / QT) * a.nkv * a.batch;
+    const int grid = (int)std::min<long long>(items, device_sm_count());
+    HRA_LAUNCH(prefill_attn_tc_kernel<HD>, dim3(grid), dim3(kTcThreads), C::SMEM, st, mq, mkv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st) {
+    const int G = a.nkv > 0 ? a.nq / a.nkv : 0;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return cudaErrorInvalidValue;
+    if (a.hd == 128) return launch_tc_hd<128>(a, st);
+    if (a.hd == 64) return launch_tc_hd<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hra

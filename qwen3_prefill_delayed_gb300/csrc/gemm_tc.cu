@@ -1259,6 +1259,22 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
 
 }  // namespace
 
+bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box) {
+    if (!get_encoder() || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    return g_encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                    const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;

@@ -154,8 +154,17 @@ struct PrefillAttnArgs {
     const int32_t* start;   // [batch] device: position of each sequence's first row (cached keys below)
     bf16* out;              // [T, nq * hd]
     int batch, max_len, n_slots, nq, nkv, hd;
+    int total_rows;         // T (rows of q)
+    int cache_batch;        // sequences the cache holds (kv_layer spans cache_batch * 2 * nkv * n_slots rows)
+    unsigned int* err;      // sticky device error word
 };
-cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, cudaStream_t st);
+// the tcgen05 kernel (attention_tc.cu): head_dim 64 or 128, n_q / n_kv in {1, 2, 4, 8}
+cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st);
+
+// cuTensorMapEncodeTiled (bf16 elements, 128-byte swizzle, zero fill out of bounds) for a tensor of
+// `rank` dims (innermost first), strides in bytes of dims 1.. and the box; `map` is a CUtensorMap.
+bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box);
 
 // Single-query attention: row i (sequence seq[i], query position pos[i]) attends slots 0..pos[i].
 struct DecodeAttnArgs {

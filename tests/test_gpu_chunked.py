@@ -7,7 +7,10 @@ cache) against the oracle's whole-sequence prefill.
   causal diagonal of the chunk straddles key tiles of cached and new positions;
 - a full-width mixed batch of single-token steps and chunks in one launch;
 - a chunk that ends in the last cache slot, and starts that run past the cache (refused before any
-  launch)."""
+  launch);
+- every GQA group size the attention kernel takes at both head dims (G = 1: 128 positions per query
+  tile; G = 8: 16 positions), with prompts spanning several query tiles and a chunk after cached
+  positions."""
 import numpy as np
 import pytest
 import torch
@@ -130,3 +133,16 @@ def test_chunk_to_the_last_slot_and_range_errors(hra):
         bb.prefill(chunk, [7, 7], cache, start_pos=[26, 0])
     with pytest.raises(hra.HraError, match="outside the cache"):
         bb.prefill(chunk, [7, 7], cache, start_pos=[0, -1])
+
+
+@pytest.mark.parametrize("nq,nkv,hd", [(8, 8, 64), (4, 4, 128), (16, 2, 64), (8, 1, 128)])
+def test_gqa_group_sizes(hra, nq, nkv, hd):
+    d = W.Dims(n_layers=2, hidden=256, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd, ffn=256, vocab=512,
+               n_codebooks=4)
+    w = W.make_backbone(d, 13, "cpu")
+    lens = [300, 129, 17]
+    tok = _tokens(9, lens, d.vocab)
+    cut = [0, 100, 0]
+    n_new = [300, 29, 17]
+    hid, cache = _run_chunks(hra, d, w, tok, lens, cut, n_new, 320)
+    _check(d, w, tok, cut, n_new, hid, cache, 320)
