@@ -191,6 +191,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ------------------------------------------------------------------ TMA
 
+// Hint: bring the 128-byte line holding `ptr` into L2 (no register result, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

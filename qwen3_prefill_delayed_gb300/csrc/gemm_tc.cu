@@ -31,7 +31,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;       // small-M kernel: TMA warp, MMA warp, 4 epilogue warps
+constexpr int kTileThreads = 320;   // tile kernel: TMA warp, MMA warp, 8 epilogue warps
 
 enum KMode : int { KM_STORE = 0, KM_RESIDUAL = 1, KM_SWIGLU = 2, KM_F32 = 3, KM_PARTIAL = 4, KM_QKROPE = 5 };
 
@@ -121,7 +122,8 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m_blk
 // shared gains) and rotate-half RoPE at the row's position, rounded once, to q_out or the K cache.
 // One row (token) per thread; the RoPE partner i + HD/2 is in the same thread.
 template <int BN, int HD>
-__device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row, bool row_ok, const QkRopeArgs& a) {
+__device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int half, int row, bool row_ok,
+                                                    const QkRopeArgs& a) {
     constexpr int HALF = HD / 2;
     const int seq = row_ok ? a.row_seq[row] : 0;
     const int pos = row_ok ? a.row_pos[row] : 0;
@@ -131,7 +133,7 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row
     // writes V heads and takes the sum of squares of q / k heads, the second applies the norm and
     // RoPE to the pairs (c, c + HD/2).  tcgen05.ld is a warp instruction: every lane issues it.
 #pragma unroll 1
-    for (int h0 = 0; h0 < BN; h0 += HD) {
+    for (int h0 = half * HD; h0 < BN; h0 += 2 * HD) {   // this warp's heads: every other one of the tile
         const int hh = (n0 + h0) / HD;   // head index in the merged row (uniform over the warp)
         if (hh >= a.nq + 2 * a.nkv) break;
         const bool is_v = hh >= a.nq + a.nkv;
@@ -197,9 +199,10 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int row
 }
 
 template <int BN>
-__device__ __forceinline__ void qk_rope_epilogue(uint32_t tq, int n0, int row, bool row_ok, const QkRopeArgs& a) {
-    if (a.hd == 128) qk_rope_epilogue_hd<BN, 128>(tq, n0, row, row_ok, a);
-    else qk_rope_epilogue_hd<BN, 64>(tq, n0, row, row_ok, a);
+__device__ __forceinline__ void qk_rope_epilogue(uint32_t tq, int n0, int half, int row, bool row_ok,
+                                                 const QkRopeArgs& a) {
+    if (a.hd == 128) qk_rope_epilogue_hd<BN, 128>(tq, n0, half, row, row_ok, a);
+    else qk_rope_epilogue_hd<BN, 64>(tq, n0, half, row, row_ok, a);
 }
 
 // Linear tile index of (mb, nb) in the raster order of unit_coords.
@@ -234,7 +237,7 @@ __device__ __forceinline__ void unit_work(int u, const GemmArgs& p, int& mb, int
 // F8: both operands E4M3 (kind::f8f6f4): a 128-byte stage row holds 128 elements instead of 64,
 // and every accumulator is scaled by the two per-tensor scales before any store.
 template <int BN, bool SWIGLU, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kTileThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
     using C = Cfg<BN>;
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);   // one arrival per epilogue warp
+            mbar_init(tempty_bar(b), 8);   // one arrival per epilogue warp
         }
         *abort_flag = 0;
         *issued_slot = 0;
@@ -371,11 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             *committed_slot = j + 1;
         }
     } else if (warp >= 2) {
-        // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (one row per thread)
+        // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (one row per thread);
+        // warps 2-5 take the first half of the tile's columns (QKV: its even heads), warps 6-9 the
+        // second half (odd heads)
         pdl_wait();
         if (blockIdx.x == 0 && warp == 2)
             for (int i = lane; i < p.zero_words; i += 32) p.zero_ptr[i] = 0u;
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        constexpr int HC = BN / 2;   // columns of a half (SwiGLU: gate + up columns of a half: HC / 2 each)
         float scale = 1.f;
         if constexpr (F8) scale = (*p.a_scale) * (*p.w_scale);
         auto scaled = [&](float (&v)[32]) {
@@ -390,6 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             const int sp = piece < 0 ? u / (p.mt * p.nt) : 0;
             const int buf = j & 1;
+            const int row = mb * BM + quad * 32 + lane;
+            const bool row_ok = row < p.M;
+            // While the MMAs of this unit run, pull the residual row segment its epilogue reads into L2.
+            if (!SWIGLU && piece < 0 && p.mode == KM_RESIDUAL && row_ok) {
+                const int n0 = nb * BN + half * HC;
+                for (int c = 0; c < HC && n0 + c < p.n_valid; c += 64)
+                    prefetch_l2(reinterpret_cast<const bf16*>(p.out) + (long long)row * p.ldo + n0 + c);
+            }
             // warp-uniform decision: tcgen05.ld below is a .sync.aligned warp instruction
             const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
             if (!ok) {
@@ -399,8 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
-            const int row = mb * BM + quad * 32 + lane;
-            const bool row_ok = row < p.M;
             const long long split_off = (long long)sp * p.split_stride;
             if (piece >= 0) {
                 // last-round K piece: raw fp32 tile [BM][BN] for the fix-up pass
@@ -408,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              ((long long)piece * p.tail_tiles + tail_index(mb, nb, p)) * (BM * BN) +
                              (long long)(quad * 32 + lane) * BN;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = half * HC; c < half * HC + HC; c += 32) {
                     float v[32];
                     tmem_ld32(tq + c, v);
                     scaled(v);
@@ -417,11 +430,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             } else if (!SWIGLU && !F8 && p.mode == KM_QKROPE) {
-                qk_rope_epilogue<BN>(tq, nb * BN, row, row_ok, p.qk);
+                qk_rope_epilogue<BN>(tq, nb * BN, half, row, row_ok, p.qk);
+            } else if (!SWIGLU && p.mode == KM_RESIDUAL) {
+                // out += acc: the chunk's residual loads are issued before its TMEM read
+                const int n0 = nb * BN;
+#pragma unroll 1
+                for (int c = half * HC; c < half * HC + HC; c += 32) {
+                    const int col = n0 + c;
+                    const int nv = row_ok ? max(0, min(32, p.n_valid - col)) : 0;
+                    uint4* o4 = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (long long)row * p.ldo + col);
+                    uint4 r4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) r4[i] = 8 * i < nv ? o4[i] : make_uint4(0u, 0u, 0u, 0u);
+                    float v[32];
+                    tmem_ld32(tq + c, v);
+                    scaled(v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (8 * i >= nv) break;
+                        float r[8];
+                        unpack8(r4[i], r);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) r[e] = r[e] + v[8 * i + e];
+                        o4[i] = pack8(r);
+                    }
+                }
             } else if (!SWIGLU) {
                 const int n0 = nb * BN;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = half * HC; c < half * HC + HC; c += 32) {
                     float v[32];
                     tmem_ld32(tq + c, v);
                     scaled(v);
@@ -431,9 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         min(32, p.n_valid - col));
                 }
             } else {
+                // gate columns [0, BN/2), up columns [BN/2, BN): this half takes output columns
+                // [half * BN/4, half * BN/4 + BN/4) of the tile's BN/2
                 const int j0 = nb * (BN / 2);
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
+                for (int c = half * (HC / 2); c < half * (HC / 2) + HC / 2; c += 32) {
                     float g[32], uu[32];
                     tmem_ld32(tq + c, g);
                     tmem_ld32(tq + BN / 2 + c, uu);
@@ -1100,7 +1139,7 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
     const long long units = (long long)pl.mt * pl.nt * pl.splits;
     const int nsm = device_sm_count();
     dim3 grid((unsigned)std::min<long long>(units, nsm));
-    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW, F8>, dim3(grid), dim3(kThreads), Cfg<BN>::SMEM, st, ma, mb, g);
+    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW, F8>, dim3(grid), dim3(kTileThreads), Cfg<BN>::SMEM, st, ma, mb, g);
     return cudaGetLastError();
 }
 
