@@ -889,6 +889,69 @@ __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int 
     *q = pack8(a);
 }
 
+// Last-round K pieces of a residual GEMM fused with the RMSNorm that follows it: one warp per row
+// (the whole row in registers, NC 16-byte chunks per lane, N = 256 * NC).  A chunk that lies in a
+// tail tile gets r = bf16(r + sum of its pieces in piece order), as tail_fixup_kernel computes it;
+// the other chunks already hold the GEMM's residual sum.  Then y = RMSNorm(r) * g over the rounded
+// row, with the compensated sum of squares of the row norm kernel.
+template <int NC>
+__global__ void tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
+                                       int mt, int group, int BNt, int M, int N, bf16* __restrict__ r,
+                                       const bf16* __restrict__ g, bf16* __restrict__ y, float eps) {
+    pdl_launch();
+    pdl_wait();
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    const int mb = row / BM, rr = row - mb * BM;
+    uint4* rrow = reinterpret_cast<uint4*>(r + (long long)row * N);
+    uint4 u[NC];
+#pragma unroll
+    for (int q = 0; q < NC; ++q) u[q] = rrow[lane + 32 * q];
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+        const int col = (lane + 32 * q) * 8;
+        const int nb = col / BNt;
+        const int band = nb / group;
+        const int lin = band * group * mt + (nb - band * group) * mt + mb;
+        if (lin < head_units) continue;
+        const int t = lin - head_units;
+        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int pc = 0; pc < pieces; ++pc) {
+            const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)rr * BNt + (col - nb * BNt);
+            const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
+            a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w; a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+        }
+        float f[8];
+        unpack8(u[q], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = f[j] + a[j];
+        u[q] = pack8(a);
+        rrow[lane + 32 * q] = u[q];
+    }
+    float ss = 0.f, sc = 0.f;
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+        float f[8];
+        unpack8(u[q], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) csum_add(ss, sc, __fmul_rn(f[j], f[j]));
+    }
+    ss = csum_warp(ss, sc);
+    const float inv = 1.0f / sqrtf(ss / (float)N + eps);
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * N);
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+        float f[8], w[8];
+        unpack8(u[q], f);
+        unpack8(gv[lane + 32 * q], w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
+        dy[lane + 32 * q] = pack8(f);
+    }
+}
+
 // Sum of split partials in split order, then the epilogue.  One thread per 8 output columns.
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long long split_stride,
                                      int M, int n_out, int ldp, int up_off, int mode, void* out, int ldo) {
@@ -1416,6 +1479,22 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
         e = sw ? launch_tile<128, true, false>(ma, mb, g, pl, st) : launch_tile<128, false, false>(ma, mb, g, pl, st);
     }
     if (c.splits_used) *c.splits_used = pl.splits;
+    if (e == cudaSuccess && pl.tail_tiles > 0 && g.mode == KM_RESIDUAL && c.norm_out != nullptr &&
+        (c.N == 2560 || c.N == 256)) {
+        // the tail pieces and the RMSNorm that follows in one pass over each row
+        const int warps = 8;
+        const dim3 grid((unsigned)((c.M + warps - 1) / warps));
+        if (c.N == 2560)
+            HRA_LAUNCH(tail_fixup_norm_kernel<10>, grid, dim3(32 * warps), 0, st, c.partial, pl.tail_splits,
+                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
+                       c.norm_gain, c.norm_out, c.norm_eps);
+        else
+            HRA_LAUNCH(tail_fixup_norm_kernel<1>, grid, dim3(32 * warps), 0, st, c.partial, pl.tail_splits,
+                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
+                       c.norm_gain, c.norm_out, c.norm_eps);
+        if (c.norm_done) *c.norm_done = true;
+        return cudaGetLastError();
+    }
     if (e == cudaSuccess && pl.tail_tiles > 0) {
         const int gw = sw ? pl.bn / 16 : pl.bn / 8;
         const long long items = (long long)pl.tail_tiles * BM * gw;
