@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary sections")
-    ap.add_argument("--kernel-case", default=None, choices=["gate_up", "qkv", "down", "audio_head"],
+    ap.add_argument("--kernel-case", default=None, choices=["gate_up", "qkv", "down", "audio_head", "attention"],
                     help="run only a few launches of one kernel at a profiling size, then exit")
     ap.add_argument("--kernel-m", type=int, default=None, help="rows (tokens / batch) of the kernel case")
     return ap.parse_args()
@@ -57,7 +57,17 @@ def kernel_case(name, m=None):
     g = torch.Generator(device=dev).manual_seed(7)
     d = W.full_dims(1)
     rnd = lambda *sh, std=1.0: (torch.randn(*sh, generator=g, device=dev) * std).to(torch.bfloat16)
-    if name == "audio_head":
+    if name == "attention":
+        # prefill of the 32 ragged prompts through 2 full-width layers: layer 0 runs the prefill
+        # attention kernel over all rows (layer 1 takes the last-rows tail)
+        wl = W.ragged_batch(dev, n_layers=2)
+        d2, p = wl["dims"], wl["prompts"]
+        bb = hra.Backbone(d2, wl["weights"])
+        cache = hra.new_kv_cache(d2, 32, wl["n_slots"], dev)
+        tok = p.tokens.to(dev)
+        for _ in range(3):
+            bb.prefill(tok, p.lengths, cache)
+    elif name == "audio_head":
         wl = W.make_audio(d, g, dev)
         head = hra.AudioHead(d, wl["head_w"], wl["code_emb"])
         bsz = m or 64
