@@ -211,7 +211,24 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
         const int hh = valid ? hh_raw : 0;
         const bf16* src = a.qkv + (long long)row * heads * HD + (long long)hh * HD + sub * E;
         float x[E];
-        if constexpr (E == 8) {
+        if (a.part != nullptr) {
+            // the projection's split-K partials, summed in split order and rounded once to bf16
+            const float* ps = a.part + (long long)row * a.ldp + (long long)hh * HD + sub * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = 0.f;
+            for (int sp = 0; sp < a.splits; ++sp) {
+#pragma unroll
+                for (int e = 0; e < E; e += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(ps + sp * a.split_stride + e);
+                    x[e] += v.x;
+                    x[e + 1] += v.y;
+                    x[e + 2] += v.z;
+                    x[e + 3] += v.w;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = round_bf(x[e]);
+        } else if constexpr (E == 8) {
             unpack8(*reinterpret_cast<const uint4*>(src), x);
         } else {
             const uint2 u = *reinterpret_cast<const uint2*>(src);
@@ -247,8 +264,20 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
         if (is_v) {
             dst = a.kv_layer + ((long long)(seq * 2 + 1) * a.nkv + (hh - a.nq - a.nkv)) * head_stride +
                   (long long)pos * HD + sub * E;
-            if constexpr (E == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-            else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+            if (a.part != nullptr) {
+                if constexpr (E == 8) {
+                    *reinterpret_cast<uint4*>(dst) = pack8(x);
+                } else {
+                    uint2 u;
+                    *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(x[0], x[1]);
+                    *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(x[2], x[3]);
+                    *reinterpret_cast<uint2*>(dst) = u;
+                }
+            } else if constexpr (E == 8) {
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+            } else {
+                *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+            }
             return;
         }
         float out[E];

@@ -1356,6 +1356,17 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
         e = sw ? launch_small<64, true>(mw, mx, a, units, ring, st) : launch_small<64, false>(mw, mx, a, units, ring, st);
     if (c.splits_used) *c.splits_used = use_partial ? pl.splits : 1;
     if (e != cudaSuccess || !use_partial || c.partial_only) return e;
+    if (c.qk != nullptr && c.epi == EPI_STORE && c.M == c.qk->rows && c.N == (c.qk->nq + 2 * c.qk->nkv) * c.qk->hd) {
+        // merged QKV: the split reduction happens inside the q/k norm + RoPE + cache-write kernel
+        QkRopeArgs qa = *c.qk;
+        qa.part = c.partial;
+        qa.splits = pl.splits;
+        qa.split_stride = (long long)c.M * ldp;
+        qa.ldp = ldp;
+        e = launch_qk_rope_kv(qa, st);
+        if (e == cudaSuccess && c.qk_done) *c.qk_done = true;
+        return e;
+    }
     return reduce_partials(c, pl.splits, ldp, st);
 }
 

@@ -59,6 +59,12 @@ struct QkRopeArgs {
     int n_slots;
     int rows, nq, nkv, hd;
     float eps;
+    // optional: take the merged row as the sum of fp32 split partials (part[s * split_stride +
+    // row * ldp + col], s in split order) rounded to bf16, instead of reading qkv
+    const float* part;
+    int splits;
+    long long split_stride;
+    int ldp;
 };
 // ------------------------------------------------------------------ projection GEMM
 enum EpiMode : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
