@@ -21,9 +21,9 @@
 //   warps 2-5  one row per thread: online softmax of S_j in fp32 (scores in log2 units, causal and
 //              length mask on the tiles that need it), P_j written to one of two shared-memory buffers
 //              as a bf16 hi + lo pair (hi the top 16 bits, lo = bf16(p - hi), so the probabilities
-//              enter PV with about 16 significant bits), the O accumulator rescaled in
-//              TMEM when a row's running max moves (only then does the softmax wait for the previous
-//              PV), and the final O / l stored as bf16.
+//              enter PV with about 16 significant bits), the O accumulator rescaled in TMEM only
+//              when a row's reference max moves by more than 2^8 (only then does the softmax wait for
+//              the previous PV), and the final O / l stored as bf16.
 // Key slots past the last valid key of a tile are zeroed in the V tile before PV, so stale cache
 // contents never reach the output (0 x NaN).
 #include <cudaTypedefs.h>
@@ -42,6 +42,7 @@ constexpr int TKT = 64;            // keys per K/V tile
 constexpr int NST = 3;             // K and V ring stages
 constexpr int kTcThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyLog2 = 8.0f;   // reference-max slack of the online softmax (log2 units)
 
 template <int HD>
 struct AttnCfg {
@@ -296,9 +297,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 4; q < TKT; ++q) mx4[q & 3] = fmaxf(mx4[q & 3], sv[q]);
                 const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
-                const float mn = fmaxf(m, mx);
+                // Lazy reference max: it moves (and O is rescaled) only when this tile's max exceeds it
+                // by more than kLazyLog2, so p = 2^(s * scale - mref) <= 2^kLazyLog2.  O / l is
+                // unchanged; the softmax of tile t then waits only for PV(t - 2), not PV(t - 1).
+                const float mn = mx > m + kLazyLog2 ? mx : m;
                 const float mref = mn == -INFINITY ? 0.f : mn;
-                const float alpha = exp2f(m - mref);
+                const float alpha = exp2f(m - mref);   // exactly 1 while the reference stays
                 // p = 2^(s * scale - mref) (one rounding of the exponent), summed in four chains
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
