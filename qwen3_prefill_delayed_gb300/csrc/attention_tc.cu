@@ -38,26 +38,36 @@ namespace hra {
 namespace {
 
 constexpr int TROWS = 128;         // MMA rows: G heads x QT positions
-constexpr int TKT = 64;            // keys per K/V tile
-constexpr int NST = 3;             // K and V ring stages
 constexpr int kTcThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyLog2 = 8.0f;   // reference-max slack of the online softmax (log2 units)
 
-template <int HD>
+// TK keys per K/V tile, NS stages in each of the K and V rings, OB TMEM accumulators for O.
+//   <64, 3, 2>: one CTA per SM; O alternates between items so an item's epilogue overlaps the next.
+//   <32, 2, 1>: ~97 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and hide each
+//               other's per-item latency (short prompts); P rows are 64 bytes (64-byte swizzle).
+template <int HD, int TK, int NS, int OB>
 struct AttnCfg {
     static constexpr int NSUB = HD / 64;                 // 64-dim (128-byte) halves of a head
     static constexpr int Q_BYTES = NSUB * TROWS * 128;   // Q tile
-    static constexpr int KV_SUB = TKT * 128;             // one 64-key x 64-dim sub-tile
+    static constexpr int KV_SUB = TK * 128;              // one TK-key x 64-dim sub-tile
     static constexpr int K_BYTES = NSUB * KV_SUB;
-    static constexpr int P_BYTES = TROWS * 128;          // 128 rows x 64 keys bf16
+    static constexpr int P_ROW = TK * 2;                 // bytes of one P row (bf16)
+    static constexpr int P_BYTES = TROWS * P_ROW;
     // Q | K stages | V stages | P buffer 0 (hi, lo) | P buffer 1 (hi, lo) | barriers
     static constexpr int OFF_K = Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NST * K_BYTES;
-    static constexpr int OFF_P = OFF_V + NST * K_BYTES;
+    static constexpr int OFF_V = OFF_K + NS * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NS * K_BYTES;
     static constexpr int OFF_BAR = OFF_P + 4 * P_BYTES;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;
-    static constexpr uint32_t TMEM_COLS = 512;           // S0 [0,64), S1 [64,128), O0 [128,256), O1 [256,384)
+    // S buffers at columns [0, TK) and [TK, 2 TK), O accumulator ob at 2 TK + 128 ob
+    static constexpr uint32_t TMEM_COLS = 2 * TK + 128 * OB <= 256 ? 256u : 512u;
+    // barriers: q_full, q_empty, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2],
+    // s_free[2], p_full[2], pv_done[2], o_free[OB], mma_idle
+    static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_VF = 2 + NS, B_KE = 2 + 2 * NS, B_VE = 2 + 3 * NS;
+    static constexpr int B_SF = 2 + 4 * NS, B_SFREE = B_SF + 2, B_PF = B_SFREE + 2, B_PV = B_PF + 2;
+    static constexpr int B_OF = B_PV + 2, B_IDLE = B_OF + OB, NBARS = B_IDLE + 1;
+    static_assert(NBARS * 8 + 5 * 4 <= 256, "barrier area");
 };
 
 struct TcAttnArgs {
@@ -72,8 +82,8 @@ struct TcAttnArgs {
 
 // Work item i (heaviest query tiles first): q tile n_qt - 1 - i / (nkv * batch), sequence and kv
 // head from i % (nkv * batch).  Returns the item's key-tile count (0: the tile is past the sequence).
-__device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, int& b, int& j, int& cu0, int& len,
-                                         int& t0, int& s0, int& kv_len) {
+__device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, int tk, int& b, int& j, int& cu0,
+                                         int& len, int& t0, int& s0, int& kv_len) {
     const int per = p.nkv * p.batch;
     const int qt = n_qt - 1 - i / per;
     const int rem = i - (i / per) * per;
@@ -85,27 +95,25 @@ __device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, i
     if (t0 >= len) return 0;
     s0 = p.start ? p.start[b] : 0;
     kv_len = s0 + min(len, t0 + p.QT);
-    return (kv_len + TKT - 1) / TKT;
+    return (kv_len + tk - 1) / tk;
 }
 
 // Persistent: each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x, ...  Every role walks
 // the same items and numbers the key tiles it handles across items (g), which fixes the K/V ring
-// stage (g % NST), the S and P buffer (g & 1) and each barrier's phase.
-template <int HD>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// stage (g % NS), the S and P buffer (g & 1) and each barrier's phase.  Every barrier's consecutive
+// completions are gated by the other side having seen the previous one, so no waiter can fall two
+// phases behind.
+template <int HD, int TK, int NS, int OB>
+__global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
     prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                            const TcAttnArgs p) {
-    using C = AttnCfg<HD>;
+    using C = AttnCfg<HD, TK, NS, OB>;
     pdl_launch();
     pdl_wait();   // the row map, Q and this layer's K/V all come from earlier kernels
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    // 0 q_full, 1 q_empty, 2-4 k_full, 5-7 v_full, 8-10 k_empty, 11-13 v_empty, 14-15 s_full,
-    // 16-17 s_free, 18-19 p_full, 20-21 pv_done, 22-23 o_free, 24 mma_idle.  Every barrier's
-    // consecutive completions are gated by the other side having seen the previous one, so no waiter
-    // can fall two phases behind.
-    uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 26);   // tmem, abort, issued K, V, Q
+    uint32_t* slots = reinterpret_cast<uint32_t*>(bars + C::NBARS);   // tmem, abort, issued K, V, Q
     volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
     auto bar = [&](int i) { return smem_u32(bars + i); };
     const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
@@ -116,7 +124,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_items = n_qt * p.nkv * p.batch;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 25; ++i) mbar_init(bar(i), (i >= 16 && i <= 19) || i == 22 || i == 23 ? 4 : 1);
+        for (int i = 0; i < C::NBARS; ++i) {
+            const bool four = (i >= C::B_SFREE && i < C::B_PV) || (i >= C::B_OF && i < C::B_IDLE);
+            mbar_init(bar(i), four ? 4 : 1);   // s_free, p_full, o_free: one arrival per softmax warp
+        }
         *abort_flag = 0;
         slots[2] = slots[3] = slots[4] = 0;
         mbar_fence_init();
@@ -136,29 +147,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 && lane < 2) {
         // lane 0: Q and the K ring; lane 1: the V ring
         const bool is_k = lane == 0;
-        const int full0 = is_k ? 2 : 5, empty0 = is_k ? 8 : 11;
+        const int full0 = is_k ? C::B_KF : C::B_VF, empty0 = is_k ? C::B_KE : C::B_VE;
         const uint32_t ring = is_k ? sK : sV;
         int g = 0, it = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
             if (is_k) {
-                if (it >= 1 && !mbar_wait(bar(1), (uint32_t)(it - 1) & 1u, abort_flag)) {
+                if (it >= 1 && !mbar_wait(bar(C::B_QE), (uint32_t)(it - 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
-                mbar_expect_tx(bar(0), C::Q_BYTES);
+                mbar_expect_tx(bar(C::B_QF), C::Q_BYTES);
 #pragma unroll
                 for (int h = 0; h < C::NSUB; ++h)
-                    tma_load_3d(sQ + h * TROWS * 128, &tmQ, bar(0), 64 * h, j * p.G, cu0 + t0);
+                    tma_load_3d(sQ + h * TROWS * 128, &tmQ, bar(C::B_QF), 64 * h, j * p.G, cu0 + t0);
                 reinterpret_cast<volatile int*>(slots)[4] = it + 1;
             }
             const long long row0 = (long long)b * p.kv_rows_per_seq + (long long)j * p.n_slots +
                                    (is_k ? 0LL : (long long)p.nkv * p.n_slots);
             for (int t = 0; t < n_kt; ++t, ++g) {
-                const int st = g % NST;
-                if (g >= NST && !mbar_wait(bar(empty0 + st), (uint32_t)(g / NST - 1) & 1u, abort_flag)) {
+                const int st = g % NS;
+                if (g >= NS && !mbar_wait(bar(empty0 + st), (uint32_t)(g / NS - 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -166,7 +177,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int h = 0; h < C::NSUB; ++h)
                     tma_load_2d(ring + st * C::K_BYTES + h * C::KV_SUB, &tmKV, bar(full0 + st), 64 * h,
-                                (int)(row0 + (long long)t * TKT));
+                                (int)(row0 + (long long)t * TK));
                 reinterpret_cast<volatile int*>(slots)[2 + lane] = g + 1;
             }
             ++it;
@@ -176,35 +187,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
         }
     } else if (warp == 1 && lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16_f32(TROWS, TKT);
+        constexpr uint32_t idesc_s = idesc_bf16_f32(TROWS, TK);
         // PV: B = V is MN-major (transpose bit 16), N = HD
         constexpr uint32_t idesc_o = idesc_bf16_f32(TROWS, HD) | (1u << 16);
         auto issue_s = [&](int gs) -> bool {
-            const int sb = gs & 1, ks = gs % NST;
-            if (!mbar_wait(bar(2 + ks), (uint32_t)(gs / NST) & 1u, abort_flag)) return false;
-            if (gs >= 2 && !mbar_wait(bar(16 + sb), (uint32_t)((gs >> 1) - 1) & 1u, abort_flag)) return false;
+            const int sb = gs & 1, ks = gs % NS;
+            if (!mbar_wait(bar(C::B_KF + ks), (uint32_t)(gs / NS) & 1u, abort_flag)) return false;
+            if (gs >= 2 && !mbar_wait(bar(C::B_SFREE + sb), (uint32_t)((gs >> 1) - 1) & 1u, abort_flag)) return false;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * TROWS * 128) + 2ull * (kk & 3);
                 const uint64_t bd = sdesc_sw128(sK + ks * C::K_BYTES + (kk >> 2) * C::KV_SUB) + 2ull * (kk & 3);
-                tc_mma_bf16(tmem + sb * TKT, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                tc_mma_bf16(tmem + sb * TK, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
-            tc_commit(bar(14 + sb));   // S ready for the softmax
-            tc_commit(bar(8 + ks));    // K stage free again
+            tc_commit(bar(C::B_SF + sb));   // S ready for the softmax
+            tc_commit(bar(C::B_KE + ks));   // K stage free again
             return true;
         };
         int g = 0, it = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
-            const uint32_t tO = tmem + 2 * TKT + (uint32_t)((it & 1) * 128);
-            if (!mbar_wait(bar(0), (uint32_t)it & 1u, abort_flag) || !issue_s(g)) {
+            const int ob = it % OB;
+            const uint32_t tO = tmem + 2 * TK + (uint32_t)(ob * 128);
+            if (!mbar_wait(bar(C::B_QF), (uint32_t)it & 1u, abort_flag) || !issue_s(g)) {
                 ok = false;
                 break;
             }
-            if (n_kt == 1) tc_commit(bar(1));   // Q read by the item's last S
+            if (n_kt == 1) tc_commit(bar(C::B_QE));   // Q read by the item's last S
             for (int t = 0; t < n_kt; ++t) {
                 const int gt = g + t;
                 if (t + 1 < n_kt) {
@@ -212,26 +224,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (t + 2 == n_kt) tc_commit(bar(1));
+                    if (t + 2 == n_kt) tc_commit(bar(C::B_QE));
                 }
-                if (!mbar_wait(bar(18 + (gt & 1)), (uint32_t)(gt >> 1) & 1u, abort_flag) ||
-                    !mbar_wait(bar(5 + gt % NST), (uint32_t)(gt / NST) & 1u, abort_flag) ||
-                    (t == 0 && it >= 2 &&
-                     !mbar_wait(bar(22 + (it & 1)), (uint32_t)((it >> 1) - 1) & 1u, abort_flag))) {
+                // O buffer ob was last read by the epilogue of item it - OB
+                if (!mbar_wait(bar(C::B_PF + (gt & 1)), (uint32_t)(gt >> 1) & 1u, abort_flag) ||
+                    !mbar_wait(bar(C::B_VF + gt % NS), (uint32_t)(gt / NS) & 1u, abort_flag) ||
+                    (t == 0 && it >= OB &&
+                     !mbar_wait(bar(C::B_OF + ob), (uint32_t)((it / OB) - 1) & 1u, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t v_base = sV + (gt % NST) * C::K_BYTES;
+                const uint32_t v_base = sV + (gt % NS) * C::K_BYTES;
                 const uint32_t ph = sP0 + (uint32_t)(2 * (gt & 1) * C::P_BYTES), pl = ph + C::P_BYTES;
 #pragma unroll
-                for (int ks = 0; ks < TKT / 16; ++ks) {
+                for (int ks = 0; ks < TK / 16; ++ks) {
                     const uint64_t bd = sdesc_sw128_mn(v_base + ks * 16 * 128, C::KV_SUB, 1024);
-                    tc_mma_bf16(tO, sdesc_sw128(ph) + 2ull * ks, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
-                    tc_mma_bf16(tO, sdesc_sw128(pl) + 2ull * ks, bd, idesc_o, 1u);
+                    const uint64_t adh = (TK == 64 ? sdesc_sw128(ph) : sdesc_sw64(ph)) + 2ull * ks;
+                    const uint64_t adl = (TK == 64 ? sdesc_sw128(pl) : sdesc_sw64(pl)) + 2ull * ks;
+                    tc_mma_bf16(tO, adh, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+                    tc_mma_bf16(tO, adl, bd, idesc_o, 1u);
                 }
-                tc_commit(bar(20 + (gt & 1)));   // P buffer gt & 1 (and O) free again
-                tc_commit(bar(11 + gt % NST));   // V stage free again
+                tc_commit(bar(C::B_PV + (gt & 1)));   // P buffer gt & 1 (and O) free again
+                tc_commit(bar(C::B_VE + gt % NS));    // V stage free again
             }
             g += n_kt;
             ++it;
@@ -240,7 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             *abort_flag = 1;
             raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
         }
-        tc_commit(bar(24));   // completes once every MMA this thread issued has finished
+        tc_commit(bar(C::B_IDLE));   // completes once every MMA this thread issued has finished
     } else if (warp >= 2) {
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                 // MMA row = TMEM lane
@@ -248,46 +263,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         int g = 0, it = 0, pv_seen = 0;   // PV(0) .. PV(pv_seen - 1) are known to be complete
         bool ok = true;
-        auto wait_pv = [&](int need) {   // PV(x) completes barrier 20 + (x & 1) for the (x >> 1)-th time
+        auto wait_pv = [&](int need) {   // PV(x) completes barrier B_PV + (x & 1) for the (x >> 1)-th time
             while (ok && pv_seen <= need) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(20 + (pv_seen & 1)), (uint32_t)(pv_seen >> 1) & 1u, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PV + (pv_seen & 1)), (uint32_t)(pv_seen >> 1) & 1u,
+                                                       abort_flag));
                 ++pv_seen;
             }
         };
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, b, j, cu0, len, t0, s0, kv_len);
+            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
             const bool row_ok = t0 + tl < len;
             const int qpos = s0 + t0 + tl;
-            const uint32_t tO = lane_base + 2 * TKT + (uint32_t)((it & 1) * 128);
+            const int ob = it % OB;
+            const uint32_t tO = lane_base + 2 * TK + (uint32_t)(ob * 128);
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < n_kt && ok; ++t) {
                 const int gt = g + t;
                 const int sb = gt & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(14 + sb), (uint32_t)(gt >> 1) & 1u, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SF + sb), (uint32_t)(gt >> 1) & 1u, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                float sv[TKT];
-                {
-                    float a[32], c[32];
-                    tmem_ld32(lane_base + sb * TKT, a);
-                    tmem_ld32(lane_base + sb * TKT + 32, c);
+                float sv[TK];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        sv[q] = a[q];
-                        sv[32 + q] = c[q];
-                    }
+                for (int c0 = 0; c0 < TK; c0 += 32) {
+                    float a[32];
+                    tmem_ld32(lane_base + sb * TK + c0, a);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) sv[c0 + q] = a[q];
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(16 + sb));   // S buffer may be reused
-                const int j0 = t * TKT;
+                if (lane == 0) mbar_arrive(bar(C::B_SFREE + sb));   // S buffer may be reused
+                const int j0 = t * TK;
                 // causal / length mask only where this tile reaches past a row's position or the
                 // keys' end (the item's first row has the smallest position, s0 + t0)
-                if (j0 + TKT > s0 + t0 + 1 || j0 + TKT > kv_len) {
+                if (j0 + TK > s0 + t0 + 1 || j0 + TK > kv_len) {
 #pragma unroll
-                    for (int q = 0; q < TKT; ++q) {
+                    for (int q = 0; q < TK; ++q) {
                         const int key = j0 + q;
                         if (key > qpos || key >= kv_len) sv[q] = -INFINITY;
                     }
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // row max in four independent chains (max is exact in any order), in log2 units
                 float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-                for (int q = 4; q < TKT; ++q) mx4[q & 3] = fmaxf(mx4[q & 3], sv[q]);
+                for (int q = 4; q < TK; ++q) mx4[q & 3] = fmaxf(mx4[q & 3], sv[q]);
                 const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
                 // Lazy reference max: it moves (and O is rescaled) only when this tile's max exceeds it
                 // by more than kLazyLog2, so p = 2^(s * scale - mref) <= 2^kLazyLog2.  O / l is
@@ -306,14 +319,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // p = 2^(s * scale - mref) (one rounding of the exponent), summed in four chains
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < TKT; ++q) {
+                for (int q = 0; q < TK; ++q) {
                     sv[q] = exp2f(fmaf(sv[q], p.scale_log2, -mref));
                     rs4[q & 3] += sv[q];
                 }
                 l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
                 m = mn;
                 // P buffer gt & 1 was last read by PV(gt - 2); O needs PV(gt - 1) done only when it is
-                // rescaled (once the running max settles, P writes and PV MMAs stream without waiting)
+                // rescaled
                 const bool rescale = t > 0 && !__all_sync(0xffffffffu, alpha == 1.f);
                 wait_pv(rescale ? gt - 1 : gt - 2);
                 if (!ok) break;
@@ -330,11 +343,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 // the item's last tile: zero the V rows of slots past the valid keys (stale cache)
                 const int valid_in_tile = kv_len - j0;
-                if (valid_in_tile < TKT) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(5 + gt % NST), (uint32_t)(gt / NST) & 1u, abort_flag));
+                if (valid_in_tile < TK) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_VF + gt % NS), (uint32_t)(gt / NS) & 1u, abort_flag));
                     if (!ok) break;
-                    const int z_rows = TKT - valid_in_tile;
-                    uint8_t* vt = smem + C::OFF_V + (gt % NST) * C::K_BYTES;
+                    const int z_rows = TK - valid_in_tile;
+                    uint8_t* vt = smem + C::OFF_V + (gt % NS) * C::K_BYTES;
                     for (int idx = r; idx < C::NSUB * z_rows * 8; idx += TROWS) {
                         const int h = idx / (z_rows * 8), rem = idx - h * z_rows * 8;
                         const int row = valid_in_tile + rem / 8, chunk = rem & 7;
@@ -342,12 +355,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-                // P as bf16 hi + lo, K-major with the 128-byte swizzle: row r, 16-byte chunk c at c ^ (r & 7)
+                // P as bf16 hi + lo, K-major: 128-byte rows (TK 64) with chunk c of row r at c ^ (r & 7),
+                // or 64-byte rows (TK 32) with chunk c at c ^ ((r >> 1) & 3)
                 {
-                    uint8_t* ph = smem + C::OFF_P + 2 * (gt & 1) * C::P_BYTES + r * 128;
+                    uint8_t* ph = smem + C::OFF_P + 2 * (gt & 1) * C::P_BYTES + r * C::P_ROW;
                     uint8_t* pl = ph + C::P_BYTES;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < TK / 8; ++c) {
                         uint32_t hw[4], lw[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             lw[e] = pack_bf2(sv[c * 8 + 2 * e] - __uint_as_float(u0),
                                              sv[c * 8 + 2 * e + 1] - __uint_as_float(u1));
                         }
-                        const int off = (c ^ (r & 7)) << 4;
+                        const int off = (TK == 64 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3))) << 4;
                         *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                         *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fence_proxy_async_smem();   // generic-proxy writes (P, zeroed V rows) before the MMA reads them
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(18 + (gt & 1)));
+                if (lane == 0) mbar_arrive(bar(C::B_PF + (gt & 1)));
             }
             // the item's output: O / l once its last PV is done
             wait_pv(g + n_kt - 1);
@@ -390,7 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(22 + (it & 1)));   // O buffer free for item it + 2
+            if (lane == 0) mbar_arrive(bar(C::B_OF + ob));   // O buffer free for item it + OB
             g += n_kt;
             ++it;
         }
@@ -407,16 +421,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         volatile int never = 0;
         if (lane == 0) {
             const int qi = reinterpret_cast<volatile int*>(slots)[4];
-            if (qi > 0) (void)mbar_wait(bar(0), (uint32_t)(qi - 1) & 1u, &never);
+            if (qi > 0) (void)mbar_wait(bar(C::B_QF), (uint32_t)(qi - 1) & 1u, &never);
         }
         const int issued = reinterpret_cast<volatile int*>(slots)[2 + lane];
-        const int full0 = lane == 0 ? 2 : 5;
-        for (int t = max(0, issued - NST); t < issued; ++t)
-            (void)mbar_wait(bar(full0 + t % NST), (uint32_t)(t / NST) & 1u, &never);
+        const int full0 = lane == 0 ? C::B_KF : C::B_VF;
+        for (int t = max(0, issued - NS); t < issued; ++t)
+            (void)mbar_wait(bar(full0 + t % NS), (uint32_t)(t / NS) & 1u, &never);
     }
     if (warp == 1 && lane == 0) {
         volatile int never = 0;
-        (void)mbar_wait(bar(24), 0u, &never);
+        (void)mbar_wait(bar(C::B_IDLE), 0u, &never);
     }
     __syncthreads();
     if (warp == 1) {
@@ -426,9 +440,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-template <int HD>
-cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
-    using C = AttnCfg<HD>;
+template <int HD, int TK, int NS, int OB>
+cudaError_t launch_tc_cfg(const PrefillAttnArgs& a, cudaStream_t st) {
+    using C = AttnCfg<HD, TK, NS, OB>;
+    constexpr int kCtasPerSm = TK == 32 ? 2 : 1;
     const int G = a.nq / a.nkv;
     const int QT = TROWS / G;
     alignas(64) CUtensorMap mq, mkv;
@@ -437,17 +452,18 @@ cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
     const uint64_t qstr[2] = {(uint64_t)HD * 2, (uint64_t)a.nq * HD * 2};
     const uint32_t qbox[3] = {64u, (uint32_t)G, (uint32_t)QT};
     if (!encode_tensor_map(&mq, 3, a.q, qdims, qstr, qbox)) return cudaErrorInvalidValue;
-    // the layer's cache as rows of hd: [cache_batch * 2 * nkv * n_slots, hd]; box 64 dims x 64 keys
+    // the layer's cache as rows of hd: [cache_batch * 2 * nkv * n_slots, hd]; box 64 dims x TK keys
     const uint64_t kvdims[2] = {(uint64_t)HD, (uint64_t)a.cache_batch * 2 * a.nkv * a.n_slots};
     const uint64_t kvstr[1] = {(uint64_t)HD * 2};
-    const uint32_t kvbox[2] = {64u, (uint32_t)TKT};
+    const uint32_t kvbox[2] = {64u, (uint32_t)TK};
     if (!encode_tensor_map(&mkv, 2, a.kv_layer, kvdims, kvstr, kvbox)) return cudaErrorInvalidValue;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(prefill_attn_tc_kernel<HD, TK, NS, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
@@ -466,9 +482,17 @@ cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
     p.kv_rows_per_seq = 2LL * a.nkv * a.n_slots;
     p.scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
     const long long items = (long long)((a.max_len + QT - 1) / QT) * a.nkv * a.batch;
-    const int grid = (int)std::min<long long>(items, device_sm_count());
-    HRA_LAUNCH(prefill_attn_tc_kernel<HD>, dim3(grid), dim3(kTcThreads), C::SMEM, st, mq, mkv, p);
+    const int grid = (int)std::min<long long>(items, (long long)device_sm_count() * kCtasPerSm);
+    HRA_LAUNCH((prefill_attn_tc_kernel<HD, TK, NS, OB>), dim3(grid), dim3(kTcThreads), C::SMEM, st, mq, mkv, p);
     return cudaGetLastError();
+}
+
+// Short query runs (the longest prompt of the batch at most 512 rows) take the two-CTAs-per-SM
+// configuration: their items have few key tiles and are bound by per-item latency.
+template <int HD>
+cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
+    if (a.max_len <= 512) return launch_tc_cfg<HD, 32, 2, 1>(a, st);
+    return launch_tc_cfg<HD, 64, 3, 2>(a, st);
 }
 
 }  // namespace

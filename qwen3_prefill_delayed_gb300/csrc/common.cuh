@@ -298,6 +298,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// K-major operand with the 64-byte swizzle: rows of 64 bytes, 8-row groups 512 bytes apart, 16-byte
+// chunk c of row r stored at chunk c ^ ((r >> 1) & 3).  Fields as sdesc_sw128 (layout type 4).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(512u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)4u << 61;
+    return d;
+}
+
 // Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per thread).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
