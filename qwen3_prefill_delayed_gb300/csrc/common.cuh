@@ -387,8 +387,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo,
     return d;
 }
 
-// ------------------------------------------------------------------ legacy warp-level MMA helpers
-// (used by the attention kernels)
+// ------------------------------------------------------------------ warp-level MMA helpers
+// (used by the single-query decode attention kernel)
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
