@@ -1001,7 +1001,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 // per row, one thread per group of 8 columns (blockDim = groups rounded up to a warp), all split
 // loads issued before the sum (split order kept); writes r = bf16(r + acc), then y = RMSNorm(r) * g
 // with the compensated sum of squares of the rounded residual.
-constexpr int kNormMaxThreads = 1024;
+constexpr int kNormMaxThreads = 512;   // hidden sizes up to 4096; 128 registers a thread (no spill)
 constexpr int kNormMaxSplits = 8;
 __global__ void __launch_bounds__(kNormMaxThreads) splitk_residual_norm_kernel(
     const float* __restrict__ part, int splits, long long split_stride, int N, bf16* __restrict__ r,
