@@ -111,3 +111,85 @@ def test_binding_refuses_cpu_tensors(hra):
     import torch
     with pytest.raises(hra.HraError, match="CUDA tensor"):
         hra.hra_linear(torch.zeros(4, 64, dtype=torch.bfloat16), torch.zeros(8, 64, dtype=torch.bfloat16))
+
+
+def test_newer_entry_points_reject_bad_arguments_without_cuda(hra):
+    """Chunked prefill, device-position decode, the AR frame, the sampled step and the FP8 calls
+    return the status codes include/hra.h documents, before touching CUDA."""
+    L = hra.lib()
+    d = _dims(hra)
+    A = 0x10000                                # aligned, never dereferenced: validation fails first
+    fake = ctypes.c_void_p(A)
+    kv = hra.HraKvCache(A, 1, 8)
+    layers = (hra.HraLayerWeights * 2)()
+    for i in range(2):
+        for f, _ in hra.HraLayerWeights._fields_:
+            setattr(layers[i], f, A)
+    w = hra.HraWeights(A, layers, A)
+    big = 1 << 30
+    lens5 = (ctypes.c_int32 * 1)(5)
+
+    # chunked prefill: start_pos NULL; start + len past the cache; negative start
+    assert L.hra_prefill_chunk(ctypes.byref(d), ctypes.byref(w), fake, lens5, None, 1, 5, ctypes.byref(kv), fake,
+                               fake, big, 0, None) == -1
+    for start in (4, -1):
+        st = (ctypes.c_int32 * 1)(start)
+        assert L.hra_prefill_chunk(ctypes.byref(d), ctypes.byref(w), fake, lens5, st, 1, 5, ctypes.byref(kv), fake,
+                                   fake, big, 0, None) == -4
+    st3 = (ctypes.c_int32 * 1)(3)                                        # 3 + 5 = 8: fits, then too small a workspace
+    assert L.hra_prefill_chunk(ctypes.byref(d), ctypes.byref(w), fake, lens5, st3, 1, 5, ctypes.byref(kv), fake,
+                               fake, 16, 0, None) == -3
+
+    # device-position decode: no positions; misaligned positions; bound outside [0, n_slots)
+    assert L.hra_decode_dev(ctypes.byref(d), ctypes.byref(w), fake, None, 7, 1, 1, ctypes.byref(kv), fake, fake,
+                            big, None) == -1
+    assert L.hra_decode_dev(ctypes.byref(d), ctypes.byref(w), fake, ctypes.c_void_p(A + 2), 7, 1, 1,
+                            ctypes.byref(kv), fake, fake, big, None) == -1
+    for bound in (8, -1):
+        assert L.hra_decode_dev(ctypes.byref(d), ctypes.byref(w), fake, fake, bound, 1, 1, ctypes.byref(kv), fake,
+                                fake, big, None) == -4
+
+    # sampled codebook step: parameter ranges, seeds, codebook size
+    def sampled(s, seeds=fake, dims=d):
+        return L.hra_codebook_step_sampled(ctypes.byref(dims), fake, fake, fake, fake, None,
+                                           ctypes.byref(s) if s is not None else None, seeds, 1, fake, fake, fake,
+                                           None, fake, big, None)
+    assert sampled(None) == -1
+    for t, k, p in ((0.0, 50, 0.95), (float("inf"), 50, 0.95), (float("nan"), 50, 0.95), (1.0, -1, 0.95),
+                    (1.0, 50, 0.0), (1.0, 50, 1.5)):
+        assert sampled(hra.HraSampling(t, k, p)) == -1, (t, k, p)
+    ok = hra.HraSampling(1.0, 50, 0.95)
+    assert sampled(ok, seeds=None) == -1
+    assert sampled(ok, dims=_dims(hra, codebook_size=3000, bos_id=2998, eoc_id=2999)) == -2
+
+    # AR frame: positions NULL; bound outside the cache; bad sampling parameters
+    def frame(pos, bound, s=None):
+        return L.hra_ar_frame(ctypes.byref(d), ctypes.byref(w), fake, fake, fake, None,
+                              ctypes.byref(s) if s is not None else None, fake if s is not None else None, fake,
+                              pos, bound, 1, ctypes.byref(kv), fake, fake, fake, fake, big, fake, big, None)
+    assert frame(None, 7) == -1
+    assert frame(fake, 8) == -4
+    assert frame(fake, 7, hra.HraSampling(-1.0, 0, 1.0)) == -1
+
+    # FP8: quantizers (n a multiple of 8, alignment), the FP8 linear (K a multiple of 128), the FP8
+    # prefill (widths a multiple of 128, layer pointers) and calibration (outputs)
+    assert L.hra_fp8_quantize_weight(fake, 12, fake, fake, None) == -1
+    assert L.hra_fp8_quantize_weight(fake, 64, ctypes.c_void_p(A + 1), fake, None) == -1
+    assert L.hra_fp8_quantize(fake, 0, fake, fake, None) == -1
+    assert L.hra_linear_fp8(fake, fake, fake, 4, 128, 192, fake, fake, 0, fake, big, None) == -1
+    assert L.hra_linear_fp8(fake, fake, fake, 4, 100, 256, fake, fake, 0, fake, big, None) == -1
+    assert L.hra_linear_fp8(fake, fake, fake, 4, 128, 256, fake, fake, 0, fake, 16, None) == -3
+    f8 = (hra.HraFp8Layer * 2)()
+    for i in range(2):
+        for f, _ in hra.HraFp8Layer._fields_:
+            setattr(f8[i], f, A)
+    assert L.hra_prefill_fp8(ctypes.byref(d), ctypes.byref(w), None, fake, lens5, 1, 5, ctypes.byref(kv), fake,
+                             fake, big, 0, None) == -1
+    assert L.hra_prefill_fp8(ctypes.byref(_dims(hra, ffn=832)), ctypes.byref(w), f8, fake, lens5, 1, 5,
+                             ctypes.byref(kv), fake, fake, big, 0, None) == -2
+    f8[1].a_scale = A + 2
+    assert L.hra_prefill_fp8(ctypes.byref(d), ctypes.byref(w), f8, fake, lens5, 1, 5, ctypes.byref(kv), fake,
+                             fake, big, 0, None) == -1
+    assert L.hra_fp8_calibrate(ctypes.byref(d), ctypes.byref(w), fake, lens5, 1, 5, ctypes.byref(kv), None, fake,
+                               fake, big, None) == -1
+    assert L.hra_launch_counter() == 0
