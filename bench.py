@@ -163,6 +163,24 @@ def events_time(fn, n, torch):
     return e0.elapsed_time(e1)
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest value of `x` over all ranks (every rank gets it); `x` itself when world == 1.
+    The whole-job time of a step is the slowest rank's."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, seconds_per_step):
+    """Weak scaling: every rank processes `units_per_rank` per step, so the job's rate is
+    world * units / (the slowest rank's time per step)."""
+    return world * units_per_rank / seconds_per_step
+
+
 def traffic_for(kernel, source_files):
     """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -299,13 +317,11 @@ def main():
     clk = clocks.stop()
     torch.cuda.synchronize()
     probe_ms, probe_n, probe_flops = hra.hra_probe_collect()
+    ms = max_over_ranks(ms, world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     ms_step = ms / args.steps
-    value = world * tokens_per_step / (ms_step / 1e3)
+    value = whole_job_rate(world, tokens_per_step, ms_step / 1e3)
 
     # roofline of the dominant kernel: the gate/up + SwiGLU projection of the full prefill layers
     gu_ms = probe_ms / max(probe_n, 1)
@@ -337,12 +353,8 @@ def main():
     t0 = time.perf_counter()
     for _ in range(args.steps):
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * tokens_per_step / e2e_s, "unit": "tokens/s",
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+    e2e = {"value": whole_job_rate(world, tokens_per_step, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": tok_host.numel() * 4,
            "d2h_bytes_per_step": hid_host.numel() * 2 + codes_host.numel() * 4}
 
