@@ -107,6 +107,15 @@ def lib():
         L.oracle_quantize_e4m3.argtypes = [_u16p, ctypes.c_int64, ctypes.c_float, _u8p]
         L.oracle_quantize_weight_e4m3.argtypes = [_u16p, ctypes.c_int64, ctypes.POINTER(ctypes.c_float), _u8p]
         L.oracle_linear_fp8.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _f32p]
+        L.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_decode.restype = ctypes.c_float
+        L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        L.oracle_e2m1_encode.restype = ctypes.c_uint8
+        L.oracle_nvfp4_global.argtypes = [_u16p, ctypes.c_int64]
+        L.oracle_nvfp4_global.restype = ctypes.c_float
+        L.oracle_quantize_nvfp4.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_float, _u8p, _u8p]
+        L.oracle_linear_nvfp4.argtypes = [_u8p, _u8p, _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_float, ctypes.c_float, _f32p]
         L.oracle_prefill_fp8.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
                                          ctypes.POINTER(OracleFp8Layer), _u16p, _i32p, _i32p, ctypes.c_int,
                                          ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int, _u16p]
@@ -379,6 +388,42 @@ def linear_fp8(x8: np.ndarray, w8: np.ndarray, scale: float) -> np.ndarray:
     N = w8.shape[0]
     y = np.empty((T, N), np.float32)
     lib().oracle_linear_fp8(x8, w8, T, N, K, float(scale), y)
+    return y
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, np.uint8).ravel()
+    return np.array([lib().oracle_e2m1_decode(int(x)) for x in c], np.float32).reshape(np.shape(codes))
+
+
+def e2m1_encode(x) -> np.ndarray:
+    a = np.asarray(x, np.float32).ravel()
+    return np.array([lib().oracle_e2m1_encode(float(v)) for v in a], np.uint8).reshape(np.shape(x))
+
+
+def nvfp4_global(x_u16: np.ndarray) -> float:
+    """Global scale max|x| / (6 * 448) of an NVFP4 tensor (1 for an all-zero tensor)."""
+    x = _c(x_u16, np.uint16)
+    return float(lib().oracle_nvfp4_global(x, x.size))
+
+
+def quantize_nvfp4(x_u16: np.ndarray, g: float):
+    """(codes [rows, K] one E2M1 code per byte, block scales [rows, K/16] E4M3) of bf16 bits x."""
+    x = _c(x_u16, np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K), np.uint8)
+    scales = np.empty((rows, K // 16), np.uint8)
+    lib().oracle_quantize_nvfp4(x, rows, K, float(g), codes, scales)
+    return codes, scales
+
+
+def linear_nvfp4(a, sa, w, sw, g_a: float, g_w: float) -> np.ndarray:
+    """fp32 y [T, N] of NVFP4 operands a [T, K] / w [N, K] with block scales sa / sw."""
+    a, sa, w, sw = (np.ascontiguousarray(v, np.uint8) for v in (a, sa, w, sw))
+    T, K = a.shape
+    N = w.shape[0]
+    y = np.empty((T, N), np.float32)
+    lib().oracle_linear_nvfp4(a, sa, w, sw, T, N, K, float(g_a), float(g_w), y)
     return y
 
 

@@ -20,7 +20,9 @@
  *     per-row seeded Philox4x32-10 noise; vLLM-Omni PR #8226, Purpose and Test Plan);
  *   - the static-FP8 variant of the prefill projections (E4M3 weights with per-tensor scales,
  *     inputs quantized with calibrated static scales) and that calibration ("fp8_chain.py",
- *     module docstring; "Stabilize Higgs Audio termination and prefill", Summary).
+ *     module docstring; "Stabilize Higgs Audio termination and prefill", Summary);
+ *   - the NVFP4 codec and block-scaled linear of the chain's FP4 band (E2M1 elements, one E4M3
+ *     scale per 16-element block, one fp32 global scale; "fp8_chain.py", BANDS).
  *
  * Arithmetic: fp32 on bf16-rounded weights and activations.  Values are rounded to bf16
  * (round-to-nearest-even) at these points and nowhere else: every RMSNorm output, the QKV
@@ -336,6 +338,97 @@ void oracle_linear_fp8(const uint8_t* x8, const uint8_t* w8, int T, int N, int K
             y[(size_t)t * N + j] = s * scale;
         }
     }
+}
+
+/* ---------------------------------------------------------------- NVFP4 (E2M1 + block scales) */
+
+/* FP4 E2M1: 1 sign bit (bit 3), 2 exponent bits (bias 1), 1 mantissa bit.  Exponent field 0 is
+ * subnormal, m * 0.5; otherwise (1 + m/2) * 2^(e-1): the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ * No infinity or NaN.  Encoding rounds to the nearest value, ties to the even mantissa, and
+ * saturates beyond 6 to +-6.  Source: the NVFP4 band of the prefill chain ("fp8_chain.py", BANDS:
+ * the FFN pair and the output projection "ride NVFP4 with dynamic block scales"); the element and
+ * scale formats are NVIDIA's published NVFP4 definition, which the pages name but do not spell out. */
+float oracle_e2m1_decode(uint8_t c) {
+    const int sgn = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    const double v = e == 0 ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+    return (float)(sgn ? -v : v);
+}
+
+uint8_t oracle_e2m1_encode(float x) {
+    const uint8_t sgn = signbit(x) ? 8 : 0;
+    const double a = fabs((double)x);
+    if (!(a < 6.0)) return sgn | 7;                    /* saturate (NaN too: the format has none) */
+    /* candidates in code order; pick the nearest, a tie going to the even mantissa */
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c < 8; ++c) {
+        const double d = fabs(a - (double)oracle_e2m1_decode((uint8_t)c));
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return sgn | (uint8_t)best;
+}
+
+/* Global scale of an NVFP4 tensor: max|x| / (6 * 448) in fp32 (1 for an all-zero tensor), so that
+ * every block scale fits E4M3. */
+float oracle_nvfp4_global(const uint16_t* x, int64_t n) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf(bf(x[i]));
+        if (a > amax) amax = a;
+    }
+    return amax > 0.0f ? amax / (6.0f * 448.0f) : 1.0f;
+}
+
+/* NVFP4 quantization of x [rows][K] (bf16), K a multiple of 16: each block of 16 consecutive
+ * elements along K gets the E4M3 scale s_b = e4m3(amax_b / (6 g)) and the codes
+ * e2m1(x / (g * dec(s_b))) (all 0 when dec(s_b) is 0); divisions in fp32.  codes: one code per
+ * byte [rows][K]; scales [rows][K / 16]. */
+void oracle_quantize_nvfp4(const uint16_t* x, int rows, int K, float g, uint8_t* codes, uint8_t* scales) {
+    const int nb = K / 16;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* xb = x + (size_t)r * K + 16 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(bf(xb[i]));
+                if (a > amax) amax = a;
+            }
+            const uint8_t sc = oracle_e4m3_encode(amax / (6.0f * g));
+            scales[(size_t)r * nb + b] = sc;
+            const float step = g * oracle_e4m3_decode(sc);
+            for (int i = 0; i < 16; ++i)
+                codes[(size_t)r * K + 16 * b + i] = step > 0.0f ? oracle_e2m1_encode(bf(xb[i]) / step) : 0;
+        }
+}
+
+/* y[t][j] = (g_a * g_w) * sum over blocks b (ascending; descending under oracle_set_sum_order(1))
+ * of dec(sa[t][b]) * dec(sw[j][b]) * (sum over the block's 16 k ascending of e2m1(a) * e2m1(w)),
+ * in fp32.  Each block's term is exact in fp32 (E2M1 products are multiples of 1/4 below 37, the
+ * two E4M3 scales have 4-bit significands), so only the sum over blocks and the final scaling
+ * round -- the order a block-scaled tensor-core MMA accumulates in. */
+void oracle_linear_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* w, const uint8_t* sw, int T, int N,
+                         int K, float g_a, float g_w, float* y) {
+    const int desc = g_sum_descending;
+    const int nb = K / 16;
+    const float g = g_a * g_w;
+    #pragma omp parallel for schedule(static)
+    for (int j = 0; j < N; ++j)
+        for (int t = 0; t < T; ++t) {
+            float acc = 0.0f;
+            for (int ib = 0; ib < nb; ++ib) {
+                const int b = desc ? nb - 1 - ib : ib;
+                float blk = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    const int k = 16 * b + i;
+                    blk += oracle_e2m1_decode(a[(size_t)t * K + k]) * oracle_e2m1_decode(w[(size_t)j * K + k]);
+                }
+                acc += (oracle_e4m3_decode(sa[(size_t)t * nb + b]) * oracle_e4m3_decode(sw[(size_t)j * nb + b])) * blk;
+            }
+            y[(size_t)t * N + j] = acc * g;
+        }
 }
 
 typedef struct {
