@@ -317,6 +317,19 @@ int hra_fp8_quantize_weight(const void* w_dev, int64_t n, void* w8_dev, float* s
 /* x8_dev[i] = e4m3(x[i] / *scale_dev) (IEEE division), n a multiple of 8. */
 int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void* x8_dev, void* stream);
 
+/* ---- NVFP4 quantization (the FP4 band of the prefill chain) ---------------------------------- */
+/* The chain's FP4 band ("fp8_chain.py", BANDS: the FFN pair and the output projection "ride NVFP4
+ * with dynamic block scales") in NVIDIA's published NVFP4 format: each block of 16 consecutive
+ * elements along K of x_dev bf16 [rows, K] gets the E4M3 scale s = e4m3(amax_block / (6 g)) and
+ * the FP4 E2M1 codes e2m1(x / (g * s)) (all 0 when g * s is 0), g = *g_dev the tensor's fp32
+ * global scale (e.g. max|x| / (6 * 448)); e2m1() rounds to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6 (ties to the even mantissa) and saturates at +-6; each step is one fp32 rounding.
+ *   codes_dev   uint8 [rows, K]: one E2M1 code per byte (sign in bit 3), 16-byte aligned.
+ *   scales_dev  uint8 [rows, K / 16]: E4M3 block scales.
+ * K a multiple of 16, x_dev 16-byte aligned, g_dev 4-byte aligned (else HRA_ERR_INVALID_ARG). */
+int hra_nvfp4_quantize(const void* x_dev, int32_t rows, int32_t K, const float* g_dev, void* codes_dev,
+                       void* scales_dev, void* stream);
+
 /* FP8 projection: out = epilogue((a8 . w8^T) * (*a_scale) * (*w_scale)), a8 E4M3 [M, K], w8 E4M3
  * [N, K] (2N rows for EPI_SWIGLU), K a multiple of 128; epilogues as hra_linear. */
 size_t hra_linear_fp8_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue);

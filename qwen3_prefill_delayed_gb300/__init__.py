@@ -34,7 +34,7 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_work
             "hra_codebook_workspace_size", "hra_codebook_step", "hra_codebook_step_sampled",
             "hra_codebook_step_noalloc",
             "hra_linear_workspace_size",
-            "hra_linear", "hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_linear_fp8_workspace_size",
+            "hra_linear", "hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_nvfp4_quantize", "hra_linear_fp8_workspace_size",
             "hra_linear_fp8", "hra_fp8_calibrate_workspace_size", "hra_fp8_calibrate",
             "hra_prefill_fp8_workspace_size", "hra_prefill_fp8",
             "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
@@ -127,6 +127,8 @@ def lib() -> ctypes.CDLL:
         i64 = ctypes.c_int64
         L.hra_fp8_quantize_weight.argtypes = [vp, i64, vp, vp, vp]
         L.hra_fp8_quantize.argtypes = [vp, i64, vp, vp, vp]
+        L.hra_nvfp4_quantize.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+        L.hra_nvfp4_quantize.restype = ctypes.c_int
         L.hra_linear_fp8_workspace_size.argtypes = [i32, i32, i32, i32]
         L.hra_linear_fp8_workspace_size.restype = sz
         L.hra_linear_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp]
@@ -527,6 +529,18 @@ def fp8_quantize(x: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Ten
     _check(lib().hra_fp8_quantize(_ptr(x, torch.bfloat16, "x"), x.numel(), _ptr(scale, torch.float32, "scale"),
                                   _ptr(x8, torch.uint8, "x8"), _stream(stream)), "hra_fp8_quantize")
     return x8
+
+
+def nvfp4_quantize(x: torch.Tensor, g: torch.Tensor, stream=None):
+    """hra_nvfp4_quantize: bf16 CUDA [rows, K] and the global scale (CUDA float32 scalar) ->
+    (E2M1 codes uint8 [rows, K], E4M3 block scales uint8 [rows, K / 16])."""
+    rows, K = x.shape
+    codes = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, K // 16, dtype=torch.uint8, device=x.device)
+    _check(lib().hra_nvfp4_quantize(_ptr(x, torch.bfloat16, "x"), rows, K, _ptr(g, torch.float32, "g"),
+                                    _ptr(codes, torch.uint8, "codes"), _ptr(scales, torch.uint8, "scales"),
+                                    _stream(stream)), "hra_nvfp4_quantize")
+    return codes, scales
 
 
 def hra_linear_fp8(a8: torch.Tensor, w8: torch.Tensor, a_scale: torch.Tensor, w_scale: torch.Tensor,

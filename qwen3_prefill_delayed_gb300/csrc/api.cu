@@ -558,6 +558,17 @@ int hra_fp8_quantize_weight(const void* w_dev, int64_t n, void* w8_dev, float* s
     return HRA_OK;
 }
 
+int hra_nvfp4_quantize(const void* x_dev, int32_t rows, int32_t K, const float* g_dev, void* codes_dev,
+                       void* scales_dev, void* stream) {
+    if (!aligned16(x_dev) || !aligned16(codes_dev) || scales_dev == nullptr || g_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(g_dev) & 3u) || rows < 1 || K < 16 || K % 16 != 0)
+        return HRA_ERR_INVALID_ARG;
+    HRA_TRY(launch_nvfp4_quantize(reinterpret_cast<const bf16*>(x_dev), rows, K, g_dev,
+                                  reinterpret_cast<uint8_t*>(codes_dev), reinterpret_cast<uint8_t*>(scales_dev),
+                                  reinterpret_cast<cudaStream_t>(stream)));
+    return HRA_OK;
+}
+
 int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void* x8_dev, void* stream) {
     if (!aligned16(x_dev) || x8_dev == nullptr || (reinterpret_cast<uintptr_t>(x8_dev) & 7u) || scale_dev == nullptr ||
         (reinterpret_cast<uintptr_t>(scale_dev) & 3u) || n < 8 || n % 8 != 0)

@@ -10,6 +10,8 @@
 // e4m3() is the round-to-nearest-even, saturating (finite overflow -> +-448) conversion.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "internal.h"
 
 namespace hra {
@@ -64,6 +66,76 @@ __global__ void absmax_kernel(const bf16* __restrict__ x, long long n, float* am
     }
 }
 
+// ---------------------------------------------------------------- NVFP4 (E2M1 + block scales)
+// The FP4 band of the prefill chain ("fp8_chain.py", BANDS: the FFN pair and the output projection
+// "ride NVFP4 with dynamic block scales"), in NVIDIA's published NVFP4 format: E2M1 elements, one
+// E4M3 scale per 16 consecutive elements along K, one fp32 global scale g per tensor.
+
+// value of a finite E4M3 code: (8 + M) 2^(E - 10) for E > 0, M 2^-9 for E = 0
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+    const int E = (c >> 3) & 15, M = c & 7;
+    const float v = E == 0 ? ldexpf((float)M, -9) : ldexpf((float)(8 + M), E - 10);
+    return (c & 0x80) ? -v : v;
+}
+
+// FP4 E2M1 code (sign in bit 3) of x: the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6; at a midpoint
+// the value with the even mantissa (even code); beyond 6 (and NaN) saturates to 6
+__device__ __forceinline__ uint32_t to_e2m1(float x) {
+    const uint32_t sgn = signbit(x) ? 8u : 0u;
+    const float a = fabsf(x);
+    if (!(a < 6.0f)) return sgn | 7u;
+    uint32_t c;
+    if (a <= 0.25f) c = 0;        // 0.25 lies between 0 and 0.5: 0
+    else if (a < 0.75f) c = 1;    // 0.75 lies between 0.5 and 1: 1
+    else if (a <= 1.25f) c = 2;   // 1.25: 1
+    else if (a < 1.75f) c = 3;    // 1.75: 2
+    else if (a <= 2.5f) c = 4;    // 2.5: 2
+    else if (a < 3.5f) c = 5;     // 3.5: 4
+    else if (a <= 5.0f) c = 6;    // 5: 4
+    else c = 7;
+    return sgn | c;
+}
+
+// One thread per 16-element block of x [rows][K]: s = e4m3(amax / (6 g)); codes =
+// e2m1(x / (g dec(s))) (0 when g dec(s) is 0); every operation a single fp32 rounding.
+__global__ void nvfp4_quantize_kernel(const bf16* __restrict__ x, int rows, int K, const float* __restrict__ g_ptr,
+                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    pdl_launch();
+    pdl_wait();
+    const int nb = K >> 4;
+    const long long nblk = (long long)rows * nb;
+    const float g = *g_ptr;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nblk;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / nb;
+        const int b = (int)(i - r * nb);
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * K + 16 * b);
+        float f0[8], f1[8], f[16];
+        unpack8(src[0], f0);
+        unpack8(src[1], f1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            f[j] = f0[j];
+            f[8 + j] = f1[j];
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        const uint8_t sc = to_e4m3(__fdiv_rn(amax, __fmul_rn(6.0f, g)));
+        scales[i] = sc;
+        const float step = __fmul_rn(g, e4m3_value(sc));
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[q] = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[q] |= (step > 0.f ? to_e2m1(__fdiv_rn(f[4 * q + e], step)) : 0u) << (8 * e);
+        }
+        *reinterpret_cast<uint4*>(codes + r * K + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // v[i] = 0 (the amax accumulators)
 __global__ void zero_floats_kernel(float* v, int n) {
     pdl_launch();
@@ -88,6 +160,15 @@ unsigned grid_for(long long n8) {
 }
 
 }  // namespace
+
+cudaError_t launch_nvfp4_quantize(const bf16* x, int rows, int K, const float* g, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t st) {
+    const long long nblk = (long long)rows * (K / 16);
+    const int threads = 256;
+    const unsigned grid = (unsigned)std::min<long long>((nblk + threads - 1) / threads, 4LL * device_sm_count());
+    HRA_LAUNCH(nvfp4_quantize_kernel, dim3(grid), dim3(threads), 0, st, x, rows, K, g, codes, scales);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fp8_quantize(const bf16* x, long long n, const float* scale, uint8_t* out, cudaStream_t st) {
     HRA_LAUNCH(fp8_quantize_kernel, dim3(grid_for(n >> 3)), dim3(256), 0, st, x, n, scale, out);

@@ -213,6 +213,9 @@ cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st);
 // ------------------------------------------------------------------ E4M3 quantization (fp8.cu)
 // out = e4m3(x / *scale), n a multiple of 8 (x 16-byte, out 8-byte aligned)
 cudaError_t launch_fp8_quantize(const bf16* x, long long n, const float* scale, uint8_t* out, cudaStream_t st);
+// NVFP4: codes [rows][K] (one E2M1 code per byte), scales [rows][K/16] E4M3; K a multiple of 16
+cudaError_t launch_nvfp4_quantize(const bf16* x, int rows, int K, const float* g, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t st);
 // *amax = max(*amax, max |x|), n a multiple of 8
 cudaError_t launch_absmax(const bf16* x, long long n, float* amax, cudaStream_t st);
 cudaError_t launch_zero_floats(float* v, int n, cudaStream_t st);

@@ -192,4 +192,8 @@ def test_newer_entry_points_reject_bad_arguments_without_cuda(hra):
                              fake, big, 0, None) == -1
     assert L.hra_fp8_calibrate(ctypes.byref(d), ctypes.byref(w), fake, lens5, 1, 5, ctypes.byref(kv), None, fake,
                                fake, big, None) == -1
+    # NVFP4 quantizer: K a multiple of 16, aligned operands
+    assert L.hra_nvfp4_quantize(fake, 4, 24, fake, fake, fake, None) == -1
+    assert L.hra_nvfp4_quantize(fake, 4, 64, ctypes.c_void_p(A + 2), fake, fake, None) == -1
+    assert L.hra_nvfp4_quantize(fake, 0, 64, fake, fake, fake, None) == -1
     assert L.hra_launch_counter() == 0
