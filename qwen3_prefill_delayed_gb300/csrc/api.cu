@@ -655,8 +655,8 @@ int hra_decode_dev(const hra_dims* dims, const hra_weights* weights, const void*
                        workspace, workspace_bytes, stream);
 }
 
-// Codebook-step workspace: error word and per-row counters (cleared by the GEMM), per-row argmax
-// candidates, then the fp32 logit partials.
+// Codebook-step workspace: error word and per-row counters (cleared by the head projection), per-row
+// argmax candidates, then the fp32 logit partials [splits][batch][K * Vc].
 struct CbLayout {
     size_t counters, cand, part;
 };
@@ -677,6 +677,7 @@ size_t hra_codebook_workspace_size(const hra_dims* dims, int32_t batch) {
     g.off = codebook_layout(dims, batch).part;
     const size_t plane = (size_t)batch * N * sizeof(float);
     size_t part = std::max(plane, linear_partial_bound(std::min(batch, 128), N, dims->hidden, EPI_F32));
+    if (batch <= kHeadMaxBatch) part = std::max(part, (size_t)kHeadMaxSplits * plane);
     if (batch > 128) part = std::max(part, linear_tail_bound());
     g.take(part);
     return g.off;
@@ -713,24 +714,41 @@ int codebook_impl(const hra_dims* dims, const void* hidden_dev, const void* head
     const CbLayout CL = codebook_layout(dims, batch);
     unsigned int* err = reinterpret_cast<unsigned int*>(base);
     float* part = reinterpret_cast<float*>(base + CL.part);
+    const double head_flops = 2.0 * batch * (double)K * Vc * H;
 
     int splits = 1;
-    LinearCall c{};
-    c.a = reinterpret_cast<const bf16*>(hidden_dev);
-    c.w = reinterpret_cast<const bf16*>(head_w_dev);
-    c.out = part;
-    c.M = batch;
-    c.N = K * Vc;
-    c.K = H;
-    c.epi = EPI_F32;
-    c.split_req = 0;
-    c.partial = part;
-    c.err = err;
-    c.partial_only = true;
-    c.splits_used = &splits;
-    c.zero_ptr = err;                 // error word + per-row counters
-    c.zero_words = 1 + batch;
-    HRA_TRY(probed(HRA_PROBE_AUDIO_HEAD, 2.0 * batch * (double)K * Vc * H, st, [&] { return launch_linear(c, st); }));
+    if (batch <= kHeadMaxBatch) {
+        // the head as 256-row tiles x K splits; the finalize sums the split planes in order
+        HeadCall hc{};
+        hc.hidden = reinterpret_cast<const bf16*>(hidden_dev);
+        hc.head_w = reinterpret_cast<const bf16*>(head_w_dev);
+        hc.partial = part;
+        hc.err = err;
+        hc.zero_ptr = err;   // error word + per-row counters
+        hc.zero_words = 1 + batch;
+        hc.splits_used = &splits;
+        hc.B = batch;
+        hc.N = K * Vc;
+        hc.H = H;
+        HRA_TRY(probed(HRA_PROBE_AUDIO_HEAD, head_flops, st, [&] { return launch_audio_head(hc, st); }));
+    } else {
+        LinearCall c{};
+        c.a = reinterpret_cast<const bf16*>(hidden_dev);
+        c.w = reinterpret_cast<const bf16*>(head_w_dev);
+        c.out = part;
+        c.M = batch;
+        c.N = K * Vc;
+        c.K = H;
+        c.epi = EPI_F32;
+        c.split_req = 0;
+        c.partial = part;
+        c.err = err;
+        c.partial_only = true;
+        c.splits_used = &splits;
+        c.zero_ptr = err;                 // error word + per-row counters
+        c.zero_words = 1 + batch;
+        HRA_TRY(probed(HRA_PROBE_AUDIO_HEAD, head_flops, st, [&] { return launch_linear(c, st); }));
+    }
 
     CodebookArgs a{};
     a.partial = part;

@@ -1,14 +1,15 @@
 // codebook.cu -- finalize of the per-frame delayed-codebook step.
 //
 // One CTA per (codebook, row) sums the audio-head logit partials (split order) and takes the argmax
-// (lowest index on ties) after adding the optional EOC bias; the last CTA of each row runs the
-// delay-pattern state machine and writes next = bf16(sum over k ascending of fp32
-// code_emb[k][code_k]) with 16-byte loads.  Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141), Summary
-// ("per-frame argmax, delay handling, and codebook embedding accumulation") and Root cause (EOC on
-// any codebook must end the stream, not only on the first).
+// (lowest index on ties) after adding the optional EOC bias; the K CTAs of a row form a thread-block
+// cluster, whose rank 0 runs the delay-pattern state machine, after which every CTA writes 1/K of
+// next = bf16(sum over k ascending of fp32 code_emb[k][code_k]) with 16-byte loads.  Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141),
+// Summary ("per-frame argmax, delay handling, and codebook embedding accumulation") and Root cause
+// (EOC on any codebook must end the stream, not only on the first).
 //
-// The sampled variant (codebook_sample_kernel) replaces the argmax with temperature / top-k /
-// top-p sampling by an exponential race on per-row seeded Philox noise; the per-row tail is shared.
+// The sampled variant (codebook_sample_kernel, one CTA per (codebook, row)) replaces the argmax with
+// temperature / top-k / top-p sampling by an exponential race on per-row seeded Philox noise; the
+// last of a row's CTAs to finish runs the same per-row tail.
 //
 // Delay rule per row (t = frame, e = eoc_frame, codebook k lags k frames):
 //   t < k -> BOS; e >= 0 and t - k >= e -> EOC; otherwise argmax.  If e < 0 and an argmaxed
@@ -24,7 +25,6 @@ namespace hra {
 namespace {
 
 constexpr int kMaxCodebooks = 16;
-constexpr int kThreads = 256;
 constexpr int kMaxSplits = 8;   // the audio-head GEMM splits K at most 8 ways
 
 __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
@@ -34,11 +34,18 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
     }
 }
 
-// The last CTA of row b to finish (all K candidates are in cand[b][*]): the delay state machine on
-// the K candidates, then next = bf16(sum_k fp32 code_emb[k][code_k]), k ascending.
-__device__ void finish_row(const CodebookArgs& a, int b, int tid, int nthreads, int* s_code) {
+// The per-row tail once all K candidates of row b are known (in shared memory `s_cand`, or else in
+// cand[b][*], written by other CTAs), with st = the row's state as read before any CTA of this step
+// could advance it: the delay state machine on the K candidates, then
+// next = bf16(sum_k fp32 code_emb[k][code_k]), k ascending.
+template <int J>
+__device__ void finish_row(const CodebookArgs& a, int b, int tid, int nthreads, int* s_code, const int* s_cand,
+                           int4 st) {
     if (tid == 0) {
-        const int4 st = a.state[b];
+        int am[kMaxCodebooks];   // the K candidates, all requested at once (from L2 when in cand[])
+#pragma unroll
+        for (int kk = 0; kk < kMaxCodebooks; ++kk)
+            if (kk < a.K) am[kk] = s_cand ? s_cand[kk] : __ldcg(a.cand + b * a.K + kk);
         const int t = st.x;
         int e = st.y, done = st.z;
         bool forced[kMaxCodebooks];
@@ -51,11 +58,11 @@ __device__ void finish_row(const CodebookArgs& a, int b, int tid, int nthreads, 
                 code[kk] = a.eoc;
                 forced[kk] = true;
             } else {
-                code[kk] = reinterpret_cast<volatile int*>(a.cand)[b * a.K + kk];
+                code[kk] = am[kk];
                 forced[kk] = false;
             }
         }
-        if (e < 0) {
+    if (e < 0) {
             int cand = INT_MAX;
             for (int kk = 0; kk < a.K; ++kk)
                 if (!forced[kk] && code[kk] == a.eoc && t - kk < cand) cand = t - kk;
@@ -77,46 +84,125 @@ __device__ void finish_row(const CodebookArgs& a, int b, int tid, int nthreads, 
 
     // next = bf16(sum_k fp32(code_emb[k][code_k])), k ascending
     const int nc = a.H >> 3;
-    for (int c = tid; c < nc; c += nthreads) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int kk = 0; kk < a.K; ++kk) {
-            const uint4 u = reinterpret_cast<const uint4*>(a.code_emb + ((long long)kk * a.Vc + s_code[kk]) * a.H)[c];
-            float f[8];
-            unpack8(u, f);
+    for (int c0 = tid; c0 < nc; c0 += J * nthreads) {
+        // J 8-column chunks per thread and eight rows at a time: 8 J rows requested before the
+        // first is added
+        float acc[J][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += f[j];
+        for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+        for (int k0 = 0; k0 < a.K; k0 += 8) {
+            uint4 u[J][8];
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c0 + j * nthreads;
+                    if (k0 + i < a.K && c < nc)
+                        u[j][i] = reinterpret_cast<const uint4*>(
+                            a.code_emb + ((long long)(k0 + i) * a.Vc + s_code[k0 + i]) * a.H)[c];
+                }
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (k0 + i < a.K && c0 + j * nthreads < nc) {
+                        float f[8];
+                        unpack8(u[j][i], f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[j][q] += f[q];
+                    }
+                }
         }
-        reinterpret_cast<uint4*>(a.next_emb + (long long)b * a.H)[c] = pack8(acc);
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int c = c0 + j * nthreads;
+            if (c < nc) reinterpret_cast<uint4*>(a.next_emb + (long long)b * a.H)[c] = pack8(acc[j]);
+        }
     }
 }
 
-// CTA (k, b): codebook k of row b.  The logits of that codebook are the split partials summed in
-// split order; the argmax (lowest index on ties, EOC bias included) goes to cand[b][k].  The last of
-// the row's K CTAs to finish (an atomic count, no waiting) runs the delay state machine on the K
-// candidates and writes next = bf16(sum_k fp32 code_emb[k][code_k]), k ascending.
-__global__ void __launch_bounds__(kThreads) codebook_finalize_kernel(const CodebookArgs a) {
+// Thread-block cluster helpers: the K CTAs of a row form one cluster and exchange the K argmax
+// results and the codes through distributed shared memory, with hardware cluster barriers.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared-memory address of `p` (this CTA's variable) in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_cluster(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Cluster of K CTAs per row b; CTA k (cluster rank k) takes codebook k.  Its logits are the split
+// partials summed in split order (all of a thread's partials are requested before the first is
+// added); the argmax (lowest index on ties, EOC bias included) goes into rank 0's shared memory.
+// After a cluster barrier rank 0 runs the delay state machine and writes the codes, state and done;
+// after a second barrier every CTA reads the codes from rank 0 and gathers 1/K of the hidden columns
+// of next = bf16(sum_k fp32 code_emb[k][code_k]), k ascending.  No global atomics, fences or
+// hand-offs through memory: spreading a row over K CTAs keeps each CTA's share of the partials
+// small, and the cluster keeps the row's tail on chip.
+constexpr int kFinThreads = 256;
+constexpr int kFinPer = 5;   // entries per thread in one pass (codebook_size <= 1280 in one pass)
+__global__ void __launch_bounds__(kFinThreads, 4) codebook_finalize_kernel(const CodebookArgs a) {
     pdl_launch();
     pdl_wait();
-    const int k = blockIdx.x, b = blockIdx.y;
+    __shared__ float s_bv[kFinThreads / 32];
+    __shared__ int s_bi[kFinThreads / 32];
+    __shared__ int s_am[kMaxCodebooks];     // rank 0: argmax of every codebook
+    __shared__ int s_code[kMaxCodebooks];   // rank 0: the codes; elsewhere: a copy
+    const int k = (int)cluster_rank(), b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KV = a.K * a.Vc;
     const long long split_stride = (long long)a.batch * KV;
     const float* base = a.partial + (long long)b * KV + (long long)k * a.Vc;
     const float bias = a.eoc_bias ? a.eoc_bias[b * a.K + k] : 0.f;
+    const int4 st = k == 0 ? a.state[b] : make_int4(0, 0, 0, 0);
 
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for (int v = tid; v < a.Vc; v += kThreads) {
-        float part[kMaxSplits];
+    for (int v0 = 0; v0 < a.Vc; v0 += kFinThreads * kFinPer) {
+        float x[kFinPer];
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) part[s] = s < a.splits ? base[s * split_stride + v] : 0.f;
-        float x = 0.f;
+        for (int i = 0; i < kFinPer; ++i) x[i] = 0.f;
+        for (int s0 = 0; s0 < a.splits; s0 += 4) {
+            float part[4][kFinPer];
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s)
-            if (s < a.splits) x += part[s];
-        if (a.logits_out) a.logits_out[((long long)b * a.K + k) * a.Vc + v] = x;
-        if (v == a.eoc && a.eoc_bias) x = x + bias;
-        better(bv, bi, x, v);
+            for (int h = 0; h < 4; ++h)
+#pragma unroll
+                for (int i = 0; i < kFinPer; ++i) {
+                    const int v = v0 + tid + i * kFinThreads;
+                    part[h][i] = (s0 + h < a.splits && v < a.Vc) ? base[(s0 + h) * split_stride + v] : 0.f;
+                }
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+#pragma unroll
+                for (int i = 0; i < kFinPer; ++i)
+                    if (s0 + h < a.splits) x[i] += part[h][i];
+        }
+#pragma unroll
+        for (int i = 0; i < kFinPer; ++i) {
+            const int v = v0 + tid + i * kFinThreads;
+            if (v < a.Vc) {
+                if (a.logits_out) a.logits_out[((long long)b * a.K + k) * a.Vc + v] = x[i];
+                const float y = (v == a.eoc && a.eoc_bias) ? x[i] + bias : x[i];
+                better(bv, bi, y, v);
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -124,10 +210,6 @@ __global__ void __launch_bounds__(kThreads) codebook_finalize_kernel(const Codeb
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         better(bv, bi, ov, oi);
     }
-    __shared__ float s_bv[kThreads / 32];
-    __shared__ int s_bi[kThreads / 32];
-    __shared__ int s_last;
-    __shared__ int s_code[kMaxCodebooks];
     if (lane == 0) {
         s_bv[warp] = bv;
         s_bi[warp] = bi;
@@ -136,19 +218,77 @@ __global__ void __launch_bounds__(kThreads) codebook_finalize_kernel(const Codeb
     if (tid == 0) {
         float fv = s_bv[0];
         int fi = s_bi[0];
-        for (int w = 1; w < kThreads / 32; ++w) better(fv, fi, s_bv[w], s_bi[w]);
+        for (int w = 1; w < kFinThreads / 32; ++w) better(fv, fi, s_bv[w], s_bi[w]);
         if (fi < 0 || fi >= a.Vc) {   // only when every logit was NaN
             raise_error(a.err, HRA_DEVERR_CODE_RANGE);
             fi = 0;
         }
-        a.cand[b * a.K + k] = fi;
-        __threadfence();
-        s_last = atomicAdd(&a.counters[b], 1) == a.K - 1;
+        st_cluster(cluster_addr(&s_am[k], 0), fi);
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    finish_row(a, b, tid, kThreads, s_code);
+    cluster_sync();
+    if (k == 0 && tid == 0) {
+        const int t = st.x;
+        int e = st.y, done = st.z;
+        bool forced[kMaxCodebooks];
+        int code[kMaxCodebooks];
+        for (int kk = 0; kk < a.K; ++kk) {
+            if (t < kk) {
+                code[kk] = a.bos;
+                forced[kk] = true;
+            } else if (e >= 0 && t - kk >= e) {
+                code[kk] = a.eoc;
+                forced[kk] = true;
+            } else {
+                code[kk] = s_am[kk];
+                forced[kk] = false;
+            }
+        }
+        if (e < 0) {
+            int cand = INT_MAX;
+            for (int kk = 0; kk < a.K; ++kk)
+                if (!forced[kk] && code[kk] == a.eoc && t - kk < cand) cand = t - kk;
+            if (cand != INT_MAX) {
+                e = cand;
+                for (int kk = 0; kk < a.K; ++kk)
+                    if (t >= kk && t - kk >= e) code[kk] = a.eoc;
+            }
+        }
+        if (e >= 0 && t >= e + a.K - 1) done = 1;
+        for (int kk = 0; kk < a.K; ++kk) {
+            s_code[kk] = code[kk];
+            a.codes[b * a.K + kk] = code[kk];
+        }
+        a.state[b] = make_int4(t + 1, e, done, 0);
+        a.done[b] = done;
+    }
+    cluster_sync();
+    if (k != 0 && tid < a.K) s_code[tid] = ld_cluster(cluster_addr(&s_code[tid], 0));
+    cluster_sync();   // rank 0's shared memory is not read after this point
+    // this CTA's share of the hidden columns: chunks [c0, c1) of 8 columns
+    const int nc = a.H >> 3;
+    const int per = (nc + a.K - 1) / a.K;
+    const int c0 = k * per, c1 = min(nc, c0 + per);
+    for (int c = c0 + tid; c < c1; c += kFinThreads) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k0 = 0; k0 < a.K; k0 += 8) {
+            uint4 u[8];   // eight rows requested before the first is added
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (k0 + i < a.K)
+                    u[i] = reinterpret_cast<const uint4*>(a.code_emb +
+                                                          ((long long)(k0 + i) * a.Vc + s_code[k0 + i]) * a.H)[c];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (k0 + i < a.K) {
+                    float f[8];
+                    unpack8(u[i], f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] += f[q];
+                }
+            }
+        }
+        reinterpret_cast<uint4*>(a.next_emb + (long long)b * a.H)[c] = pack8(acc);
+    }
 }
 
 // ------------------------------------------------------------------ sampled step
@@ -163,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) codebook_finalize_kernel(const Codeb
 
 constexpr int kSampleThreads = 1024;
 constexpr int kSortN = 2048;   // entries sorted per codebook (codebook_size <= kSortN)
+constexpr int kFastKeep = 256; // top-k sets up to this size are sorted alone (no full sort)
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
 // SC 2011): ten rounds of (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
@@ -218,6 +359,10 @@ __global__ void __launch_bounds__(kSampleThreads) codebook_sample_kernel(const C
     const int k = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     __shared__ unsigned long long s_key[kSortN];
+    __shared__ unsigned long long s_list[kFastKeep];
+    __shared__ unsigned int s_hist[256];
+    __shared__ int s_sel[2];
+    __shared__ int s_cnt;
     __shared__ float s_red[32];
     __shared__ int s_redi[32];
     __shared__ int s_last;
@@ -226,36 +371,126 @@ __global__ void __launch_bounds__(kSampleThreads) codebook_sample_kernel(const C
     const long long split_stride = (long long)a.batch * KV;
     const float* base = a.partial + (long long)b * KV + (long long)k * a.Vc;
     const float bias = a.eoc_bias ? a.eoc_bias[b * a.K + k] : 0.f;
-    const int frame = a.state[b].x;   // read before the row's last CTA advances the state
+    const int4 st0 = a.state[b];      // read before the row's last CTA advances the state
+    const int frame = st0.x;
     const uint64_t seed = a.seeds[b];
 
-    // z and the sort keys (padding sorts last)
-    for (int v = tid; v < kSortN; v += kSampleThreads) {
+    // z and the sort keys: ascending keys = z descending, then index ascending (padding sorts last)
+    uint32_t mine[2] = {0u, 0u};   // order-preserving bits of z of entries tid, tid + 1024 (0: none)
+    float xs[2] = {0.f, 0.f};      // the two entries' logits: all partials requested before any is added
+    for (int s0 = 0; s0 < a.splits; s0 += 4) {
+        float part[4][2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int v = tid + h * kSampleThreads;
+                part[q][h] = (s0 + q < a.splits && v < a.Vc) ? base[(s0 + q) * split_stride + v] : 0.f;
+            }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (s0 + q < a.splits) xs[h] += part[q][h];
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = tid + h * kSampleThreads;
         unsigned long long key = ~0ull;
         if (v < a.Vc) {
-            float x = 0.f;
-            for (int sp = 0; sp < a.splits; ++sp) x += base[sp * split_stride + v];
+            float x = xs[h];
             if (a.logits_out) a.logits_out[((long long)b * a.K + k) * a.Vc + v] = x;
             if (v == a.eoc && a.eoc_bias) x = x + bias;
             float z = x / a.temperature;
             if (z != z) z = -INFINITY;
-            key = ((unsigned long long)(~sortable(z)) << 32) | (uint32_t)v;
+            if (z == 0.f) z = 0.f;   // -0 sorts with +0 (equal values tie on the index)
+            mine[h] = sortable(z);
+            key = ((unsigned long long)(~mine[h]) << 32) | (uint32_t)v;
         }
         s_key[v] = key;
     }
     __syncthreads();
-    // bitonic sort, ascending keys; thread t compares the pair (i, i + stride)
-    for (int size = 2; size <= kSortN; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int i = 2 * tid - (tid & (stride - 1));
-            const int j = i + stride;
-            const bool up = (i & size) == 0;
-            const unsigned long long x = s_key[i], y = s_key[j];
-            if ((x > y) == up) {
-                s_key[i] = y;
-                s_key[j] = x;
+    // Top-k without sorting every entry: select the top_k-th largest z by its bits, eight at a time
+    // (a 256-bin histogram of the entries that match the bits chosen so far), keep every entry at
+    // or above it, and sort only those.  The kept prefix is then exactly the one a full sort gives.
+    // Top-k off, or more than kFastKeep entries at or above the threshold: the full sort below.
+    bool sorted = false;
+    if (a.top_k > 0 && a.top_k < a.Vc) {
+        uint32_t prefix = 0u, pmask = 0u;
+        int need = a.top_k;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            if (tid < 256) s_hist[tid] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (mine[h] != 0u && (mine[h] & pmask) == prefix) atomicAdd(&s_hist[(mine[h] >> shift) & 255u], 1u);
+            __syncthreads();
+            if (warp == 0) {
+                // lane l holds bins 8l .. 8l + 7; `above` = entries in the bins above a bin
+                unsigned int c[8], tot = 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = s_hist[8 * lane + i];
+                    tot += c[i];
+                }
+                unsigned int suf = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned int y = __shfl_down_sync(0xffffffffu, suf, o);
+                    if (lane + o < 32) suf += y;
+                }
+                unsigned int above = suf - tot;
+#pragma unroll
+                for (int i = 7; i >= 0; --i) {
+                    if (above < (unsigned)need && (unsigned)need <= above + c[i]) {
+                        s_sel[0] = 8 * lane + i;
+                        s_sel[1] = need - (int)above;
+                    }
+                    above += c[i];
+                }
             }
             __syncthreads();
+            prefix |= (uint32_t)s_sel[0] << shift;
+            pmask |= 255u << shift;
+            need = s_sel[1];
+        }
+        const int n_keep = __syncthreads_count(mine[0] >= prefix) + __syncthreads_count(mine[1] >= prefix);
+        if (n_keep <= kFastKeep) {
+            if (tid == 0) s_cnt = 0;
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (mine[h] >= prefix)
+                    s_list[atomicAdd(&s_cnt, 1)] =
+                        ((unsigned long long)(~mine[h]) << 32) | (uint32_t)(tid + h * kSampleThreads);
+            __syncthreads();
+            s_key[tid] = ~0ull;
+            s_key[tid + kSampleThreads] = ~0ull;
+            __syncthreads();
+            if (tid < n_keep) {
+                const unsigned long long me = s_list[tid];
+                int rank = 0;
+                for (int j = 0; j < n_keep; ++j) rank += s_list[j] < me ? 1 : 0;
+                s_key[rank] = me;
+            }
+            __syncthreads();
+            sorted = true;
+        }
+    }
+    if (!sorted) {
+        // bitonic sort, ascending keys; thread t compares the pair (i, i + stride)
+        for (int size = 2; size <= kSortN; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const int i = 2 * tid - (tid & (stride - 1));
+                const int j = i + stride;
+                const bool up = (i & size) == 0;
+                const unsigned long long x = s_key[i], y = s_key[j];
+                if ((x > y) == up) {
+                    s_key[i] = y;
+                    s_key[j] = x;
+                }
+                __syncthreads();
+            }
         }
     }
     const float z0 = key_z(s_key[0]);
@@ -352,7 +587,7 @@ __global__ void __launch_bounds__(kSampleThreads) codebook_sample_kernel(const C
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    finish_row(a, b, tid, kSampleThreads, s_code);
+    finish_row<1>(a, b, tid, kSampleThreads, s_code, nullptr, st0);
 }
 
 }  // namespace
@@ -363,7 +598,33 @@ cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st) {
         if (a.Vc > kSortN) return cudaErrorInvalidValue;
         HRA_LAUNCH(codebook_sample_kernel, dim3(a.K, a.batch), dim3(kSampleThreads), 0, st, a);
     } else {
-        HRA_LAUNCH(codebook_finalize_kernel, dim3(a.K, a.batch), dim3(kThreads), 0, st, a);
+        // one cluster of K CTAs per row (K <= 8 portable; up to 16 with the non-portable opt-in)
+        static bool configured[64] = {false};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (a.K > 8 && (dev < 0 || dev >= 64 || !configured[dev])) {
+            e = cudaFuncSetAttribute(codebook_finalize_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) configured[dev] = true;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.K, a.batch);
+        cfg.blockDim = dim3(kFinThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = a.K;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        count_launches(1);
+        e = cudaLaunchKernelEx(&cfg, codebook_finalize_kernel, a);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -1372,6 +1372,10 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
 
 }  // namespace
 
+bool make_map_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    return get_encoder() && make_map(m, base, rows, cols, box_rows, 2);
+}
+
 bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
                        const uint32_t* box) {
     if (!get_encoder() || rank < 1 || rank > 5) return false;

@@ -210,6 +210,33 @@ struct CodebookArgs {
 };
 cudaError_t launch_codebook_finalize(const CodebookArgs& a, cudaStream_t st);
 
+// ------------------------------------------------------------------ audio-head projection, batch <= 128 (head.cu)
+constexpr int kHeadMaxBatch = 128;
+constexpr int kHeadMaxSplits = 8;
+
+// Work split of the head: nt tiles of 256 weight rows x `splits` K ranges of kbps 64-wide blocks.
+struct HeadPlan {
+    int nt, splits, kbps;
+};
+HeadPlan head_plan(int N, int H);
+
+// partial[split][b][n] = sum over the split's K range of hidden[b][k] * head_w[n][k] (fp32).
+struct HeadCall {
+    const bf16* hidden;         // [B, H]
+    const bf16* head_w;         // [N, H]
+    float* partial;             // [splits][B][N]
+    unsigned int* err;
+    unsigned int* zero_ptr;     // cleared by the first CTA once the kernels ahead have finished
+    int zero_words;
+    int* splits_used;           // optional: receives the number of K splits
+    int B, N, H;
+};
+cudaError_t launch_audio_head(const HeadCall& c, cudaStream_t st);
+
+// 2-D bf16 tensor map [rows, cols] (cols innermost), 64-element x box_rows boxes, 128-byte
+// swizzle; encodings are cached by (base, shape, box).
+bool make_map_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
+
 // ------------------------------------------------------------------ E4M3 quantization (fp8.cu)
 // out = e4m3(x / *scale), n a multiple of 8 (x 16-byte, out 8-byte aligned)
 cudaError_t launch_fp8_quantize(const bf16* x, long long n, const float* scale, uint8_t* out, cudaStream_t st);

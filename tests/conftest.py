@@ -17,3 +17,19 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the parity records of this session (tests/parity.py AUDIT) as JSON: to
+    $HRA_PARITY_AUDIT, else gpurun_out/parity_audit.json under the repository root."""
+    try:
+        import parity
+    except Exception:
+        return
+    if not parity.AUDIT:
+        return
+    import json
+    path = os.environ.get("HRA_PARITY_AUDIT") or os.path.join(ROOT, "gpurun_out", "parity_audit.json")
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    with open(path, "w") as f:
+        json.dump(parity.AUDIT, f, indent=0)
