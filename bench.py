@@ -323,14 +323,21 @@ def main():
     ms_step = ms / args.steps
     value = whole_job_rate(world, tokens_per_step, ms_step / 1e3)
 
-    # roofline of the dominant kernel: the gate/up + SwiGLU projection of the full prefill layers
+    # roofline of the dominant kernel: the gate/up + SwiGLU projection of the full prefill layers.
+    # The timed region is sub-second and the box holds its full clock through it, so the peak is the
+    # measured burst bf16 rate; the sustained-peak and clock-normalised fractions are given beside it.
     gu_ms = probe_ms / max(probe_n, 1)
     gu_flops = probe_flops / max(probe_n, 1)
     achieved = gu_flops / (gu_ms / 1e3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sm_max = peaks.get("sm_max_mhz") or (clk or {}).get("sm_max_mhz")
+    sm_run = (clk or {}).get("sm_mhz")
     roofline = {"bound": "tensor", "kernel": "gemm_bf16_tc_kernel<256,SwiGLU> (gate/up, full layers)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"{peaks_kind} bf16 sustained",
+                "peak_kind": f"{peaks_kind} bf16 burst",
+                "frac_of_sustained": achieved / sustained,
+                "frac_at_max_clock": (achieved * sm_max / sm_run / peak) if sm_max and sm_run else None,
                 "traffic": traffic_for("gate_up", ["qwen3_prefill_delayed_gb300/csrc/gemm_tc.cu"]),
                 "launch_ms": gu_ms, "flops_per_launch": gu_flops, "launches_timed": probe_n}
 
@@ -370,11 +377,12 @@ def main():
             def getter(n):
                 return {"embed": w["embed"].cpu(), "final_norm": w["final_norm"].cpu(),
                         "layers": [{k: v.cpu() for k, v in w["layers"][i].items()} for i in range(n)]}
-            t_s, toks = oracle_sample(d, getter, p, 2, seq)
-            cpu_baseline = {"value": toks / (t_s * 18), "unit": "tokens/s", "cores": oracle.max_threads(),
+            oracle.set_threads(oracle.max_threads())
+            t_s, toks = oracle_sample(d, getter, p, d.n_layers, seq)
+            cpu_baseline = {"value": toks / t_s, "unit": "tokens/s", "cores": oracle.max_threads(),
                             "kind": "oracle",
-                            "sample": f"oracle prefill of the median prompt ({toks} tokens) through 2 of 36 layers "
-                                      f"({t_s:.1f} s); tokens/s scaled by 2/36"}
+                            "sample": f"oracle prefill of the median prompt ({toks} tokens) through all "
+                                      f"{d.n_layers} layers ({t_s:.1f} s), OpenMP over all host cores"}
         except Exception as ex:   # the baseline is reported, never required
             cpu_baseline = {"error": repr(ex)}
     del cache
@@ -445,7 +453,74 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
     except Exception as ex:
         out["long_prompts"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
+    # ---- the CPU oracle on each configuration's workload (single thread and all host cores)
+    try:
+        out["oracle_timing"] = bench_oracle_configs(W)
+    except Exception as ex:
+        out["oracle_timing"] = {"error": repr(ex)}
     return out
+
+
+def bench_oracle_configs(W):
+    """The oracle as it stands, timed on the host cores for each configuration's workload: the tiny
+    model's whole run and one full-width layer at P = 6 / 13 single-threaded; the codebook step at
+    batch 1 single-threaded and at 1 / 32 / 64 on all cores; the long-prompt workload as one prompt
+    of 1024 tokens through one layer on all cores (a stated subset, scaled per layer)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    ncore = oracle.max_threads()
+    res = {"cores_all": ncore}
+
+    def timed(fn, threads):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        r = fn()
+        return time.perf_counter() - t0, r
+
+    # tiny model: P = 13 prefill, then 6 frames of codebook step + decode pass (2 layers, K = 4)
+    wl = W.tiny_reference("cpu")
+    d, pr = wl["dims"], wl["prompts"]
+    hw = oracle.host_weights_from(d, wl["weights"])
+    head_u, tab_u = W.to_u16(wl["audio"]["head_w"]), W.to_u16(wl["audio"]["code_emb"])
+
+    def tiny_run():
+        kv, h = oracle.prefill(d, hw, pr.tokens.numpy(), pr.lengths, wl["n_slots"])
+        st = np.array([[0, -1, 0, 0]], np.int32)
+        for t in range(wl["frames"]):
+            _, nxt, _, _ = oracle.codebook_step(d, h, head_u, tab_u, st, wl["eoc_bias"][t].numpy())
+            h = oracle.decode(d, hw, nxt, [pr.lengths[0] + t], kv, wl["n_slots"])
+    t1, _ = timed(tiny_run, 1)
+    res["tiny_prefill13_plus_6_frames"] = {"threads": 1, "seconds": t1}
+    # one full-width layer, batch 1, P = 6 and 13
+    sl = W.single_layer(13, "cpu")
+    ds = sl["dims"]
+    hws = oracle.host_weights_from(ds, sl["weights"])
+    for P in (6, 13):
+        pp = W.make_prompts(1, 1, P, P, ds.vocab, fixed_len=P)
+        for thr in (1, ncore):
+            t, _ = timed(lambda: oracle.prefill(ds, hws, pp.tokens.numpy(), pp.lengths, 2048), thr)
+            res[f"single_layer_P{P}_threads{thr}"] = {"ms_per_layer": t * 1e3}
+    del hws, sl
+    # codebook step: head [8 x 1026, 2560], 8 tables
+    dc = W.full_dims(0)
+    au = W.make_audio(dc, W._gen(3, "cpu"), "cpu")
+    hu, tu = W.to_u16(au["head_w"]), W.to_u16(au["code_emb"])
+    for B, thr in ((1, 1), (1, ncore), (32, ncore), (64, ncore)):
+        ch = W.make_decode_chain(dc, 3, B, 1)
+        st = ch.state0.numpy().copy()
+        t, _ = timed(lambda: oracle.codebook_step(dc, W.to_u16(ch.hidden[0]), hu, tu, st, ch.eoc_bias[0].numpy()), thr)
+        res[f"codebook_B{B}_threads{thr}"] = {"seconds_per_step": t, "frames_per_s": B / t}
+    # long prompts: one 1024-token prompt through one full-width layer, all cores
+    dl = W.full_dims(1)
+    wlay = W.make_backbone(dl, 4, "cpu")
+    hwl = oracle.host_weights_from(dl, wlay)
+    pl = W.make_prompts(4, 1, 1024, 1024, dl.vocab, fixed_len=1024)
+    t, _ = timed(lambda: oracle.prefill(dl, hwl, pl.tokens.numpy(), pl.lengths, 1024), ncore)
+    res["long_prompt_1024_one_layer_threads_all"] = {"seconds": t, "tokens_per_s_36_layers": 1024 / (t * 36)}
+    oracle.set_threads(ncore)
+    return res
 
 
 def bench_codebook(hra, W, torch, dev, hbm, peaks_kind):
@@ -550,8 +625,8 @@ def bench_chunked(hra, W, torch, dev, w_backbone):
 def bench_fp8(hra, W, torch, dev, w_backbone, peaks):
     """FP8 (E4M3) projections with static activation scales calibrated on a fixed calibration batch
     (4 prompts of 64 tokens, their own seed), then the ragged batch's prefill; the gate/up GEMM is
-    reported against the FP8 peak = the measured bf16 sustained peak x 2 (the nominal dense
-    FP8 / BF16 tensor-rate ratio of the part)."""
+    reported against the FP8 peak = the measured bf16 burst peak x 2 (the nominal dense FP8 / BF16
+    tensor-rate ratio of the part)."""
     d = W.full_dims(36)
     p = W.make_prompts(2, 32, 16, 256, d.vocab)
     bb = hra.Backbone(d, w_backbone)
@@ -574,7 +649,7 @@ def bench_fp8(hra, W, torch, dev, w_backbone, peaks):
     run()
     hra.hra_probe_select("none")
     gu_ms, gu_n, gu_flops = hra.hra_probe_collect()
-    peak8 = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak8 = 2.0 * peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     tf = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
     del cache, f8
     return {"prefill_tokens_per_s": p.total / (ms / 1e3), "prefill_ms": ms, "bf16_prefill_ms": ms16,

@@ -6,17 +6,18 @@
  *      RMSNorm, merged QKV projection, per-head q/k RMSNorm + RoPE with the KV-cache write, causal
  *      attention over the used keys of ragged prompts, o-projection, residual + RMSNorm, SwiGLU
  *      gate/up/down MLP -- returning the last position's final hidden and the filled cache.
- *      Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141), Summary
- *      ("kernelize the Higgs BF16 batched prefill path for embedding lookup, projection GEMMs,
- *      q/k norm + RoPE, and KV writes"); the per-layer chain and the used-key rule follow
- *      "flashrt-structures 0.2.0, prefill_tower/fp8_chain.py", module docstring and run().
+ *      Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141), Summary (the
+ *      BF16 batched prefill is kernelized: embedding lookup, projection GEMMs, q/k norm + RoPE
+ *      and the KV writes); the per-layer chain and the used-key rule follow the
+ *      "flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its description and its
+ *      per-layer chain.
  *   2. hra_codebook_step: per-frame delayed-codebook step -- audio-head projection to K codebook
  *      logit rows, per-codebook argmax under the delay pattern, BOS/EOC handling with stop flags,
  *      and the sum of the K codebook embeddings into the next input.
- *      Source: FlashRT PR #141, Summary ("shared delayed-codebook helper for per-frame argmax,
- *      delay handling, and codebook embedding accumulation") and Root cause (delayed EOC).
+ *      Source: FlashRT PR #141, Summary (one shared delayed-codebook helper takes the per-frame
+ *      argmax, applies the delays and sums the codebook embeddings) and Root cause (delayed EOC).
  * hra_decode is the single-token backbone pass of the autoregressive audio loop (FlashRT PR #141,
- * Performance: "AR decode ms/frame"); its input is the summed codebook embedding.
+ * Performance: the AR decode time per frame); its input is the summed codebook embedding.
  *
  * Conventions for every entry point:
  *   - Pointers named *_dev / device buffers are CUDA device pointers owned by the caller; the
@@ -262,8 +263,12 @@ int hra_ar_frame(const hra_dims* dims, const hra_weights* weights, const void* h
  *   - Limit: accepted while hra_codebook_workspace_size(dims, batch) <= 32 MiB (batch <= 127 for
  *     8 codebooks x 1026 entries at hidden 2560); larger requests return HRA_ERR_WORKSPACE and
  *     enqueue nothing.
- *   - The first call on a device looks up the scratch address for that device; make that first
- *     call before any stream capture.
+ *   - The first call on a device loads the scratch for that device (CUDA loads the module that
+ *     holds it on first use, which reserves the 32 MiB then) and looks up its address: make one
+ *     warm-up call outside any deadline path and before any stream capture.
+ *   - Device error bits (HRA_DEVERR_*) are not reported: they land in the private scratch, which no
+ *     caller can pass to hra_device_error.  A caller that needs them uses hra_codebook_step with a
+ *     workspace of its own.
  *   - Every call on a device shares the one scratch array, which keeps the last call's contents;
  *     the step clears its error word and overwrites every partial it reads.  Calls that overlap on
  *     the GPU (different streams without ordering) race on the scratch and must be serialised by
@@ -291,7 +296,8 @@ int hra_linear(const void* a_dev, const void* w_dev, void* out_dev, int32_t M, i
                void* stream);
 
 /* ---- static-FP8 variant of the prefill projections ------------------------------------------ */
-/* The FP8 band of the prefill chain ("fp8_chain.py", module docstring: RMSNorm->FP8, merged-QKV,
+/* The FP8 band of the prefill chain ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its
+ * description: RMSNorm then FP8, merged-QKV,
  * output, gate/up and down FP8 GEMMs with static activation scales; "Stabilize Higgs Audio
  * termination and prefill", Summary: activation scales calibrated on a fixed prompt):
  *   weights      w8 = e4m3(w / s_w) with one per-tensor scale s_w = max|w| / 448;
@@ -318,15 +324,17 @@ int hra_fp8_quantize_weight(const void* w_dev, int64_t n, void* w8_dev, float* s
 int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void* x8_dev, void* stream);
 
 /* ---- NVFP4 quantization (the FP4 band of the prefill chain) ---------------------------------- */
-/* The chain's FP4 band ("fp8_chain.py", BANDS: the FFN pair and the output projection "ride NVFP4
- * with dynamic block scales") in NVIDIA's published NVFP4 format: each block of 16 consecutive
+/* The chain's FP4 band (the fp8_chain page, its precision bands: the FFN pair and the output
+ * projection in NVFP4, with block scales computed from the data) in NVIDIA's published NVFP4 format: each block of 16 consecutive
  * elements along K of x_dev bf16 [rows, K] gets the E4M3 scale s = e4m3(amax_block / (6 g)) and
  * the FP4 E2M1 codes e2m1(x / (g * s)) (all 0 when g * s is 0), g = *g_dev the tensor's fp32
  * global scale (e.g. max|x| / (6 * 448)); e2m1() rounds to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4,
  * 6 (ties to the even mantissa) and saturates at +-6; each step is one fp32 rounding.
  *   codes_dev   uint8 [rows, K]: one E2M1 code per byte (sign in bit 3), 16-byte aligned.
  *   scales_dev  uint8 [rows, K / 16]: E4M3 block scales.
- * K a multiple of 16, x_dev 16-byte aligned, g_dev 4-byte aligned (else HRA_ERR_INVALID_ARG). */
+ * K a multiple of 16, x_dev 16-byte aligned, g_dev 4-byte aligned (else HRA_ERR_INVALID_ARG).
+ * *g_dev must be finite and > 0 (it is device memory, so this is not checked): with any other value
+ * the codes and scales are unspecified. */
 int hra_nvfp4_quantize(const void* x_dev, int32_t rows, int32_t K, const float* g_dev, void* codes_dev,
                        void* scales_dev, void* stream);
 

@@ -11,7 +11,8 @@
  *     projection, per-head q/k RMSNorm + rotate-half RoPE with the KV-cache write, causal GQA
  *     attention over the used keys, o-projection + residual, RMSNorm, SwiGLU MLP + residual,
  *     final RMSNorm at the last used position ("Stabilize Higgs Audio termination and prefill",
- *     Summary; "flashrt_structures/impls/prefill_tower/fp8_chain.py", module docstring and run());
+ *     Summary; "flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its description and its
+ *     per-layer chain);
  *   - the single-token decode pass through the same layers, fed an embedding;
  *   - the per-frame delayed-codebook step: audio-head logits, per-codebook argmax under the delay
  *     pattern with BOS/EOC handling and stop flags, and the sum of the K codebook embeddings
@@ -19,10 +20,10 @@
  *   - the same step with each codebook sampled (temperature, top-k, top-p, exponential race on
  *     per-row seeded Philox4x32-10 noise; vLLM-Omni PR #8226, Purpose and Test Plan);
  *   - the static-FP8 variant of the prefill projections (E4M3 weights with per-tensor scales,
- *     inputs quantized with calibrated static scales) and that calibration ("fp8_chain.py",
- *     module docstring; "Stabilize Higgs Audio termination and prefill", Summary);
+ *     inputs quantized with calibrated static scales) and that calibration (the fp8_chain page,
+ *     its description; "Stabilize Higgs Audio termination and prefill", Summary);
  *   - the NVFP4 codec and block-scaled linear of the chain's FP4 band (E2M1 elements, one E4M3
- *     scale per 16-element block, one fp32 global scale; "fp8_chain.py", BANDS).
+ *     scale per 16-element block, one fp32 global scale; the fp8_chain page, its precision bands).
  *
  * Arithmetic: fp32 on bf16-rounded weights and activations.  Values are rounded to bf16
  * (round-to-nearest-even) at these points and nowhere else: every RMSNorm output, the QKV
@@ -101,12 +102,12 @@ void oracle_set_threads(int n) {
 /* ---------------------------------------------------------------- RMSNorm */
 
 /* y[r] = bf16((x[r] * (1/sqrt(ss/n + eps))) * g), ss = sum_squares(x[r]), per row of n.
- * Source: RMSNorm before each projection and the final norm ("fp8_chain.py", run(): the final
+ * Source: RMSNorm before each projection and the final norm (the fp8_chain page, its per-layer chain: the final
  * hidden is fin * rsqrt(mean(fin^2) + eps) * final_w). */
 /* Sum of squares of n bf16 values as the fp32 rounding of the exact sum: each square of a bf16
  * value is exact in double and the double sum carries ~2^-53 relative error, so the result does not
  * depend on any summation order (the CUDA path reaches the same fp32 value by compensated
- * summation).  This is the "mean(x^2)" of RMSNorm evaluated once, correctly rounded. */
+ * summation).  This is the mean of squares of RMSNorm evaluated once, correctly rounded. */
 static float sum_squares(const uint16_t* x, int n) {
     double s = 0.0;
     for (int i = 0; i < n; ++i) s += (double)bf(x[i]) * (double)bf(x[i]);
@@ -178,8 +179,8 @@ void oracle_rope_table(int n_pos, int hd, double theta, float* cos_t, float* sin
 
 /* One head: RMSNorm over hd with gain g (kept fp32), then rotate-half RoPE at position pos,
  * rounded once to bf16.  Source: per-head q/k norm + RoPE before the cache write ("Stabilize Higgs
- * Audio termination and prefill", Summary: "q/k norm + RoPE, and KV writes"; "fp8_chain.py":
- * keys kept in host rotate-half layout in the cache). */
+ * Audio termination and prefill", Summary: q/k norm, RoPE and the KV writes belong to the
+ * kernelized prefill; the fp8_chain page: keys kept in host rotate-half layout in the cache). */
 static void head_norm_rope(const uint16_t* x, const uint16_t* g, int hd, float eps,
                            const float* cos_p, const float* sin_p, uint16_t* out) {
     float xn[256];
@@ -216,8 +217,8 @@ void oracle_qk_norm_rope(const uint16_t* x, const uint16_t* g, const int32_t* po
  *   kc  [nkv][n_slots][hd], vc [nkv][n_slots][hd]   one sequence's cache for one layer
  *   out [n][nq*hd]    bf16(sum_j p_j v_j / sum_j p_j), p_j = exp(s_j - max s), s_j = q.k_j / sqrt(hd)
  *   probs (optional) [n][nq][n_keys_max]: the normalised probabilities (fp32), zeros past pos.
- * Source: dense attention "over exactly the used keys" with trailing pads ("fp8_chain.py", module
- * docstring and _prefill_mask_facts); causal because the backbone is a decoder. */
+ * Source: dense attention over the used keys only, with trailing pads (the fp8_chain page, its
+ * description and its mask check); causal because the backbone is a decoder. */
 void oracle_attend(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, int n_slots,
                    int q_pos0, int n, int nq, int nkv, int hd, uint16_t* out,
                    float* probs, int n_keys_max) {
@@ -272,7 +273,7 @@ void oracle_attend(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, in
  * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.  Encoding rounds to the
  * nearest code, ties to an even mantissa, and saturates finite overflow to +-448 (the satfinite
  * conversion); NaN stays NaN.  Source: the static-FP8 chain's E4M3 weights and activations
- * ("fp8_chain.py", module docstring: RMSNorm->FP8, FP8 GEMMs, FP8_MAX). */
+ * (the fp8_chain page, its description: RMSNorm then FP8, the FP8 GEMMs and the E4M3 maximum). */
 float oracle_e4m3_decode(uint8_t c) {
     const int sgn = c >> 7, E = (c >> 3) & 15, M = c & 7;
     if (E == 15 && M == 7) return NAN;
@@ -345,8 +346,8 @@ void oracle_linear_fp8(const uint8_t* x8, const uint8_t* w8, int T, int N, int K
 /* FP4 E2M1: 1 sign bit (bit 3), 2 exponent bits (bias 1), 1 mantissa bit.  Exponent field 0 is
  * subnormal, m * 0.5; otherwise (1 + m/2) * 2^(e-1): the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
  * No infinity or NaN.  Encoding rounds to the nearest value, ties to the even mantissa, and
- * saturates beyond 6 to +-6.  Source: the NVFP4 band of the prefill chain ("fp8_chain.py", BANDS:
- * the FFN pair and the output projection "ride NVFP4 with dynamic block scales"); the element and
+ * saturates beyond 6 to +-6.  Source: the NVFP4 band of the prefill chain (the fp8_chain page, its precision
+ * bands: the FFN pair and the output projection in NVFP4 with per-block scales); the element and
  * scale formats are NVIDIA's published NVFP4 definition, which the pages name but do not spell out. */
 float oracle_e2m1_decode(uint8_t c) {
     const int sgn = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
@@ -466,7 +467,7 @@ static float silu(float x) { return x / (1.0f + expf(-x)); }
  *   kv     this sequence's layer-0 cache block; layer l starts at kv + l * layer_stride;
  *          within a layer: K [nkv][n_slots][hd] then V [nkv][n_slots][hd]
  *   hidden [n][H] final-RMSNorm output of every new row (may be NULL)
- * Per layer ("fp8_chain.py", run(): norm -> QKV -> split/RoPE/cache -> attend -> o-proj, residual
+ * Per layer (the fp8_chain page, its per-layer chain: norm -> QKV -> split/RoPE/cache -> attend -> o-proj, residual
  * add -> norm -> gate/up -> gated activation -> down, residual add; SwiGLU replaces that page's
  * GeGLU for the Qwen3-style backbone):
  *   y = RMSNorm(r; attn_norm); qkv = bf16(y W_qkv^T)
@@ -547,7 +548,7 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
  * Each new position attends every slot up to itself.  last_hidden [B][H] = final RMSNorm of
  * position starts[b] + len_b - 1.  Returns 0, or -1 on a bad argument.
  * Source: batched prefill with KV writes ("Stabilize Higgs Audio termination and prefill",
- * Summary); pads trail and only the used keys are attended ("fp8_chain.py", module docstring);
+ * Summary); pads trail and only the used keys are attended (the fp8_chain page, its description);
  * mixed batches of prefill chunks and single-token steps under one launch bound taken from the
  * real batch (vLLM-Omni PR #8226, Purpose). */
 static int prefill_impl(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
@@ -589,8 +590,8 @@ int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const orac
 
 /* FP8 variant of the prefill from position 0: every projection of every layer runs on E4M3 weights
  * fp8[l] and on its input quantized with that layer's static activation scale, the result scaled
- * by activation scale * weight scale; everything else is the bf16 prefill ("fp8_chain.py", module
- * docstring: static-FP8 merged-QKV, output, gate/up and down GEMMs). */
+ * by activation scale * weight scale; everything else is the bf16 prefill (the fp8_chain page, its
+ * description: static-FP8 merged-QKV, output, gate/up and down GEMMs). */
 int oracle_prefill_fp8(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
                        const oracle_fp8_layer* fp8, const uint16_t* final_norm, const int32_t* tokens,
                        const int32_t* seq_lens, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,

@@ -4,7 +4,7 @@
 // and the stream-ordered kernel sequence of each operation.  No allocation, no synchronisation
 // (except hra_device_error, which exists to synchronise).
 //
-// Prefill per layer ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py", run(); "Stabilize
+// Prefill per layer ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its per-layer chain; "Stabilize
 // Higgs Audio termination and prefill", Summary):
 //   QKV GEMM -> q/k norm + RoPE + KV write -> causal attention -> o GEMM (+residual)
 //   -> RMSNorm -> gate/up GEMM (+SwiGLU) -> down GEMM (+residual) -> RMSNorm (next layer / final)

@@ -2,9 +2,9 @@
 //
 // Semantics: row i of sequence b (position p_i) with q head h attends cache slots 0..p_i of kv head
 // h / (n_q / n_kv) with softmax(q.k / sqrt(hd)); slots past the sequence's length carry zero
-// weight and are never used ("fp8_chain.py", module docstring: attention "over exactly the used
-// keys (pads trail, so a used-key count carries the host's mask)"; causal here because the
-// backbone is a decoder).
+// weight and are never used ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its
+// description: attention covers only the used keys, and since pads trail, a count of used keys
+// stands for the mask; causal here because the backbone is a decoder).
 //
 // decode_attn_kernel   one query per row (decode pass, last prefill layer): the keys are split
 //                      across CTAs and stream through a 3-stage cp.async ring; the G = n_q / n_kv

@@ -2,7 +2,7 @@
 //
 // Semantics: row i of sequence b (position start_b + i) with
 // q head h attends cache slots 0 .. start_b + i of kv head h / (n_q / n_kv) with
-// softmax(q.k / sqrt(hd)) ("fp8_chain.py", module docstring: attention over exactly the used keys;
+// softmax(q.k / sqrt(hd)) ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its description: attention runs over the used keys only;
 // causal because the backbone is a decoder).
 //
 // A work item = one kv head of one sequence and QT = 128 / G consecutive query positions, for all

@@ -4,7 +4,8 @@
 // (lowest index on ties) after adding the optional EOC bias; the K CTAs of a row form a thread-block
 // cluster, whose rank 0 runs the delay-pattern state machine, after which every CTA writes 1/K of
 // next = bf16(sum over k ascending of fp32 code_emb[k][code_k]) with 16-byte loads.  Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141),
-// Summary ("per-frame argmax, delay handling, and codebook embedding accumulation") and Root cause
+// Summary (one shared helper takes the per-frame argmax, applies the delays and sums the codebook
+// embeddings) and Root cause
 // (EOC on any codebook must end the stream, not only on the first).
 //
 // The sampled variant (codebook_sample_kernel, one CTA per (codebook, row)) replaces the argmax with

@@ -7,8 +7,8 @@
 //   rmsnorm           RMSNorm of rows (optionally gathered), or a plain row gather
 //   qk_rope_kv        per-head q/k RMSNorm + rotate-half RoPE, q to scratch, K/V into the cache
 //                     (half a warp per head)
-//                     (same page: "q/k norm + RoPE, and KV writes"; "fp8_chain.py": keys in host
-//                     rotate-half layout in the cache)
+//                     (same page: q/k norm, RoPE and the KV writes; the fp8_chain page: keys in
+//                     the host rotate-half layout in the cache)
 // One warp per row (a CTA per row for q/k/v heads); 16-byte vector loads; shuffle reductions.
 #include <algorithm>
 

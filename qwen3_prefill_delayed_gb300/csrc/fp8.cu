@@ -1,6 +1,6 @@
 // fp8.cu -- E4M3 quantization for the static-FP8 variant of the prefill projections.
 //
-// The variant ("fp8_chain.py", module docstring: RMSNorm->FP8, merged-QKV / output / gate-up /
+// The variant ("flashrt-structures 0.2.0, prefill_tower/fp8_chain.py" page, its description: RMSNorm then FP8, merged-QKV / output / gate-up /
 // down FP8 GEMMs with static activation scales; "Stabilize Higgs Audio termination and prefill",
 // Summary: the activation scales come from a fixed calibration prompt):
 //   weights     w8 = e4m3(w / s_w), s_w = max|w| / 448 (1 for an all-zero tensor), once;
@@ -67,8 +67,8 @@ __global__ void absmax_kernel(const bf16* __restrict__ x, long long n, float* am
 }
 
 // ---------------------------------------------------------------- NVFP4 (E2M1 + block scales)
-// The FP4 band of the prefill chain ("fp8_chain.py", BANDS: the FFN pair and the output projection
-// "ride NVFP4 with dynamic block scales"), in NVIDIA's published NVFP4 format: E2M1 elements, one
+// The FP4 band of the prefill chain (same page, its precision bands: the output projection and the
+// FFN pair run in NVFP4 with per-block scales computed on the fly), in NVIDIA's published NVFP4 format: E2M1 elements, one
 // E4M3 scale per 16 consecutive elements along K, one fp32 global scale g per tensor.
 
 // value of a finite E4M3 code: (8 + M) 2^(E - 10) for E > 0, M 2^-9 for E = 0

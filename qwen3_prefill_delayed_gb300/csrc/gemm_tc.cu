@@ -5,7 +5,8 @@
 // plain bf16 store, in-place residual add (r = bf16(r + acc)), SwiGLU over the gate and up rows
 // of a merged [2F, K] weight (h = bf16(silu(bf16(g)) * bf16(u))), or fp32 store.  These are the
 // projection GEMMs of the batched prefill ("Stabilize Higgs Audio termination and prefill",
-// Summary: "projection GEMMs"; merged QKV and merged gate/up as in "fp8_chain.py", run()) and the
+// Summary: the projection GEMMs; merged QKV and merged gate/up as in the "flashrt-structures 0.2.0,
+// prefill_tower/fp8_chain.py" page, its per-layer chain) and the
 // audio-head projection.
 //
 // One CTA owns a 128 x BN output tile (M = 128 rows of A per tcgen05.mma, N = BN weight rows):

@@ -12,7 +12,9 @@
 
 namespace {
 
-// 32 MiB per device, reserved when the library's module loads and held until exit.
+// 32 MiB per device, held until exit.  The module that holds it is loaded lazily by CUDA: on each
+// device the first cudaGetSymbolAddress below loads it, and the driver reserves the array then, so
+// that first call is the slow one.
 constexpr size_t kScratchBytes = 32u << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 

@@ -69,7 +69,7 @@ def _run_chunks(hra, d, w, tok, lens, cut, n_new, n_slots, full_last=False):
     return hid, cache
 
 
-def _check(d, w, tok, cut, n_new, hid, cache, n_slots):
+def _check(d, w, tok, cut, n_new, hid, cache, n_slots, tier="deep"):
     hw = oracle.host_weights_from(d, w)
     ends = [c + n for c, n in zip(cut, n_new)]
     t_o = tok[:, :max(ends)].copy()
@@ -77,10 +77,10 @@ def _check(d, w, tok, cut, n_new, hid, cache, n_slots):
     with oracle.sum_order(True):
         kv_a, hid_a = oracle.prefill(d, hw, t_o, ends, n_slots)
     got = cache.float().cpu().numpy()
-    assert_parity(to_np(hid), ref_np(hid_o), ref_np(hid_a), what="last hidden")
+    assert_parity(to_np(hid), ref_np(hid_o), ref_np(hid_a), what="last hidden", tier=tier)
     for b, e in enumerate(ends):
         assert_parity(got[:, b, :, :, :e].astype(np.float64), ref_np(kv_o[:, b, :, :, :e]),
-                      ref_np(kv_a[:, b, :, :, :e]), what=f"kv seq {b}")
+                      ref_np(kv_a[:, b, :, :, :e]), what=f"kv seq {b}", tier=tier)
         assert np.all(np.isnan(got[:, b, :, :, e:])), f"seq {b}: slots past position {e - 1} were written"
 
 
@@ -93,7 +93,7 @@ def test_tiny_mixed_chunks(hra, full_last):
     cut = [0, 9, 5, 6]
     n_new = [13, 1, 7, 1]
     hid, cache = _run_chunks(hra, d, w, tok, lens, cut, n_new, 32, full_last)
-    _check(d, w, tok, cut, n_new, hid, cache, 32)
+    _check(d, w, tok, cut, n_new, hid, cache, 32, tier="layer")
 
 
 def test_full_width_chunks_straddle_tiles(hra):
@@ -126,7 +126,7 @@ def test_chunk_to_the_last_slot_and_range_errors(hra):
     cut = [25, 0]
     n_new = [7, 20]                      # sequence 0 ends in slot 31 of 32
     hid, cache = _run_chunks(hra, d, w, tok, lens, cut, n_new, 32)
-    _check(d, w, tok, cut, n_new, hid, cache, 32)
+    _check(d, w, tok, cut, n_new, hid, cache, 32, tier="layer")
     bb = hra.Backbone(d, _dev(w))
     chunk = _pack([tok[0, :7], tok[1, :7]], d.vocab).to(DEV)
     with pytest.raises(hra.HraError, match="outside the cache"):

@@ -1,4 +1,5 @@
-"""GPU parity of the static-FP8 variant against the oracle ("fp8_chain.py", module docstring;
+"""GPU parity of the static-FP8 variant against the oracle (the "flashrt-structures 0.2.0,
+prefill_tower/fp8_chain.py" page, its description;
 "Stabilize Higgs Audio termination and prefill", Summary):
 
 - E4M3 weight and activation quantization: codes and scales bit-exact;

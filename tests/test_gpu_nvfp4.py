@@ -1,5 +1,6 @@
 """GPU parity of the NVFP4 quantizer (hra_nvfp4_quantize) against the pinned oracle
-(oracle_quantize_nvfp4; the chain's FP4 band, "fp8_chain.py", BANDS): codes and block scales bit
+(oracle_quantize_nvfp4; the chain's FP4 band, the fp8_chain page's precision bands): codes and
+block scales bit
 for bit on the same bf16 input and the same global scale, over magnitudes that put block scales in
 the E4M3 normal and subnormal ranges, an all-zero block and saturating elements."""
 import numpy as np

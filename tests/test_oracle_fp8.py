@@ -1,4 +1,5 @@
-"""Pins of the oracle's static-FP8 variant ("fp8_chain.py", module docstring: E4M3 weights with
+"""Pins of the oracle's static-FP8 variant (the "flashrt-structures 0.2.0, prefill_tower/fp8_chain.py"
+page, its description: E4M3 weights with
 per-tensor scales, inputs quantized with calibrated static scales; "Stabilize Higgs Audio
 termination and prefill", Summary: calibration on a fixed prompt):
 

@@ -1,6 +1,6 @@
-"""Pins of the oracle's NVFP4 codec and block-scaled linear (the prefill chain's FP4 band:
-"fp8_chain.py", BANDS -- the FFN pair and the output projection "ride NVFP4 with dynamic block
-scales"; element and scale formats from NVIDIA's published NVFP4 definition):
+"""Pins of the oracle's NVFP4 codec and block-scaled linear (the prefill chain's FP4 band: the
+fp8_chain page's precision bands put the FFN pair and the output projection in NVFP4 with block
+scales computed from the data; element and scale formats from NVIDIA's published NVFP4 definition):
 
 - E2M1 from the format's definition: the 16 codes decode to m/2 (exponent field 0) or
   (1 + m/2) 2^(e-1); finite codes re-encode to themselves; midpoints go to the even mantissa;
