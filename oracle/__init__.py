@@ -53,6 +53,11 @@ class OracleFp8Layer(ctypes.Structure):
                 ("w_down", ctypes.c_void_p), ("w_scale", ctypes.c_float * 4), ("a_scale", ctypes.c_float * 4)]
 
 
+class OracleNvfp4Layer(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("codes", ctypes.c_void_p * 4), ("scales", ctypes.c_void_p * 4),
+                ("w_scale", ctypes.c_float * 4), ("a_scale", ctypes.c_float * 4)]
+
+
 _lib = None
 
 
@@ -121,7 +126,10 @@ def lib():
                                          ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int, _u16p]
         L.oracle_calibrate.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer), _u16p, _i32p,
                                        _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]
-        for f in ("oracle_prefill_fp8", "oracle_calibrate"):
+        L.oracle_prefill_nvfp4.argtypes = [ctypes.POINTER(OracleDims), _u16p, ctypes.POINTER(OracleLayer),
+                                           ctypes.POINTER(OracleNvfp4Layer), _u16p, _i32p, _i32p, ctypes.c_int,
+                                           ctypes.c_int, _u16p, ctypes.c_int, ctypes.c_int, _u16p]
+        for f in ("oracle_prefill_fp8", "oracle_calibrate", "oracle_prefill_nvfp4"):
             getattr(L, f).restype = ctypes.c_int
         for f in ("oracle_prefill", "oracle_prefill_chunk", "oracle_decode", "oracle_codebook_step",
                   "oracle_max_threads"):
@@ -462,6 +470,63 @@ def prefill_fp8(d, w: "HostWeights", f8: Fp8Weights, tokens: np.ndarray, lens, n
                                   lens, B, P, kv, B, n_slots, last)
     if rc != 0:
         raise ValueError("oracle_prefill_fp8 rejected its arguments")
+    return kv, last
+
+
+class Nvfp4Weights:
+    """The NVFP4 band of every layer (the fp8_chain page, its precision bands): the merged QKV as
+    E4M3 with a per-tensor scale (static input scale a_scale[l, 0]); the output, gate/up and down
+    weights as E2M1 codes + E4M3 block scales under a per-tensor global scale g_w = max|w| / 2688,
+    their inputs quantized per call under the static global scale a_scale[l, p] (e.g. the
+    calibration's max |input| / 2688)."""
+
+    def __init__(self, hw: "HostWeights", a_scale: np.ndarray):
+        self.keep, self.w_scale = [], []
+        for lay in hw.layers:
+            sc, q = quantize_weight_e4m3(lay["w_qkv"])
+            entry = {"w_qkv": q, "codes": [None], "scales": [None]}
+            ws = [sc]
+            for name in ("w_o", "w_gate_up", "w_down"):
+                w = lay[name]
+                g = nvfp4_global(w)
+                c, s = quantize_nvfp4(w, g)
+                entry["codes"].append(c)
+                entry["scales"].append(s)
+                ws.append(g)
+            self.keep.append(entry)
+            self.w_scale.append(ws)
+        self.a_scale = np.asarray(a_scale, np.float32)
+        self.table = (OracleNvfp4Layer * len(self.keep))()
+        for l, e in enumerate(self.keep):
+            self.table[l].w_qkv = e["w_qkv"].ctypes.data
+            for p in range(4):
+                self.table[l].codes[p] = None if e["codes"][p] is None else e["codes"][p].ctypes.data
+                self.table[l].scales[p] = None if e["scales"][p] is None else e["scales"][p].ctypes.data
+                self.table[l].w_scale[p] = float(self.w_scale[l][p])
+                self.table[l].a_scale[p] = float(self.a_scale[l, p])
+
+
+def nvfp4_a_scales(amax: np.ndarray) -> np.ndarray:
+    """Static input scales of the NVFP4 band from the calibration amax [L, 4]: the QKV input's E4M3
+    scale amax / 448 (1 where amax is 0); the other inputs' NVFP4 global scale amax / (6 * 448)."""
+    a = np.asarray(amax, np.float32)
+    out = np.empty_like(a)
+    out[:, 0] = np.where(a[:, 0] > 0, a[:, 0] / np.float32(448.0), np.float32(1.0))
+    out[:, 1:] = np.where(a[:, 1:] > 0, a[:, 1:] / np.float32(6.0 * 448.0), np.float32(1.0))
+    return out
+
+
+def prefill_nvfp4(d, w: "HostWeights", nv: Nvfp4Weights, tokens: np.ndarray, lens, n_slots: int):
+    """Returns (kv, last_hidden) of the NVFP4-band variant."""
+    tokens = _c(tokens, np.int32)
+    lens = _c(lens, np.int32)
+    B, P = tokens.shape
+    kv = np.zeros(kv_shape(d, B, n_slots), np.uint16)
+    last = np.empty((B, d.hidden), np.uint16)
+    rc = lib().oracle_prefill_nvfp4(ctypes.byref(make_dims(d)), w.embed, w.table, nv.table, w.final_norm, tokens,
+                                    lens, B, P, kv, B, n_slots, last)
+    if rc != 0:
+        raise ValueError("oracle_prefill_nvfp4 rejected its arguments")
     return kv, last
 
 

@@ -438,15 +438,42 @@ typedef struct {
     float a_scale[4];                                   /* static scale of each projection's input */
 } oracle_fp8_layer;
 
-/* One projection: bf16 (w8 == NULL) or FP8 (the input quantized with the static scale as, the
- * result scaled by as * ws).  amax (optional) receives the max |input| seen. */
+/* NVFP4 band of the prefill chain (the fp8_chain page, its precision bands): the merged QKV stays
+ * in static FP8, the output, gate/up and down projections run in NVFP4.
+ *   w_qkv, w_scale[0], a_scale[0]      E4M3 QKV weights, their scale and the static input scale
+ *   codes[p], scales[p] (p = 1, 2, 3)  E2M1 weight codes [N][K] (one per byte) and E4M3 block
+ *                                      scales [N][K/16] of the output, gate/up and down weights
+ *   w_scale[p], a_scale[p] (p >= 1)    the weights' fp32 global scale g_w, and the static fp32
+ *                                      global scale g_a of the projection's input (its block scales
+ *                                      are computed from each call's data) */
+typedef struct {
+    const uint8_t* w_qkv;
+    const uint8_t* codes[4];
+    const uint8_t* scales[4];
+    float w_scale[4];
+    float a_scale[4];
+} oracle_nvfp4_layer;
+
+/* One projection: bf16 (w8 == NULL and wc == NULL), FP8 (w8: the input quantized with the static
+ * scale as, the result scaled by as * ws) or NVFP4 (wc / wsc: the input quantized to E2M1 codes with
+ * per-16-element E4M3 block scales under the global scale as, then the block-scaled linear with
+ * g_a = as, g_w = ws).  amax (optional) receives the max |input| seen. */
 static void project(const uint16_t* x, const uint16_t* w, const uint8_t* w8, float ws, float as, int n, int N,
-                    int K, float* y, float* amax) {
+                    int K, float* y, float* amax, const uint8_t* wc, const uint8_t* wsc) {
     if (amax) {
         for (size_t i = 0; i < (size_t)n * K; ++i) {
             const float a = fabsf(bf(x[i]));
             if (a > *amax) *amax = a;
         }
+    }
+    if (wc != NULL) {
+        uint8_t* xc = (uint8_t*)malloc((size_t)n * K);
+        uint8_t* xs = (uint8_t*)malloc((size_t)n * (K / 16));
+        oracle_quantize_nvfp4(x, n, K, as, xc, xs);
+        oracle_linear_nvfp4(xc, xs, wc, wsc, n, N, K, as, ws, y);
+        free(xc);
+        free(xs);
+        return;
     }
     if (w8 == NULL) {
         oracle_linear(x, w, n, N, K, y);
@@ -477,7 +504,8 @@ static float silu(float x) { return x / (1.0f + expf(-x)); }
  *   r = bf16(r + h W_down^T) */
 static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const uint16_t* final_norm,
                          const uint16_t* x_in, int start, int n, uint16_t* kv, size_t layer_stride,
-                         int n_slots, uint16_t* hidden, const oracle_fp8_layer* fp8, float* amax) {
+                         int n_slots, uint16_t* hidden, const oracle_fp8_layer* fp8, float* amax,
+                         const oracle_nvfp4_layer* nv4) {
     const int H = d->hidden, nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim, F = d->ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d->rms_eps;
@@ -501,8 +529,14 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
         uint16_t* vc = kc + (size_t)nkv * n_slots * hd;
         /* attention block */
         oracle_rmsnorm(r, L->attn_norm, n, H, eps, y);
-        project(y, L->w_qkv, fp8 ? fp8[l].w_qkv : NULL, fp8 ? fp8[l].w_scale[0] : 1.0f, fp8 ? fp8[l].a_scale[0] : 1.0f,
-                n, Dqkv, H, acc, amax ? amax + 4 * l : NULL);
+        /* the quantized projection p of layer l: FP8 (fp8, or the NVFP4 band's QKV) or NVFP4 */
+#define PROJ_W8(p, fld) (fp8 ? fp8[l].fld : (nv4 && (p) == 0) ? nv4[l].w_qkv : NULL)
+#define PROJ_WS(p) (fp8 ? fp8[l].w_scale[p] : nv4 ? nv4[l].w_scale[p] : 1.0f)
+#define PROJ_AS(p) (fp8 ? fp8[l].a_scale[p] : nv4 ? nv4[l].a_scale[p] : 1.0f)
+#define PROJ_WC(p) (nv4 && (p) > 0 ? nv4[l].codes[p] : NULL)
+#define PROJ_WSC(p) (nv4 && (p) > 0 ? nv4[l].scales[p] : NULL)
+        project(y, L->w_qkv, PROJ_W8(0, w_qkv), PROJ_WS(0), PROJ_AS(0), n, Dqkv, H, acc, amax ? amax + 4 * l : NULL,
+                PROJ_WC(0), PROJ_WSC(0));
         for (size_t i = 0; i < (size_t)n * Dqkv; ++i) qkv[i] = to_bf(acc[i]);
         for (int i = 0; i < n; ++i) {
             int pos = start + i;
@@ -520,21 +554,26 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
             }
         }
         oracle_attend(qr, kc, vc, n_slots, start, n, nq, nkv, hd, att, NULL, 0);
-        project(att, L->w_o, fp8 ? fp8[l].w_o : NULL, fp8 ? fp8[l].w_scale[1] : 1.0f, fp8 ? fp8[l].a_scale[1] : 1.0f,
-                n, H, Dq, acc, amax ? amax + 4 * l + 1 : NULL);
+        project(att, L->w_o, PROJ_W8(1, w_o), PROJ_WS(1), PROJ_AS(1), n, H, Dq, acc, amax ? amax + 4 * l + 1 : NULL,
+                PROJ_WC(1), PROJ_WSC(1));
         for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
         /* MLP block */
         oracle_rmsnorm(r, L->mlp_norm, n, H, eps, y);
-        project(y, L->w_gate_up, fp8 ? fp8[l].w_gate_up : NULL, fp8 ? fp8[l].w_scale[2] : 1.0f,
-                fp8 ? fp8[l].a_scale[2] : 1.0f, n, 2 * F, H, acc, amax ? amax + 4 * l + 2 : NULL);
+        project(y, L->w_gate_up, PROJ_W8(2, w_gate_up), PROJ_WS(2), PROJ_AS(2), n, 2 * F, H, acc,
+                amax ? amax + 4 * l + 2 : NULL, PROJ_WC(2), PROJ_WSC(2));
         for (int i = 0; i < n; ++i)
             for (int j = 0; j < F; ++j) {
                 float g = bf(to_bf(acc[(size_t)i * 2 * F + j]));
                 float u = bf(to_bf(acc[(size_t)i * 2 * F + F + j]));
                 hmid[(size_t)i * F + j] = to_bf(silu(g) * u);
             }
-        project(hmid, L->w_down, fp8 ? fp8[l].w_down : NULL, fp8 ? fp8[l].w_scale[3] : 1.0f,
-                fp8 ? fp8[l].a_scale[3] : 1.0f, n, H, F, acc, amax ? amax + 4 * l + 3 : NULL);
+        project(hmid, L->w_down, PROJ_W8(3, w_down), PROJ_WS(3), PROJ_AS(3), n, H, F, acc,
+                amax ? amax + 4 * l + 3 : NULL, PROJ_WC(3), PROJ_WSC(3));
+#undef PROJ_W8
+#undef PROJ_WS
+#undef PROJ_AS
+#undef PROJ_WC
+#undef PROJ_WSC
         for (size_t i = 0; i < (size_t)n * H; ++i) r[i] = to_bf(bf(r[i]) + acc[i]);
     }
     if (hidden) oracle_rmsnorm(r, final_norm, n, H, eps, hidden);
@@ -554,7 +593,8 @@ static void forward_rows(const oracle_dims* d, const oracle_layer* layers, const
 static int prefill_impl(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
                         const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
                         const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
-                        uint16_t* last_hidden, const oracle_fp8_layer* fp8, float* amax) {
+                        uint16_t* last_hidden, const oracle_fp8_layer* fp8, float* amax,
+                        const oracle_nvfp4_layer* nv4) {
     const int H = d->hidden;
     const size_t blk = (size_t)2 * d->n_kv_heads * n_slots * d->head_dim;
     if (B < 1 || B > kv_batch) return -1;
@@ -572,7 +612,7 @@ static int prefill_impl(const oracle_dims* d, const uint16_t* embed, const oracl
             memcpy(x + (size_t)i * H, embed + (size_t)tokens[(size_t)b * P_max + i] * H,
                    sizeof(uint16_t) * H);
         forward_rows(d, layers, final_norm, x, s0, n, kv + (size_t)b * blk, (size_t)kv_batch * blk,
-                     n_slots, hid, fp8, amax);
+                     n_slots, hid, fp8, amax, nv4);
         memcpy(last_hidden + (size_t)b * H, hid + (size_t)(n - 1) * H, sizeof(uint16_t) * H);
         free(x);
         free(hid);
@@ -585,7 +625,7 @@ int oracle_prefill_chunk(const oracle_dims* d, const uint16_t* embed, const orac
                          const int32_t* starts, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
                          uint16_t* last_hidden) {
     return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, starts, B, P_max, kv, kv_batch, n_slots,
-                        last_hidden, NULL, NULL);
+                        last_hidden, NULL, NULL, NULL);
 }
 
 /* FP8 variant of the prefill from position 0: every projection of every layer runs on E4M3 weights
@@ -598,7 +638,21 @@ int oracle_prefill_fp8(const oracle_dims* d, const uint16_t* embed, const oracle
                        uint16_t* last_hidden) {
     if (fp8 == NULL) return -1;
     return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch, n_slots,
-                        last_hidden, fp8, NULL);
+                        last_hidden, fp8, NULL, NULL);
+}
+
+/* NVFP4-band variant of the prefill from position 0 (the fp8_chain page, its precision bands): the
+ * merged QKV in static FP8, the output, gate/up and down projections in NVFP4 -- E2M1 weights with
+ * E4M3 block scales and an fp32 global scale, each input quantized per call to E2M1 with block
+ * scales from its own data under a static global scale; everything else is the bf16 prefill. */
+int oracle_prefill_nvfp4(const oracle_dims* d, const uint16_t* embed, const oracle_layer* layers,
+                         const oracle_nvfp4_layer* nv4, const uint16_t* final_norm, const int32_t* tokens,
+                         const int32_t* seq_lens, int B, int P_max, uint16_t* kv, int kv_batch, int n_slots,
+                         uint16_t* last_hidden) {
+    if (nv4 == NULL) return -1;
+    if (d->hidden % 16 != 0 || (d->n_q_heads * d->head_dim) % 16 != 0 || d->ffn % 16 != 0) return -1;
+    return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch, n_slots,
+                        last_hidden, NULL, NULL, nv4);
 }
 
 /* Calibration of the static activation scales (FlashRT PR #141, Summary: FP8 activation scales
@@ -613,7 +667,7 @@ int oracle_calibrate(const oracle_dims* d, const uint16_t* embed, const oracle_l
     uint16_t* kv = (uint16_t*)calloc(per, sizeof(uint16_t));
     uint16_t* last = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)B * d->hidden);
     const int rc = prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, B, n_slots,
-                                last, NULL, amax);
+                                last, NULL, amax, NULL);
     free(kv);
     free(last);
     return rc;
@@ -626,7 +680,7 @@ int oracle_prefill(const oracle_dims* d, const uint16_t* embed, const oracle_lay
                    const uint16_t* final_norm, const int32_t* tokens, const int32_t* seq_lens,
                    int B, int P_max, uint16_t* kv, int kv_batch, int n_slots, uint16_t* last_hidden) {
     return prefill_impl(d, embed, layers, final_norm, tokens, seq_lens, NULL, B, P_max, kv, kv_batch, n_slots,
-                        last_hidden, NULL, NULL);
+                        last_hidden, NULL, NULL, NULL);
 }
 
 /* Single-token decode pass: row b is the embedding in_emb[b] at position pos[b]; it writes cache
@@ -643,7 +697,7 @@ int oracle_decode(const oracle_dims* d, const oracle_layer* layers, const uint16
         if (pos[b] < 0 || pos[b] >= n_slots) return -1;
     for (int b = 0; b < B; ++b)
         forward_rows(d, layers, final_norm, in_emb + (size_t)b * H, pos[b], 1, kv + (size_t)b * blk,
-                     (size_t)kv_batch * blk, n_slots, hidden + (size_t)b * H, NULL, NULL);
+                     (size_t)kv_batch * blk, n_slots, hidden + (size_t)b * H, NULL, NULL, NULL);
     return 0;
 }
 

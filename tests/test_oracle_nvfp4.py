@@ -16,6 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
+import workloads as W
 
 GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
@@ -149,3 +150,57 @@ def test_linear_nvfp4_equals_bf16_linear_when_scales_are_one(orc):
     ab = oracle.bf16_bits(oracle.e2m1_decode(ca))
     wb = oracle.bf16_bits(oracle.e2m1_decode(cw))
     np.testing.assert_array_equal(y, orc.linear(ab, wb))
+
+
+def _nvfp4_setup(orc, d, w, tok, lens):
+    hw = orc.host_weights_from(d, w)
+    amax = orc.calibrate(d, hw, tok, lens, 32)
+    return hw, amax
+
+
+def test_nvfp4_band_scales(orc):
+    """The band's static input scales: amax / 448 for the QKV input (its FP8 scale), amax / (6 * 448)
+    for the NVFP4 inputs, 1 where amax is 0."""
+    amax = np.array([[448.0, 2688.0, 0.0, 5.0]], np.float32)
+    np.testing.assert_array_equal(orc.nvfp4_a_scales(amax), np.array([[1.0, 1.0, 1.0, np.float32(5.0) / np.float32(2688.0)]],
+                                                                      np.float32))
+
+
+def test_nvfp4_prefill_pins(orc):
+    """The NVFP4-band prefill: batch/pad invariant bit for bit; its layer-0 K/V (QKV in the band's
+    static FP8) equal the FP8 prefill's with the same QKV weights and scale; it stays close to the
+    bf16 prefill but farther from it than the FP8 variant (the NVFP4 band does quantize, more
+    coarsely); and each NVFP4 projection's inputs are quantized (the band's activation codes), so
+    moving one NVFP4 input scale moves the result while moving an unused one does not."""
+    d = W.tiny_dims()
+    w = W.make_backbone(d, 0, "cpu")
+    g = np.random.default_rng(14)
+    lens = [13, 6, 9]
+    tok = np.zeros((3, 13), np.int32)
+    for b, n in enumerate(lens):
+        tok[b, :n] = g.integers(0, d.vocab, n)
+    hw, amax = _nvfp4_setup(orc, d, w, tok, lens)
+    a_sc = orc.nvfp4_a_scales(amax)
+    nv = orc.Nvfp4Weights(hw, a_sc)
+    kv4, last4 = orc.prefill_nvfp4(d, hw, nv, tok, lens, 32)
+    for b in range(3):
+        t1 = np.full((1, 20), d.vocab + 3, np.int32)
+        t1[0, :lens[b]] = tok[b, :lens[b]]
+        kv1, last1 = orc.prefill_nvfp4(d, hw, nv, t1, [lens[b]], 32)
+        np.testing.assert_array_equal(last1[0], last4[b])
+        np.testing.assert_array_equal(kv1[:, 0], kv4[:, b])
+    # layer 0's K/V depend only on the embedding, the first norm and the band's FP8 QKV
+    f8 = orc.Fp8Weights(hw, amax / np.float32(448.0))
+    kv8, last8 = orc.prefill_fp8(d, hw, f8, tok, lens, 32)
+    np.testing.assert_array_equal(kv4[0], kv8[0])
+    assert np.any(kv4[1] != kv8[1])
+    _, last16 = orc.prefill(d, hw, tok, lens, 32)
+    a4, a8, c = (orc.bf16_value(x).astype(np.float64) for x in (last4, last8, last16))
+    cos = lambda u, v: np.sum(u * v, axis=1) / np.linalg.norm(u, axis=1) / np.linalg.norm(v, axis=1)
+    assert np.all(cos(a4, c) > 0.95), cos(a4, c)
+    assert np.all(1 - cos(a4, c) > 1 - cos(a8, c)), (cos(a4, c), cos(a8, c))
+    # the gate/up input's global scale matters; halving it changes the result
+    a2 = a_sc.copy()
+    a2[:, 2] = a2[:, 2] * np.float32(0.5)
+    _, last_h = orc.prefill_nvfp4(d, hw, orc.Nvfp4Weights(hw, a2), tok, lens, 32)
+    assert np.any(last_h != last4)
