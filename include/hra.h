@@ -338,6 +338,58 @@ int hra_fp8_quantize(const void* x_dev, int64_t n, const float* scale_dev, void*
 int hra_nvfp4_quantize(const void* x_dev, int32_t rows, int32_t K, const float* g_dev, void* codes_dev,
                        void* scales_dev, void* stream);
 
+/* NVFP4 weights for the band: w_dev bf16 [rows, K] -> *g_dev = max|w| / (6 * 448) (1 for an all-zero
+ * tensor; fp32, on the device) and the codes / block scales of hra_nvfp4_quantize under it.
+ * w_dev and codes_dev 16-byte aligned, g_dev 4-byte aligned, K a multiple of 16. */
+int hra_nvfp4_quantize_weight(const void* w_dev, int32_t rows, int32_t K, void* codes_dev, void* scales_dev,
+                              float* g_dev, void* stream);
+
+/* NVFP4 projection (the band's GEMM): out = epilogue((*g_a) (*g_w) sum_k e2m1(a[m][k]) dec(sa[m][k/16])
+ * e2m1(w[n][k]) dec(sw[n][k/16])), fp32 accumulation; a_codes [M, K] and w_codes [N, K] (2N rows
+ * for HRA_EPI_SWIGLU: gate rows, then up rows) one E2M1 code per byte, a_scales [M, K/16] and
+ * w_scales [N, K/16] E4M3; g_a, g_w device fp32 scalars; epilogues as hra_linear.  K a multiple of
+ * 64, N of 8; codes, out and workspace 16-byte aligned.  The product of an E2M1 value and its E4M3
+ * block scale is exact in f16, so the tensor cores run on those f16 values and the sum differs
+ * from the exact NVFP4 sum only by the order of fp32 additions. */
+size_t hra_linear_nvfp4_workspace_size(void);
+int hra_linear_nvfp4(const void* a_codes_dev, const void* a_scales_dev, const void* w_codes_dev,
+                     const void* w_scales_dev, void* out_dev, int32_t M, int32_t N, int32_t K,
+                     const float* g_a_dev, const float* g_w_dev, int32_t epilogue, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* The NVFP4 band of the prefill chain (the fp8_chain page, its precision bands): the merged QKV
+ * stays in static FP8; the output, gate/up and down projections run in NVFP4 -- E2M1 weights with
+ * E4M3 block scales and a global scale, each input quantized per call (block scales from its own
+ * data) under a static global scale.
+ *   w_qkv        E4M3 [(nq + 2 nkv) hd, H] (hra_fp8_quantize_weight)
+ *   codes[p], scales[p], p = 1 (w_o), 2 (w_gate_up), 3 (w_down): hra_nvfp4_quantize_weight output;
+ *                entry 0 unused
+ *   w_scale      device float [4]: [0] the QKV weight scale, [1..3] the weights' global scales g_w
+ *   a_scale      device float [4]: [0] the QKV input's static E4M3 scale (calibration amax / 448),
+ *                [1..3] the inputs' static NVFP4 global scales (calibration amax / (6 * 448)) */
+typedef struct {
+    const void* w_qkv;
+    const void* codes[4];
+    const void* scales[4];
+    const float* w_scale;
+    const float* a_scale;
+} hra_nvfp4_layer;
+
+/* The band's static input scales from hra_fp8_calibrate's amax_dev [n_layers][4] (device): the
+ * QKV input's E4M3 scale amax / 448 and the other three inputs' NVFP4 global scales amax / (6 * 448)
+ * (1 where amax is 0), into scale_dev [n_layers][4] (device, the layers' a_scale arrays). */
+int hra_nvfp4_band_scales(const float* amax_dev, float* scale_dev, int32_t n_layers, void* stream);
+
+/* hra_prefill with the NVFP4 band in every layer (nvfp4_layers: host array [n_layers]); everything
+ * else (embedding, norms, RoPE, attention, SwiGLU, residuals) is the bf16 prefill's.  hidden must
+ * be a multiple of 128 (else HRA_ERR_UNSUPPORTED). */
+size_t hra_prefill_nvfp4_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens,
+                                        int32_t max_len);
+int hra_prefill_nvfp4(const hra_dims* dims, const hra_weights* weights, const hra_nvfp4_layer* nvfp4_layers,
+                      const int32_t* tokens_dev, const int32_t* seq_lens, int32_t batch, int32_t max_len,
+                      const hra_kv_cache* kv, void* last_hidden_dev, void* workspace,
+                      size_t workspace_bytes, uint32_t flags, void* stream);
+
 /* FP8 projection: out = epilogue((a8 . w8^T) * (*a_scale) * (*w_scale)), a8 E4M3 [M, K], w8 E4M3
  * [N, K] (2N rows for EPI_SWIGLU), K a multiple of 128; epilogues as hra_linear. */
 size_t hra_linear_fp8_workspace_size(int32_t M, int32_t N, int32_t K, int32_t epilogue);

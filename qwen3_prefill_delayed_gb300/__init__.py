@@ -37,6 +37,9 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_work
             "hra_linear", "hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_nvfp4_quantize", "hra_linear_fp8_workspace_size",
             "hra_linear_fp8", "hra_fp8_calibrate_workspace_size", "hra_fp8_calibrate",
             "hra_prefill_fp8_workspace_size", "hra_prefill_fp8",
+            "hra_nvfp4_quantize_weight", "hra_linear_nvfp4_workspace_size", "hra_linear_nvfp4",
+            "hra_nvfp4_band_scales",
+            "hra_prefill_nvfp4_workspace_size", "hra_prefill_nvfp4",
             "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
             "hra_device_error", "hra_status_string"]
 PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6,
@@ -73,6 +76,11 @@ class HraKvCache(ctypes.Structure):
 class HraFp8Layer(ctypes.Structure):
     _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("w_scale", ctypes.c_void_p), ("a_scale", ctypes.c_void_p)]
+
+
+class HraNvfp4Layer(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("codes", ctypes.c_void_p * 4), ("scales", ctypes.c_void_p * 4),
+                ("w_scale", ctypes.c_void_p), ("a_scale", ctypes.c_void_p)]
 
 
 class HraSampling(ctypes.Structure):
@@ -140,8 +148,18 @@ def lib() -> ctypes.CDLL:
         L.hra_prefill_fp8_workspace_size.restype = sz
         L.hra_prefill_fp8.argtypes = [dp, ctypes.POINTER(HraWeights), ctypes.POINTER(HraFp8Layer), vp,
                                       ctypes.POINTER(i32), i32, i32, ctypes.POINTER(HraKvCache), vp, vp, sz, u32, vp]
+        L.hra_nvfp4_quantize_weight.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+        L.hra_nvfp4_band_scales.argtypes = [vp, vp, i32, vp]
+        L.hra_linear_nvfp4_workspace_size.argtypes = []
+        L.hra_linear_nvfp4_workspace_size.restype = sz
+        L.hra_linear_nvfp4.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32, vp, sz, vp]
+        L.hra_prefill_nvfp4_workspace_size.argtypes = [dp, i32, i32, i32]
+        L.hra_prefill_nvfp4_workspace_size.restype = sz
+        L.hra_prefill_nvfp4.argtypes = [dp, ctypes.POINTER(HraWeights), ctypes.POINTER(HraNvfp4Layer), vp,
+                                        ctypes.POINTER(i32), i32, i32, ctypes.POINTER(HraKvCache), vp, vp, sz, u32, vp]
         for f in ("hra_fp8_quantize_weight", "hra_fp8_quantize", "hra_linear_fp8", "hra_fp8_calibrate",
-                  "hra_prefill_fp8"):
+                  "hra_prefill_fp8", "hra_nvfp4_quantize_weight", "hra_linear_nvfp4", "hra_prefill_nvfp4",
+                  "hra_nvfp4_band_scales"):
             getattr(L, f).restype = ctypes.c_int
         L.hra_linear_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.hra_linear_workspace_size.restype = sz
@@ -623,6 +641,109 @@ class Fp8Backbone:
                                      _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
                                      ws.numel(), PREFILL_FULL_LAST_LAYER if full_last_layer else 0,
                                      _stream(stream)), "hra_prefill_fp8")
+        self.last_ws = ws
+        return out
+
+
+def nvfp4_quantize_weight(w: torch.Tensor, stream=None):
+    """hra_nvfp4_quantize_weight: bf16 CUDA [rows, K] -> (E2M1 codes uint8 [rows, K], E4M3 block
+    scales uint8 [rows, K / 16], global scale float32 [1] = max|w| / (6 * 448))."""
+    rows, K = w.shape
+    codes = torch.empty(rows, K, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(rows, K // 16, dtype=torch.uint8, device=w.device)
+    g = torch.empty(1, dtype=torch.float32, device=w.device)
+    _check(lib().hra_nvfp4_quantize_weight(_ptr(w, torch.bfloat16, "w"), rows, K, _ptr(codes, torch.uint8, "codes"),
+                                           _ptr(scales, torch.uint8, "scales"), _ptr(g, torch.float32, "g"),
+                                           _stream(stream)), "hra_nvfp4_quantize_weight")
+    return codes, scales, g
+
+
+def hra_linear_nvfp4(a_codes: torch.Tensor, a_scales: torch.Tensor, w_codes: torch.Tensor, w_scales: torch.Tensor,
+                     g_a: torch.Tensor, g_w: torch.Tensor, epilogue: int = EPI_STORE,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """hra_linear_nvfp4: NVFP4 operands (codes uint8 one per byte, block scales uint8 E4M3, global
+    scales CUDA float32 scalars) -> out [M, N] (bf16, or fp32 for EPI_F32)."""
+    M, K = a_codes.shape
+    N = w_codes.shape[0] // 2 if epilogue == EPI_SWIGLU else w_codes.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32 if epilogue == EPI_F32 else torch.bfloat16,
+                          device=a_codes.device)
+    ws = torch.empty(lib().hra_linear_nvfp4_workspace_size(), dtype=torch.uint8, device=a_codes.device)
+    _check(lib().hra_linear_nvfp4(_ptr(a_codes, torch.uint8, "a_codes"), _ptr(a_scales, torch.uint8, "a_scales"),
+                                  _ptr(w_codes, torch.uint8, "w_codes"), _ptr(w_scales, torch.uint8, "w_scales"),
+                                  _ptr(out, None, "out"), M, N, K, _ptr(g_a, torch.float32, "g_a"),
+                                  _ptr(g_w, torch.float32, "g_w"), epilogue, _ptr(ws, None, "workspace"), ws.numel(),
+                                  _stream(stream)), "hra_linear_nvfp4")
+    return out
+
+
+class Nvfp4Backbone:
+    """The NVFP4-band variant of a Backbone: the merged QKV in E4M3 (hra_fp8_quantize_weight), the
+    output, gate/up and down weights in NVFP4 (hra_nvfp4_quantize_weight); the static input scales
+    come from hra_fp8_calibrate's amax (QKV: amax / 448; the NVFP4 inputs: amax / (6 * 448))."""
+
+    NV = ("w_o", "w_gate_up", "w_down")
+
+    def __init__(self, bb: "Backbone"):
+        self.bb = bb
+        d = bb.d
+        dev = bb.device
+        self.w_scale = torch.empty(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self.keep = []
+        for l, lay in enumerate(bb.w["layers"]):
+            w8, sc = fp8_quantize_weight(lay["w_qkv"])
+            self.w_scale[l, 0] = sc[0]
+            entry = {"w_qkv": w8, "codes": [None], "scales": [None]}
+            for i, name in enumerate(self.NV):
+                c, s, g = nvfp4_quantize_weight(lay[name])
+                entry["codes"].append(c)
+                entry["scales"].append(s)
+                self.w_scale[l, 1 + i] = g[0]
+            self.keep.append(entry)
+        self.fp8 = Fp8Backbone.__new__(Fp8Backbone)   # only for its calibration pass
+        self.fp8.bb = bb
+        self.fp8.amax = torch.zeros(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self.fp8.a_scale = torch.ones(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self.a_scale = torch.ones(d.n_layers, 4, dtype=torch.float32, device=dev)
+        self._table()
+
+    def _table(self):
+        t = (HraNvfp4Layer * len(self.keep))()
+        for l, e in enumerate(self.keep):
+            t[l].w_qkv = e["w_qkv"].data_ptr()
+            for p in range(1, 4):
+                t[l].codes[p] = e["codes"][p].data_ptr()
+                t[l].scales[p] = e["scales"][p].data_ptr()
+            t[l].w_scale = self.w_scale[l].data_ptr()
+            t[l].a_scale = self.a_scale[l].data_ptr()
+        self.table = t
+
+    def calibrate(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor, stream=None):
+        """hra_fp8_calibrate's amax, then a_scale [n_layers, 4] as described above."""
+        amax, _ = self.fp8.calibrate(tokens, seq_lens, cache, stream=stream)
+        _check(lib().hra_nvfp4_band_scales(_ptr(amax, torch.float32, "amax"), _ptr(self.a_scale, torch.float32, "a_scale"),
+                                           self.bb.d.n_layers, _stream(stream)), "hra_nvfp4_band_scales")
+        return amax, self.a_scale
+
+    def prefill_workspace_size(self, batch, total, max_len) -> int:
+        return lib().hra_prefill_nvfp4_workspace_size(ctypes.byref(self.bb.dims), batch, total, max_len)
+
+    def prefill(self, tokens: torch.Tensor, seq_lens: Sequence[int], cache: torch.Tensor,
+                out: Optional[torch.Tensor] = None, full_last_layer: bool = False,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """hra_prefill_nvfp4 -> last hidden [B, H] bf16."""
+        B, P = tokens.shape
+        lens = (ctypes.c_int32 * B)(*[int(x) for x in seq_lens])
+        if out is None:
+            out = torch.empty(B, self.bb.d.hidden, dtype=torch.bfloat16, device=tokens.device)
+        need = self.prefill_workspace_size(B, int(sum(seq_lens)), P)
+        ws = workspace if workspace is not None else self.bb.ws.get(need, tokens.device)
+        kv = self.bb.kv(cache)
+        _check(lib().hra_prefill_nvfp4(ctypes.byref(self.bb.dims), ctypes.byref(self.bb.table), self.table,
+                                       _ptr(tokens, torch.int32, "tokens"), lens, B, P, ctypes.byref(kv),
+                                       _ptr(out, torch.bfloat16, "last_hidden"), _ptr(ws, None, "workspace"),
+                                       ws.numel(), PREFILL_FULL_LAST_LAYER if full_last_layer else 0,
+                                       _stream(stream)), "hra_prefill_nvfp4")
         self.last_ws = ws
         return out
 

@@ -75,7 +75,7 @@ struct Region {
 
 // Offsets (bytes) of every buffer inside a caller workspace.
 struct Layout {
-    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, total;
+    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, xs, total;
     int attn_splits;
 };
 
@@ -103,7 +103,8 @@ bool audio_dims_ok(const hra_dims* d) {
 
 // Shared plan of the backbone passes.  `rows` = packed rows that run the full layers, `last_rows`
 // = rows of the last-layer tail (batch), `rope_rows` = rows of the RoPE table.
-Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, int max_pos, bool fp8 = false) {
+Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, int max_pos, bool fp8 = false,
+                      bool nvfp4 = false) {
     const size_t H = d.hidden, hd = d.head_dim, Dq = (size_t)d.n_q_heads * hd;
     const size_t Dqkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * hd, F = d.ffn;
     const size_t T = (size_t)std::max(rows, batch);
@@ -134,7 +135,9 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     L.attn_splits = decode_attention_splits(batch, d.n_kv_heads, max_pos);
     L.apart = g.take(decode_attention_scratch_bytes(batch, d.n_q_heads, d.head_dim, L.attn_splits));
     // FP8 variant: the E4M3 copy of the current projection's input (the widest input is the FFN's)
-    L.x8 = fp8 ? g.take(T * std::max(std::max(H, Dq), F)) : 0;
+    L.x8 = (fp8 || nvfp4) ? g.take(T * std::max(std::max(H, Dq), F)) : 0;
+    // NVFP4 band: the E4M3 block scales of that input (one per 16 elements)
+    L.xs = nvfp4 ? g.take(T * std::max(std::max(H, Dq), F) / 16) : 0;
     L.total = g.off;
     return L;
 }
@@ -164,6 +167,8 @@ struct QuantCtx {
     float* amax;
     uint8_t* x8;
     int layer;
+    const hra_nvfp4_layer* nv4;   // NVFP4 band: QKV in FP8 from here, the other three in NVFP4
+    uint8_t* xs;                  // block scales of the quantized input (NVFP4)
 };
 enum Proj : int { PROJ_QKV = 0, PROJ_O = 1, PROJ_GATE_UP = 2, PROJ_DOWN = 3 };
 
@@ -181,7 +186,42 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
         cudaError_t e = launch_absmax(a, (long long)M * K, qc->amax + 4 * qc->layer + proj, st);
         if (e != cudaSuccess) return e;
     }
-    if (qc != nullptr && qc->layers != nullptr) {
+    if (qc != nullptr && qc->nv4 != nullptr && proj != PROJ_QKV) {
+        // NVFP4: the input to E2M1 codes + per-16 E4M3 block scales under its static global scale,
+        // then the NVFP4 GEMM; the RMSNorm that follows a residual projection runs on its own
+        const hra_nvfp4_layer& f = qc->nv4[qc->layer];
+        cudaError_t e = launch_nvfp4_quantize(a, M, K, f.a_scale + proj, qc->x8, qc->xs, st);
+        if (e != cudaSuccess) return e;
+        Nvfp4Call n{};
+        n.a_codes = qc->x8;
+        n.a_scales = qc->xs;
+        n.w_codes = reinterpret_cast<const uint8_t*>(f.codes[proj]);
+        n.w_scales = reinterpret_cast<const uint8_t*>(f.scales[proj]);
+        n.g_a = f.a_scale + proj;
+        n.g_w = f.w_scale + proj;
+        n.out = out;
+        n.err = P.at<unsigned int>(L.err);
+        n.M = M;
+        n.N = N;
+        n.K = K;
+        n.epi = epi;
+        const double n_w = epi == EPI_SWIGLU ? 2.0 * N : (double)N;
+        const int cls = probe_class == HRA_PROBE_GATE_UP ? HRA_PROBE_GATE_UP : HRA_PROBE_NONE;
+        e = probed(cls, 2.0 * M * (double)K * n_w, st, [&] { return launch_linear_nvfp4(n, st); });
+        if (e != cudaSuccess || norm_out == nullptr) return e;
+        return launch_rmsnorm(reinterpret_cast<const bf16*>(out), norm_rows, reinterpret_cast<const bf16*>(norm_gain),
+                              norm_out, nullptr, norm_rows ? norm_nrows : M, N, eps, st);
+    }
+    if (qc != nullptr && qc->nv4 != nullptr) {   // the band's QKV: static FP8
+        const hra_nvfp4_layer& f = qc->nv4[qc->layer];
+        cudaError_t e = launch_fp8_quantize(a, (long long)M * K, f.a_scale, qc->x8, st);
+        if (e != cudaSuccess) return e;
+        a = reinterpret_cast<const bf16*>(qc->x8);
+        w = f.w_qkv;
+        c.fp8 = true;
+        c.a_scale = f.a_scale;
+        c.w_scale = f.w_scale;
+    } else if (qc != nullptr && qc->layers != nullptr) {
         const hra_fp8_layer& f = qc->layers[qc->layer];
         const void* w8s[4] = {f.w_qkv, f.w_o, f.w_gate_up, f.w_down};
         cudaError_t e = launch_fp8_quantize(a, (long long)M * K, f.a_scale + proj, qc->x8, st);
@@ -229,7 +269,8 @@ bool layer_ptrs_ok(const hra_layer_weights& l) {
 int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, const Ptrs& P, const Layout& L,
                int rows, int batch, int max_len, bool prefill, bool full_last, bf16* out_hidden,
                const int32_t* seq_lens_host, int max_pos, cudaStream_t st, int rope_rows = 0,
-               const int32_t* start_host = nullptr, const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr) {
+               const int32_t* start_host = nullptr, const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr,
+               const hra_nvfp4_layer* nv4 = nullptr) {
     const int H = d.hidden, hd = d.head_dim, nq = d.n_q_heads, nkv = d.n_kv_heads, F = d.ffn;
     const int Dq = nq * hd, Dqkv = (nq + 2 * nkv) * hd;
     const float eps = d.rms_eps;
@@ -259,8 +300,9 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
         const bool last = l == d.n_layers - 1;
-        const QuantCtx qc{fp8, amax, fp8 ? P.at<uint8_t>(L.x8) : nullptr, l};
-        const QuantCtx* qcp = (fp8 != nullptr || amax != nullptr) ? &qc : nullptr;
+        const QuantCtx qc{fp8, amax, (fp8 || nv4) ? P.at<uint8_t>(L.x8) : nullptr, l, nv4,
+                          nv4 ? P.at<uint8_t>(L.xs) : nullptr};
+        const QuantCtx* qcp = (fp8 != nullptr || amax != nullptr || nv4 != nullptr) ? &qc : nullptr;
         QkRopeArgs qa{};
         qa.qkv = qkv;
         qa.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
@@ -421,7 +463,8 @@ constexpr int H_ALIGN_FP8(int k) { return k % 128; }
 int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t* tokens_dev, const int32_t* seq_lens,
                  const int32_t* start_pos, int32_t batch, int32_t max_len, const hra_kv_cache* kv,
                  void* last_hidden_dev, void* workspace, size_t workspace_bytes, uint32_t flags, void* stream,
-                 const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr, bool validate_only = false) {
+                 const hra_fp8_layer* fp8 = nullptr, float* amax = nullptr, bool validate_only = false,
+                 const hra_nvfp4_layer* nv4 = nullptr) {
     if (dims == nullptr || weights == nullptr || tokens_dev == nullptr || seq_lens == nullptr || kv == nullptr)
         return HRA_ERR_INVALID_ARG;
     if (!dims_ok(dims)) return HRA_ERR_UNSUPPORTED;
@@ -458,7 +501,18 @@ int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t
                 return HRA_ERR_INVALID_ARG;
         }
     }
-    const Layout L = backbone_layout(d, batch, (int)T, max_end, max_end - 1, fp8 != nullptr);
+    if (nv4 != nullptr) {
+        if (H_ALIGN_FP8(d.hidden) != 0) return HRA_ERR_UNSUPPORTED;   // the band's FP8 QKV: 128-element K blocks
+        for (int l = 0; l < d.n_layers; ++l) {
+            const hra_nvfp4_layer& f = nv4[l];
+            if (!aligned16(f.w_qkv) || f.w_scale == nullptr || f.a_scale == nullptr ||
+                (reinterpret_cast<uintptr_t>(f.w_scale) & 3u) || (reinterpret_cast<uintptr_t>(f.a_scale) & 3u))
+                return HRA_ERR_INVALID_ARG;
+            for (int p = 1; p < 4; ++p)
+                if (!aligned16(f.codes[p]) || f.scales[p] == nullptr) return HRA_ERR_INVALID_ARG;
+        }
+    }
+    const Layout L = backbone_layout(d, batch, (int)T, max_end, max_end - 1, fp8 != nullptr, nv4 != nullptr);
     if (workspace_bytes < L.total) return HRA_ERR_WORKSPACE;
     if (validate_only) return HRA_OK;
 
@@ -474,7 +528,7 @@ int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t
                                  P.at<bf16>(L.y), (int)T, d.hidden, d.rms_eps, P.at<unsigned int>(L.err), st));
     return run_layers(d, *weights, *kv, P, L, (int)T, batch, max_len, true,
                       (flags & HRA_PREFILL_FULL_LAST_LAYER) != 0, reinterpret_cast<bf16*>(last_hidden_dev), seq_lens,
-                      max_end - 1, st, max_end, start_pos, fp8, amax);
+                      max_end - 1, st, max_end, start_pos, fp8, amax, nv4);
 }
 
 }  // namespace
@@ -507,6 +561,74 @@ int hra_prefill_fp8(const hra_dims* dims, const hra_weights* weights, const hra_
     if (fp8_layers == nullptr) return HRA_ERR_INVALID_ARG;
     return prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last_hidden_dev, workspace,
                         workspace_bytes, flags, stream, fp8_layers, nullptr);
+}
+
+size_t hra_prefill_nvfp4_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {
+    if (!dims_ok(dims) || batch < 1 || total_tokens < batch || max_len < 1) return 0;
+    return backbone_layout(*dims, batch, total_tokens, max_len, max_len - 1, false, true).total;
+}
+
+int hra_prefill_nvfp4(const hra_dims* dims, const hra_weights* weights, const hra_nvfp4_layer* nvfp4_layers,
+                      const int32_t* tokens_dev, const int32_t* seq_lens, int32_t batch, int32_t max_len,
+                      const hra_kv_cache* kv, void* last_hidden_dev, void* workspace, size_t workspace_bytes,
+                      uint32_t flags, void* stream) {
+    if (nvfp4_layers == nullptr) return HRA_ERR_INVALID_ARG;
+    return prefill_impl(dims, weights, tokens_dev, seq_lens, nullptr, batch, max_len, kv, last_hidden_dev, workspace,
+                        workspace_bytes, flags, stream, nullptr, nullptr, false, nvfp4_layers);
+}
+
+int hra_nvfp4_quantize_weight(const void* w_dev, int32_t rows, int32_t K, void* codes_dev, void* scales_dev,
+                              float* g_dev, void* stream) {
+    if (!aligned16(w_dev) || !aligned16(codes_dev) || scales_dev == nullptr || g_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(g_dev) & 3u) || rows < 1 || K < 16 || K % 16 != 0)
+        return HRA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bf16* w = reinterpret_cast<const bf16*>(w_dev);
+    HRA_TRY(launch_zero_floats(g_dev, 1, st));
+    HRA_TRY(launch_absmax(w, (long long)rows * K, g_dev, st));
+    HRA_TRY(launch_amax_div(g_dev, g_dev, 1, 6.0f * 448.0f, st));   // g = max|w| / (6 * 448), 1 if 0
+    HRA_TRY(launch_nvfp4_quantize(w, rows, K, g_dev, reinterpret_cast<uint8_t*>(codes_dev),
+                                  reinterpret_cast<uint8_t*>(scales_dev), st));
+    return HRA_OK;
+}
+
+int hra_nvfp4_band_scales(const float* amax_dev, float* scale_dev, int32_t n_layers, void* stream) {
+    if (amax_dev == nullptr || scale_dev == nullptr || (reinterpret_cast<uintptr_t>(amax_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(scale_dev) & 3u) || n_layers < 1)
+        return HRA_ERR_INVALID_ARG;
+    HRA_TRY(launch_nvfp4_band_scales(amax_dev, scale_dev, n_layers, reinterpret_cast<cudaStream_t>(stream)));
+    return HRA_OK;
+}
+
+size_t hra_linear_nvfp4_workspace_size(void) { return 256; }
+
+int hra_linear_nvfp4(const void* a_codes_dev, const void* a_scales_dev, const void* w_codes_dev,
+                     const void* w_scales_dev, void* out_dev, int32_t M, int32_t N, int32_t K, const float* g_a_dev,
+                     const float* g_w_dev, int32_t epilogue, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!aligned16(a_codes_dev) || !aligned16(w_codes_dev) || a_scales_dev == nullptr || w_scales_dev == nullptr ||
+        !aligned16(out_dev) || !aligned16(workspace) || g_a_dev == nullptr || g_w_dev == nullptr ||
+        (reinterpret_cast<uintptr_t>(g_a_dev) & 3u) || (reinterpret_cast<uintptr_t>(g_w_dev) & 3u))
+        return HRA_ERR_INVALID_ARG;
+    if (M < 1 || N < 8 || N % 8 != 0 || K < 64 || K % 64 != 0) return HRA_ERR_INVALID_ARG;
+    if (epilogue < EPI_STORE || epilogue > EPI_F32) return HRA_ERR_INVALID_ARG;
+    if (workspace_bytes < hra_linear_nvfp4_workspace_size()) return HRA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    HRA_TRY(cudaMemsetAsync(workspace, 0, 4, st));
+    Nvfp4Call n{};
+    n.a_codes = reinterpret_cast<const uint8_t*>(a_codes_dev);
+    n.a_scales = reinterpret_cast<const uint8_t*>(a_scales_dev);
+    n.w_codes = reinterpret_cast<const uint8_t*>(w_codes_dev);
+    n.w_scales = reinterpret_cast<const uint8_t*>(w_scales_dev);
+    n.g_a = g_a_dev;
+    n.g_w = g_w_dev;
+    n.out = out_dev;
+    n.err = reinterpret_cast<unsigned int*>(workspace);
+    n.M = M;
+    n.N = N;
+    n.K = K;
+    n.epi = epilogue;
+    HRA_TRY(launch_linear_nvfp4(n, st));
+    return HRA_OK;
 }
 
 size_t hra_fp8_calibrate_workspace_size(const hra_dims* dims, int32_t batch, int32_t total_tokens, int32_t max_len) {

@@ -1373,6 +1373,17 @@ cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
 
 }  // namespace
 
+bool make_map_u8(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
     return get_encoder() && make_map(m, base, rows, cols, box_rows, 2);
 }

@@ -233,6 +233,30 @@ struct HeadCall {
 };
 cudaError_t launch_audio_head(const HeadCall& c, cudaStream_t st);
 
+// ------------------------------------------------------------------ NVFP4 projection (nvfp4.cu)
+// out = epilogue((g_a g_w) sum_k e2m1(a) dec(sa) e2m1(w) dec(sw)); codes one per byte [rows][K],
+// block scales [rows][K/16] E4M3; w has N rows (2N for EPI_SWIGLU: gate rows, then up rows).
+struct Nvfp4Call {
+    const uint8_t* a_codes;
+    const uint8_t* a_scales;
+    const uint8_t* w_codes;
+    const uint8_t* w_scales;
+    const float* g_a;       // device scalars
+    const float* g_w;
+    void* out;
+    unsigned int* err;
+    int M, N, K;            // K a multiple of 64
+    int epi;                // EPI_STORE / EPI_RESIDUAL / EPI_SWIGLU / EPI_F32
+};
+cudaError_t launch_linear_nvfp4(const Nvfp4Call& c, cudaStream_t st);
+// NVFP4 band input scales from the calibration amax [n_layers][4] (see hra_nvfp4_band_scales)
+cudaError_t launch_nvfp4_band_scales(const float* amax, float* scale, int n_layers, cudaStream_t st);
+// out[i] = amax[i] > 0 ? amax[i] / div : 1
+cudaError_t launch_amax_div(const float* amax, float* out, int n, float div, cudaStream_t st);
+
+// 2-D uint8 tensor map [rows, cols] (cols innermost), boxes of 64 bytes x box_rows, no swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
+
 // 2-D bf16 tensor map [rows, cols] (cols innermost), 64-element x box_rows boxes, 128-byte
 // swizzle; encodings are cached by (base, shape, box).
 bool make_map_2d(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
