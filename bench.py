@@ -447,6 +447,12 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
     except Exception as ex:
         out["fp8_prefill"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
+    # ---- the NVFP4 band of the prefill projections on the same ragged batch
+    try:
+        out["nvfp4_prefill"] = bench_nvfp4(hra, W, torch, dev, w_backbone, peaks)
+    except Exception as ex:
+        out["nvfp4_prefill"] = {"error": repr(ex)}
+    torch.cuda.empty_cache()
     # ---- long prompts + 64 AR frames
     try:
         out["long_prompts"] = bench_long(hra, W, torch, dev, w_backbone)
@@ -655,6 +661,42 @@ def bench_fp8(hra, W, torch, dev, w_backbone, peaks):
     return {"prefill_tokens_per_s": p.total / (ms / 1e3), "prefill_ms": ms, "bf16_prefill_ms": ms16,
             "gate_up_tflops": tf, "gate_up_frac_of_fp8_peak": tf / peak8 if tf else None,
             "fp8_peak_tflops": peak8, "calibration": "4 prompts x 64 tokens, seed 99"}
+
+
+def bench_nvfp4(hra, W, torch, dev, w_backbone, peaks):
+    """The NVFP4 band (QKV in static FP8; output, gate/up and down in NVFP4 with per-call block
+    scales), calibrated on the FP8 variant's calibration batch, then the ragged batch's prefill.
+    The gate/up NVFP4 GEMM runs its MMAs on the exact f16 expansion of the NVFP4 values, so it is
+    reported against the measured bf16 burst peak (the rate of those MMAs) and against the nominal
+    dense FP4 rate (6 x that peak, the part's FP4 / BF16 ratio)."""
+    d = W.full_dims(36)
+    p = W.make_prompts(2, 32, 16, 256, d.vocab)
+    bb = hra.Backbone(d, w_backbone)
+    nv = hra.Nvfp4Backbone(bb)
+    cal = W.make_prompts(99, 4, 64, 64, d.vocab, fixed_len=64)
+    cache = hra.new_kv_cache(d, 32, 2048, dev)
+    nv.calibrate(cal.tokens.to(dev), cal.lengths, cache)
+    tok = p.tokens.to(dev)
+    out = torch.empty(32, d.hidden, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(nv.prefill_workspace_size(32, p.total, p.max_len), dtype=torch.uint8, device=dev)
+    run = lambda: nv.prefill(tok, p.lengths, cache, out=out, workspace=ws)
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    ms = events_time(run, 5, torch) / 5
+    hra.hra_probe_select("gate_up")
+    run()
+    hra.hra_probe_select("none")
+    gu_ms, gu_n, gu_flops = hra.hra_probe_collect()
+    bf = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    tf = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
+    wbytes = sum(nv.keep[l]["codes"][q].numel() + nv.keep[l]["scales"][q].numel()
+                 for l in range(d.n_layers) for q in (1, 2, 3))
+    del cache, nv
+    return {"prefill_tokens_per_s": p.total / (ms / 1e3), "prefill_ms": ms, "gate_up_tflops": tf,
+            "gate_up_frac_of_bf16_burst": tf / bf if tf else None,
+            "gate_up_frac_of_fp4_nominal": tf / (6.0 * bf) if tf else None,
+            "nvfp4_weight_bytes": wbytes, "calibration": "4 prompts x 64 tokens, seed 99"}
 
 
 def bench_long(hra, W, torch, dev, w_backbone):

@@ -15,7 +15,8 @@
 //
 // One CTA per 128 x 256 output tile (SwiGLU: 128 gate + the 128 matching up columns):
 //   warp 0     TMA of the E2M1 code tiles (64 K x 128 rows boxes, no swizzle) into a 3-stage ring;
-//   warps 2-9  expand codes x block scales into 128-byte-swizzled f16 tiles (a 2-stage ring), then,
+//   warps 2-9  expand codes x block scales into 128-byte-swizzled f16 tiles (a 3-stage ring; the
+//              hardware's E2M1 and E4M3 conversions to f16, then one f16 multiply each), then,
 //              after the last k-block, the epilogue from TMEM (two warps per lane quarter);
 //   warp 1     TMEM allocation and the MMA issue (one lane), 4 x (128 x 256 x 16) per k-block.
 #include <cuda_fp16.h>
@@ -32,7 +33,7 @@ constexpr int kNvThreads = 320;
 constexpr int kNvDeq = 256;          // expanding threads (warps 2-9)
 constexpr int kNvBN = 256;
 constexpr int kCodeStages = 3;
-constexpr int kHalfStages = 2;
+constexpr int kHalfStages = 3;
 constexpr int kACodes = 128 * 64;    // bytes
 constexpr int kWCodes = kNvBN * 64;
 constexpr int kCodeStage = kACodes + kWCodes;
@@ -61,22 +62,20 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Four E2M1 codes (one per byte, sign in bit 3) -> four f16 (two f16x2 words): the magnitude's high
-// byte comes from an 8-entry byte table (0, 0.5, 1, 1.5, 2, 3, 4, 6 have zero low bytes in f16).
-__device__ __forceinline__ uint2 e2m1x4_to_f16(uint32_t w) {
-    const uint32_t idx = w & 0x07070707u;
-    const uint32_t sgn = (w & 0x08080808u) << 4;
-    const uint32_t t = idx | (idx >> 4);
-    const uint32_t sel = (t & 0xFFu) | ((t >> 8) & 0xFF00u);
-    const uint32_t hb = __byte_perm(0x3E3C3800u, 0x46444240u, sel) | sgn;
-    return make_uint2(__byte_perm(hb, 0u, 0x1404), __byte_perm(hb, 0u, 0x3424));
+// Two E2M1 codes in the low bytes of w (one code per byte, sign in bit 3) -> f16x2 (the first code
+// in the low half), exactly: the codes are packed into one byte and converted by the hardware.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+    const uint32_t packed = (w & 0x0Fu) | ((w >> 4) & 0xF0u);
+    uint32_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(d) : "r"(packed));
+    return d;
 }
 
-// E4M3 code -> its value as f16 (exact: 4-bit significands between 2^-9 and 448).
-__device__ __forceinline__ __half e4m3_to_half(uint32_t c) {
-    const int E = (c >> 3) & 15, Mn = c & 7;
-    const float v = E == 0 ? ldexpf((float)Mn, -9) : ldexpf((float)(8 + Mn), E - 10);
-    return __float2half_rn((c & 0x80u) ? -v : v);
+// Two E4M3 codes in the low 16 bits of w -> f16x2 (exact).
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(w));
+    return *reinterpret_cast<__half2*>(&d);
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
@@ -96,7 +95,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     uint8_t* halfs = smem;                                           // f16 ring (1024-aligned stages)
     uint8_t* codes = smem + kHalfStages * kHalfStage;                // code ring
     uint64_t* bars = reinterpret_cast<uint64_t*>(codes + kCodeStages * kCodeStage);
-    // bars: code_full[3], code_empty[3], half_full[2], half_empty[2], tfull
+    // bars: code_full[3], code_empty[3], half_full[3], half_empty[3], tfull
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kCodeStages + 2 * kHalfStages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
@@ -207,36 +206,42 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             }
         }
     } else {
-        // ---- expansion: chunk q = td + 256 j (j < 12) of the k-block: A rows 0..127, then W rows
-        // 0..255, 8 chunks of 8 codes per 64-element row
+        // ---- expansion: block q = td + 256 j (j < 6) of the k-block -- 16 codes sharing one scale --
+        // A rows 0..127, then W rows 0..255, four 16-element blocks per 64-element row
         pdl_wait();
         asm volatile("bar.sync 2, 288;" ::: "memory");
         const int td = threadIdx.x - 64;
-        constexpr int kChunks = (kACodes + kWCodes) / 8 / kNvDeq;   // 12
-        // the global row of each chunk's block scales, or -1 past the matrix
-        const uint8_t* srow[kChunks];
+        constexpr int kBlocks = (kACodes + kWCodes) / 16 / kNvDeq;   // 6
+        const uint8_t* srow[kBlocks];   // the block's scale in k-block 0, or null past the matrix
+        uint32_t src_off[kBlocks], dst0[kBlocks], dst1[kBlocks];
 #pragma unroll
-        for (int j = 0; j < kChunks; ++j) {
+        for (int j = 0; j < kBlocks; ++j) {
             const int q = td + kNvDeq * j;
-            if (q < 1024) {
-                const int m = m0 + (q >> 3);
-                srow[j] = m < p.M ? p.a_scales + (long long)m * nb16 + ((q & 7) >> 1) : nullptr;
+            const bool is_a = q < 512;
+            const int r = is_a ? (q >> 2) : ((q - 512) >> 2);
+            const int blk = q & 3;
+            if (is_a) {
+                const int m = m0 + r;
+                srow[j] = m < p.M ? p.a_scales + (long long)m * nb16 + blk : nullptr;
             } else {
-                const int r = (q - 1024) >> 3;
-                const int wr = (r < 128 ? wrow0 + r : wrow1 + r - 128);
-                srow[j] = wr < p.w_rows ? p.w_scales + (long long)wr * nb16 + ((q & 7) >> 1) : nullptr;
+                const int wr = r < 128 ? wrow0 + r : wrow1 + r - 128;
+                srow[j] = wr < p.w_rows ? p.w_scales + (long long)wr * nb16 + blk : nullptr;
             }
+            src_off[j] = (is_a ? 0u : (uint32_t)kACodes) + (uint32_t)(r * 64 + blk * 16);
+            const uint32_t base = (is_a ? 0u : (uint32_t)kAHalf) + (uint32_t)(r * 128);
+            dst0[j] = base + (uint32_t)(((2 * blk) ^ (r & 7)) << 4);
+            dst1[j] = base + (uint32_t)(((2 * blk + 1) ^ (r & 7)) << 4);
         }
         int cs = 0, hs = 0;
         uint32_t cph = 0, hph = 0;
         bool ok = true;
-        uint8_t sc[kChunks];
+        uint32_t sc[kBlocks];
 #pragma unroll
-        for (int j = 0; j < kChunks; ++j) sc[j] = srow[j] ? __ldg(srow[j]) : 0;
+        for (int j = 0; j < kBlocks; ++j) sc[j] = srow[j] ? __ldg(srow[j]) : 0u;
         for (int i = 0; i < n_kb; ++i) {
-            uint8_t scn[kChunks];   // next k-block's scales, requested before this one is expanded
+            uint32_t scn[kBlocks];   // next k-block's scales, requested before this one is expanded
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) scn[j] = (srow[j] && i + 1 < n_kb) ? __ldg(srow[j] + 4 * (i + 1)) : 0;
+            for (int j = 0; j < kBlocks; ++j) scn[j] = (srow[j] && i + 1 < n_kb) ? __ldg(srow[j] + 4 * (i + 1)) : 0u;
             if (!mbar_wait(code_full(cs), cph, abort_flag) || !mbar_wait(half_empty(hs), hph ^ 1u, abort_flag)) {
                 *abort_flag = 1;
                 raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
@@ -246,21 +251,20 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             const uint8_t* cst = codes + cs * kCodeStage;
             uint8_t* hst = halfs + hs * kHalfStage;
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) {
-                const int q = td + kNvDeq * j;
-                const bool is_a = q < 1024;
-                const int r = is_a ? (q >> 3) : ((q - 1024) >> 3);
-                const int c = q & 7;
-                const uint2 cw = *reinterpret_cast<const uint2*>(cst + (is_a ? 0 : kACodes) + r * 64 + c * 8);
-                const __half hs_ = e4m3_to_half(sc[j]);
-                const __half2 s2 = __halves2half2(hs_, hs_);
-                const uint2 lo = e2m1x4_to_f16(cw.x), hi = e2m1x4_to_f16(cw.y);
-                uint4 o;
-                o.x = hmul2_u32(lo.x, s2);
-                o.y = hmul2_u32(lo.y, s2);
-                o.z = hmul2_u32(hi.x, s2);
-                o.w = hmul2_u32(hi.y, s2);
-                *reinterpret_cast<uint4*>(hst + (is_a ? 0 : kAHalf) + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+            for (int j = 0; j < kBlocks; ++j) {
+                const uint4 cw = *reinterpret_cast<const uint4*>(cst + src_off[j]);   // 16 codes
+                const __half2 s2 = e4m3x2_to_half2(sc[j] | (sc[j] << 8));
+                uint4 o0, o1;
+                o0.x = hmul2_u32(e2m1x2_to_f16x2(cw.x), s2);
+                o0.y = hmul2_u32(e2m1x2_to_f16x2(cw.x >> 16), s2);
+                o0.z = hmul2_u32(e2m1x2_to_f16x2(cw.y), s2);
+                o0.w = hmul2_u32(e2m1x2_to_f16x2(cw.y >> 16), s2);
+                o1.x = hmul2_u32(e2m1x2_to_f16x2(cw.z), s2);
+                o1.y = hmul2_u32(e2m1x2_to_f16x2(cw.z >> 16), s2);
+                o1.z = hmul2_u32(e2m1x2_to_f16x2(cw.w), s2);
+                o1.w = hmul2_u32(e2m1x2_to_f16x2(cw.w >> 16), s2);
+                *reinterpret_cast<uint4*>(hst + dst0[j]) = o0;
+                *reinterpret_cast<uint4*>(hst + dst1[j]) = o1;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
                 mbar_arrive(code_empty(cs));
             }
 #pragma unroll
-            for (int j = 0; j < kChunks; ++j) sc[j] = scn[j];
+            for (int j = 0; j < kBlocks; ++j) sc[j] = scn[j];
             if (++cs == kCodeStages) {
                 cs = 0;
                 cph ^= 1u;
