@@ -1,5 +1,6 @@
 import os
 import sys
+import tempfile
 
 import pytest
 
@@ -21,7 +22,7 @@ def orc():
 
 def pytest_sessionfinish(session, exitstatus):
     """Write the parity records of this session (tests/parity.py AUDIT) as JSON: to
-    $HRA_PARITY_AUDIT, else gpurun_out/parity_audit.json under the repository root."""
+    $HRA_PARITY_AUDIT, else parity_audit.json in the system's temporary directory."""
     try:
         import parity
     except Exception:
@@ -29,7 +30,7 @@ def pytest_sessionfinish(session, exitstatus):
     if not parity.AUDIT:
         return
     import json
-    path = os.environ.get("HRA_PARITY_AUDIT") or os.path.join(ROOT, "gpurun_out", "parity_audit.json")
-    os.makedirs(os.path.dirname(path), exist_ok=True)
+    path = os.environ.get("HRA_PARITY_AUDIT") or os.path.join(tempfile.gettempdir(), "parity_audit.json")
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
     with open(path, "w") as f:
         json.dump(parity.AUDIT, f, indent=0)
