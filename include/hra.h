@@ -443,6 +443,21 @@ uint64_t hra_launch_counter(void);
 int hra_probe_select(int kernel_class);
 int hra_probe_collect(double* total_ms, int64_t* launches, double* total_work);
 
+/* ---- decoder-pass form ---------------------------------------------------------------------- */
+/* Selects how a backbone pass over at most 64 token rows in BF16 runs (hra_decode, hra_decode_dev,
+ * hra_ar_frame, and hra_prefill / hra_prefill_chunk calls with at most 64 packed rows):
+ *   enable != 0: one persistent cooperative kernel walks every layer, with grid-wide barriers
+ *     between the phases of a layer, and streams the next projection's weights into shared memory
+ *     across those barriers (FlashRT PR #141, Performance: the AR decode time per frame;
+ *     vLLM-Omni PR #8226, Step-overhead reductions);
+ *   enable == 0 (default): one kernel per step of each layer, chained by programmatic dependent
+ *     launch (measured faster on GB300 for the batch sizes of the path).
+ * Both compute the same arithmetic (results may differ in the order of fp32 split sums).  In the
+ * persistent form every row runs every layer, including a prefill's last layer.  The setting is
+ * process-wide; calls already enqueued or captured keep the form they were issued with.  Returns
+ * the previous setting (0 or 1). */
+int32_t hra_set_decode_pass(int32_t enable);
+
 /* ---- errors --------------------------------------------------------------------------------- */
 /* Synchronise `stream` and return the sticky HRA_DEVERR_* bits of the last call that used this
  * workspace (each call clears them first), or a negative status. */

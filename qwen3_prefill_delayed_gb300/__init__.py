@@ -40,7 +40,7 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_work
             "hra_nvfp4_quantize_weight", "hra_linear_nvfp4_workspace_size", "hra_linear_nvfp4",
             "hra_nvfp4_band_scales",
             "hra_prefill_nvfp4_workspace_size", "hra_prefill_nvfp4",
-            "hra_launch_counter", "hra_probe_select", "hra_probe_collect",
+            "hra_launch_counter", "hra_probe_select", "hra_probe_collect", "hra_set_decode_pass",
             "hra_device_error", "hra_status_string"]
 PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6,
          "decode_attention": 7, "decode_linear": 8}
@@ -169,6 +169,8 @@ def lib() -> ctypes.CDLL:
         L.hra_launch_counter.restype = ctypes.c_uint64
         L.hra_probe_select.argtypes = [ctypes.c_int]
         L.hra_probe_select.restype = ctypes.c_int
+        L.hra_set_decode_pass.argtypes = [i32]
+        L.hra_set_decode_pass.restype = i32
         L.hra_probe_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                         ctypes.POINTER(ctypes.c_double)]
         L.hra_probe_collect.restype = ctypes.c_int
@@ -756,6 +758,12 @@ def hra_device_error(workspace: torch.Tensor, stream=None) -> int:
 def hra_launch_counter() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib().hra_launch_counter())
+
+
+def hra_set_decode_pass(enable: bool) -> bool:
+    """Run passes over at most 64 BF16 rows as one persistent kernel (True) or as one kernel per
+    step of each layer (False, the default); returns the previous setting."""
+    return bool(lib().hra_set_decode_pass(1 if enable else 0))
 
 
 def hra_probe_select(kernel_class: str) -> None:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhra.so")
 SOURCES = ["api.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "elementwise.cu", "codebook.cu", "fp8.cu",
-           "noalloc.cu", "head.cu", "nvfp4.cu"]
+           "noalloc.cu", "head.cu", "nvfp4.cu", "decode_pass.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -75,7 +75,8 @@ struct Region {
 
 // Offsets (bytes) of every buffer inside a caller workspace.
 struct Layout {
-    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, xs, total;
+    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, xs, sync, total;
+    size_t part_bytes;
     int attn_splits;
 };
 
@@ -132,12 +133,15 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     part = std::max(part, linear_partial_bound(m_split, (int)H, (int)F, EPI_RESIDUAL));
     if (std::max(rows, batch) > 128) part = std::max(part, linear_tail_bound());
     L.part = g.take(part);
+    L.part_bytes = part;
     L.attn_splits = decode_attention_splits(batch, d.n_kv_heads, max_pos);
     L.apart = g.take(decode_attention_scratch_bytes(batch, d.n_q_heads, d.head_dim, L.attn_splits));
     // FP8 variant: the E4M3 copy of the current projection's input (the widest input is the FFN's)
     L.x8 = (fp8 || nvfp4) ? g.take(T * std::max(std::max(H, Dq), F)) : 0;
     // NVFP4 band: the E4M3 block scales of that input (one per 16 elements)
     L.xs = nvfp4 ? g.take(T * std::max(std::max(H, Dq), F) / 16) : 0;
+    // counters and per-row sums of the persistent decoder pass (M <= 64 rows)
+    L.sync = g.take(decode_pass_sync_bytes((int)std::min<size_t>(T, 64), d.n_kv_heads, (int)F, (int)H));
     L.total = g.off;
     return L;
 }
@@ -296,6 +300,66 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
     }
     const int lin_probe = prefill ? 0 : HRA_PROBE_DECODE_LINEAR;
 
+    // At most 64 rows in BF16, when selected (hra_set_decode_pass): the whole pass is one persistent
+    // kernel (decode_pass.cu).  Every row runs every layer; the final norm goes to the last row of
+    // each sequence (prefill) or to every row (decode).
+    if (g_decode_pass_enabled && rows <= 64 && fp8 == nullptr && amax == nullptr && nv4 == nullptr &&
+        d.n_layers <= kDecodePassMaxLayers) {
+        DecodePassCall c{};
+        for (int l = 0; l < d.n_layers; ++l) {
+            const hra_layer_weights& lw = w.layers[l];
+            DecodePassLayer& dl = c.layers[l];
+            dl.w_qkv = reinterpret_cast<const bf16*>(lw.w_qkv);
+            dl.w_o = reinterpret_cast<const bf16*>(lw.w_o);
+            dl.w_gate_up = reinterpret_cast<const bf16*>(lw.w_gate_up);
+            dl.w_down = reinterpret_cast<const bf16*>(lw.w_down);
+            dl.attn_norm = reinterpret_cast<const bf16*>(lw.attn_norm);
+            dl.q_norm = reinterpret_cast<const bf16*>(lw.q_norm);
+            dl.k_norm = reinterpret_cast<const bf16*>(lw.k_norm);
+            dl.mlp_norm = reinterpret_cast<const bf16*>(lw.mlp_norm);
+            dl.kv = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
+        }
+        c.final_norm = reinterpret_cast<const bf16*>(w.final_norm);
+        c.L = d.n_layers;
+        c.M = rows;
+        c.H = H;
+        c.nq = nq;
+        c.nkv = nkv;
+        c.hd = hd;
+        c.F = F;
+        c.n_slots = kv.n_slots;
+        c.eps = eps;
+        c.rope = P.at<float2>(L.rope);
+        c.rope_rows = prefill ? rope_rows : batch;
+        c.rope_row_is_pos = prefill ? 1 : 0;
+        c.row_seq = row_seq;
+        c.row_pos = row_pos;
+        c.last_row = prefill ? last_row : nullptr;
+        c.n_out = prefill ? batch : rows;
+        int mp = 0;
+        for (int b = 0; b < batch && seq_lens_host != nullptr; ++b)
+            mp = std::max(mp, prefill ? (start_host ? start_host[b] : 0) + seq_lens_host[b] - 1 : seq_lens_host[b]);
+        c.max_pos = seq_lens_host != nullptr ? mp : max_pos;
+        c.r = r;
+        c.y = y;
+        c.q = q;
+        c.att = att;
+        c.h = h;
+        c.out = out_hidden;
+        c.part = P.at<float>(L.part);
+        c.part_bytes = L.part_bytes;
+        c.apart = P.at<float>(L.apart);
+        // the attention scratch holds L.attn_splits splits of `batch` rows
+        c.attn_splits_max = std::max(1, L.attn_splits * batch / std::max(1, rows));
+        c.sync = P.at<unsigned int>(L.sync);
+        c.sync_zeroed = true;   // cleared by the call's row-map kernel
+        c.err = P.at<unsigned int>(L.err);
+        if (decode_pass_supported(c)) {
+            HRA_TRY(launch_decode_pass(c, st));
+            return HRA_OK;
+        }
+    }
+
     for (int l = 0; l < d.n_layers; ++l) {
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
@@ -421,6 +485,12 @@ extern "C" {
 
 uint64_t hra_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int32_t hra_set_decode_pass(int32_t enable) {
+    const bool prev = hra::g_decode_pass_enabled;
+    hra::g_decode_pass_enabled = enable != 0;
+    return prev ? 1 : 0;
+}
+
 int hra_probe_select(int kernel_class) {
     std::lock_guard<std::mutex> lk(g_probe.mu);
     g_probe.active = kernel_class;
@@ -520,7 +590,8 @@ int prefill_impl(const hra_dims* dims, const hra_weights* weights, const int32_t
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
     HRA_TRY(launch_build_rowmap(meta, (int)T, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
                                 P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), P.at<int32_t>(L.start),
-                                P.at<unsigned int>(L.err), st));
+                                P.at<unsigned int>(L.err), st, P.at<unsigned int>(L.sync),
+                                decode_pass_counter_words(std::min((int)T, 64), d.n_kv_heads)));
     HRA_TRY(launch_rope_table(max_end, nullptr, d.head_dim, (double)d.rope_theta, P.at<float2>(L.rope), st));
     HRA_TRY(launch_embed_rmsnorm(tokens_dev, max_len, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.cu),
                                  reinterpret_cast<const bf16*>(weights->embed), d.vocab,
@@ -748,7 +819,7 @@ int decode_impl(const hra_dims* dims, const hra_weights* weights, const void* in
     const Ptrs P{reinterpret_cast<uint8_t*>(workspace)};
     HRA_TRY(launch_build_rowmap(meta, batch, P.at<int32_t>(L.row_seq), P.at<int32_t>(L.row_pos),
                                 P.at<int32_t>(L.cu), P.at<int32_t>(L.last_row), nullptr, P.at<unsigned int>(L.err),
-                                st));
+                                st, P.at<unsigned int>(L.sync), decode_pass_counter_words(std::min(batch, 64), d.n_kv_heads)));
     HRA_TRY(launch_rope_table(batch, P.at<int32_t>(L.row_pos), d.head_dim, (double)d.rope_theta,
                               P.at<float2>(L.rope), st));
     // r = input embedding, y = RMSNorm(r) with layer 0's attention gain

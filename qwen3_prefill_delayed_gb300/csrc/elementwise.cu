@@ -19,10 +19,13 @@ namespace hra {
 namespace {
 
 __global__ void build_rowmap_kernel(const SeqMeta meta, int T, int32_t* row_seq, int32_t* row_pos,
-                                    int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err) {
+                                    int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
+                                    unsigned int* zero_ptr, int zero_words) {
     pdl_launch();
     pdl_wait();
     if (err != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *err = 0u;   // first kernel of a call
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0u;
     __shared__ int32_t s_vals[kMaxBatch + 1];
     const int B = meta.batch;
     const int nvals = meta.mode == 0 ? B + 1 : B;
@@ -310,11 +313,11 @@ inline unsigned blocks_for(long long threads, int per_block) {
 
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
                                 int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
-                                cudaStream_t st) {
+                                cudaStream_t st, unsigned int* zero_ptr, int zero_words) {
     const int threads = 256;
     const unsigned blocks = meta.mode == 2 ? 1u : blocks_for(total_rows > 0 ? total_rows : 1, threads);
     HRA_LAUNCH(build_rowmap_kernel, dim3(blocks), dim3(threads), 0, st, meta, total_rows, row_seq, row_pos, cu, last_row,
-               seq_start, err);
+               seq_start, err, zero_ptr, zero_ptr ? zero_words : 0);
     return cudaGetLastError();
 }
 

@@ -129,10 +129,11 @@ struct SeqMeta {
 
 // Writes row_seq[T], row_pos[T] (sequence index and position of each packed row), and for prefill
 // cu[batch+1], last_row[batch]; for decode last_row[b] = b.  Also clears the call's error word.
-// Prefill also writes seq_start[batch] = meta.start (may be null for decode).
+// Prefill also writes seq_start[batch] = meta.start (may be null for decode).  zero_words words at
+// zero_ptr are cleared as well (the counters of the persistent decoder pass).
 cudaError_t launch_build_rowmap(const SeqMeta& meta, int total_rows, int32_t* row_seq, int32_t* row_pos,
                                 int32_t* cu, int32_t* last_row, int32_t* seq_start, unsigned int* err,
-                                cudaStream_t st);
+                                cudaStream_t st, unsigned int* zero_ptr = nullptr, int zero_words = 0);
 
 // cos/sin table, transposed: entry (row r, pair i) at i * n_rows + r (float2), for position
 // pos_of_row[r] (or r when null).
@@ -187,6 +188,55 @@ struct DecodeAttnArgs {
 int decode_attention_splits(int rows, int nkv, int max_pos);
 size_t decode_attention_scratch_bytes(int rows, int nq, int hd, int splits);
 cudaError_t launch_decode_attention(const DecodeAttnArgs& a, cudaStream_t st);
+
+// ------------------------------------------------------------------ persistent decoder pass
+// Every layer over M <= 64 token rows in one cooperative launch (decode_pass.cu): the arithmetic of
+// the layer-by-layer path, with grid-wide barriers between the phases of a layer.
+constexpr int kDecodePassMaxLayers = 40;
+struct DecodePassLayer {
+    const bf16* w_qkv;
+    const bf16* w_o;
+    const bf16* w_gate_up;
+    const bf16* w_down;
+    const bf16* attn_norm;
+    const bf16* q_norm;
+    const bf16* k_norm;
+    const bf16* mlp_norm;
+    bf16* kv;                 // this layer's cache block [cache_batch][2][nkv][n_slots][hd]
+};
+struct DecodePassCall {
+    DecodePassLayer layers[kDecodePassMaxLayers];
+    const bf16* final_norm;
+    int L, M, H, nq, nkv, hd, F, n_slots;
+    float eps;
+    const float2* rope;       // transposed table (see QkRopeArgs)
+    int rope_rows, rope_row_is_pos;
+    const int32_t* row_seq;
+    const int32_t* row_pos;
+    const int32_t* last_row;  // output row b = row last_row[b], b < n_out; null: output row b = row b
+    int n_out;
+    int max_pos;              // upper bound of every row's position (sizes the attention's key splits)
+    bf16* r;                  // residual [M, H] (in: the layer-0 input), y [M, H] (in: its RMSNorm)
+    bf16* y;
+    bf16* q;                  // [M, nq * hd]
+    bf16* att;                // [M, nq * hd]
+    bf16* h;                  // [M, F]
+    bf16* out;                // [n_out, H] final-norm output
+    float* part;              // projection split partials
+    size_t part_bytes;
+    float* apart;             // attention split partials
+    int attn_splits_max;      // splits the attention scratch holds
+    unsigned int* sync;       // decode_pass_sync_bytes(M, nkv, F, H) bytes
+    bool sync_zeroed;         // the first decode_pass_counter_words(M, nkv) words of sync are zero
+    unsigned int* err;
+};
+int decode_pass_counter_words(int M, int nkv);
+bool decode_pass_supported(const DecodePassCall& c);
+size_t decode_pass_scratch_bytes(int M, int H, int nq, int nkv, int hd, int F, int nsm);
+size_t decode_pass_sync_bytes(int M, int nkv, int F, int H);
+cudaError_t launch_decode_pass(const DecodePassCall& c, cudaStream_t st);
+// process-wide switch between the persistent pass (default) and the layer-by-layer kernels
+extern bool g_decode_pass_enabled;
 
 // ------------------------------------------------------------------ codebook step finalize
 struct CodebookArgs {

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import workloads as W
-from parity import assert_parity, ref_np, to_np
+from parity import ARGMAX_MARGIN, assert_parity, ref_np, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,21 +50,42 @@ def test_tiny_graph_loop_matches_oracle(hra):
     hw = oracle.host_weights_from(d, wl["weights"])
     head_u, tab_u = W.to_u16(wl["audio"]["head_w"]), W.to_u16(wl["audio"]["code_emb"])
 
+    codes_g = loop.codes_seq.cpu().numpy()
+    K, Vc = d.n_codebooks, d.codebook_size
+
     def oracle_loop():
+        """The oracle's loop; where its codes differ from the GPU's it checks that the oracle's own
+        top-1 / top-2 margin is a near-tie (the stated bar: 0.1) and continues from the GPU's codes."""
         kv, h = oracle.prefill(d, hw, p.tokens.numpy(), p.lengths, n_slots)
         st = np.array([[0, -1, 0, 0]], np.int32)
-        codes, dones = [], []
+        codes, dones, excused = [], [], 0
         for t in range(F):
-            c, nxt, dn, _ = oracle.codebook_step(d, h, head_u, tab_u, st, wl["eoc_bias"][t].numpy())
+            bias = wl["eoc_bias"][t].numpy()
+            st0 = st.copy()
+            c, nxt, dn, lg = oracle.codebook_step(d, h, head_u, tab_u, st, bias)
+            if not np.array_equal(c, codes_g[t]):
+                for k in np.nonzero(c[0] != codes_g[t, 0])[0]:
+                    z = lg[0, k] + np.where(np.arange(Vc) == d.eoc_id, bias[0, k], 0.0)
+                    top = np.sort(z)[-2:]
+                    assert top[1] - top[0] <= ARGMAX_MARGIN, f"frame {t} codebook {k}: argmax differs"
+                excused += 1
+                c = codes_g[t].copy()
+                nxt = oracle.code_embed_sum(tab_u, c)
+                st = st0
+                forced = np.full((1, K, Vc), -1e30, np.float32)
+                for k in range(K):
+                    forced[0, k, c[0, k]] = 0.0
+                _, dn = oracle.delay_step(K, Vc, d.bos_id, d.eoc_id, forced, None, st)
             codes.append(c)
             dones.append(dn)
             h = oracle.decode(d, hw, nxt, [n + t], kv, n_slots)
-        return kv, h, st, np.stack(codes), np.stack(dones)
+        return kv, h, st, np.stack(codes), np.stack(dones), excused
 
-    kv_o, h_o, st_o, codes_o, done_o = oracle_loop()
+    kv_o, h_o, st_o, codes_o, done_o, excused = oracle_loop()
     with oracle.sum_order(True):
-        kv_a, h_a, _, _, _ = oracle_loop()
-    assert loop.codes_seq.cpu().numpy().tolist() == codes_o.tolist()
+        kv_a, h_a, _, _, _, _ = oracle_loop()
+    assert excused <= 1, f"{excused} frames needed the near-tie excuse"
+    assert codes_g.tolist() == codes_o.tolist()
     assert loop.done_seq.cpu().numpy().tolist() == done_o.tolist()
     assert loop.done_seq[:, 0].cpu().tolist() == [0, 0, 0, 0, 0, 1]
     assert loop.state.cpu().numpy().tolist() == st_o.tolist()

@@ -108,6 +108,7 @@ def test_tiny_ar_loop(hra, tiny):
     st_o = np.array([[0, -1, 0, 0]], np.int32)
     K = d.n_codebooks
     logits = torch.empty(1, K, d.codebook_size, dtype=torch.float32, device=DEV)
+    excused = 0
     for t in range(tiny["frames"]):
         bias = tiny["eoc_bias"][t]
         st_before = state.cpu().numpy().copy()
@@ -121,7 +122,18 @@ def test_tiny_ar_loop(hra, tiny):
         c_chk, d_chk = oracle.delay_step(K, d.codebook_size, d.bos_id, d.eoc_id, lg, bias.numpy(), st_chk)
         assert codes.cpu().numpy().tolist() == c_chk.tolist()
         assert state.cpu().numpy().tolist() == st_chk.tolist() and done.cpu().numpy().tolist() == d_chk.tolist()
-        assert codes.cpu().numpy().tolist() == c_o.tolist(), f"frame {t}"
+        c_g = codes.cpu().numpy()
+        if not np.array_equal(c_g, c_o):
+            # the stated bar: codes agree wherever the oracle's top-1 / top-2 margin exceeds 0.1; at
+            # a near-tie the oracle continues from the GPU's codes (its state machine on the GPU's
+            # logits was checked bit-exact above)
+            for k in np.nonzero(c_o[0] != c_g[0])[0]:
+                z = lg_o[0, k] + np.where(np.arange(d.codebook_size) == d.eoc_id, bias[0, k].item(), 0.0)
+                top = np.sort(z)[-2:]
+                assert top[1] - top[0] <= ARGMAX_MARGIN, f"frame {t} codebook {k}: argmax differs"
+            excused += 1
+            n_o = oracle.code_embed_sum(tab_u, c_g)
+            st_o = st_chk.copy()
         assert done.item() == int(t == 5) and state[0, 1].item() == (2 if t >= 2 else -1)
         np.testing.assert_array_equal(W.to_u16(nxt.cpu()), n_o)
         pos = p.lengths[0] + t
@@ -130,6 +142,7 @@ def test_tiny_ar_loop(hra, tiny):
         with oracle.sum_order(True):
             hid_a = oracle.decode(d, tiny["hw"], n_o, [pos], kv_a, n_slots)
         assert_parity(to_np(hid), ref_np(hid_o), ref_np(hid_a), what=f"decode hidden frame {t}")
+    assert excused <= 1, f"{excused} frames needed the near-tie excuse"
     n = p.lengths[0] + tiny["frames"]
     _check_kv(cache, kv_o, kv_a, [n], "kv after decode")
 
