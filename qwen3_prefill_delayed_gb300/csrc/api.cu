@@ -182,10 +182,9 @@ cudaError_t linear(const bf16* a, const void* w, void* out, int M, int N, int K,
                    const Layout& L, cudaStream_t st, int probe_class = HRA_PROBE_NONE,
                    const void* norm_gain = nullptr, bf16* norm_out = nullptr, float eps = 0.f,
                    const int32_t* norm_rows = nullptr, int norm_nrows = 0, const QkRopeArgs* qk = nullptr,
-                   bool* qk_done = nullptr, bool shallow_ring = false, const QuantCtx* qc = nullptr,
+                   bool* qk_done = nullptr, const QuantCtx* qc = nullptr,
                    int proj = PROJ_QKV) {
     LinearCall c{};
-    c.shallow_ring = shallow_ring;
     if (qc != nullptr && qc->amax != nullptr) {
         cudaError_t e = launch_absmax(a, (long long)M * K, qc->amax + 4 * qc->layer + proj, st);
         if (e != cudaSuccess) return e;
@@ -386,7 +385,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         qa.eps = eps;
         bool qk_done = false;
         HRA_TRY(linear(y, lw.w_qkv, qkv, rows, Dqkv, H, EPI_STORE, P, L, st, prefill ? HRA_PROBE_QKV : lin_probe, nullptr,
-                       nullptr, 0.f, nullptr, 0, &qa, &qk_done, false, qcp, PROJ_QKV));
+                       nullptr, 0.f, nullptr, 0, &qa, &qk_done, qcp, PROJ_QKV));
         if (!qk_done) HRA_TRY(launch_qk_rope_kv(qa, st));
 
         const bool tail = prefill && last && !full_last;
@@ -418,20 +417,20 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             }
             HRA_TRY(linear(att, lw.w_o, r, rows, H, Dq, EPI_RESIDUAL, P, L, st,
                            prefill ? HRA_PROBE_O_PROJ : lin_probe, lw.mlp_norm, y, eps, nullptr, 0, nullptr,
-                           nullptr, /*shallow_ring=*/!prefill, qcp, PROJ_O));
+                           nullptr, qcp, PROJ_O));
             HRA_TRY(linear(y, lw.w_gate_up, h, rows, F, H, EPI_SWIGLU, P, L, st,
                            prefill ? HRA_PROBE_GATE_UP : lin_probe, nullptr, nullptr, 0.f, nullptr, 0, nullptr,
-                           nullptr, false, qcp, PROJ_GATE_UP));
+                           nullptr, qcp, PROJ_GATE_UP));
             if (!last) {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st,
                                prefill ? HRA_PROBE_DOWN : lin_probe, w.layers[l + 1].attn_norm, y, eps, nullptr, 0,
-                               nullptr, nullptr, false, qcp, PROJ_DOWN));
+                               nullptr, nullptr, qcp, PROJ_DOWN));
             } else if (!prefill) {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, lin_probe, w.final_norm,
-                               out_hidden, eps, nullptr, 0, nullptr, nullptr, false, qcp, PROJ_DOWN));
+                               out_hidden, eps, nullptr, 0, nullptr, nullptr, qcp, PROJ_DOWN));
             } else {
                 HRA_TRY(linear(h, lw.w_down, r, rows, H, F, EPI_RESIDUAL, P, L, st, HRA_PROBE_DOWN,
-                               w.final_norm, out_hidden, eps, last_row, batch, nullptr, nullptr, false, qcp,
+                               w.final_norm, out_hidden, eps, last_row, batch, nullptr, nullptr, qcp,
                                PROJ_DOWN));
             }
         } else {
@@ -454,11 +453,11 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             HRA_TRY(launch_decode_attention(da, st));
             HRA_TRY(launch_rmsnorm(r, last_row, nullptr, nullptr, rl, batch, H, eps, st));   // gather
             HRA_TRY(linear(att, lw.w_o, rl, batch, H, Dq, EPI_RESIDUAL, P, L, st, 0, lw.mlp_norm, y, eps, nullptr, 0,
-                           nullptr, nullptr, /*shallow_ring=*/true, qcp, PROJ_O));
+                           nullptr, nullptr, qcp, PROJ_O));
             HRA_TRY(linear(y, lw.w_gate_up, h, batch, F, H, EPI_SWIGLU, P, L, st, 0, nullptr, nullptr, 0.f, nullptr, 0,
-                           nullptr, nullptr, false, qcp, PROJ_GATE_UP));
+                           nullptr, nullptr, qcp, PROJ_GATE_UP));
             HRA_TRY(linear(h, lw.w_down, rl, batch, H, F, EPI_RESIDUAL, P, L, st, 0, w.final_norm, out_hidden, eps,
-                           nullptr, 0, nullptr, nullptr, false, qcp, PROJ_DOWN));
+                           nullptr, 0, nullptr, nullptr, qcp, PROJ_DOWN));
         }
     }
     return HRA_OK;

@@ -219,14 +219,27 @@ __global__ void qk_rope_kv_kernel(const QkRopeArgs a) {
             const float* ps = a.part + (long long)row * a.ldp + (long long)hh * HD + sub * E;
 #pragma unroll
             for (int e = 0; e < E; ++e) x[e] = 0.f;
-            for (int sp = 0; sp < a.splits; ++sp) {
+            constexpr int kBatch = 8;   // split partials loaded together before they are added
+            for (int s0 = 0; s0 < a.splits; s0 += kBatch) {
+                float4 v[kBatch][E / 4];
 #pragma unroll
-                for (int e = 0; e < E; e += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(ps + sp * a.split_stride + e);
-                    x[e] += v.x;
-                    x[e + 1] += v.y;
-                    x[e + 2] += v.z;
-                    x[e + 3] += v.w;
+                for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+                    for (int e = 0; e < E / 4; ++e)
+                        v[b][e] = s0 + b < a.splits
+                                      ? *reinterpret_cast<const float4*>(ps + (s0 + b) * a.split_stride + 4 * e)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    if (s0 + b < a.splits) {
+#pragma unroll
+                        for (int e = 0; e < E / 4; ++e) {
+                            x[4 * e] += v[b][e].x;
+                            x[4 * e + 1] += v[b][e].y;
+                            x[4 * e + 2] += v[b][e].z;
+                            x[4 * e + 3] += v[b][e].w;
+                        }
+                    }
                 }
             }
 #pragma unroll

@@ -32,7 +32,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;       // small-M kernel: TMA warp, MMA warp, 4 epilogue warps
 constexpr int kTileThreads = 320;   // tile kernel: TMA warp, MMA warp, 8 epilogue warps
 
 enum KMode : int { KM_STORE = 0, KM_RESIDUAL = 1, KM_SWIGLU = 2, KM_F32 = 3, KM_PARTIAL = 4, KM_QKROPE = 5 };
@@ -522,319 +521,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     }
 }
 
-// ------------------------------------------------------------------ small M: weights as the MMA rows
-// For M <= 64 activation rows the operands swap roles: a 128-row weight tile is the tcgen05 A
-// operand and the (zero-padded) activation rows are its N = NB columns, so no shared memory is
-// spent on empty activation rows and ~10 stages of weight tiles stay in flight per SM.  The
-// accumulator D[weight row][activation row] (NB columns) is written back transposed; a warp's
-// stores cover 32 consecutive output columns.  SwiGLU tiles hold 64 gate and 64 up rows and always
-// go through fp32 partials (the reduction applies the activation).
-// Weight ring of the small-M kernel, chosen per launch.  Deep (about 200 KB): enough bytes in
-// flight for a long weight stream.  Shallow (about 100 KB): two CTAs fit on an SM, so a launch that
-// follows an attention or GEMM kernel starts streaming its weights while that kernel drains.
-constexpr int kSmallRingDeep = 200 * 1024;
-constexpr int kSmallRingShallow = 100 * 1024;
-constexpr int kSwigluXchBytes = 64 * 17 * 4;   // up-row accumulators handed to the gate rows
-
-template <int NB>
-struct SwCfg {
-    static constexpr int A_BYTES = 128 * BK * 2;
-    static constexpr int B_BYTES = NB * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int MAX_STAGES = kSmallRingDeep / STAGE_BYTES > 12 ? 12 : kSmallRingDeep / STAGE_BYTES;
-    static constexpr int stages_for(int ring_bytes) {
-        return ring_bytes / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : ring_bytes / STAGE_BYTES;
-    }
-    // ring, alignment slack, barriers and slots, SwiGLU exchange
-    static constexpr int smem_bytes(int stages) { return stages * STAGE_BYTES + 1024 + 256 + kSwigluXchBytes; }
-    static constexpr uint32_t TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
-};
-
-struct SwArgs {
-    void* out;
-    unsigned int* err;
-    long long split_stride;
-    int M;           // activation rows (<= NB)
-    int n_valid;     // valid output columns (N, or F for SwiGLU)
-    int ldo;
-    int n_kb, kb_per_split;
-    int up_row0;     // SwiGLU: first up row in W (= F)
-    int mode;        // KM_STORE / KM_RESIDUAL / KM_SWIGLU (one K split) / KM_F32 / KM_PARTIAL
-    int nt, splits;
-    unsigned int* zero_ptr;
-    int zero_words;
-    int rpu;         // > 0: unit u covers weight rows [u*rpu, u*rpu + rpu) over the whole K (rpu < 128;
-                     // the tile rows past rpu stay zero); 0: 128-row tiles
-    int w_box_bytes; // bytes of one weight box (rpu or 128 rows x 128 B)
-    int stages;      // ring depth of this launch (<= SwCfg::MAX_STAGES)
-};
-
-// OR of `v` over the four epilogue warps (named barrier 1, 128 threads); every one of them gets
-// the same answer.
-__device__ __forceinline__ bool bar_or_epilogue(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, 128, pi;\n"
-        " selp.u32 %0, 1, 0, po;\n}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
-template <int NB, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_smallm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const SwArgs p) {
-    using C = SwCfg<NB>;
-    pdl_launch();
-    const int S = p.stages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
-    int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
-    float* xch = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES + 256);   // [64][17]
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = p.nt * p.splits;
-
-    auto full_bar = [&](int s) { return smem_u32(bars + s); };
-    auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
-    auto tfull_bar = [&](int b) { return smem_u32(bars + 2 * S + b); };
-    auto tempty_bar = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
-    auto a_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
-    auto b_tile = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);
-        }
-        *abort_flag = 0;
-        *issued_slot = 0;
-        *committed_slot = 0;
-        mbar_fence_init();
-        tma_prefetch_map(&tmW);
-        tma_prefetch_map(&tmX);
-    }
-    if (p.rpu > 0) {   // rows [rpu, 128) of every weight tile are never loaded: make them zero once
-        for (int s = 0; s < S; ++s) {
-            uint4* t = reinterpret_cast<uint4*>(smem + s * C::STAGE_BYTES + p.rpu * 128);
-            const int n16 = (128 - p.rpu) * 128 / 16;
-            for (int i = threadIdx.x; i < n16; i += blockDim.x) t[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const int stage_tx = p.w_box_bytes + C::B_BYTES;
-
-    if (warp == 0 && lane == 0) {
-        auto load_w = [&](int s, int kx, int nb) {
-            if (p.rpu > 0) {
-                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * p.rpu);
-            } else if (SWIGLU) {
-                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * 64);
-                tma_load_2d(a_tile(s) + C::A_BYTES / 2, &tmW, full_bar(s), kx, p.up_row0 + nb * 64);
-            } else {
-                tma_load_2d(a_tile(s), &tmW, full_bar(s), kx, nb * 128);
-            }
-        };
-        // weight tiles of the first ring stages before waiting for earlier kernels
-        int pre = 0;
-        for (int u = blockIdx.x; u < units && pre < S; u += gridDim.x) {
-            const int sp = u / p.nt, nb = u - sp * p.nt;
-            const int kb0 = sp * p.kb_per_split;
-            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-            for (int kb = kb0; kb < kb1 && pre < S; ++kb, ++pre) {
-                mbar_expect_tx(full_bar(pre), stage_tx);
-                load_w(pre, kb * BK, nb);
-            }
-        }
-        pdl_wait();
-        int it = 0, s = 0;          // ring slot of iteration it, and that slot's phase
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int sp = u / p.nt, nb = u - sp * p.nt;
-            const int kb0 = sp * p.kb_per_split;
-            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-            for (int kb = kb0; kb < kb1; ++kb, ++it, s = s + 1 == S ? 0 : s + 1, ph ^= (s == 0 ? 1u : 0u)) {
-                const int kx = kb * BK;
-                if (it >= pre) {
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
-                        *abort_flag = 1;
-                        raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(full_bar(s), stage_tx);
-                    load_w(s, kx, nb);
-                }
-                tma_load_2d(b_tile(s), &tmX, full_bar(s), kx, 0);
-            }
-        }
-        *issued_slot = ok ? it : max(it, pre);
-    } else if (warp == 1 && lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
-        int it = 0, j = 0, s = 0;   // ring slot of iteration it, and that slot's phase
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
-            const int sp = u / p.nt;
-            const int kb0 = sp * p.kb_per_split;
-            const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
-            const int buf = j & 1;
-            const uint32_t d_tmem = tmem + (uint32_t)(buf * NB);
-            if (!mbar_wait(tempty_bar(buf), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
-                *abort_flag = 1;
-                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                break;
-            }
-            tc_fence_after();
-            for (int kb = kb0; kb < kb1; ++kb, ++it, s = s + 1 == S ? 0 : s + 1, ph ^= (s == 0 ? 1u : 0u)) {
-                if (!mbar_wait(full_bar(s), ph, abort_flag)) {
-                    *abort_flag = 1;
-                    raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t ad = sdesc_sw128(a_tile(s));
-                const uint64_t bd = sdesc_sw128(b_tile(s));
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                tc_commit(empty_bar(s));
-            }
-            tc_commit(tfull_bar(buf));
-            *committed_slot = j + 1;
-        }
-    } else if (warp >= 2) {
-        pdl_wait();
-        if (blockIdx.x == 0 && warp == 2)
-            for (int i = lane; i < p.zero_words; i += 32) p.zero_ptr[i] = 0u;
-        const int quad = warp & 3;
-        const int r = quad * 32 + lane;   // weight row inside the tile
-        int j = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
-            const int sp = u / p.nt, nb = u - sp * p.nt;
-            const int buf = j & 1;
-            bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(buf), (uint32_t)(j >> 1) & 1u, abort_flag));
-            // the SwiGLU hand-off below synchronises the four epilogue warps, so they agree first
-            if (SWIGLU && p.mode == KM_SWIGLU) ok = !bar_or_epilogue(!ok);
-            if (!ok) {
-                *abort_flag = 1;
-                raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * NB);
-            if (SWIGLU && p.mode == KM_SWIGLU) {
-                // tile rows 0..63 are gate rows and 64..127 the matching up rows: quads 2 and 3 hand
-                // their accumulators to quads 0 and 1 (same lane) through shared memory, 16 columns
-                // at a time, and the gate threads write h = bf16(silu(bf16(g)) * bf16(u)).
-                const int jj = nb * 64 + (r & 63);
-                const bool ok_col = jj < p.n_valid;
-#pragma unroll
-                for (int c = 0; c < NB; c += 16) {
-                    float v[16];
-                    tmem_ld16(tq + c, v);
-                    if (quad >= 2) {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) xch[(r - 64) * 17 + q] = v[q];
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (quad < 2 && ok_col) {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            const int b = c + q;
-                            if (b < p.M)
-                                reinterpret_cast<bf16*>(p.out)[(long long)b * p.ldo + jj] =
-                                    f2bf(silu_f(round_bf(v[q])) * round_bf(xch[r * 17 + q]));
-                        }
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(buf));
-                continue;
-            }
-            int col;
-            bool col_ok;
-            if (SWIGLU) {
-                const int jj = nb * 64 + (r & 63);
-                col_ok = jj < p.n_valid;
-                col = r < 64 ? jj : p.up_row0 + jj;
-            } else if (p.rpu > 0) {
-                col = nb * p.rpu + r;
-                col_ok = r < p.rpu && col < p.n_valid;
-            } else {
-                col = nb * 128 + r;
-                col_ok = col < p.n_valid;
-            }
-            const long long split_off = (long long)sp * p.split_stride;
-#pragma unroll
-            for (int c = 0; c < NB; c += 16) {
-                float v[16];
-                tmem_ld16(tq + c, v);
-                if (col_ok) {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int b = c + q;
-                        if (b < p.M) {
-                            const long long off = (long long)b * p.ldo + col;
-                            if (p.mode == KM_PARTIAL || p.mode == KM_F32) {
-                                reinterpret_cast<float*>(p.out)[split_off + off] = v[q];
-                            } else if (p.mode == KM_RESIDUAL) {
-                                bf16* o = reinterpret_cast<bf16*>(p.out) + off;
-                                *o = f2bf(bf2f(*o) + v[q]);
-                            } else {
-                                reinterpret_cast<bf16*>(p.out)[off] = f2bf(v[q]);
-                            }
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (*abort_flag && warp == 0 && lane == 0) {
-        volatile int never = 0;
-        const int issued = *issued_slot;
-        for (int i = max(0, issued - S); i < issued; ++i)
-            (void)mbar_wait(full_bar(i % S), (uint32_t)(i / S) & 1u, &never);
-        const int committed = *committed_slot;
-        for (int jj = max(0, committed - 2); jj < committed; ++jj)
-            (void)mbar_wait(tfull_bar(jj & 1), (uint32_t)(jj >> 1) & 1u, &never);
-    }
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
-}
-
 // Fix-up of the last-round K pieces: sum the pieces of each tail tile in piece order, then apply
 // the tile's epilogue.  One thread per 8 D-columns of one row (SwiGLU: 8 gate + the 8 matching up).
 __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
@@ -965,17 +651,30 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
     const int col = (int)(idx % groups) * 8;
     float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = 0; s < splits; ++s) {
-        const float* p = part + s * split_stride + (long long)row * ldp + col;
-        const float4 x0 = *reinterpret_cast<const float4*>(p);
-        const float4 x1 = *reinterpret_cast<const float4*>(p + 4);
-        a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
-        a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
-        if (mode == KM_SWIGLU) {
-            const float4 y0 = *reinterpret_cast<const float4*>(p + up_off);
-            const float4 y1 = *reinterpret_cast<const float4*>(p + up_off + 4);
-            u[0] += y0.x; u[1] += y0.y; u[2] += y0.z; u[3] += y0.w;
-            u[4] += y1.x; u[5] += y1.y; u[6] += y1.z; u[7] += y1.w;
+    constexpr int kBatch = 4;   // split partials loaded together before they are added
+    const bool sw = mode == KM_SWIGLU;
+    for (int s0 = 0; s0 < splits; s0 += kBatch) {
+        float4 x[kBatch][4];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const float* p = part + (s0 + b) * split_stride + (long long)row * ldp + col;
+            const bool ok = s0 + b < splits;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            x[b][0] = ok ? *reinterpret_cast<const float4*>(p) : z;
+            x[b][1] = ok ? *reinterpret_cast<const float4*>(p + 4) : z;
+            x[b][2] = ok && sw ? *reinterpret_cast<const float4*>(p + up_off) : z;
+            x[b][3] = ok && sw ? *reinterpret_cast<const float4*>(p + up_off + 4) : z;
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (s0 + b < splits) {
+                a[0] += x[b][0].x; a[1] += x[b][0].y; a[2] += x[b][0].z; a[3] += x[b][0].w;
+                a[4] += x[b][1].x; a[5] += x[b][1].y; a[6] += x[b][1].z; a[7] += x[b][1].w;
+                if (sw) {
+                    u[0] += x[b][2].x; u[1] += x[b][2].y; u[2] += x[b][2].z; u[3] += x[b][2].w;
+                    u[4] += x[b][3].x; u[5] += x[b][3].y; u[6] += x[b][3].z; u[7] += x[b][3].w;
+                }
+            }
         }
     }
     const long long o = (long long)row * ldo + col;
@@ -1003,7 +702,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 // loads issued before the sum (split order kept); writes r = bf16(r + acc), then y = RMSNorm(r) * g
 // with the compensated sum of squares of the rounded residual.
 constexpr int kNormMaxThreads = 512;   // hidden sizes up to 4096; 128 registers a thread (no spill)
-constexpr int kNormMaxSplits = 8;
+constexpr int kNormMaxSplits = 16;
+constexpr int kNormSplitBatch = 8;      // split partials loaded together before they are added
 __global__ void __launch_bounds__(kNormMaxThreads) splitk_residual_norm_kernel(
     const float* __restrict__ part, int splits, long long split_stride, int N, bf16* __restrict__ r,
     const bf16* __restrict__ gain, bf16* __restrict__ y, float eps) {
@@ -1017,24 +717,29 @@ __global__ void __launch_bounds__(kNormMaxThreads) splitk_residual_norm_kernel(
     float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float ss = 0.f, sc = 0.f;
     if (active) {
-        float4 x0[kNormMaxSplits], x1[kNormMaxSplits];
-#pragma unroll
-        for (int s = 0; s < kNormMaxSplits; ++s) {
-            if (s < splits) {
-                const float* p = part + s * split_stride + (long long)row * N + col;
-                x0[s] = *reinterpret_cast<const float4*>(p);
-                x1[s] = *reinterpret_cast<const float4*>(p + 4);
-            }
-        }
         uint4* rp = reinterpret_cast<uint4*>(r + (long long)row * N + col);
         float rr[8];
         unpack8(*rp, rr);
         float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int s = 0; s < kNormMaxSplits; ++s) {
-            if (s < splits) {
-                a[0] += x0[s].x; a[1] += x0[s].y; a[2] += x0[s].z; a[3] += x0[s].w;
-                a[4] += x1[s].x; a[5] += x1[s].y; a[6] += x1[s].z; a[7] += x1[s].w;
+        for (int s0 = 0; s0 < kNormMaxSplits; s0 += kNormSplitBatch) {
+            if (s0 < splits) {
+                float4 x0[kNormSplitBatch], x1[kNormSplitBatch];
+#pragma unroll
+                for (int b = 0; b < kNormSplitBatch; ++b) {
+                    if (s0 + b < splits) {
+                        const float* p = part + (s0 + b) * split_stride + (long long)row * N + col;
+                        x0[b] = *reinterpret_cast<const float4*>(p);
+                        x1[b] = *reinterpret_cast<const float4*>(p + 4);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kNormSplitBatch; ++b) {
+                    if (s0 + b < splits) {
+                        a[0] += x0[b].x; a[1] += x0[b].y; a[2] += x0[b].z; a[3] += x0[b].w;
+                        a[4] += x1[b].x; a[5] += x1[b].y; a[6] += x1[b].z; a[7] += x1[b].w;
+                    }
+                }
             }
         }
 #pragma unroll
@@ -1208,90 +913,7 @@ cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm
 }
 
 
-// ---- small-M (swap-AB) plan: units = N tiles x K splits over persistent CTAs; the per-SM critical
-// path is ceil(units / SMs) x (K blocks per unit), plus a small cost per extra split (partials).
-constexpr int kSmallM = 64;
-
-struct SmallPlan {
-    int nb;          // padded activation rows: 16, 32 or 64
-    int nt, splits, kbps;
-    int rpu = 0;     // > 0: row-range units of rpu weight rows over the whole K (nt = units)
-};
-
-// Cost of one extra launch (a split-K reduction and its kernel boundary) in the plan's unit, one
-// 128-row weight k-block per SM round (about 0.3 us at full bandwidth).
-constexpr double kReduceLaunchCost = 10.0;
-
-SmallPlan make_small_plan(int M, int N, int K, int epi, int split_req, int nsm, bool reduce_free) {
-    const double reduce_cost = reduce_free ? 0.0 : kReduceLaunchCost;
-    const int n_kb = K / BK;
-    const int per_tile = epi == EPI_SWIGLU ? 64 : 128;
-    const int nt = (N + per_tile - 1) / per_tile;
-    SmallPlan best{M <= 16 ? 16 : M <= 32 ? 32 : 64, nt, 1, n_kb};
-    double best_cost = 1e30;
-    for (int s = 1; s <= std::min(8, n_kb); ++s) {
-        if (split_req > 0 && s != std::min(split_req, std::min(8, n_kb))) continue;
-        const int kbps = (n_kb + s - 1) / s;
-        const int splits = (n_kb + kbps - 1) / kbps;
-        const long long units = (long long)nt * splits;
-        const long long rounds = (units + nsm - 1) / nsm;
-        const double cost = (double)rounds * (kbps + 0.75) + 0.05 * (splits - 1) * ((M + 15) / 16) +
-                            (splits > 1 ? reduce_cost : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best.splits = splits;
-            best.kbps = kbps;
-        }
-    }
-    // Row ranges: units of rpu whole weight rows (rpu <= 128) times s K splits, sized so the units
-    // cover the SMs about once.  A stage then carries rpu x 128 B of weights; with fewer than ~96 KB
-    // of weights in flight per SM the stream is latency-bound, so such plans are charged for it.
-    if (epi != EPI_SWIGLU && split_req == 0) {
-        const int nb_pad = M <= 16 ? 16 : M <= 32 ? 32 : 64;
-        const int stage_bytes = 128 * BK * 2 + nb_pad * BK * 2;
-        const int stages = std::min(12, kSmallRingDeep / stage_bytes);
-        for (int s = 1; s <= std::min(8, n_kb); ++s) {
-            const int rpu = (int)(((long long)N * s + nsm - 1) / nsm);
-            if (rpu < 8 || rpu > 128) continue;
-            const int kbps = (n_kb + s - 1) / s;
-            const int splits = (n_kb + kbps - 1) / kbps;
-            const double inflight = (double)rpu * 128 * stages;
-            const double latency_factor = std::min(1.0, inflight / (96.0 * 1024));
-            const long long units = (long long)((N + rpu - 1) / rpu) * splits;
-            const long long rounds = (units + nsm - 1) / nsm;
-            const double cost = rounds * (kbps * (rpu / 128.0) / latency_factor + 0.75) +
-                                0.05 * (splits - 1) * ((M + 15) / 16) + (splits > 1 ? reduce_cost : 0.0);
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best.rpu = rpu;
-                best.nt = (N + rpu - 1) / rpu;
-                best.splits = splits;
-                best.kbps = kbps;
-            }
-        }
-    }
-    return best;
-}
-
-template <int NB, bool SW>
-cudaError_t launch_small(const CUtensorMap& mw, const CUtensorMap& mx, SwArgs a, int units, int ring_bytes,
-                         cudaStream_t st) {
-    using C = SwCfg<NB>;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(gemm_smallm_kernel<NB, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::smem_bytes(C::MAX_STAGES));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
-    a.stages = C::stages_for(ring_bytes);
-    dim3 grid((unsigned)std::min(units, device_sm_count()));
-    HRA_LAUNCH(gemm_smallm_kernel<NB, SW>, dim3(grid), dim3(kThreads), C::smem_bytes(a.stages), st, mw, mx, a);
-    return cudaGetLastError();
-}
+constexpr int kSmallM = 64;   // at most this many rows take the head-form path below
 
 // Reduction / epilogue pass shared by both GEMM paths once fp32 partials exist.
 cudaError_t reduce_partials(const LinearCall& c, int splits, int ldp, cudaStream_t st) {
@@ -1311,64 +933,44 @@ cudaError_t reduce_partials(const LinearCall& c, int splits, int ldp, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_linear_small(const LinearCall& c, cudaStream_t st) {
-    const SmallPlan pl = make_small_plan(c.M, c.N, c.K, c.epi, c.split_req, device_sm_count(), c.partial_only);
+// At most 64 BF16 rows: the audio-head kernel's form (head.cu) -- 256 weight rows a tile as the
+// MMA's N side, so that one instruction consumes 256 rows x 16 K of weights -- over tiles x K splits
+// (up to kSmallHeadSplits), fp32 partial planes [split][M][ldp], then the epilogue's reduction.
+constexpr int kSmallHeadSplits = 16;
+
+cudaError_t launch_linear_small_head(const LinearCall& c, cudaStream_t st) {
     const bool sw = c.epi == EPI_SWIGLU;
-    const int w_rows = sw ? 2 * c.N : c.N;
-    CUtensorMap mw, mx;
-    const int w_box = pl.rpu > 0 ? pl.rpu : (sw ? 64 : 128);
-    if (!make_map(&mw, c.w, w_rows, c.K, w_box)) return cudaErrorInvalidValue;
-    if (!make_map(&mx, c.a, c.M, c.K, pl.nb)) return cudaErrorInvalidValue;
-    // Every split goes through fp32 partials; otherwise the epilogue writes the output.
-    const bool use_partial = pl.splits > 1;
-    SwArgs a;
-    a.err = c.err;
-    a.M = c.M;
-    a.n_valid = c.N;
-    a.n_kb = c.K / BK;
-    a.kb_per_split = pl.kbps;
-    a.up_row0 = c.N;
-    a.nt = pl.nt;
-    a.splits = pl.splits;
-    a.rpu = pl.rpu;
-    a.w_box_bytes = (pl.rpu > 0 ? pl.rpu : 128) * BK * 2;
-    a.zero_ptr = c.zero_ptr;
-    a.zero_words = c.zero_ptr ? c.zero_words : 0;
-    const int ldp = sw ? 2 * c.N : c.N;
-    if (use_partial) {
-        a.out = c.partial;
-        a.mode = KM_PARTIAL;
-        a.ldo = ldp;
-        a.split_stride = (long long)c.M * ldp;
-    } else {
-        a.out = c.out;
-        a.mode = c.epi == EPI_STORE ? KM_STORE : c.epi == EPI_RESIDUAL ? KM_RESIDUAL : sw ? KM_SWIGLU : KM_F32;
-        a.ldo = c.N;
-        a.split_stride = 0;
-    }
-    const int ring = c.shallow_ring ? kSmallRingShallow : kSmallRingDeep;
-    const int units = pl.nt * pl.splits;
-    cudaError_t e;
-    if (pl.nb == 16)
-        e = sw ? launch_small<16, true>(mw, mx, a, units, ring, st) : launch_small<16, false>(mw, mx, a, units, ring, st);
-    else if (pl.nb == 32)
-        e = sw ? launch_small<32, true>(mw, mx, a, units, ring, st) : launch_small<32, false>(mw, mx, a, units, ring, st);
-    else
-        e = sw ? launch_small<64, true>(mw, mx, a, units, ring, st) : launch_small<64, false>(mw, mx, a, units, ring, st);
-    if (c.splits_used) *c.splits_used = use_partial ? pl.splits : 1;
-    if (e != cudaSuccess || !use_partial || c.partial_only) return e;
+    const int ldp = sw ? 2 * c.N : c.N;   // gate/up: gate columns then up columns, as the weight's rows
+    HeadCall h{};
+    h.hidden = c.a;
+    h.head_w = c.w;
+    h.partial = c.partial;
+    h.err = c.err;
+    h.zero_ptr = c.zero_ptr;
+    h.zero_words = c.zero_ptr ? c.zero_words : 0;
+    int splits = 1;
+    h.splits_used = &splits;
+    h.B = c.M;
+    h.N = ldp;
+    h.H = c.K;
+    h.max_splits = kSmallHeadSplits;
+    h.split_req = c.split_req;
+    h.no_l2_prefetch = true;
+    cudaError_t e = launch_audio_head(h, st);
+    if (c.splits_used) *c.splits_used = splits;
+    if (e != cudaSuccess || c.partial_only) return e;
     if (c.qk != nullptr && c.epi == EPI_STORE && c.M == c.qk->rows && c.N == (c.qk->nq + 2 * c.qk->nkv) * c.qk->hd) {
         // merged QKV: the split reduction happens inside the q/k norm + RoPE + cache-write kernel
         QkRopeArgs qa = *c.qk;
         qa.part = c.partial;
-        qa.splits = pl.splits;
+        qa.splits = splits;
         qa.split_stride = (long long)c.M * ldp;
         qa.ldp = ldp;
         e = launch_qk_rope_kv(qa, st);
         if (e == cudaSuccess && c.qk_done) *c.qk_done = true;
         return e;
     }
-    return reduce_partials(c, pl.splits, ldp, st);
+    return reduce_partials(c, splits, ldp, st);
 }
 
 }  // namespace
@@ -1417,11 +1019,11 @@ int device_sm_count() {
 }
 
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool partial_only) {
-    if (M <= kSmallM) {
-        const SmallPlan sp = make_small_plan(M, N, K, epi, split_req, device_sm_count(), partial_only);
-        if (sp.splits <= 1) return 0;
+    (void)partial_only;
+    if (M <= kSmallM) {   // the head-form path always writes its partial planes
         const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
-        return (size_t)sp.splits * (size_t)M * ldp * sizeof(float);
+        const HeadPlan hp = head_plan((int)ldp, K, kSmallHeadSplits, split_req);
+        return (size_t)hp.splits * (size_t)M * ldp * sizeof(float);
     }
     const Plan pl = make_plan(M, N, K, epi, split_req, device_sm_count());
     if (pl.tail_tiles > 0) return (size_t)pl.tail_splits * pl.tail_tiles * BM * pl.bn * sizeof(float);
@@ -1435,12 +1037,13 @@ size_t linear_tail_bound() { return (size_t)device_sm_count() * BM * 256 * sizeo
 size_t linear_partial_bound(int m_max, int N, int K, int epi) {
     if (m_max > BM) m_max = BM;
     const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
-    return 8 * (size_t)m_max * ldp * sizeof(float);
+    const size_t splits = m_max <= kSmallM ? kSmallHeadSplits : 8;
+    return splits * (size_t)m_max * ldp * sizeof(float);
 }
 
 cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     if (!get_encoder()) return cudaErrorNotSupported;
-    if (c.M <= kSmallM && !c.fp8) return launch_linear_small(c, st);   // FP8 always takes the tile path
+    if (c.M <= kSmallM && !c.fp8) return launch_linear_small_head(c, st);   // FP8 always takes the tile path
     const int nsm = device_sm_count();
     const int ke = c.fp8 ? 2 * BK : BK;
     if (c.fp8 && (c.K % ke != 0 || c.a_scale == nullptr || c.w_scale == nullptr)) return cudaErrorInvalidValue;

@@ -1,8 +1,10 @@
-// head.cu -- the audio-head projection of the delayed-codebook step for up to 128 rows.
+// head.cu -- weight-streaming projections over at most 128 activation rows: the audio head of the
+// delayed-codebook step, and every projection of a backbone pass over at most 64 token rows (the
+// decode pass; launch_linear_small_head in gemm_tc.cu adds the split reduction and its epilogue).
 //
 // Source: "Stabilize Higgs Audio termination and prefill" (FlashRT PR #141), Summary (per-frame
-// argmax over the audio head's codebook logits); the argmax, delay state machine and embedding sum
-// that follow run in codebook.cu.
+// argmax over the audio head's codebook logits) and Performance (the AR decode time per frame); the
+// argmax, delay state machine and embedding sum that follow the audio head run in codebook.cu.
 //
 // logits[b][n] = sum_k hidden[b][k] * head_w[n][k] for the n = K * Vc head rows.  With at most 128
 // activation rows this is a stream of the 42 MB head through the tensor cores, and the tensor core
@@ -17,7 +19,7 @@
 // stream: the head is constant, so one step's weight stream starts while the previous step ends.
 //
 // Roles (192 threads): warp 0 TMA producer (128-byte swizzled boxes: activations 64 K x B rows,
-// weights 64 K x 256 rows), warp 1 TMEM allocation + MMA issue (one lane), warps 2-5 epilogue
+// weights 64 K x 256 rows, 4 ring stages), warp 1 TMEM allocation + MMA issue (one lane), warps 2-5 epilogue
 // (tcgen05.ld of their 32-lane quarter: one activation row per thread, 256 fp32 columns).
 #include <algorithm>
 
@@ -29,16 +31,18 @@ namespace {
 
 constexpr int kHeadThreads = 192;
 constexpr int kHeadBN = 256;        // weight rows per tile (MMA N)
-constexpr int kHeadStages = 4;
 
+// Ring stage = activation tile (128 rows, NBX of them loaded) + weight tile.
 template <int NBX>
 struct HeadCfg {
-    static constexpr int A_BYTES = 128 * 64 * 2;       // activation tile: 128 rows (NBX loaded)
+    static constexpr int A_BYTES = 128 * 64 * 2;       // activation tile
     static constexpr int B_BYTES = kHeadBN * 64 * 2;   // weight tile
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int SMEM = kHeadStages * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int STAGES = 4;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t TMEM_COLS = kHeadBN;
-    static_assert(128 * (kHeadBN + 4) * 4 <= kHeadStages * STAGE, "the staging tile must fit in the ring");
+    static_assert(128 * (kHeadBN + 4) * 4 <= STAGES * STAGE, "the staging tile must fit in the ring");
+    static_assert(A_BYTES % 1024 == 0 && STAGE % 1024 == 0, "tiles stay 1024-byte aligned (128-byte swizzle)");
 };
 
 struct HeadArgs {
@@ -51,6 +55,7 @@ struct HeadArgs {
     unsigned int* err;
     unsigned int* zero_ptr;   // CTA 0 clears zero_words words here once earlier kernels are done
     int zero_words;
+    int l2_prefetch;          // send the CTA's later weight tiles towards L2 before waiting
 };
 
 // OR of `v` over the four epilogue warps (named barrier 1, 128 threads); all of them get the answer.
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     audio_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const HeadArgs p) {
     using C = HeadCfg<NBX>;
-    constexpr int S = kHeadStages;
+    constexpr int S = C::STAGES;
     pdl_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,7 +123,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             }
             // and the rest of this CTA's weight tiles towards L2, so the whole head is in flight
             // while the kernels ahead finish
-            for (int i = pre; i < nkb; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * 64, tile * kHeadBN);
+            if (p.l2_prefetch)
+                for (int i = pre; i < nkb; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * 64, tile * kHeadBN);
             pdl_wait();
             int s = 0, i = 0;
             uint32_t ph = 0;
@@ -264,12 +270,12 @@ cudaError_t launch_head_nb(const CUtensorMap& mw, const CUtensorMap& mx, const H
 
 }  // namespace
 
-HeadPlan head_plan(int N, int H) {
+HeadPlan head_plan(int N, int H, int max_splits, int split_req) {
     HeadPlan pl;
     const int nsm = device_sm_count();
     const int n_kb = H / 64;
     pl.nt = (N + kHeadBN - 1) / kHeadBN;
-    int s = std::max(1, std::min({nsm / pl.nt, n_kb, kHeadMaxSplits}));
+    int s = split_req > 0 ? std::min(split_req, n_kb) : std::max(1, std::min({nsm / pl.nt, n_kb, max_splits}));
     pl.kbps = (n_kb + s - 1) / s;
     pl.splits = (n_kb + pl.kbps - 1) / pl.kbps;
     return pl;
@@ -277,7 +283,7 @@ HeadPlan head_plan(int N, int H) {
 
 cudaError_t launch_audio_head(const HeadCall& c, cudaStream_t st) {
     if (c.B < 1 || c.B > kHeadMaxBatch) return cudaErrorInvalidValue;
-    const HeadPlan pl = head_plan(c.N, c.H);
+    const HeadPlan pl = head_plan(c.N, c.H, c.max_splits > 0 ? c.max_splits : kHeadMaxSplits, c.split_req);
     const int nbx = c.B <= 16 ? 16 : c.B <= 32 ? 32 : c.B <= 64 ? 64 : 128;
     CUtensorMap mw, mx;
     if (!make_map_2d(&mw, c.head_w, c.N, c.H, kHeadBN)) return cudaErrorInvalidValue;
@@ -294,6 +300,7 @@ cudaError_t launch_audio_head(const HeadCall& c, cudaStream_t st) {
     p.err = c.err;
     p.zero_ptr = c.zero_ptr;
     p.zero_words = c.zero_ptr ? c.zero_words : 0;
+    p.l2_prefetch = c.no_l2_prefetch ? 0 : 1;
     if (c.splits_used) *c.splits_used = pl.splits;
     const int grid = pl.nt * pl.splits;
     if (nbx == 16) return launch_head_nb<16>(mw, mx, p, grid, st);

@@ -95,9 +95,7 @@ struct LinearCall {
     // per-head q/k norm + RoPE + K/V cache write itself (out is not written) and sets *qk_done.
     const QkRopeArgs* qk;
     bool* qk_done;
-    // small-M path: stream the weights through the shallow ring, so that the launch fits on an SM
-    // beside a kernel that still holds much shared memory (the attention before the o-projection)
-    bool shallow_ring;    // FP8: a and w hold E4M3 codes (K a multiple of 128); the accumulators are scaled by
+    // FP8: a and w hold E4M3 codes (K a multiple of 128); the accumulators are scaled by
     // (*a_scale) * (*w_scale), device scalars.  Always runs the tile kernel (any M).
     bool fp8;
     const float* a_scale;
@@ -268,7 +266,9 @@ constexpr int kHeadMaxSplits = 8;
 struct HeadPlan {
     int nt, splits, kbps;
 };
-HeadPlan head_plan(int N, int H);
+// Tiles of 256 head rows times K splits, at most max_splits (split_req > 0 forces that many), over
+// the SMs about once.
+HeadPlan head_plan(int N, int H, int max_splits = kHeadMaxSplits, int split_req = 0);
 
 // partial[split][b][n] = sum over the split's K range of hidden[b][k] * head_w[n][k] (fp32).
 struct HeadCall {
@@ -280,6 +280,9 @@ struct HeadCall {
     int zero_words;
     int* splits_used;           // optional: receives the number of K splits
     int B, N, H;
+    int max_splits;             // 0: kHeadMaxSplits
+    int split_req;              // > 0: exactly this many K splits
+    bool no_l2_prefetch;        // do not send the CTA's later weight tiles towards L2 ahead of use
 };
 cudaError_t launch_audio_head(const HeadCall& c, cudaStream_t st);
 
