@@ -140,7 +140,8 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     L.x8 = (fp8 || nvfp4) ? g.take(T * std::max(std::max(H, Dq), F)) : 0;
     // NVFP4 band: the E4M3 block scales of that input (one per 16 elements)
     L.xs = nvfp4 ? g.take(T * std::max(std::max(H, Dq), F) / 16) : 0;
-    // counters and per-row sums of the persistent decoder pass (M <= 64 rows)
+    // counters and per-row sums of the persistent decoder pass (M <= 64 rows), cleared by the
+    // call's row-map kernel
     L.sync = g.take(decode_pass_sync_bytes((int)std::min<size_t>(T, 64), d.n_kv_heads, (int)F, (int)H));
     L.total = g.off;
     return L;

@@ -32,6 +32,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int kMaxTailPieces = 4;   // K pieces of a last-round tile
 constexpr int kTileThreads = 320;   // tile kernel: TMA warp, MMA warp, 8 epilogue warps
 
 enum KMode : int { KM_STORE = 0, KM_RESIDUAL = 1, KM_SWIGLU = 2, KM_F32 = 3, KM_PARTIAL = 4, KM_QKROPE = 5 };
@@ -582,7 +583,7 @@ __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int 
 // the other chunks already hold the GEMM's residual sum.  Then y = RMSNorm(r) * g over the rounded
 // row, with the compensated sum of squares of the row norm kernel.
 template <int NC>
-__global__ void tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
+__global__ void __launch_bounds__(256, 2) tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
                                        int mt, int group, int BNt, int M, int N, bf16* __restrict__ r,
                                        const bf16* __restrict__ g, bf16* __restrict__ y, float eps) {
     pdl_launch();
@@ -592,9 +593,13 @@ __global__ void tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces,
     if (row >= M) return;
     const int mb = row / BM, rr = row - mb * BM;
     uint4* rrow = reinterpret_cast<uint4*>(r + (long long)row * N);
-    uint4 u[NC];
+    const uint4* gv = reinterpret_cast<const uint4*>(g);
+    // the row, and the gains, requested before anything waits for them
+    uint4 u[NC], gw[NC];
 #pragma unroll
     for (int q = 0; q < NC; ++q) u[q] = rrow[lane + 32 * q];
+#pragma unroll
+    for (int q = 0; q < NC; ++q) gw[q] = gv[lane + 32 * q];
 #pragma unroll
     for (int q = 0; q < NC; ++q) {
         const int col = (lane + 32 * q) * 8;
@@ -603,11 +608,23 @@ __global__ void tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces,
         const int lin = band * group * mt + (nb - band * group) * mt + mb;
         if (lin < head_units) continue;
         const int t = lin - head_units;
+        // every piece of the chunk requested before the first is added (piece order kept)
+        float4 x0[kMaxTailPieces], x1[kMaxTailPieces];
+#pragma unroll
+        for (int pc = 0; pc < kMaxTailPieces; ++pc) {
+            if (pc < pieces) {
+                const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)rr * BNt + (col - nb * BNt);
+                x0[pc] = *reinterpret_cast<const float4*>(src);
+                x1[pc] = *reinterpret_cast<const float4*>(src + 4);
+            }
+        }
         float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int pc = 0; pc < pieces; ++pc) {
-            const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)rr * BNt + (col - nb * BNt);
-            const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
-            a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w; a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+#pragma unroll
+        for (int pc = 0; pc < kMaxTailPieces; ++pc) {
+            if (pc < pieces) {
+                a[0] += x0[pc].x; a[1] += x0[pc].y; a[2] += x0[pc].z; a[3] += x0[pc].w;
+                a[4] += x1[pc].x; a[5] += x1[pc].y; a[6] += x1[pc].z; a[7] += x1[pc].w;
+            }
         }
         float f[8];
         unpack8(u[q], f);
@@ -626,13 +643,12 @@ __global__ void tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces,
     }
     ss = csum_warp(ss, sc);
     const float inv = 1.0f / sqrtf(ss / (float)N + eps);
-    const uint4* gv = reinterpret_cast<const uint4*>(g);
     uint4* dy = reinterpret_cast<uint4*>(y + (long long)row * N);
 #pragma unroll
     for (int q = 0; q < NC; ++q) {
         float f[8], w[8];
         unpack8(u[q], f);
-        unpack8(gv[lane + 32 * q], w);
+        unpack8(gw[q], w);
 #pragma unroll
         for (int j = 0; j < 8; ++j) f[j] = (f[j] * inv) * w[j];
         dy[lane + 32 * q] = pack8(f);
@@ -837,13 +853,13 @@ struct Plan {
 };
 
 // Last-round split: when the final round of tiles fills at most half the SMs, each of its tiles is
-// cut into up to 4 K pieces that run on the SMs that would otherwise idle.
+// cut into up to kMaxTailPieces K pieces that run on the SMs that would otherwise idle.
 void plan_tail(Plan& pl, int n_kb, int nsm) {
     const long long units = (long long)pl.mt * pl.nt;
     const long long rounds = (units + nsm - 1) / nsm;
     const long long tail = units - (rounds - 1) * nsm;
     if (pl.splits != 1 || rounds < 2 || tail * 2 > nsm) return;
-    int S = (int)std::min<long long>(4, nsm / tail);
+    int S = (int)std::min<long long>(kMaxTailPieces, nsm / tail);
     while (S > 1 && n_kb < 2 * S) --S;
     if (S < 2) return;
     pl.head_units = (int)((rounds - 1) * nsm);
