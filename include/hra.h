@@ -458,6 +458,19 @@ int hra_probe_collect(double* total_ms, int64_t* launches, double* total_work);
  * the previous setting (0 or 1). */
 int32_t hra_set_decode_pass(int32_t enable);
 
+/* ---- projection GEMM form ------------------------------------------------------------------- */
+/* Selects how the BF16 projection GEMMs of at least 512 rows run (the QKV, o, gate/up and down
+ * projections of hra_prefill / hra_prefill_chunk and hra_linear; "Stabilize Higgs Audio
+ * termination and prefill", Summary: the projection GEMMs):
+ *   enable != 0 (default): on clusters of two CTAs, each pair computing 256 x 256 output tiles
+ *     with one M = 256 tensor-core MMA per K step (each CTA stages its 128 activation rows and
+ *     half of the weight rows);
+ *   enable == 0: one CTA per 128 x 256 (or 128 x 128) tile.
+ * Both compute the same arithmetic; the K pieces of a last round (and so the fp32 order of their
+ * sums) can differ.  Process-wide; calls already enqueued or captured keep their form.  Returns
+ * the previous setting (0 or 1). */
+int32_t hra_set_gemm_pairs(int32_t enable);
+
 /* ---- errors --------------------------------------------------------------------------------- */
 /* Synchronise `stream` and return the sticky HRA_DEVERR_* bits of the last call that used this
  * workspace (each call clears them first), or a negative status. */

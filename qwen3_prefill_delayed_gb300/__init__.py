@@ -41,7 +41,7 @@ EXPORTED = ["hra_prefill_workspace_size", "hra_prefill", "hra_prefill_chunk_work
             "hra_nvfp4_band_scales",
             "hra_prefill_nvfp4_workspace_size", "hra_prefill_nvfp4",
             "hra_launch_counter", "hra_probe_select", "hra_probe_collect", "hra_set_decode_pass",
-            "hra_device_error", "hra_status_string"]
+            "hra_set_gemm_pairs", "hra_device_error", "hra_status_string"]
 PROBE = {"none": 0, "qkv": 1, "o_proj": 2, "gate_up": 3, "down": 4, "attention": 5, "audio_head": 6,
          "decode_attention": 7, "decode_linear": 8}
 
@@ -171,6 +171,8 @@ def lib() -> ctypes.CDLL:
         L.hra_probe_select.restype = ctypes.c_int
         L.hra_set_decode_pass.argtypes = [i32]
         L.hra_set_decode_pass.restype = i32
+        L.hra_set_gemm_pairs.argtypes = [i32]
+        L.hra_set_gemm_pairs.restype = i32
         L.hra_probe_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                         ctypes.POINTER(ctypes.c_double)]
         L.hra_probe_collect.restype = ctypes.c_int
@@ -764,6 +766,12 @@ def hra_set_decode_pass(enable: bool) -> bool:
     """Run passes over at most 64 BF16 rows as one persistent kernel (True) or as one kernel per
     step of each layer (False, the default); returns the previous setting."""
     return bool(lib().hra_set_decode_pass(1 if enable else 0))
+
+
+def hra_set_gemm_pairs(enable: bool) -> bool:
+    """Run projection GEMMs of at least 512 BF16 rows on 2-CTA clusters (True, the default) or on
+    single CTAs (False); returns the previous setting."""
+    return bool(lib().hra_set_gemm_pairs(1 if enable else 0))
 
 
 def hra_probe_select(kernel_class: str) -> None:

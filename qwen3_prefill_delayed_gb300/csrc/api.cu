@@ -491,6 +491,12 @@ int32_t hra_set_decode_pass(int32_t enable) {
     return prev ? 1 : 0;
 }
 
+int32_t hra_set_gemm_pairs(int32_t enable) {
+    const bool prev = hra::g_gemm_pairs;
+    hra::g_gemm_pairs = enable != 0;
+    return prev ? 1 : 0;
+}
+
 int hra_probe_select(int kernel_class) {
     std::lock_guard<std::mutex> lk(g_probe.mu);
     g_probe.active = kernel_class;

@@ -62,11 +62,14 @@ struct GemmArgs {
     const float* w_scale;
 };
 
-template <int BN>
+// PAIR: two CTAs (a 2-CTA cluster) share each 256 x BN tile through one M = 256 MMA; each CTA
+// stages its 128 rows of A and half of the BN weight rows, so a stage is 32 KB instead of 48 KB and
+// the same shared memory holds six stages (1.6x the loads in flight per byte consumed).
+template <int BN, bool PAIR = false>
 struct Cfg {
-    static constexpr int STAGES = BN >= 256 ? 4 : 6;
+    static constexpr int STAGES = PAIR ? 6 : (BN >= 256 ? 4 : 6);
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;   // this CTA's weight rows
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
     // two fp32 accumulators of BN columns each: the epilogue drains one while the MMA fills the other
@@ -237,12 +240,20 @@ __device__ __forceinline__ void unit_work(int u, const GemmArgs& p, int& mb, int
 // Persistent: each CTA walks work units blockIdx.x, blockIdx.x + gridDim.x, ...
 // F8: both operands E4M3 (kind::f8f6f4): a 128-byte stage row holds 128 elements instead of 64,
 // and every accumulator is scaled by the two per-tensor scales before any store.
-template <int BN, bool SWIGLU, bool F8>
+// PAIR: the grid is 2-CTA clusters and cluster c walks units c, c + gridDim.x / 2, ...; a unit is
+// a 256 x BN tile, CTA rank r owns its rows [128 r, 128 r + 128).  Both CTAs load their A rows and
+// their half of the weight rows (SwiGLU: rank 0 the gate rows, rank 1 the up rows), and both
+// loads complete on rank 0's stage barrier; rank 0 issues the M = 256 MMAs and commits each stage
+// and each accumulator to both CTAs' barriers; each CTA's epilogue drains its own tensor memory
+// and arrives on rank 0's accumulator-free barrier.
+template <int BN, bool SWIGLU, bool F8, bool PAIR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
-    using C = Cfg<BN>;
+    static_assert(!PAIR || (BN == 256 && !F8), "CTA pairs: bf16, 256-wide tiles");
+    using C = Cfg<BN, PAIR>;
     constexpr int KE = F8 ? 2 * BK : BK;   // elements per K block (one 128-byte row)
+    constexpr int BMU = PAIR ? 2 * BM : BM;   // rows of a work unit's tile
     pdl_launch();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,9 +263,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* issued_slot = reinterpret_cast<int*>(tmem_slot + 2);
     int* committed_slot = reinterpret_cast<int*>(tmem_slot + 3);
+    int* peer_slot = reinterpret_cast<int*>(tmem_slot + 4);   // PAIR, rank 0: rank 1's issued count, abort flag
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.tail_tiles > 0 ? p.head_units + p.tail_tiles * p.tail_splits : p.mt * p.nt * p.splits;
+    const uint32_t rank = PAIR ? cta_rank_in_cluster() : 0u;
+    const int walker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // this CTA's (pair's) first unit
+    const int walkers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + C::STAGES + s); };
@@ -270,50 +285,70 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 8);   // one arrival per epilogue warp
+            mbar_init(tempty_bar(b), PAIR ? 16 : 8);   // one arrival per epilogue warp (of both CTAs)
         }
         *abort_flag = 0;
         *issued_slot = 0;
         *committed_slot = 0;
+        peer_slot[0] = 0;
+        peer_slot[1] = 0;
         mbar_fence_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    // PAIR: the peer's barriers are initialised before any load or commit can reach them
+    if constexpr (PAIR) cluster_barrier_sync();
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer: one continuous stage ring across all of this CTA's units
+        // PAIR: this CTA's boxes complete on rank 0's barrier, which rank 0 arms for both CTAs' bytes
+        auto load = [&](uint32_t dst, const CUtensorMap* map, int s, int x, int y) {
+            if constexpr (PAIR) tma_load_2d_pair(dst, map, smem_in_cta(full_bar(s), 0), x, y);
+            else tma_load_2d(dst, map, full_bar(s), x, y);
+        };
+        constexpr uint32_t kStageTx = PAIR ? 2 * C::STAGE_BYTES : C::STAGE_BYTES;
+        const bool arms = !PAIR || rank == 0;
         auto load_w = [&](int s, int kx, int nb) {
             if (SWIGLU) {
                 const int j0 = nb * (BN / 2);
-                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, j0);
-                tma_load_2d(b_tile(s) + C::B_BYTES / 2, &tmB, full_bar(s), kx, p.up_row0 + j0);
+                if constexpr (PAIR) {
+                    load(b_tile(s), &tmB, s, kx, rank == 0 ? j0 : p.up_row0 + j0);
+                } else {
+                    load(b_tile(s), &tmB, s, kx, j0);
+                    load(b_tile(s) + C::B_BYTES / 2, &tmB, s, kx, p.up_row0 + j0);
+                }
             } else {
-                tma_load_2d(b_tile(s), &tmB, full_bar(s), kx, nb * BN);
+                load(b_tile(s), &tmB, s, kx, nb * BN + (int)rank * (BN / 2));
             }
         };
         // Weight tiles of the first ring stages do not depend on earlier kernels: fetch them before
         // waiting for those kernels (the activation half of each stage follows after the wait).
         int pre = 0;
-        for (int u = blockIdx.x; u < units && pre < C::STAGES; u += gridDim.x) {
+        for (int u = walker; u < units && pre < C::STAGES; u += walkers) {
             int mb, nb, kb0, kb1, piece;
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
-                mbar_expect_tx(full_bar(pre), C::STAGE_BYTES);
+                if (arms) mbar_expect_tx(full_bar(pre), kStageTx);
                 load_w(pre, kb * KE, nb);
             }
         }
         pdl_wait();
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int u = walker; u < units && ok; u += walkers) {
             int mb, nb, kb0, kb1, piece;
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -327,24 +362,25 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    if (arms) mbar_expect_tx(full_bar(s), kStageTx);
                     load_w(s, kx, nb);
                 }
-                tma_load_2d(a_tile(s), &tmA, full_bar(s), kx, mb * BM);
+                load(a_tile(s), &tmA, s, kx, mb * BMU + (int)rank * BM);
             }
         }
         *issued_slot = ok ? it : max(it, pre);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && (!PAIR || rank == 0)) {
         // ---------------- MMA issuer: accumulator buffer j % 2 for this CTA's j-th unit
-        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BMU, BN);
         int it = 0, j = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+        for (int u = walker; u < units && ok; u += walkers, ++j) {
             int mb, nb, kb0, kb1, piece;
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             const int buf = j & 1;
             const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
-            if (!mbar_wait(tempty_bar(buf), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
+            const uint32_t tpar = ((uint32_t)(j >> 1) & 1u) ^ 1u;
+            if (!(PAIR ? mbar_wait_cluster(tempty_bar(buf), tpar, abort_flag) : mbar_wait(tempty_bar(buf), tpar, abort_flag))) {
                 *abort_flag = 1;
                 raise_error(p.err, HRA_DEVERR_WAIT_TIMEOUT);
                 break;
@@ -366,12 +402,16 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 for (int k = 0; k < 4; ++k) {   // 4 x 32 bytes of each 128-byte row
                     if constexpr (F8)
                         tc_mma_f8(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    else if constexpr (PAIR)
+                        tc_mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     else
                         tc_mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                 }
-                tc_commit(empty_bar(s));
+                if constexpr (PAIR) tc_commit_pair(empty_bar(s), 0x3);
+                else tc_commit(empty_bar(s));
             }
-            tc_commit(tfull_bar(buf));
+            if constexpr (PAIR) tc_commit_pair(tfull_bar(buf), 0x3);
+            else tc_commit(tfull_bar(buf));
             *committed_slot = j + 1;
         }
     } else if (warp >= 2) {
@@ -393,12 +433,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             }
         };
         int j = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+        for (int u = walker; u < units; u += walkers, ++j) {
             int mb, nb, kb0, kb1, piece;
             unit_work(u, p, mb, nb, kb0, kb1, piece);
             const int sp = piece < 0 ? u / (p.mt * p.nt) : 0;
             const int buf = j & 1;
-            const int row = mb * BM + quad * 32 + lane;
+            const int trow = (int)rank * BM + quad * 32 + lane;   // row within the unit's tile
+            const int row = mb * BMU + trow;
             const bool row_ok = row < p.M;
             // While the MMAs of this unit run, pull the residual row segment its epilogue reads into L2.
             if (!SWIGLU && piece < 0 && p.mode == KM_RESIDUAL && row_ok) {
@@ -419,8 +460,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             if (piece >= 0) {
                 // last-round K piece: raw fp32 tile [BM][BN] for the fix-up pass
                 float* dst = p.tail_part +
-                             ((long long)piece * p.tail_tiles + tail_index(mb, nb, p)) * (BM * BN) +
-                             (long long)(quad * 32 + lane) * BN;
+                             ((long long)piece * p.tail_tiles + tail_index(mb, nb, p)) * (BMU * BN) +
+                             (long long)trow * BN;
 #pragma unroll 1
                 for (int c = half * HC; c < half * HC + HC; c += 32) {
                     float v[32];
@@ -497,40 +538,55 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             // this warp is done reading accumulator `buf`: hand it back to the MMA issuer
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_remote(smem_in_cta(tempty_bar(buf), 0));
+                else mbar_arrive(tempty_bar(buf));
+            }
         }
     }
 
     // ---------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp == 0 && lane == 0) {
-        // Let every TMA load and MMA this CTA issued land before its shared memory and TMEM go.
+    if constexpr (PAIR) {
+        // Rank 1's loads complete on rank 0's barriers, so rank 0 does the waiting for both: rank 1
+        // reports how far its loads went and whether it gave up a wait.
+        if (rank == 1 && threadIdx.x == 0) {
+            st_shared_cluster(smem_in_cta(smem_u32(peer_slot), 0), (uint32_t)*issued_slot);
+            st_shared_cluster(smem_in_cta(smem_u32(peer_slot + 1), 0), (uint32_t)*abort_flag);
+        }
+        cluster_barrier_sync();
+    }
+    if ((*abort_flag || (PAIR && peer_slot[1])) && rank == 0 && warp == 0 && lane == 0) {
+        // Let every TMA load and MMA issued land before the shared memory and TMEM go.
         volatile int never = 0;
-        const int issued = *issued_slot;
+        const int issued = max(*issued_slot, peer_slot[0]);
         for (int i = max(0, issued - C::STAGES); i < issued; ++i)
             (void)mbar_wait(full_bar(i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u, &never);
         const int committed = *committed_slot;
         for (int jj = max(0, committed - 2); jj < committed; ++jj)
             (void)mbar_wait(tfull_bar(jj & 1), (uint32_t)(jj >> 1) & 1u, &never);
     }
-    __syncthreads();
+    if constexpr (PAIR) cluster_barrier_sync();   // rank 1 stays until rank 0 has seen every copy land
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+        else tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
 // Fix-up of the last-round K pieces: sum the pieces of each tail tile in piece order, then apply
 // the tile's epilogue.  One thread per 8 D-columns of one row (SwiGLU: 8 gate + the 8 matching up).
+// Tiles are BMt x BNt (BMt = 256 when CTA pairs computed them).
 __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
-                                  int mt, int group, int BNt, int swiglu, int M, int n_valid, int ldo, int mode,
-                                  void* out) {
+                                  int mt, int group, int BMt, int BNt, int swiglu, int M, int n_valid, int ldo,
+                                  int mode, void* out) {
     pdl_launch();
     pdl_wait();
     const int gw = swiglu ? BNt / 16 : BNt / 8;
-    const long long per_tile = (long long)BM * gw;
+    const long long per_tile = (long long)BMt * gw;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= per_tile * tail_tiles) return;
     const int t = (int)(idx / per_tile);
@@ -542,11 +598,11 @@ __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int 
     const int band = lin / band_units;
     const int within = lin - band * band_units;
     const int mb = within % mt, nb = band * group + within / mt;
-    const int row = mb * BM + r;
+    const int row = mb * BMt + r;
     if (row >= M) return;
     float a[8] = {0, 0, 0, 0, 0, 0, 0, 0}, u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     for (int pc = 0; pc < pieces; ++pc) {
-        const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)r * BNt + cg;
+        const float* src = tp + ((long long)pc * tail_tiles + t) * ((long long)BMt * BNt) + (long long)r * BNt + cg;
         const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
         a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w; a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
         if (swiglu) {
@@ -584,14 +640,14 @@ __global__ void tail_fixup_kernel(const float* __restrict__ tp, int pieces, int 
 // row, with the compensated sum of squares of the row norm kernel.
 template <int NC>
 __global__ void __launch_bounds__(256, 2) tail_fixup_norm_kernel(const float* __restrict__ tp, int pieces, int tail_tiles, int head_units,
-                                       int mt, int group, int BNt, int M, int N, bf16* __restrict__ r,
+                                       int mt, int group, int BMt, int BNt, int M, int N, bf16* __restrict__ r,
                                        const bf16* __restrict__ g, bf16* __restrict__ y, float eps) {
     pdl_launch();
     pdl_wait();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
-    const int mb = row / BM, rr = row - mb * BM;
+    const int mb = row / BMt, rr = row - mb * BMt;
     uint4* rrow = reinterpret_cast<uint4*>(r + (long long)row * N);
     const uint4* gv = reinterpret_cast<const uint4*>(g);
     // the row, and the gains, requested before anything waits for them
@@ -613,7 +669,7 @@ __global__ void __launch_bounds__(256, 2) tail_fixup_norm_kernel(const float* __
 #pragma unroll
         for (int pc = 0; pc < kMaxTailPieces; ++pc) {
             if (pc < pieces) {
-                const float* src = tp + ((long long)pc * tail_tiles + t) * (BM * BNt) + (long long)rr * BNt + (col - nb * BNt);
+                const float* src = tp + ((long long)pc * tail_tiles + t) * ((long long)BMt * BNt) + (long long)rr * BNt + (col - nb * BNt);
                 x0[pc] = *reinterpret_cast<const float4*>(src);
                 x1[pc] = *reinterpret_cast<const float4*>(src + 4);
             }
@@ -850,6 +906,8 @@ struct Plan {
     int kbps;
     int mt, nt;
     int head_units = 0, tail_tiles = 0, tail_splits = 1, kb_per_tail = 0;
+    bool pair = false;   // 2-CTA clusters on 256 x 256 tiles
+    int bmt = BM;        // rows of a tile
 };
 
 // Last-round split: when the final round of tiles fills at most half the SMs, each of its tiles is
@@ -908,23 +966,99 @@ Plan make_plan(int M, int N, int K, int epi, int split_req, int nsm, int ke = BK
     return best;
 }
 
-template <int BN, bool SW, bool F8>
-cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, const Plan& pl,
-                        cudaStream_t st) {
+// Rows from which the projection GEMM runs on CTA pairs (at least two 256-row tiles).
+constexpr int kPairMinM = 512;
+
+template <int BN, bool SW, bool F8, bool PAIR>
+cudaError_t configure_tile() {
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, SW, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<BN>::SMEM);
+        e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, SW, F8, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<BN, PAIR>::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    return cudaSuccess;
+}
+
+// CTA pairs that can be resident at once (one CTA per SM; a pair needs two SMs of one GPC).
+int pair_walkers() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return device_sm_count() / 2;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (configure_tile<256, false, false, true>() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * device_sm_count());
+            cfg.blockDim = dim3(kTileThreads);
+            cfg.dynamicSmemBytes = Cfg<256, true>::SMEM;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<256, false, false, true>, &cfg) != cudaSuccess)
+                n = 0;
+            (void)cudaGetLastError();
+        }
+        cached[dev] = n > 0 ? std::min(n, device_sm_count() / 2) : device_sm_count() / 2;
+    }
+    return cached[dev];
+}
+
+// 256 x 256 tiles over CTA pairs: no K split; a last round that leaves more than half of the pairs
+// idle runs as K pieces, as on single CTAs.
+Plan make_plan_pair(int M, int N, int K, int epi, int npairs) {
+    const int n_kb = K / BK;
+    const int dcols = epi == EPI_SWIGLU ? 2 * N : N;
+    Plan pl{256, 1, n_kb, (M + 2 * BM - 1) / (2 * BM), (dcols + 255) / 256};
+    pl.pair = true;
+    pl.bmt = 2 * BM;
+    plan_tail(pl, n_kb, npairs);
+    return pl;
+}
+
+bool use_pairs(int M, int split_req, bool fp8, bool partial_only) {
+    return g_gemm_pairs && !fp8 && !partial_only && M >= kPairMinM && split_req <= 1;
+}
+
+template <int BN, bool SW, bool F8, bool PAIR>
+cudaError_t launch_tile(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, const Plan& pl,
+                        cudaStream_t st) {
+    cudaError_t e = configure_tile<BN, SW, F8, PAIR>();
+    if (e != cudaSuccess) return e;
     const long long units = (long long)pl.mt * pl.nt * pl.splits;
-    const int nsm = device_sm_count();
-    dim3 grid((unsigned)std::min<long long>(units, nsm));
-    HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW, F8>, dim3(grid), dim3(kTileThreads), Cfg<BN>::SMEM, st, ma, mb, g);
+    if constexpr (PAIR) {
+        const int pairs = (int)std::min<long long>(units, pair_walkers());
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * pairs);
+        cfg.blockDim = dim3(kTileThreads);
+        cfg.dynamicSmemBytes = Cfg<BN, PAIR>::SMEM;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        count_launches(1);
+        e = cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<BN, SW, F8, PAIR>, ma, mb, g);
+        if (e != cudaSuccess) return e;
+    } else {
+        const int nsm = device_sm_count();
+        dim3 grid((unsigned)std::min<long long>(units, nsm));
+        HRA_LAUNCH(gemm_bf16_tc_kernel<BN, SW, F8, PAIR>, dim3(grid), dim3(kTileThreads), Cfg<BN, PAIR>::SMEM, st, ma,
+                   mb, g);
+    }
     return cudaGetLastError();
 }
 
@@ -1022,6 +1156,8 @@ bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* di
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool g_gemm_pairs = true;
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -1035,19 +1171,21 @@ int device_sm_count() {
 }
 
 size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool partial_only) {
-    (void)partial_only;
     if (M <= kSmallM) {   // the head-form path always writes its partial planes
         const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
         const HeadPlan hp = head_plan((int)ldp, K, kSmallHeadSplits, split_req);
         return (size_t)hp.splits * (size_t)M * ldp * sizeof(float);
     }
-    const Plan pl = make_plan(M, N, K, epi, split_req, device_sm_count());
-    if (pl.tail_tiles > 0) return (size_t)pl.tail_splits * pl.tail_tiles * BM * pl.bn * sizeof(float);
+    const Plan pl = use_pairs(M, split_req, false, partial_only) ? make_plan_pair(M, N, K, epi, pair_walkers())
+                                                                   : make_plan(M, N, K, epi, split_req, device_sm_count());
+    if (pl.tail_tiles > 0) return (size_t)pl.tail_splits * pl.tail_tiles * pl.bmt * pl.bn * sizeof(float);
     if (pl.splits <= 1) return 0;
     const size_t ldp = epi == EPI_SWIGLU ? 2 * (size_t)N : (size_t)N;
     return (size_t)pl.splits * (size_t)M * ldp * sizeof(float);
 }
 
+// Tail pieces x tail tiles stay within the walkers (SMs, or pairs of 256-row tiles): either way at
+// most SMs x 128 rows x 256 columns of fp32.
 size_t linear_tail_bound() { return (size_t)device_sm_count() * BM * 256 * sizeof(float); }
 
 size_t linear_partial_bound(int m_max, int N, int K, int epi) {
@@ -1063,7 +1201,8 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     const int nsm = device_sm_count();
     const int ke = c.fp8 ? 2 * BK : BK;
     if (c.fp8 && (c.K % ke != 0 || c.a_scale == nullptr || c.w_scale == nullptr)) return cudaErrorInvalidValue;
-    Plan pl = make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm, ke);
+    Plan pl = use_pairs(c.M, c.split_req, c.fp8, c.partial_only) ? make_plan_pair(c.M, c.N, c.K, c.epi, pair_walkers())
+                                                                : make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm, ke);
     if (c.partial_only) pl.tail_tiles = 0;   // the caller reads one output plane from the partial buffer
     const bool fuse_qk =
         !c.fp8 && c.qk != nullptr && c.epi == EPI_STORE && pl.splits == 1 && pl.bn % c.qk->hd == 0;
@@ -1074,7 +1213,7 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
 
     CUtensorMap ma, mb;
     if (!make_map(&ma, c.a, c.M, c.K, BM, esize)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, c.w, w_rows, c.K, sw ? pl.bn / 2 : pl.bn, esize)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, c.w, w_rows, c.K, (sw || pl.pair) ? pl.bn / 2 : pl.bn, esize)) return cudaErrorInvalidValue;
 
     GemmArgs g{};
     g.err = c.err;
@@ -1114,15 +1253,22 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     }
 
     cudaError_t e;
-    if (c.fp8) {
+    if (pl.pair) {
+        e = sw ? launch_tile<256, true, false, true>(ma, mb, g, pl, st)
+               : launch_tile<256, false, false, true>(ma, mb, g, pl, st);
+    } else if (c.fp8) {
         if (pl.bn == 256)
-            e = sw ? launch_tile<256, true, true>(ma, mb, g, pl, st) : launch_tile<256, false, true>(ma, mb, g, pl, st);
+            e = sw ? launch_tile<256, true, true, false>(ma, mb, g, pl, st)
+                   : launch_tile<256, false, true, false>(ma, mb, g, pl, st);
         else
-            e = sw ? launch_tile<128, true, true>(ma, mb, g, pl, st) : launch_tile<128, false, true>(ma, mb, g, pl, st);
+            e = sw ? launch_tile<128, true, true, false>(ma, mb, g, pl, st)
+                   : launch_tile<128, false, true, false>(ma, mb, g, pl, st);
     } else if (pl.bn == 256) {
-        e = sw ? launch_tile<256, true, false>(ma, mb, g, pl, st) : launch_tile<256, false, false>(ma, mb, g, pl, st);
+        e = sw ? launch_tile<256, true, false, false>(ma, mb, g, pl, st)
+               : launch_tile<256, false, false, false>(ma, mb, g, pl, st);
     } else {
-        e = sw ? launch_tile<128, true, false>(ma, mb, g, pl, st) : launch_tile<128, false, false>(ma, mb, g, pl, st);
+        e = sw ? launch_tile<128, true, false, false>(ma, mb, g, pl, st)
+               : launch_tile<128, false, false, false>(ma, mb, g, pl, st);
     }
     if (c.splits_used) *c.splits_used = pl.splits;
     if (e == cudaSuccess && pl.tail_tiles > 0 && g.mode == KM_RESIDUAL && c.norm_out != nullptr &&
@@ -1132,21 +1278,21 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
         const dim3 grid((unsigned)((c.M + warps - 1) / warps));
         if (c.N == 2560)
             HRA_LAUNCH(tail_fixup_norm_kernel<10>, grid, dim3(32 * warps), 0, st, c.partial, pl.tail_splits,
-                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
+                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bmt, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
                        c.norm_gain, c.norm_out, c.norm_eps);
         else
             HRA_LAUNCH(tail_fixup_norm_kernel<1>, grid, dim3(32 * warps), 0, st, c.partial, pl.tail_splits,
-                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
+                       pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bmt, pl.bn, c.M, c.N, reinterpret_cast<bf16*>(c.out),
                        c.norm_gain, c.norm_out, c.norm_eps);
         if (c.norm_done) *c.norm_done = true;
         return cudaGetLastError();
     }
     if (e == cudaSuccess && pl.tail_tiles > 0) {
         const int gw = sw ? pl.bn / 16 : pl.bn / 8;
-        const long long items = (long long)pl.tail_tiles * BM * gw;
-        HRA_LAUNCH(tail_fixup_kernel, dim3((unsigned)((items + 255) / 256)), dim3(256), 0, st, 
-            c.partial, pl.tail_splits, pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bn, sw ? 1 : 0, c.M, c.N, c.N,
-            g.mode, c.out);
+        const long long items = (long long)pl.tail_tiles * pl.bmt * gw;
+        HRA_LAUNCH(tail_fixup_kernel, dim3((unsigned)((items + 255) / 256)), dim3(256), 0, st,
+            c.partial, pl.tail_splits, pl.tail_tiles, pl.head_units, pl.mt, 8, pl.bmt, pl.bn, sw ? 1 : 0, c.M, c.N,
+            c.N, g.mode, c.out);
         return cudaGetLastError();
     }
     if (e != cudaSuccess || pl.splits <= 1 || c.partial_only) return e;

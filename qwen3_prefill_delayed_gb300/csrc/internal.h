@@ -233,8 +233,11 @@ bool decode_pass_supported(const DecodePassCall& c);
 size_t decode_pass_scratch_bytes(int M, int H, int nq, int nkv, int hd, int F, int nsm);
 size_t decode_pass_sync_bytes(int M, int nkv, int F, int H);
 cudaError_t launch_decode_pass(const DecodePassCall& c, cudaStream_t st);
-// process-wide switch between the persistent pass (default) and the layer-by-layer kernels
+// process-wide switch between the persistent pass (opt-in) and the layer-by-layer kernels (default)
 extern bool g_decode_pass_enabled;
+// process-wide switch: projection GEMMs of at least 512 BF16 rows on 2-CTA clusters (default) or
+// on single CTAs
+extern bool g_gemm_pairs;
 
 // ------------------------------------------------------------------ codebook step finalize
 struct CodebookArgs {

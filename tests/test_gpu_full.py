@@ -1,9 +1,10 @@
 """GPU parity at the full-width workload sizes, in the launch configuration the benchmark times.
 
 - 36-layer backbone, 32 ragged prompts (lengths 16..256), 2048-slot cache: the oracle recomputes
-  the two shortest sequences and the shortest one longer than 64 tokens (more than one attention
-  key tile, so the heaviest-first schedule at depth) end to end (every layer's K/V and the last
-  hidden); every sequence's unused cache slots must stay untouched.
+  the two shortest sequences, the shortest one longer than 64 tokens (more than one attention
+  key tile, so the heaviest-first schedule at depth) and the last one (its rows end the batch, in
+  the last, partly empty 256-row tile of the projection GEMMs) end to end (every layer's K/V and
+  the last hidden); every sequence's unused cache slots must stay untouched.
 - the same backbone's autoregressive audio loop: the shortest prompt prefilled, then three K = 8
   frames (codebook step + 36-layer decode pass) captured in one CUDA graph, against the oracle's
   prefill + codebook step + decode chain: codes, stop flags and the delay state bit for bit (a
@@ -58,7 +59,7 @@ def test_ragged_batch_36_layers(hra, ragged):
     _untouched(cache, p.lengths)
     order = sorted(range(len(p.lengths)), key=lambda b: p.lengths[b])
     longer = next(b for b in order if p.lengths[b] > 64)
-    for idx in (order[:2], [longer]):
+    for idx in (order[:2], [longer], [len(p.lengths) - 1]):
         lens = [p.lengths[b] for b in idx]
         tok = p.tokens[idx].numpy()
         kv_o, hid_o = oracle.prefill(d, hw, tok, lens, max(lens))

@@ -1,6 +1,7 @@
 """GPU parity of the tensor-core projection GEMM (through the C ABI's hra_linear) against the
 oracle's fp32 linear, for every epilogue, ragged M / N tails, several M tiles and forced or
-automatic K splits."""
+automatic K splits.  Shapes of at least 512 rows run in both GEMM forms: on 2-CTA clusters
+(256-row tiles, the default) and on single CTAs."""
 import numpy as np
 import pytest
 import torch
@@ -42,6 +43,10 @@ CASES = [
     (4255, 2560, 2560, "residual", 0),     # 340 tiles: the last round runs as 4 K pieces per tile
     (4255, 2560, 1024, "swiglu", 0),       # 680 tiles: last round in 2 K pieces
     (4255, 2560, 640, "store", 0),
+    (4196, 2560, 2560, "residual", 0),     # pairs: the last 256-row tile's second CTA has no valid row
+    (2600, 2560, 4096, "residual", 0),     # pairs: 110 tiles, the last round in 2 K pieces
+    (600, 6144, 2560, "store", 0),         # pairs: 3 x 24 tiles, one round
+    (1000, 1000, 512, "swiglu", 0),        # ragged N: the last gate/up tile runs past F
     (3, 4104, 256, "f32", 0),
     (1, 8208, 2560, "f32", 0),             # row ranges of 54 weight rows per CTA, whole K
     (8, 6144, 2560, "store", 0),           # row ranges of 41 rows
@@ -57,8 +62,19 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,N,K,epi,split", CASES)
-def test_linear(hra, M, N, K, epi, split):
+PAIR_MIN_M = 512   # the library's threshold for the 2-CTA form
+CASES_BOTH = [c + (True,) for c in CASES] + [c + (False,) for c in CASES if c[0] >= PAIR_MIN_M]
+
+
+@pytest.fixture()
+def gemm_form(hra, request):
+    prev = hra.hra_set_gemm_pairs(request.param)
+    yield request.param
+    hra.hra_set_gemm_pairs(prev)
+
+
+@pytest.mark.parametrize("M,N,K,epi,split,gemm_form", CASES_BOTH, indirect=["gemm_form"])
+def test_linear(hra, M, N, K, epi, split, gemm_form):
     code = {"store": hra.EPI_STORE, "residual": hra.EPI_RESIDUAL, "swiglu": hra.EPI_SWIGLU, "f32": hra.EPI_F32}[epi]
     rows = 2 * N if epi == "swiglu" else N
     x = _rand((M, K), 1.0, M * 7 + K)
