@@ -333,12 +333,13 @@ def main():
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     sm_max = peaks.get("sm_max_mhz") or (clk or {}).get("sm_max_mhz")
     sm_run = (clk or {}).get("sm_mhz")
-    roofline = {"bound": "tensor", "kernel": "gemm_bf16_tc_kernel<256,SwiGLU> (gate/up, full layers)",
+    roofline = {"bound": "tensor", "kernel": "gemm_bf16_tc_kernel<256,SwiGLU,bf16,pair> (gate/up on 2-CTA clusters, full layers)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": f"{peaks_kind} bf16 burst",
                 "frac_of_sustained": achieved / sustained,
                 "frac_at_max_clock": (achieved * sm_max / sm_run / peak) if sm_max and sm_run else None,
-                "traffic": traffic_for("gate_up", ["qwen3_prefill_delayed_gb300/csrc/gemm_tc.cu"]),
+                "traffic": traffic_for("gate_up", ["qwen3_prefill_delayed_gb300/csrc/gemm_tc.cu",
+                                                      "qwen3_prefill_delayed_gb300/csrc/common.cuh"]),
                 "launch_ms": gu_ms, "flops_per_launch": gu_flops, "launches_timed": probe_n}
 
     # ---------------- end to end through the public API with host buffers

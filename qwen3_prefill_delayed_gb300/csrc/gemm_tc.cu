@@ -250,7 +250,7 @@ template <int BN, bool SWIGLU, bool F8, bool PAIR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs p) {
-    static_assert(!PAIR || (BN == 256 && !F8), "CTA pairs: bf16, 256-wide tiles");
+    static_assert(!PAIR || BN == 256, "CTA pairs: 256-wide tiles");
     using C = Cfg<BN, PAIR>;
     constexpr int KE = F8 ? 2 * BK : BK;   // elements per K block (one 128-byte row)
     constexpr int BMU = PAIR ? 2 * BM : BM;   // rows of a work unit's tile
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         *issued_slot = ok ? it : max(it, pre);
     } else if (warp == 1 && lane == 0 && (!PAIR || rank == 0)) {
         // ---------------- MMA issuer: accumulator buffer j % 2 for this CTA's j-th unit
-        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BMU, BN);
+        constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BMU, BN) : idesc_bf16_f32(BMU, BN);
         int it = 0, j = 0;
         bool ok = true;
         for (int u = walker; u < units && ok; u += walkers, ++j) {
@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 const uint64_t bd = sdesc_sw128(b_tile(s));
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {   // 4 x 32 bytes of each 128-byte row
-                    if constexpr (F8)
+                    if constexpr (F8 && PAIR)
+                        tc_mma_f8_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    else if constexpr (F8)
                         tc_mma_f8(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     else if constexpr (PAIR)
                         tc_mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
@@ -1014,8 +1016,8 @@ int pair_walkers() {
 
 // 256 x 256 tiles over CTA pairs: no K split; a last round that leaves more than half of the pairs
 // idle runs as K pieces, as on single CTAs.
-Plan make_plan_pair(int M, int N, int K, int epi, int npairs) {
-    const int n_kb = K / BK;
+Plan make_plan_pair(int M, int N, int K, int epi, int npairs, int ke = BK) {
+    const int n_kb = K / ke;
     const int dcols = epi == EPI_SWIGLU ? 2 * N : N;
     Plan pl{256, 1, n_kb, (M + 2 * BM - 1) / (2 * BM), (dcols + 255) / 256};
     pl.pair = true;
@@ -1024,8 +1026,8 @@ Plan make_plan_pair(int M, int N, int K, int epi, int npairs) {
     return pl;
 }
 
-bool use_pairs(int M, int split_req, bool fp8, bool partial_only) {
-    return g_gemm_pairs && !fp8 && !partial_only && M >= kPairMinM && split_req <= 1;
+bool use_pairs(int M, int split_req, bool partial_only) {
+    return g_gemm_pairs && !partial_only && M >= kPairMinM && split_req <= 1;
 }
 
 template <int BN, bool SW, bool F8, bool PAIR>
@@ -1176,7 +1178,7 @@ size_t linear_partial_bytes(int M, int N, int K, int epi, int split_req, bool pa
         const HeadPlan hp = head_plan((int)ldp, K, kSmallHeadSplits, split_req);
         return (size_t)hp.splits * (size_t)M * ldp * sizeof(float);
     }
-    const Plan pl = use_pairs(M, split_req, false, partial_only) ? make_plan_pair(M, N, K, epi, pair_walkers())
+    const Plan pl = use_pairs(M, split_req, partial_only) ? make_plan_pair(M, N, K, epi, pair_walkers())
                                                                    : make_plan(M, N, K, epi, split_req, device_sm_count());
     if (pl.tail_tiles > 0) return (size_t)pl.tail_splits * pl.tail_tiles * pl.bmt * pl.bn * sizeof(float);
     if (pl.splits <= 1) return 0;
@@ -1201,8 +1203,8 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     const int nsm = device_sm_count();
     const int ke = c.fp8 ? 2 * BK : BK;
     if (c.fp8 && (c.K % ke != 0 || c.a_scale == nullptr || c.w_scale == nullptr)) return cudaErrorInvalidValue;
-    Plan pl = use_pairs(c.M, c.split_req, c.fp8, c.partial_only) ? make_plan_pair(c.M, c.N, c.K, c.epi, pair_walkers())
-                                                                : make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm, ke);
+    Plan pl = use_pairs(c.M, c.split_req, c.partial_only) ? make_plan_pair(c.M, c.N, c.K, c.epi, pair_walkers(), ke)
+                                                         : make_plan(c.M, c.N, c.K, c.epi, c.split_req, nsm, ke);
     if (c.partial_only) pl.tail_tiles = 0;   // the caller reads one output plane from the partial buffer
     const bool fuse_qk =
         !c.fp8 && c.qk != nullptr && c.epi == EPI_STORE && pl.splits == 1 && pl.bn % c.qk->hd == 0;
@@ -1253,7 +1255,10 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
     }
 
     cudaError_t e;
-    if (pl.pair) {
+    if (pl.pair && c.fp8) {
+        e = sw ? launch_tile<256, true, true, true>(ma, mb, g, pl, st)
+               : launch_tile<256, false, true, true>(ma, mb, g, pl, st);
+    } else if (pl.pair) {
         e = sw ? launch_tile<256, true, false, true>(ma, mb, g, pl, st)
                : launch_tile<256, false, false, true>(ma, mb, g, pl, st);
     } else if (c.fp8) {

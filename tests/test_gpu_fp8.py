@@ -5,7 +5,8 @@ prefill_tower/fp8_chain.py" page, its description;
 - E4M3 weight and activation quantization: codes and scales bit-exact;
 - the FP8 tcgen05 GEMM (kind::f8f6f4) against the oracle's FP8 linear on the same codes and scales,
   for every epilogue and the plan shapes of the tile kernel (M below one tile, split K, several
-  rounds with last-round K pieces, SwiGLU with a ragged tile);
+  rounds with last-round K pieces, SwiGLU with a ragged tile), from 512 rows in both GEMM forms
+  (2-CTA clusters and single CTAs);
 - calibration: max |input| of every projection within one bf16 step of the oracle's;
 - the FP8 prefill against the oracle's FP8 prefill (both given the oracle's calibrated activation
   scales, so no oracle input comes from the GPU), tiny model and one full-width layer; its noise
@@ -57,11 +58,21 @@ CASES = [
     (130, 1000, 512, "swiglu"),             # ragged SwiGLU tile
     (1000, 2560, 1024, "residual"),
     (4255, 2560, 640, "store"),             # several rounds; the last one in K pieces
+    (1000, 1536, 1024, "swiglu"),           # 2-CTA form: gate rows in one CTA, up rows in the other
 ]
+PAIR_MIN_M = 512   # the library's threshold for the 2-CTA form
+CASES_BOTH = [c + (True,) for c in CASES] + [c + (False,) for c in CASES if c[0] >= PAIR_MIN_M]
 
 
-@pytest.mark.parametrize("M,N,K,epi", CASES)
-def test_fp8_linear(hra, M, N, K, epi):
+@pytest.fixture()
+def gemm_form(hra, request):
+    prev = hra.hra_set_gemm_pairs(request.param)
+    yield request.param
+    hra.hra_set_gemm_pairs(prev)
+
+
+@pytest.mark.parametrize("M,N,K,epi,gemm_form", CASES_BOTH, indirect=["gemm_form"])
+def test_fp8_linear(hra, M, N, K, epi, gemm_form):
     code = {"store": hra.EPI_STORE, "residual": hra.EPI_RESIDUAL, "swiglu": hra.EPI_SWIGLU, "f32": hra.EPI_F32}[epi]
     rows = 2 * N if epi == "swiglu" else N
     w = _rand((rows, K), 0.02, N + K)
