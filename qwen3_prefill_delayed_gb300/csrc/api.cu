@@ -75,7 +75,8 @@ struct Region {
 
 // Offsets (bytes) of every buffer inside a caller workspace.
 struct Layout {
-    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, xs, sync, total;
+    size_t err, row_seq, row_pos, cu, last_row, start, rope, r, y, qkv, q, att, h, rl, part, apart, x8, xs, sync, asched,
+        total;
     size_t part_bytes;
     int attn_splits;
 };
@@ -143,6 +144,8 @@ Layout backbone_layout(const hra_dims& d, int batch, int rows, int rope_rows, in
     // counters and per-row sums of the persistent decoder pass (M <= 64 rows), cleared by the
     // call's row-map kernel
     L.sync = g.take(decode_pass_sync_bytes((int)std::min<size_t>(T, 64), d.n_kv_heads, (int)F, (int)H));
+    // the prefill attention's work list (built once per call)
+    L.asched = g.take(attention_schedule_bytes((int)T, batch));
     L.total = g.off;
     return L;
 }
@@ -360,6 +363,11 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         }
     }
 
+    // the prefill attention's work list: the same sequences for every layer
+    if (prefill && (d.n_layers > 1 || full_last))
+        HRA_TRY(launch_attention_schedule(P.at<int32_t>(L.cu), P.at<int32_t>(L.start), batch, max_len, nq, nkv,
+                                          P.at<int32_t>(L.asched), st));
+
     for (int l = 0; l < d.n_layers; ++l) {
         const hra_layer_weights& lw = w.layers[l];
         bf16* kvl = reinterpret_cast<bf16*>(kv.base) + (size_t)l * layer_elems;
@@ -393,7 +401,8 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         if (!tail) {
             if (prefill) {
                 PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), P.at<int32_t>(L.start), att, batch, max_len,
-                                   kv.n_slots, nq, nkv, hd, rows, kv.batch, P.at<unsigned int>(L.err)};
+                                   kv.n_slots, nq, nkv, hd, rows, kv.batch, P.at<unsigned int>(L.err),
+                                   P.at<int32_t>(L.asched)};
                 HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] {
                     return launch_prefill_attention_tc(pa, st);
                 }));

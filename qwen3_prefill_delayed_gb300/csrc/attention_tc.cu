@@ -8,8 +8,11 @@
 // A work item = one kv head of one sequence and QT = 128 / G consecutive query positions, for all
 // G = n_q / n_kv q heads of that kv head: the 128 rows of every tcgen05.mma are (position, head)
 // pairs, row r = (position r / G, head r % G), so each K/V tile is loaded once for the G heads.
-// The kernel is persistent (one CTA per SM walks the items, heaviest first) and its pipelines run
-// across items: the next item's Q and K/V stream in while this one's softmax and PV finish, and O
+// The kernel is persistent (two CTAs per SM) and its pipelines run across items.  The items come
+// from a work list built once per call (attn_schedule_kernel): the non-empty (query tile, sequence)
+// pairs sorted by their key-tile count, heaviest first, each for every kv head; CTA c takes list
+// entries in snake order (c, 2 grid - 1 - c, 2 grid + c, ...), so every round pairs a heavier and
+// a lighter item and all CTAs finish close together.  Within a CTA, the next item's Q and K/V stream in while this one's softmax and PV finish, and O
 // alternates between two TMEM accumulators so one item's epilogue overlaps the next item's MMAs.
 //   warp 0     TMA: lane 0 the Q tile (a 3-D box of 64 dims x G heads x QT positions per 64-dim
 //              half) and a 3-stage ring of 64-key K tiles, lane 1 the V ring, straight from the
@@ -79,17 +82,73 @@ struct TcAttnArgs {
     int batch, max_len, n_slots, nq, nkv, G, QT;
     long long kv_rows_per_seq;   // 2 * nkv * n_slots: rows of one sequence in the cache's row view
     float scale_log2;
+    const int32_t* sched;        // [0] = pairs, then (query tile << 16 | sequence), heaviest first
 };
 
-// Work item i (heaviest query tiles first): q tile n_qt - 1 - i / (nkv * batch), sequence and kv
-// head from i % (nkv * batch).  Returns the item's key-tile count (0: the tile is past the sequence).
-__device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, int tk, int& b, int& j, int& cu0,
-                                         int& len, int& t0, int& s0, int& kv_len) {
-    const int per = p.nkv * p.batch;
-    const int qt = n_qt - 1 - i / per;
-    const int rem = i - (i / per) * per;
-    b = rem / p.nkv;
-    j = rem - b * p.nkv;
+// Work-list builder: one CTA.  Pair (q tile qt, sequence b) is non-empty when qt * QT < len_b; its
+// weight is its key-tile count ceil((start_b + min(len_b, (qt + 1) QT)) / TK).  Counting sort by
+// weight, heaviest first (the order inside one weight is immaterial: items are independent).
+constexpr int kSchedBins = 1024;
+constexpr int kLaunchedTK = 32;   // keys per tile of the launched configuration (the list's weights)
+__global__ void __launch_bounds__(1024) attn_schedule_kernel(const int32_t* __restrict__ cu,
+                                                             const int32_t* __restrict__ start, int batch, int n_qt,
+                                                             int QT, int TK, int32_t* __restrict__ sched) {
+    pdl_launch();
+    pdl_wait();
+    __shared__ int hist[kSchedBins];
+    __shared__ int total;
+    for (int i = threadIdx.x; i < kSchedBins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int n_pairs = n_qt * batch;
+    auto bin_of = [&](int pr, int& code) -> int {   // -1: empty pair
+        const int qt = pr / batch, b = pr - qt * batch;
+        const int len = cu[b + 1] - cu[b];
+        const int t0 = qt * QT;
+        if (t0 >= len) return -1;
+        const int kv = (start ? start[b] : 0) + min(len, t0 + QT);
+        code = (qt << 16) | b;
+        return kSchedBins - 1 - min(kSchedBins - 1, (kv + TK - 1) / TK);   // heaviest first
+    };
+    for (int pr = threadIdx.x; pr < n_pairs; pr += blockDim.x) {
+        int code;
+        const int bin = bin_of(pr, code);
+        if (bin >= 0) atomicAdd(&hist[bin], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {   // exclusive scan of the histogram: 32 bins a lane, then across lanes
+        constexpr int per = kSchedBins / 32;
+        int s = 0;
+        for (int i = 0; i < per; ++i) s += hist[threadIdx.x * per + i];
+        int incl = s;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if ((int)threadIdx.x >= o) incl += v;
+        }
+        int run = incl - s;
+        for (int i = 0; i < per; ++i) {
+            const int h = hist[threadIdx.x * per + i];
+            hist[threadIdx.x * per + i] = run;
+            run += h;
+        }
+        if (threadIdx.x == 31) total = incl;
+    }
+    __syncthreads();
+    for (int pr = threadIdx.x; pr < n_pairs; pr += blockDim.x) {
+        int code;
+        const int bin = bin_of(pr, code);
+        if (bin >= 0) sched[1 + atomicAdd(&hist[bin], 1)] = code;
+    }
+    if (threadIdx.x == 0) sched[0] = total;
+}
+
+// List entry s: pair s / nkv of the work list, kv head s % nkv.  Returns the item's key-tile count.
+__device__ __forceinline__ int attn_item(const TcAttnArgs& p, int s, int tk, int& b, int& j, int& cu0, int& len,
+                                         int& t0, int& s0, int& kv_len) {
+    const int pi = s / p.nkv;
+    const int code = p.sched[1 + pi];
+    j = s - pi * p.nkv;
+    b = code & 0xFFFF;
+    const int qt = code >> 16;
     cu0 = p.cu[b];
     len = p.cu[b + 1] - cu0;
     t0 = qt * p.QT;
@@ -99,7 +158,12 @@ __device__ __forceinline__ int attn_item(const TcAttnArgs& p, int n_qt, int i, i
     return (kv_len + tk - 1) / tk;
 }
 
-// Persistent: each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x, ...  Every role walks
+// The k-th list entry of this CTA: snake order over the grid.
+__device__ __forceinline__ int snake_entry(int k) {
+    return k * (int)gridDim.x + ((k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+// Persistent: each CTA walks list entries snake_entry(0), snake_entry(1), ...  Every role walks
 // the same items and numbers the key tiles it handles across items (g), which fixes the K/V ring
 // stage (g % NS), the S and P buffer (g & 1) and each barrier's phase.  Every barrier's consecutive
 // completions are gated by the other side having seen the previous one, so no waiter can fall two
@@ -121,8 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
     const uint32_t sP0 = smem_u32(smem + C::OFF_P);   // buffer q: hi at sP0 + 2q P_BYTES, lo right after
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_qt = (p.max_len + p.QT - 1) / p.QT;
-    const int n_items = n_qt * p.nkv * p.batch;
+    const int n_items = p.sched[0] * p.nkv;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBARS; ++i) {
@@ -152,8 +215,10 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
         const uint32_t ring = is_k ? sK : sV;
         int g = 0, it = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
+        for (int k = 0; ok; ++k) {
+            const int i = snake_entry(k);
+            if (i >= n_items) break;
+            const int n_kt = attn_item(p, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
             if (is_k) {
                 if (it >= 1 && !mbar_wait(bar(C::B_QE), (uint32_t)(it - 1) & 1u, abort_flag)) {
@@ -208,8 +273,10 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
         };
         int g = 0, it = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
+        for (int k = 0; ok; ++k) {
+            const int i = snake_entry(k);
+            if (i >= n_items) break;
+            const int n_kt = attn_item(p, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
             const int ob = it % OB;
             const uint32_t tO = tmem + 2 * TK + (uint32_t)(ob * 128);
@@ -271,8 +338,10 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
                 ++pv_seen;
             }
         };
-        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            const int n_kt = attn_item(p, n_qt, i, TK, b, j, cu0, len, t0, s0, kv_len);
+        for (int k = 0; ok; ++k) {
+            const int i = snake_entry(k);
+            if (i >= n_items) break;
+            const int n_kt = attn_item(p, i, TK, b, j, cu0, len, t0, s0, kv_len);
             if (n_kt == 0) continue;
             const bool row_ok = t0 + tl < len;
             const int qpos = s0 + t0 + tl;
@@ -482,6 +551,7 @@ cudaError_t launch_tc_cfg(const PrefillAttnArgs& a, cudaStream_t st) {
     p.QT = QT;
     p.kv_rows_per_seq = 2LL * a.nkv * a.n_slots;
     p.scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
+    p.sched = a.sched;
     const long long items = (long long)((a.max_len + QT - 1) / QT) * a.nkv * a.batch;
     const int grid = (int)std::min<long long>(items, (long long)device_sm_count() * kCtasPerSm);
     HRA_LAUNCH((prefill_attn_tc_kernel<HD, TK, NS, OB>), dim3(grid), dim3(kTcThreads), C::SMEM, st, mq, mkv, p);
@@ -493,14 +563,31 @@ cudaError_t launch_tc_cfg(const PrefillAttnArgs& a, cudaStream_t st) {
 // layer) it beats <64, 3, 2>.
 template <int HD>
 cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
-    return launch_tc_cfg<HD, 32, 2, 1>(a, st);
+    return launch_tc_cfg<HD, kLaunchedTK, 2, 1>(a, st);
 }
 
 }  // namespace
 
+size_t attention_schedule_bytes(int rows, int batch) {
+    // pairs <= sum_b ceil(len_b / QT) <= rows / QT + batch, QT >= 16
+    return ((size_t)rows / 16 + (size_t)batch + 2) * sizeof(int32_t);
+}
+
+cudaError_t launch_attention_schedule(const int32_t* cu, const int32_t* start, int batch, int max_len, int nq,
+                                      int nkv, int32_t* sched, cudaStream_t st) {
+    const int G = nkv > 0 ? nq / nkv : 0;
+    if ((G != 1 && G != 2 && G != 4 && G != 8) || batch < 1 || batch > 65535 || sched == nullptr)
+        return cudaErrorInvalidValue;
+    const int QT = TROWS / G;
+    const int n_qt = (max_len + QT - 1) / QT;
+    HRA_LAUNCH(attn_schedule_kernel, dim3(1), dim3(1024), 0, st, cu, start, batch, n_qt, QT, kLaunchedTK, sched);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st) {
     const int G = a.nkv > 0 ? a.nq / a.nkv : 0;
     if (G != 1 && G != 2 && G != 4 && G != 8) return cudaErrorInvalidValue;
+    if (a.sched == nullptr) return cudaErrorInvalidValue;
     if (a.hd == 128) return launch_tc_hd<128>(a, st);
     if (a.hd == 64) return launch_tc_hd<64>(a, st);
     return cudaErrorInvalidValue;

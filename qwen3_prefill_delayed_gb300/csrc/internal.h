@@ -162,9 +162,15 @@ struct PrefillAttnArgs {
     int total_rows;         // T (rows of q)
     int cache_batch;        // sequences the cache holds (kv_layer spans cache_batch * 2 * nkv * n_slots rows)
     unsigned int* err;      // sticky device error word
+    const int32_t* sched;   // work list from launch_attention_schedule (same batch, lengths and starts)
 };
 // the tcgen05 kernel (attention_tc.cu): head_dim 64 or 128, n_q / n_kv in {1, 2, 4, 8}
 cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st);
+// The prefill attention's work list for one call's sequences (the same for every layer): the
+// non-empty (query tile, sequence) pairs sorted by key tiles, heaviest first; sched[0] = count.
+size_t attention_schedule_bytes(int rows, int batch);
+cudaError_t launch_attention_schedule(const int32_t* cu, const int32_t* start, int batch, int max_len, int nq,
+                                      int nkv, int32_t* sched, cudaStream_t st);
 
 // cuTensorMapEncodeTiled (bf16 elements, 128-byte swizzle, zero fill out of bounds) for a tensor of
 // `rank` dims (innermost first), strides in bytes of dims 1.. and the box; `map` is a CUtensorMap.
