@@ -88,6 +88,14 @@ def kernel_case(name, m=None):
     print(f"kernel case {name} done")
 
 
+_T0 = time.perf_counter()
+
+
+def log(msg):
+    """Progress on stderr (stdout carries only the JSON line)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -274,6 +282,7 @@ def main():
     peaks, peaks_kind = load_peaks()
 
     # ---------------- main workload
+    log("main workload")
     wl = W.ragged_batch(dev)
     d, p, w = wl["dims"], wl["prompts"], wl["weights"]
     B = len(p.lengths)
@@ -343,6 +352,7 @@ def main():
                 "launch_ms": gu_ms, "flops_per_launch": gu_flops, "launches_timed": probe_n}
 
     # ---------------- end to end through the public API with host buffers
+    log("end to end")
     tok_host = p.tokens.clone().pin_memory()
     hid_host = torch.empty(B, d.hidden, dtype=torch.bfloat16).pin_memory()
     codes_host = torch.empty(B, d.n_codebooks, dtype=torch.int32).pin_memory()
@@ -379,6 +389,7 @@ def main():
                 return {"embed": w["embed"].cpu(), "final_norm": w["final_norm"].cpu(),
                         "layers": [{k: v.cpu() for k, v in w["layers"][i].items()} for i in range(n)]}
             oracle.set_threads(oracle.max_threads())
+            log("cpu baseline")
             t_s, toks = oracle_sample(d, getter, p, d.n_layers, seq)
             cpu_baseline = {"value": toks / t_s, "unit": "tokens/s", "cores": oracle.max_threads(),
                             "kind": "oracle",
@@ -400,6 +411,7 @@ def main():
                        "l2": "inputs larger than L2 (8.05 GB of weights streamed per step)"},
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk, "extra": extra}
+    log("done")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -410,6 +422,7 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
     out = {}
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     # ---- single full-width layer, batch 1, P = 6 and 13 (HBM-bound: 201.85 MB of weights)
+    log("single full-width layer")
     try:
         wl = W.single_layer(13, dev)
         d = wl["dims"]
@@ -432,35 +445,41 @@ def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
     except Exception as ex:
         out["single_layer_prefill"] = {"error": repr(ex)}
     # ---- chained codebook decode, 200 steps in one CUDA graph
+    log("codebook decode")
     try:
         out["codebook_decode"] = bench_codebook(hra, W, torch, dev, hbm, peaks_kind)
     except Exception as ex:
         out["codebook_decode"] = {"error": repr(ex)}
     # ---- the ragged batch prefilled in two chunks (the second reads the first from the cache)
+    log("chunked prefill")
     try:
         out["chunked_prefill"] = bench_chunked(hra, W, torch, dev, w_backbone)
     except Exception as ex:
         out["chunked_prefill"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
     # ---- the static-FP8 variant of the prefill projections on the same ragged batch
+    log("fp8 prefill")
     try:
         out["fp8_prefill"] = bench_fp8(hra, W, torch, dev, w_backbone, peaks)
     except Exception as ex:
         out["fp8_prefill"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
     # ---- the NVFP4 band of the prefill projections on the same ragged batch
+    log("nvfp4 prefill")
     try:
         out["nvfp4_prefill"] = bench_nvfp4(hra, W, torch, dev, w_backbone, peaks)
     except Exception as ex:
         out["nvfp4_prefill"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
     # ---- long prompts + 64 AR frames
+    log("long prompts")
     try:
         out["long_prompts"] = bench_long(hra, W, torch, dev, w_backbone)
     except Exception as ex:
         out["long_prompts"] = {"error": repr(ex)}
     torch.cuda.empty_cache()
     # ---- the CPU oracle on each configuration's workload (single thread and all host cores)
+    log("oracle timing")
     try:
         out["oracle_timing"] = bench_oracle_configs(W)
     except Exception as ex:
