@@ -363,8 +363,9 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
         }
     }
 
-    // the prefill attention's work list: the same sequences for every layer
-    if (prefill && (d.n_layers > 1 || full_last))
+    // the prefill attention's work list: the same sequences for every layer (a single sequence needs
+    // none: its query tiles in order)
+    if (prefill && batch > 1 && (d.n_layers > 1 || full_last))
         HRA_TRY(launch_attention_schedule(P.at<int32_t>(L.cu), P.at<int32_t>(L.start), batch, max_len, nq, nkv,
                                           P.at<int32_t>(L.asched), st));
 
@@ -402,7 +403,7 @@ int run_layers(const hra_dims& d, const hra_weights& w, const hra_kv_cache& kv, 
             if (prefill) {
                 PrefillAttnArgs pa{q, kvl, P.at<int32_t>(L.cu), P.at<int32_t>(L.start), att, batch, max_len,
                                    kv.n_slots, nq, nkv, hd, rows, kv.batch, P.at<unsigned int>(L.err),
-                                   P.at<int32_t>(L.asched)};
+                                   batch > 1 ? P.at<int32_t>(L.asched) : nullptr};
                 HRA_TRY(probed(HRA_PROBE_ATTENTION, attn_work, st, [&] {
                     return launch_prefill_attention_tc(pa, st);
                 }));

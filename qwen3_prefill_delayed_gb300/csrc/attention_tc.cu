@@ -12,7 +12,8 @@
 // from a work list built once per call (attn_schedule_kernel): the non-empty (query tile, sequence)
 // pairs sorted by their key-tile count, heaviest first, each for every kv head; CTA c takes list
 // entries in snake order (c, 2 grid - 1 - c, 2 grid + c, ...), so every round pairs a heavier and
-// a lighter item and all CTAs finish close together.  Within a CTA, the next item's Q and K/V stream in while this one's softmax and PV finish, and O
+// a lighter item and all CTAs finish close together (a single sequence needs no list: its query
+// tiles, last first).  Within a CTA, the next item's Q and K/V stream in while this one's softmax and PV finish, and O
 // alternates between two TMEM accumulators so one item's epilogue overlaps the next item's MMAs.
 //   warp 0     TMA: lane 0 the Q tile (a 3-D box of 64 dims x G heads x QT positions per 64-dim
 //              half) and a 3-stage ring of 64-key K tiles, lane 1 the V ring, straight from the
@@ -82,7 +83,8 @@ struct TcAttnArgs {
     int batch, max_len, n_slots, nq, nkv, G, QT;
     long long kv_rows_per_seq;   // 2 * nkv * n_slots: rows of one sequence in the cache's row view
     float scale_log2;
-    const int32_t* sched;        // [0] = pairs, then (query tile << 16 | sequence), heaviest first
+    const int32_t* sched;        // [0] = pairs, then (query tile << 16 | sequence), heaviest first;
+                                 // null for one sequence: pair i is its query tile n_qt - 1 - i
 };
 
 // Work-list builder: one CTA.  Pair (q tile qt, sequence b) is non-empty when qt * QT < len_b; its
@@ -145,10 +147,16 @@ __global__ void __launch_bounds__(1024) attn_schedule_kernel(const int32_t* __re
 __device__ __forceinline__ int attn_item(const TcAttnArgs& p, int s, int tk, int& b, int& j, int& cu0, int& len,
                                          int& t0, int& s0, int& kv_len) {
     const int pi = s / p.nkv;
-    const int code = p.sched[1 + pi];
     j = s - pi * p.nkv;
-    b = code & 0xFFFF;
-    const int qt = code >> 16;
+    int qt;
+    if (p.sched != nullptr) {
+        const int code = p.sched[1 + pi];
+        b = code & 0xFFFF;
+        qt = code >> 16;
+    } else {   // one sequence: its query tiles, last (heaviest) first
+        b = 0;
+        qt = (p.max_len + p.QT - 1) / p.QT - 1 - pi;
+    }
     cu0 = p.cu[b];
     len = p.cu[b + 1] - cu0;
     t0 = qt * p.QT;
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
     const uint32_t sP0 = smem_u32(smem + C::OFF_P);   // buffer q: hi at sP0 + 2q P_BYTES, lo right after
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = p.sched[0] * p.nkv;
+    const int n_items = (p.sched != nullptr ? p.sched[0] : (p.max_len + p.QT - 1) / p.QT) * p.nkv;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBARS; ++i) {
@@ -587,7 +595,7 @@ cudaError_t launch_attention_schedule(const int32_t* cu, const int32_t* start, i
 cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st) {
     const int G = a.nkv > 0 ? a.nq / a.nkv : 0;
     if (G != 1 && G != 2 && G != 4 && G != 8) return cudaErrorInvalidValue;
-    if (a.sched == nullptr) return cudaErrorInvalidValue;
+    if (a.sched == nullptr && a.batch != 1) return cudaErrorInvalidValue;
     if (a.hd == 128) return launch_tc_hd<128>(a, st);
     if (a.hd == 64) return launch_tc_hd<64>(a, st);
     return cudaErrorInvalidValue;

@@ -162,7 +162,8 @@ struct PrefillAttnArgs {
     int total_rows;         // T (rows of q)
     int cache_batch;        // sequences the cache holds (kv_layer spans cache_batch * 2 * nkv * n_slots rows)
     unsigned int* err;      // sticky device error word
-    const int32_t* sched;   // work list from launch_attention_schedule (same batch, lengths and starts)
+    const int32_t* sched;   // work list from launch_attention_schedule (same batch, lengths and starts);
+                            // may be null for a single sequence
 };
 // the tcgen05 kernel (attention_tc.cu): head_dim 64 or 128, n_q / n_kv in {1, 2, 4, 8}
 cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, cudaStream_t st);
