@@ -56,6 +56,7 @@ struct GemmArgs {
     float* tail_part;
     unsigned int* zero_ptr;   // CTA 0 clears zero_words words here once earlier kernels are done
     int zero_words;
+    int v8;                   // outputs 32-byte aligned (rows and base): epilogues move 32 bytes an instruction
     QkRopeArgs qk;            // KM_QKROPE: per-head q/k norm + RoPE + K/V cache write in the epilogue
     // FP8 operands: the accumulators are multiplied by (*a_scale) * (*w_scale) (device scalars)
     const float* a_scale;
@@ -79,9 +80,43 @@ struct Cfg {
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
 // Store 32 fp32 values of one output row starting at column `col`; `nv` columns are valid
-// (multiple of 8 for bf16, of 4 for fp32).
+// (multiple of 8 for bf16, of 4 for fp32).  v8: the chunk is 32-byte aligned (whole chunks move in
+// 32-byte accesses).
 __device__ __forceinline__ void store_row_chunk(int mode, void* out, long long off, const float (&v)[32],
-                                                int nv) {
+                                                int nv, bool v8) {
+    if (v8 && nv == 32) {
+        if (mode == KM_F32 || mode == KM_PARTIAL) {
+            float* p = reinterpret_cast<float*>(out) + off;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                st_global_32(p + 8 * i, f4_as_u4(v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3]),
+                             f4_as_u4(v[8 * i + 4], v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]));
+            return;
+        }
+        bf16* p = reinterpret_cast<bf16*>(out) + off;
+        uint4 r[4];
+        if (mode == KM_RESIDUAL) {
+            ld_global_32(p, r[0], r[1]);
+            ld_global_32(p + 16, r[2], r[3]);
+        }
+        uint4 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = v[8 * i + j];
+            if (mode == KM_RESIDUAL) {
+                float rr[8];
+                unpack8(r[i], rr);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = rr[j] + f[j];
+            }
+            o[i] = pack8(f);
+        }
+        st_global_32(p, o[0], o[1]);
+        st_global_32(p + 16, o[2], o[3]);
+        return;
+    }
     if (mode == KM_F32 || mode == KM_PARTIAL) {
         float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + off);
 #pragma unroll
@@ -127,7 +162,7 @@ __device__ __forceinline__ void unit_coords(int u, const GemmArgs& p, int& m_blk
 // One row (token) per thread; the RoPE partner i + HD/2 is in the same thread.
 template <int BN, int HD>
 __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int half, int row, bool row_ok,
-                                                    const QkRopeArgs& a) {
+                                                    const QkRopeArgs& a, bool v8) {
     constexpr int HALF = HD / 2;
     const int seq = row_ok ? a.row_seq[row] : 0;
     const int pos = row_ok ? a.row_pos[row] : 0;
@@ -153,8 +188,13 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int hal
             for (int q = 0; q < 32; ++q) v[q] = round_bf(v[q]);
             if (is_v) {
                 if (row_ok) {
+                    if (v8) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(vdst + c + e) = pack8(v + e);
+                        for (int e = 0; e < 32; e += 16) st_global_32(vdst + c + e, pack8(v + e), pack8(v + e + 8));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(vdst + c + e) = pack8(v + e);
+                    }
                 }
             } else {
 #pragma unroll
@@ -183,20 +223,32 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int hal
             tmem_ld32(tq + h0 + HALF + c, xh);
             if (!row_ok) continue;
 #pragma unroll
-            for (int e8 = 0; e8 < 32; e8 += 8) {
-                float lo[8], hi[8], g_lo[8], g_hi[8];
-                unpack8(*reinterpret_cast<const uint4*>(gain + c + e8), g_lo);
-                unpack8(*reinterpret_cast<const uint4*>(gain + HALF + c + e8), g_hi);
+            for (int e16 = 0; e16 < 32; e16 += 16) {
+                float lo[16], hi[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xa = __fmul_rn(__fmul_rn(round_bf(xl[e8 + e]), inv), g_lo[e]);
-                    const float xb = __fmul_rn(__fmul_rn(round_bf(xh[e8 + e]), inv), g_hi[e]);
-                    const float2 t = cs[(long long)(c + e8 + e) * a.rope_rows];   // (cos, sin)
-                    lo[e] = __fsub_rn(__fmul_rn(xa, t.x), __fmul_rn(xb, t.y));
-                    hi[e] = __fadd_rn(__fmul_rn(xb, t.x), __fmul_rn(xa, t.y));
+                for (int e8 = 0; e8 < 16; e8 += 8) {
+                    float g_lo[8], g_hi[8];
+                    unpack8(*reinterpret_cast<const uint4*>(gain + c + e16 + e8), g_lo);
+                    unpack8(*reinterpret_cast<const uint4*>(gain + HALF + c + e16 + e8), g_hi);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int k = e16 + e8 + e;
+                        const float xa = __fmul_rn(__fmul_rn(round_bf(xl[k]), inv), g_lo[e]);
+                        const float xb = __fmul_rn(__fmul_rn(round_bf(xh[k]), inv), g_hi[e]);
+                        const float2 t = cs[(long long)(c + k) * a.rope_rows];   // (cos, sin)
+                        lo[e8 + e] = __fsub_rn(__fmul_rn(xa, t.x), __fmul_rn(xb, t.y));
+                        hi[e8 + e] = __fadd_rn(__fmul_rn(xb, t.x), __fmul_rn(xa, t.y));
+                    }
                 }
-                *reinterpret_cast<uint4*>(dst + c + e8) = pack8(lo);
-                *reinterpret_cast<uint4*>(dst + HALF + c + e8) = pack8(hi);
+                if (v8) {
+                    st_global_32(dst + c + e16, pack8(lo), pack8(lo + 8));
+                    st_global_32(dst + HALF + c + e16, pack8(hi), pack8(hi + 8));
+                } else {
+                    *reinterpret_cast<uint4*>(dst + c + e16) = pack8(lo);
+                    *reinterpret_cast<uint4*>(dst + c + e16 + 8) = pack8(lo + 8);
+                    *reinterpret_cast<uint4*>(dst + HALF + c + e16) = pack8(hi);
+                    *reinterpret_cast<uint4*>(dst + HALF + c + e16 + 8) = pack8(hi + 8);
+                }
             }
         }
     }
@@ -204,9 +256,9 @@ __device__ __forceinline__ void qk_rope_epilogue_hd(uint32_t tq, int n0, int hal
 
 template <int BN>
 __device__ __forceinline__ void qk_rope_epilogue(uint32_t tq, int n0, int half, int row, bool row_ok,
-                                                 const QkRopeArgs& a) {
-    if (a.hd == 128) qk_rope_epilogue_hd<BN, 128>(tq, n0, half, row, row_ok, a);
-    else qk_rope_epilogue_hd<BN, 64>(tq, n0, half, row, row_ok, a);
+                                                 const QkRopeArgs& a, bool v8) {
+    if (a.hd == 128) qk_rope_epilogue_hd<BN, 128>(tq, n0, half, row, row_ok, a, v8);
+    else qk_rope_epilogue_hd<BN, 64>(tq, n0, half, row, row_ok, a, v8);
 }
 
 // Linear tile index of (mb, nb) in the raster order of unit_coords.
@@ -469,12 +521,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     float v[32];
                     tmem_ld32(tq + c, v);
                     scaled(v);
-                    float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q)   // tail planes are 256-byte aligned, rows BN floats
+                        st_global_32(dst + c + 8 * q, f4_as_u4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]),
+                                     f4_as_u4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]));
                 }
             } else if (!SWIGLU && !F8 && p.mode == KM_QKROPE) {
-                qk_rope_epilogue<BN>(tq, nb * BN, half, row, row_ok, p.qk);
+                qk_rope_epilogue<BN>(tq, nb * BN, half, row, row_ok, p.qk, p.v8 != 0);
             } else if (!SWIGLU && p.mode == KM_RESIDUAL) {
                 // out += acc: the chunk's residual loads are issued before its TMEM read
                 const int n0 = nb * BN;
@@ -483,20 +536,34 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     const int col = n0 + c;
                     const int nv = row_ok ? max(0, min(32, p.n_valid - col)) : 0;
                     uint4* o4 = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (long long)row * p.ldo + col);
+                    const bool wide = p.v8 != 0 && nv == 32;
                     uint4 r4[4];
+                    if (wide) {
+                        ld_global_32(o4, r4[0], r4[1]);
+                        ld_global_32(o4 + 2, r4[2], r4[3]);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) r4[i] = 8 * i < nv ? o4[i] : make_uint4(0u, 0u, 0u, 0u);
+                        for (int i = 0; i < 4; ++i) r4[i] = 8 * i < nv ? o4[i] : make_uint4(0u, 0u, 0u, 0u);
+                    }
                     float v[32];
                     tmem_ld32(tq + c, v);
                     scaled(v);
+                    uint4 w4[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        if (8 * i >= nv) break;
                         float r[8];
                         unpack8(r4[i], r);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) r[e] = r[e] + v[8 * i + e];
-                        o4[i] = pack8(r);
+                        w4[i] = pack8(r);
+                    }
+                    if (wide) {
+                        st_global_32(o4, w4[0], w4[1]);
+                        st_global_32(o4 + 2, w4[2], w4[3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (8 * i < nv) o4[i] = w4[i];
                     }
                 }
             } else if (!SWIGLU) {
@@ -509,7 +576,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     const int col = n0 + c;
                     if (row_ok && col < p.n_valid)
                         store_row_chunk(p.mode, p.out, split_off + (long long)row * p.ldo + col, v,
-                                        min(32, p.n_valid - col));
+                                        min(32, p.n_valid - col), p.v8 != 0);
                 }
             } else {
                 // gate columns [0, BN/2), up columns [BN/2, BN): this half takes output columns
@@ -527,12 +594,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         const int nv = min(32, p.n_valid - col);
                         if (p.mode == KM_PARTIAL) {
                             const long long base = split_off + (long long)row * p.ldo;
-                            store_row_chunk(KM_PARTIAL, p.out, base + col, g, nv);
-                            store_row_chunk(KM_PARTIAL, p.out, base + p.up_row0 + col, uu, nv);
+                            store_row_chunk(KM_PARTIAL, p.out, base + col, g, nv, p.v8 != 0);
+                            store_row_chunk(KM_PARTIAL, p.out, base + p.up_row0 + col, uu, nv, p.v8 != 0);
                         } else {
 #pragma unroll
                             for (int q = 0; q < 32; ++q) g[q] = silu_f(round_bf(g[q])) * round_bf(uu[q]);
-                            store_row_chunk(KM_STORE, p.out, (long long)row * p.ldo + col, g, nv);
+                            store_row_chunk(KM_STORE, p.out, (long long)row * p.ldo + col, g, nv, p.v8 != 0);
                         }
                     }
                 }
@@ -1252,6 +1319,14 @@ cudaError_t launch_linear(const LinearCall& c, cudaStream_t st) {
         g.mode = KM_QKROPE;
         g.qk = *c.qk;
         if (c.qk_done) *c.qk_done = true;
+    }
+    // 32-byte epilogue accesses when every output row starts 32-byte aligned
+    {
+        const size_t esz = g.mode == KM_F32 || g.mode == KM_PARTIAL ? 4 : 2;
+        const auto a32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+        bool ok = a32(g.out) && ((size_t)g.ldo * esz) % 32 == 0 && (g.split_stride * (long long)esz) % 32 == 0;
+        if (g.mode == KM_QKROPE) ok = a32(g.qk.q_out) && a32(g.qk.kv_layer);
+        g.v8 = ok ? 1 : 0;
     }
 
     cudaError_t e;
