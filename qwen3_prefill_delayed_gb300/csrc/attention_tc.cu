@@ -85,6 +85,7 @@ struct TcAttnArgs {
     float scale_log2;
     const int32_t* sched;        // [0] = pairs, then (query tile << 16 | sequence), heaviest first;
                                  // null for one sequence: pair i is its query tile n_qt - 1 - i
+    int v8;                      // out 32-byte aligned: O rows leave in 32-byte stores
 };
 
 // Work-list builder: one CTA.  Pair (q tile qt, sequence b) is non-empty when qt * QT < len_b; its
@@ -472,11 +473,16 @@ __global__ void __launch_bounds__(kTcThreads, (TK == 32 ? 2 : 1))
                 tmem_ld32(tO + c, o);
                 if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        float f[8];
+                    for (int e = 0; e < 32; e += 16) {
+                        float f[16];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) f[q] = o[e + q] * il;
-                        *reinterpret_cast<uint4*>(dst + c + e) = pack8(f);
+                        for (int q = 0; q < 16; ++q) f[q] = o[e + q] * il;
+                        if (p.v8) {
+                            st_global_32(dst + c + e, pack8(f), pack8(f + 8));
+                        } else {
+                            *reinterpret_cast<uint4*>(dst + c + e) = pack8(f);
+                            *reinterpret_cast<uint4*>(dst + c + e + 8) = pack8(f + 8);
+                        }
                     }
                 }
             }
@@ -560,6 +566,7 @@ cudaError_t launch_tc_cfg(const PrefillAttnArgs& a, cudaStream_t st) {
     p.kv_rows_per_seq = 2LL * a.nkv * a.n_slots;
     p.scale_log2 = (1.0f / sqrtf((float)HD)) * kLog2e;
     p.sched = a.sched;
+    p.v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;   // rows (nq hd bf16) and heads are 32-byte multiples
     const long long items = (long long)((a.max_len + QT - 1) / QT) * a.nkv * a.batch;
     const int grid = (int)std::min<long long>(items, (long long)device_sm_count() * kCtasPerSm);
     HRA_LAUNCH((prefill_attn_tc_kernel<HD, TK, NS, OB>), dim3(grid), dim3(kTcThreads), C::SMEM, st, mq, mkv, p);
