@@ -9,16 +9,20 @@
 // prefill_tower/fp8_chain.py" page, its per-layer chain) and the
 // audio-head projection.
 //
-// One CTA owns a 128 x BN output tile (M = 128 rows of A per tcgen05.mma, N = BN weight rows):
-//   warp 0     TMA producer: streams 128x64 A boxes and BNx64 W boxes (128-byte swizzle) into a
+// Persistent kernel, one CTA per SM walking 128 x BN output tiles (M = 128 rows of A per
+// tcgen05.mma, N = BN weight rows), or -- from 512 rows, the default -- 2-CTA clusters walking
+// 256 x 256 tiles with one cta_group::2 MMA of M = 256 per K step (each CTA stages its 128 rows of
+// A and half of the weight rows):
+//   warp 0     TMA producer: streams 128x64 A boxes and W boxes (128-byte swizzle) into a
 //              STAGES-deep shared-memory ring, one mbarrier pair per stage;
-//   warp 1     allocates BN TMEM columns; one elected lane issues 4 tcgen05.mma (K = 16 each) per
-//              64-wide K block and commits each stage back to the producer;
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane TMEM quadrant (one output row per thread),
-//              fused epilogue math, 16-byte vector stores.
-// Small-M calls (decode rows, the last prefill layer, the audio head) split K across CTAs so the
-// weight stream covers every SM; the fp32 partials are summed in split order by a second kernel
-// that then applies the epilogue.
+//   warp 1     allocates two accumulators of BN TMEM columns; one elected lane issues 4
+//              tcgen05.mma (K = 16 each) per 64-wide K block and commits each stage back to the
+//              producer (for a pair: rank 0 only, committing to both CTAs);
+//   warps 2-9  epilogue: tcgen05.ld of their 32-lane TMEM quadrant (one output row per thread),
+//              fused epilogue math, 32-byte (else 16-byte) vector stores, while the MMA fills the
+//              other accumulator.
+// A last round of tiles that would leave most SMs idle runs as K pieces summed by a fix-up kernel.
+// Calls of at most 64 rows take the head-form kernel of head.cu through launch_linear_small_head.
 #include <algorithm>
 #include <cudaTypedefs.h>
 #include <mutex>
