@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--kernel-case", default=None, choices=["gate_up", "qkv", "down", "audio_head", "attention"],
                     help="run only a few launches of one kernel at a profiling size, then exit")
     ap.add_argument("--kernel-m", type=int, default=None, help="rows (tokens / batch) of the kernel case")
+    ap.add_argument("--deadline", type=float, default=300.0,
+                    help="seconds after start by which the JSON line is printed even if a secondary "
+                         "section has not finished (it is then listed under extra.truncated)")
     return ap.parse_args()
 
 
@@ -89,6 +92,42 @@ def kernel_case(name, m=None):
 
 
 _T0 = time.perf_counter()
+_EMIT = {"lock": None, "done": False}
+
+
+def arm_deadline(line, extra, seconds):
+    """Print `line` (with the secondary sections measured so far) and end the process if the main
+    thread has not printed by `seconds` after start: a section stuck in a blocking call cannot
+    keep the measured numbers from being reported."""
+    import threading
+    _EMIT["lock"] = threading.Lock()
+
+    def watch():
+        time.sleep(max(0.0, seconds - (time.perf_counter() - _T0)))
+        with _EMIT["lock"]:
+            if _EMIT["done"]:
+                return
+            _EMIT["done"] = True
+            out = dict(line)
+            out["extra"] = dict(extra)
+            out["extra"]["truncated"] = f"secondary sections still running at {seconds:.0f} s were skipped"
+            print(json.dumps(out), flush=True)
+            log("deadline: line printed, exiting")
+        os._exit(0)
+
+    threading.Thread(target=watch, daemon=True).start()
+
+
+def emit(line):
+    lock = _EMIT["lock"]
+    if lock is None:
+        print(json.dumps(line), flush=True)
+        return
+    with lock:
+        if _EMIT["done"]:
+            return
+        _EMIT["done"] = True
+        print(json.dumps(line), flush=True)
 
 
 def log(msg):
@@ -378,6 +417,16 @@ def main():
 
     extra = {}
     cpu_baseline = None
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and token ids)",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": "16..256",
+                       "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (8.05 GB of weights streamed per step)"},
+            "roofline": roofline, "cpu_baseline": {"error": "not reached before the deadline"}, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk, "extra": extra}
+    if rank == 0:
+        arm_deadline(line, extra, args.deadline)
     if rank == 0 and world == 1:
         try:
             import oracle
@@ -397,29 +446,22 @@ def main():
                                       f"{d.n_layers} layers ({t_s:.1f} s), OpenMP over all host cores"}
         except Exception as ex:   # the baseline is reported, never required
             cpu_baseline = {"error": repr(ex)}
+    line["cpu_baseline"] = cpu_baseline
     del cache
     torch.cuda.empty_cache()
 
     if not args.no_extra:
-        extra = run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone=w)
+        run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone=w, out=extra)
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and token ids)",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": "16..256",
-                       "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (8.05 GB of weights streamed per step)"},
-            "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
-            "gpu_launches": int(launches), "clocks": clk, "extra": extra}
     log("done")
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(line)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone):
-    out = {}
+def run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone, out):
+    """Fill `out` section by section (a deadline print reports the sections done so far)."""
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     # ---- single full-width layer, batch 1, P = 6 and 13 (HBM-bound: 201.85 MB of weights)
     log("single full-width layer")
