@@ -83,14 +83,17 @@ struct TcAttnArgs {
     int batch, max_len, n_slots, nq, nkv, G, QT;
     long long kv_rows_per_seq;   // 2 * nkv * n_slots: rows of one sequence in the cache's row view
     float scale_log2;
-    const int32_t* sched;        // [0] = pairs, then (query tile << 16 | sequence), heaviest first;
-                                 // null for one sequence: pair i is its query tile n_qt - 1 - i
+    const int32_t* sched;        // [0] = pairs; pair i's record at sched + 8 (i + 1): sequence, first
+                                 // packed row, length, first query position in it, start position,
+                                 // keys (start + min(length, t0 + QT)); heaviest first.  Null for one
+                                 // sequence: pair i is its query tile n_qt - 1 - i
     int v8;                      // out 32-byte aligned: O rows leave in 32-byte stores
 };
 
 // Work-list builder: one CTA.  Pair (q tile qt, sequence b) is non-empty when qt * QT < len_b; its
 // weight is its key-tile count ceil((start_b + min(len_b, (qt + 1) QT)) / TK).  Counting sort by
-// weight, heaviest first (the order inside one weight is immaterial: items are independent).
+// weight, heaviest first (the order inside one weight is immaterial: items are independent).  Each
+// entry is the pair's whole record (32 bytes), so an item's set-up is one load, not a chain.
 constexpr int kSchedBins = 1024;
 constexpr int kLaunchedTK = 32;   // keys per tile of the launched configuration (the list's weights)
 __global__ void __launch_bounds__(1024) attn_schedule_kernel(const int32_t* __restrict__ cu,
@@ -139,7 +142,13 @@ __global__ void __launch_bounds__(1024) attn_schedule_kernel(const int32_t* __re
     for (int pr = threadIdx.x; pr < n_pairs; pr += blockDim.x) {
         int code;
         const int bin = bin_of(pr, code);
-        if (bin >= 0) sched[1 + atomicAdd(&hist[bin], 1)] = code;
+        if (bin >= 0) {
+            const int b = code & 0xFFFF, qt = code >> 16;
+            const int c0 = cu[b], len = cu[b + 1] - c0, t0 = qt * QT, s0 = start ? start[b] : 0;
+            int4* rec = reinterpret_cast<int4*>(sched + 8 * (1 + atomicAdd(&hist[bin], 1)));
+            rec[0] = make_int4(b, c0, len, t0);
+            rec[1] = make_int4(s0, s0 + min(len, t0 + QT), 0, 0);
+        }
     }
     if (threadIdx.x == 0) sched[0] = total;
 }
@@ -149,15 +158,20 @@ __device__ __forceinline__ int attn_item(const TcAttnArgs& p, int s, int tk, int
                                          int& t0, int& s0, int& kv_len) {
     const int pi = s / p.nkv;
     j = s - pi * p.nkv;
-    int qt;
-    if (p.sched != nullptr) {
-        const int code = p.sched[1 + pi];
-        b = code & 0xFFFF;
-        qt = code >> 16;
-    } else {   // one sequence: its query tiles, last (heaviest) first
-        b = 0;
-        qt = (p.max_len + p.QT - 1) / p.QT - 1 - pi;
+    if (p.sched != nullptr) {   // the pair's record, both halves requested together
+        const int4* rec = reinterpret_cast<const int4*>(p.sched + 8 * (1 + pi));
+        const int4 r0 = rec[0], r1 = rec[1];
+        b = r0.x;
+        cu0 = r0.y;
+        len = r0.z;
+        t0 = r0.w;
+        s0 = r1.x;
+        kv_len = r1.y;
+        return (kv_len + tk - 1) / tk;
     }
+    // one sequence: its query tiles, last (heaviest) first
+    b = 0;
+    const int qt = (p.max_len + p.QT - 1) / p.QT - 1 - pi;
     cu0 = p.cu[b];
     len = p.cu[b + 1] - cu0;
     t0 = qt * p.QT;
@@ -584,8 +598,9 @@ cudaError_t launch_tc_hd(const PrefillAttnArgs& a, cudaStream_t st) {
 }  // namespace
 
 size_t attention_schedule_bytes(int rows, int batch) {
-    // pairs <= sum_b ceil(len_b / QT) <= rows / QT + batch, QT >= 16
-    return ((size_t)rows / 16 + (size_t)batch + 2) * sizeof(int32_t);
+    // pairs <= sum_b ceil(len_b / QT) <= rows / QT + batch, QT >= 16; a 32-byte record each after
+    // a 32-byte head holding the count
+    return ((size_t)rows / 16 + (size_t)batch + 2) * 8 * sizeof(int32_t);
 }
 
 cudaError_t launch_attention_schedule(const int32_t* cu, const int32_t* start, int batch, int max_len, int nq,
