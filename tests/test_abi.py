@@ -197,3 +197,27 @@ def test_newer_entry_points_reject_bad_arguments_without_cuda(hra):
     assert L.hra_nvfp4_quantize(fake, 4, 64, ctypes.c_void_p(A + 2), fake, fake, None) == -1
     assert L.hra_nvfp4_quantize(fake, 0, 64, fake, fake, fake, None) == -1
     assert L.hra_launch_counter() == 0
+
+
+def test_form_switches_return_the_previous_setting(hra):
+    """hra_set_gemm_pairs and hra_set_decode_pass are host-side flags: each returns the setting it
+    replaced, and the defaults are the 2-CTA GEMMs on and the persistent decoder pass off."""
+    assert hra.hra_set_gemm_pairs(False) is True
+    assert hra.hra_set_gemm_pairs(True) is False
+    assert hra.hra_set_gemm_pairs(True) is True
+    assert hra.hra_set_decode_pass(True) is False
+    assert hra.hra_set_decode_pass(False) is True
+
+
+def test_linear_workspace_covers_both_gemm_forms(hra):
+    """The workspace size of a projection of at least 512 rows is valid in both GEMM forms (the last
+    round's K pieces are sized for the form that runs)."""
+    L = hra.lib()
+    sizes = {}
+    for pairs in (True, False):
+        prev = hra.hra_set_gemm_pairs(pairs)
+        try:
+            sizes[pairs] = L.hra_linear_workspace_size(4255, 2560, 4096, 1, 0)
+        finally:
+            hra.hra_set_gemm_pairs(prev)
+    assert all(s >= 256 for s in sizes.values())
