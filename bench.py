@@ -450,7 +450,9 @@ def main():
     del cache
     torch.cuda.empty_cache()
 
-    if not args.no_extra:
+    # the secondary sections (other configurations, the CPU oracle's timings) run at N = 1 only: the
+    # multi-GPU lines report the replicated main workload, and N ranks would share the host's cores
+    if not args.no_extra and world == 1:
         run_extra(hra, W, torch, dev, peaks, peaks_kind, w_backbone=w, out=extra)
 
     log("done")
